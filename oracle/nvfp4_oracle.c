@@ -1,0 +1,449 @@
+/*
+ * nvfp4_oracle.c -- plain, slow, single-threaded CPU oracle for NVFP4 quantization
+ * and the block-scaled GEMM.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Only tests/, __graft_entry__.smoke() and the
+ * cpu_baseline / reference legs of bench.py may load this library.  The CUDA
+ * path never calls, links or includes anything here, and nothing here is
+ * shared with it (no headers, tables, helpers or constants).
+ *
+ * Source of the method: the news page "NVIDIA NVFP4 paper: 4-bit pretrain hits
+ * FP8 parity (12B, 10T tokens)" (zubnet.ai, English edition; the Portuguese,
+ * French and Hindi editions say the same), cited below as [page ¶n]:
+ *   ¶2  -- E2M1 elements in 16-element blocks, an E4M3 scale per block, an FP32
+ *          per-tensor scale on top; 16x16 Random Hadamard Transforms with random
+ *          +-1 sign vectors applied only to the Wgrad inputs; 2D (16x16) block
+ *          scaling for weights so forward and backward see the same quantized
+ *          weights; stochastic rounding on gradients only.
+ *   ¶4  -- the three techniques are required together (skipping SR biases the
+ *          gradients, skipping the RHT breaks Wgrad statistics, skipping 2D
+ *          scaling breaks fwd/bwd consistency).
+ * The page fixes no formulas.  Every step it leaves open is marked [reading]
+ * below; each reading is the plainest one consistent with the page.
+ *
+ * Arithmetic: every float operation below is one IEEE binary32 operation with
+ * round-to-nearest-even, evaluated in the order written.  The file must be
+ * compiled with -ffp-contract=off and without -ffast-math (GCC contracts
+ * a*b+c into an FMA by default on aarch64, which would change results).
+ *
+ * Parity status per function (what pins it, see tests/test_oracle_pins.py):
+ *   e2m1 decode / RNE / SR encode, e4m3 decode / encode, Philox, RHT,
+ *   tensor and block scales, 2D consistency, dequant + fp64 GEMM: pinned.
+ *   Model-level quality (loss, downstream accuracy): parity unpinned, out of
+ *   scope (needs training runs).
+ */
+#include <float.h>
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#if defined(__FAST_MATH__)
+#error "the oracle must not be built with -ffast-math"
+#endif
+
+/* ------------------------------------------------------------------------- */
+/* O1. E2M1 elements [page ¶2: "E2M1 elements"].                              */
+/* E2M1 = 1 sign bit, 2 exponent bits (bias 1), 1 mantissa bit.  Magnitude     */
+/* codes 0..7 are 0, 0.5, 1, 1.5, 2, 3, 4, 6; bit 3 is the sign.               */
+/* ------------------------------------------------------------------------- */
+static const double kE2M1Magnitude[8] = {0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0};
+
+double orc_e2m1_value(int code) {
+    double mag = kE2M1Magnitude[code & 7];
+    return (code & 8) ? -mag : mag;
+}
+
+/* ------------------------------------------------------------------------- */
+/* O1. E4M3 block scales [page ¶2: "E4M3 scale factors"].                      */
+/* E4M3: sign, 4 exponent bits (bias 7), 3 mantissa bits, no infinities, the   */
+/* all-ones pattern S.1111.111 is NaN, largest finite 448, smallest subnormal  */
+/* 2^-9.  Block scales are non-negative (sign bit 0).                          */
+/* ------------------------------------------------------------------------- */
+double orc_e4m3_value(int code) {
+    int s = (code >> 7) & 1, e = (code >> 3) & 15, m = code & 7;
+    double v;
+    if (e == 15 && m == 7) return NAN;
+    if (e == 0) v = ldexp((double)m, -9);                 /* subnormal: m/8 * 2^-6 */
+    else v = ldexp(1.0 + (double)m / 8.0, e - 7);
+    return s ? -v : v;
+}
+
+/* [reading] Block scale cast: round to nearest, ties to even mantissa, with    */
+/* saturation to 448 (values above the largest finite code map to 448).        */
+/* Magnitudes below half the smallest subnormal (2^-10) round to 0; exactly     */
+/* 2^-10 is a tie between 0 and 2^-9 and goes to the even code 0.              */
+/* Written from the format's definition: find the binade, quantize the         */
+/* mantissa to 3 bits with RNE, handle the carry into the next binade.         */
+uint8_t orc_e4m3_encode(float v) {
+    uint8_t sign = 0;
+    double a = (double)v;                  /* exact widening */
+    if (a < 0) { sign = 0x80; a = -a; }
+    if (isnan(a)) return 0x7F | sign;
+    if (a >= 448.0) return 0x7E | sign;    /* saturate (satfinite) */
+    /* quantum of the E4M3 grid around a: 2^(e-3) for binade [2^e, 2^(e+1)), e >= -6;
+       2^-9 (subnormal spacing) below 2^-6. */
+    int e;
+    if (a < ldexp(1.0, -6)) e = -6;
+    else { frexp(a, &e); e -= 1; }         /* a in [2^e, 2^(e+1)) */
+    double q = ldexp(1.0, e - 3);
+    double n = a / q;                      /* exact: power-of-two division */
+    double fl = floor(n);
+    double rem = n - fl;                   /* exact */
+    double k;
+    if (rem > 0.5) k = fl + 1;
+    else if (rem < 0.5) k = fl;
+    else k = (fmod(fl, 2.0) == 0.0) ? fl : fl + 1;   /* tie: even count of quanta */
+    double r = k * q;                      /* the rounded magnitude, on the grid */
+    if (r > 448.0) r = 448.0;
+    if (r == 0.0) return sign;
+    /* re-encode the exact grid value into bits */
+    if (r < ldexp(1.0, -6)) {
+        int m = (int)(r / ldexp(1.0, -9));
+        return (uint8_t)(sign | m);
+    }
+    int e2;
+    frexp(r, &e2); e2 -= 1;                 /* r in [2^e2, 2^(e2+1)) */
+    int m = (int)((r / ldexp(1.0, e2) - 1.0) * 8.0);
+    return (uint8_t)(sign | ((e2 + 7) << 3) | m);
+}
+
+/* ------------------------------------------------------------------------- */
+/* O4. Element encode, round-to-nearest-even [page ¶2: SR on gradients only,   */
+/* so every other tensor rounds deterministically].                            */
+/* [reading] ties go to the code with an even magnitude index (mantissa bit 0); */
+/* magnitudes above 6 saturate to 6; the sign bit is copied from the input, so  */
+/* a negative input that rounds to zero gives code 8 (-0).                      */
+/* Implemented as the nearest grid point, found by scanning the grid.          */
+/* ------------------------------------------------------------------------- */
+int orc_e2m1_encode_rne(float y) {
+    int sign = signbit(y) ? 8 : 0;
+    float a = fabsf(y);
+    if (isnan(a)) return sign | 7;         /* unreachable: NaN inputs are rejected */
+    if (a >= 6.0f) return sign | 7;
+    int best = 0;
+    for (int k = 1; k < 8; ++k) {
+        double d_best = fabs((double)a - kE2M1Magnitude[best]);
+        double d_k = fabs((double)a - kE2M1Magnitude[k]);
+        if (d_k < d_best || (d_k == d_best && (k % 2) == 0)) best = k;
+    }
+    return sign | best;
+}
+
+/* ------------------------------------------------------------------------- */
+/* O4. Element encode, stochastic rounding [page ¶2: "stochastic rounding on   */
+/* gradients only"; ¶4: without it the gradients are biased].                  */
+/* [reading] saturate |y| to 6; take the neighbouring grid points lo <= a < hi  */
+/* and p = (a - lo) / (hi - lo) (exact: Sterbenz, power-of-two spacing); with   */
+/* 16 random bits r, round to hi iff r * 2^-16 < p.  So E[value] is within      */
+/* 2^-16 of the spacing of a.                                                  */
+/* ------------------------------------------------------------------------- */
+int orc_e2m1_encode_sr(float y, uint32_t r16) {
+    int sign = signbit(y) ? 8 : 0;
+    float a = fabsf(y);
+    if (a >= 6.0f) return sign | 7;
+    int lo = 0;
+    while (lo < 7 && (float)kE2M1Magnitude[lo + 1] <= a) ++lo;   /* grid[lo] <= a < grid[lo+1] */
+    float glo = (float)kE2M1Magnitude[lo], ghi = (float)kE2M1Magnitude[lo + 1];
+    float p = (a - glo) / (ghi - glo);     /* exact in binary32 */
+    float u = (float)(r16 & 0xFFFFu) * (1.0f / 65536.0f);
+    return sign | ((u < p) ? lo + 1 : lo);
+}
+
+/* ------------------------------------------------------------------------- */
+/* O6. Philox4x32-10, from Salmon, Moraes, Dror, Shaw, "Parallel Random         */
+/* Numbers: As Easy as 1, 2, 3" (SC'11): ten rounds of the Philox S-box on a    */
+/* 4x32-bit counter under a 2x32-bit key, the key bumped by the Weyl constants  */
+/* between rounds.                                                             */
+/* ------------------------------------------------------------------------- */
+void orc_philox4x32_10(const uint32_t ctr[4], const uint32_t key[2], uint32_t out[4]) {
+    const uint32_t mult0 = 0xD2511F53u, mult1 = 0xCD9E8D57u;      /* round multipliers */
+    const uint32_t weyl0 = 0x9E3779B9u, weyl1 = 0xBB67AE85u;      /* key schedule */
+    uint32_t x0 = ctr[0], x1 = ctr[1], x2 = ctr[2], x3 = ctr[3];
+    uint32_t k0 = key[0], k1 = key[1];
+    for (int round = 0; round < 10; ++round) {
+        if (round > 0) { k0 += weyl0; k1 += weyl1; }
+        uint64_t p0 = (uint64_t)mult0 * x0;
+        uint64_t p1 = (uint64_t)mult1 * x2;
+        uint32_t hi0 = (uint32_t)(p0 >> 32), lo0 = (uint32_t)p0;
+        uint32_t hi1 = (uint32_t)(p1 >> 32), lo1 = (uint32_t)p1;
+        uint32_t y0 = hi1 ^ x1 ^ k0;
+        uint32_t y1 = lo1;
+        uint32_t y2 = hi0 ^ x3 ^ k1;
+        uint32_t y3 = lo0;
+        x0 = y0; x1 = y1; x2 = y2; x3 = y3;
+    }
+    out[0] = x0; out[1] = x1; out[2] = x2; out[3] = x3;
+}
+
+/* [reading] random bits for the SR decision of element idx (row-major index in */
+/* the quantized operand's logical [rows, cols] shape): one Philox call per 8   */
+/* elements, key = (seed lo, seed hi), counter = (lo32(idx/8), hi32(idx/8),     */
+/* stream, offset); element idx takes the 16-bit half (idx & 1) (0 = low half) */
+/* of output word ((idx >> 1) & 3).                                            */
+uint32_t orc_sr_bits(uint64_t seed, uint32_t stream, uint32_t offset, uint64_t idx) {
+    uint64_t g = idx >> 3;
+    uint32_t ctr[4] = {(uint32_t)g, (uint32_t)(g >> 32), stream, offset};
+    uint32_t key[2] = {(uint32_t)seed, (uint32_t)(seed >> 32)};
+    uint32_t w[4];
+    orc_philox4x32_10(ctr, key, w);
+    uint32_t word = w[(idx >> 1) & 3];
+    return (idx & 1) ? (word >> 16) : (word & 0xFFFFu);
+}
+
+/* ------------------------------------------------------------------------- */
+/* O5. 16x16 Random Hadamard Transform [page ¶2: "16x16 Random Hadamard        */
+/* Transforms with random +-1 sign vectors applied only to Wgrad inputs"].     */
+/* [reading] R = (1/4) H16 diag(s), H16 the Sylvester Hadamard matrix           */
+/* H[i][j] = (-1)^popcount(i & j) (orthonormal after the 1/4, so               */
+/* (R dY)^T (R X) = dY^T X exactly in real arithmetic).  One sign vector s per  */
+/* call: s_j = -1 iff bit j of word 0 of Philox4x32-10(key = seed, ctr = 0).    */
+/* H16 is the product of four sparse stage matrices S_8 S_4 S_2 S_1; stage h    */
+/* maps (t_i, t_{i+h}) -> (t_i + t_{i+h}, t_i - t_{i+h}) for every i with       */
+/* i & h == 0.  [reading] evaluation order, pinned for bit parity: multiply by   */
+/* the signs, apply the stages for h = 1, 2, 4, 8 in turn (each entry one fp32  */
+/* add or subtract, the lower index first), then multiply by 0.25 (exact).      */
+/* ------------------------------------------------------------------------- */
+uint32_t orc_rht_sign_mask(uint64_t seed) {
+    uint32_t ctr[4] = {0, 0, 0, 0};
+    uint32_t key[2] = {(uint32_t)seed, (uint32_t)(seed >> 32)};
+    uint32_t w[4];
+    orc_philox4x32_10(ctr, key, w);
+    return w[0] & 0xFFFFu;
+}
+
+/* Entry (i, j) of stage matrix S_h, as an integer in {-1, 0, +1}. */
+static int stage_entry(int h, int i, int j) {
+    if ((i & h) == 0) return (j == i || j == i + h) ? 1 : 0;     /* top row of the pair */
+    /* bottom row i = base + h: +1 at base, -1 at i */
+    if (j == i - h) return 1;
+    if (j == i) return -1;
+    return 0;
+}
+
+/* The product S_8 S_4 S_2 S_1 as a dense integer matrix (for the pins). */
+void orc_hadamard_stage_product(int32_t H[256]) {
+    int32_t acc[256], tmp[256];
+    for (int i = 0; i < 16; ++i)
+        for (int j = 0; j < 16; ++j) acc[i * 16 + j] = (i == j);
+    for (int h = 1; h <= 8; h <<= 1) {                  /* acc <- S_h * acc */
+        for (int i = 0; i < 16; ++i)
+            for (int j = 0; j < 16; ++j) {
+                int32_t s = 0;
+                for (int k = 0; k < 16; ++k) s += stage_entry(h, i, k) * acc[k * 16 + j];
+                tmp[i * 16 + j] = s;
+            }
+        memcpy(acc, tmp, sizeof(acc));
+    }
+    memcpy(H, acc, sizeof(acc));
+}
+
+/* y = R v: explicit sparse matrix-vector products by the stage matrices.  Each
+   output entry is the first non-zero term plus the second one, so it is the
+   single fp32 a+b or a-b of the butterfly. */
+void orc_rht16(const float v[16], uint32_t sign_mask, float y[16]) {
+    float t[16], u[16];
+    for (int j = 0; j < 16; ++j) t[j] = ((sign_mask >> j) & 1) ? -v[j] : v[j];
+    for (int h = 1; h <= 8; h <<= 1) {
+        for (int i = 0; i < 16; ++i) {
+            int first = 1;
+            float acc = 0.0f;
+            for (int j = 0; j < 16; ++j) {
+                int s = stage_entry(h, i, j);
+                if (s == 0) continue;
+                float term = (s > 0) ? t[j] : -t[j];
+                if (first) { acc = term; first = 0; }
+                else acc = acc + term;
+            }
+            u[i] = acc;
+        }
+        memcpy(t, u, sizeof(t));
+    }
+    for (int j = 0; j < 16; ++j) y[j] = t[j] * 0.25f;
+}
+
+/* ------------------------------------------------------------------------- */
+/* Quantization of one operand.                                               */
+/* ------------------------------------------------------------------------- */
+enum { ORC_F32 = 0, ORC_BF16 = 1 };
+enum { ORC_ROUND_RNE = 0, ORC_ROUND_SR = 1 };
+enum { ORC_BLOCK_1X16_ROW = 0, ORC_BLOCK_1X16_COL = 1, ORC_BLOCK_16X16 = 2 };
+enum { ORC_OK = 0, ORC_ERR_ARG = 1, ORC_ERR_NONFINITE = 7 };
+
+static float load_elem(const void* x, int dtype, int64_t ldx, int64_t r, int64_t c) {
+    if (dtype == ORC_F32) return ((const float*)x)[r * ldx + c];
+    uint16_t b = ((const uint16_t*)x)[r * ldx + c];
+    uint32_t bits = (uint32_t)b << 16;                    /* bf16 -> fp32 is exact */
+    float f;
+    memcpy(&f, &bits, 4);
+    return f;
+}
+
+/* O2. [reading] tensor scale: s_enc = 2688 / amax_t (2688 = 6 * 448, so the
+   largest block maps to the top E4M3 scale and its largest element to 6),
+   clamped to FLT_MAX; s_enc = 1 when amax_t = 0.  The stored FP32 per-tensor
+   scale [page ¶2] is s_dec = 1 / s_enc. */
+static float tensor_s_enc(float amax_t) {
+    if (amax_t == 0.0f) return 1.0f;
+    float s = 2688.0f / amax_t;
+    if (s > FLT_MAX) s = FLT_MAX;
+    return s;
+}
+
+/* O3. [reading] block scale S_b = e4m3(RN((amax_b / 6) * s_enc)) and the
+   element multiplier e_b = RN(s_enc / S_b) (clamped to FLT_MAX; 0 if S_b = 0). */
+static uint8_t block_scale_code(float amax_b, float s_enc) {
+    float t = amax_b / 6.0f;
+    t = t * s_enc;
+    return orc_e4m3_encode(t);
+}
+
+static float block_multiplier(uint8_t sb_code, float s_enc) {
+    float sb = (float)orc_e4m3_value(sb_code);
+    if (sb == 0.0f) return 0.0f;
+    float e = s_enc / sb;
+    if (e > FLT_MAX) e = FLT_MAX;
+    return e;
+}
+
+/*
+ * orc_quantize: quantize x [R, C] (row pitch ldx elements) to NVFP4.
+ *
+ * The quantized operand T has logical shape [rows, cols] with blocks along cols:
+ *   1X16_ROW : T = x,   [R, C], 1x16 blocks;
+ *   1X16_COL : T = x^T, [C, R], 1x16 blocks along R, optionally T's rows RHT'd
+ *              per 16-chunk (the Wgrad operands, [page ¶2]);
+ *   16X16    : T = x,   [R, C], one scale per 16x16 tile (weights, [page ¶2]).
+ * Outputs: codes [rows, cols/2] (element 2j in the low nibble of byte j, 2j+1 in
+ * the high nibble), scales [rows, cols/16] (16X16: [rows/16, cols/16]), s_dec,
+ * and amax_t.  Only output rows [row_begin, row_end) of T are encoded (the
+ * tensor amax is always over all of T); pass row_end < 0 for all rows.  Output
+ * buffers are indexed by the absolute output row.
+ * SR random bits: stream 1 for 1X16_COL, 0 otherwise.
+ */
+int orc_quantize(const void* x, int dtype, int64_t R, int64_t C, int64_t ldx,
+                 int block, int round_mode, int rht,
+                 uint64_t sr_seed, uint32_t sr_offset, uint64_t rht_seed,
+                 uint8_t* codes, uint8_t* scales, float* s_dec_out, float* amax_out,
+                 int64_t row_begin, int64_t row_end) {
+    if (R < 0 || C < 0 || ldx < C) return ORC_ERR_ARG;
+    if (rht && block != ORC_BLOCK_1X16_COL) return ORC_ERR_ARG;
+    int64_t rows = (block == ORC_BLOCK_1X16_COL) ? C : R;
+    int64_t cols = (block == ORC_BLOCK_1X16_COL) ? R : C;
+    if (cols % 16 != 0) return ORC_ERR_ARG;
+    if (block == ORC_BLOCK_16X16 && rows % 16 != 0) return ORC_ERR_ARG;
+    if (row_end < 0 || row_end > rows) row_end = rows;
+    if (row_begin < 0) row_begin = 0;
+    if (block == ORC_BLOCK_16X16 && (row_begin % 16 != 0 || row_end % 16 != 0)) return ORC_ERR_ARG;
+
+    /* Step 1: T in fp32 (with the RHT for the Wgrad operands). */
+    float* T = (float*)malloc(sizeof(float) * (size_t)(rows * cols > 0 ? rows * cols : 1));
+    if (!T) return ORC_ERR_ARG;
+    for (int64_t i = 0; i < rows; ++i)
+        for (int64_t j = 0; j < cols; ++j)
+            T[i * cols + j] = (block == ORC_BLOCK_1X16_COL) ? load_elem(x, dtype, ldx, j, i)
+                                                          : load_elem(x, dtype, ldx, i, j);
+    if (rht) {
+        uint32_t mask = orc_rht_sign_mask(rht_seed);
+        for (int64_t i = 0; i < rows; ++i)
+            for (int64_t j = 0; j < cols; j += 16) orc_rht16(&T[i * cols + j], mask, &T[i * cols + j]);
+    }
+
+    /* Step 2: tensor amax over T, exactly as it will be quantized. */
+    float amax_t = 0.0f;
+    int finite = 1;
+    for (int64_t i = 0; i < rows * cols; ++i) {
+        float a = fabsf(T[i]);
+        if (!isfinite(a)) finite = 0;
+        else if (a > amax_t) amax_t = a;
+    }
+    if (!finite) { free(T); return ORC_ERR_NONFINITE; }
+    if (amax_out) *amax_out = amax_t;
+
+    /* Step 3: tensor scale. */
+    float s_enc = tensor_s_enc(amax_t);
+    float s_dec = 1.0f / s_enc;
+    if (s_dec_out) *s_dec_out = s_dec;
+
+    /* Steps 4-5: block scales, element codes, nibble packing. */
+    uint32_t stream = (block == ORC_BLOCK_1X16_COL) ? 1u : 0u;
+    int bh = (block == ORC_BLOCK_16X16) ? 16 : 1;       /* block height in rows */
+    for (int64_t i0 = row_begin; i0 < row_end; i0 += bh) {
+        for (int64_t j0 = 0; j0 < cols; j0 += 16) {
+            float amax_b = 0.0f;
+            for (int di = 0; di < bh; ++di)
+                for (int dj = 0; dj < 16; ++dj) {
+                    float a = fabsf(T[(i0 + di) * cols + j0 + dj]);
+                    if (a > amax_b) amax_b = a;
+                }
+            uint8_t sb = block_scale_code(amax_b, s_enc);
+            float e_b = block_multiplier(sb, s_enc);
+            if (block == ORC_BLOCK_16X16) scales[(i0 / 16) * (cols / 16) + j0 / 16] = sb;
+            else scales[i0 * (cols / 16) + j0 / 16] = sb;
+            for (int di = 0; di < bh; ++di)
+                for (int dj = 0; dj < 16; ++dj) {
+                    int64_t i = i0 + di, j = j0 + dj;
+                    float y = T[i * cols + j] * e_b;
+                    int code;
+                    if (round_mode == ORC_ROUND_SR)
+                        code = orc_e2m1_encode_sr(y, orc_sr_bits(sr_seed, stream, sr_offset,
+                                                                 (uint64_t)(i * cols + j)));
+                    else
+                        code = orc_e2m1_encode_rne(y);
+                    uint8_t* byte = &codes[i * (cols / 2) + j / 2];
+                    if ((j & 1) == 0) *byte = (uint8_t)((*byte & 0xF0) | code);
+                    else *byte = (uint8_t)((*byte & 0x0F) | (code << 4));
+                }
+        }
+    }
+    free(T);
+    return ORC_OK;
+}
+
+/* ------------------------------------------------------------------------- */
+/* O8. Dequantization: x_hat = val(code) * S_b * s_dec, in fp64 (exact: at most */
+/* 2 + 4 + 24 significant bits).  block2d selects one scale per 16x16 tile.     */
+/* Rows [row_begin, row_end) of the operand are written to out[(i-row_begin)]. */
+/* ------------------------------------------------------------------------- */
+void orc_dequant(const uint8_t* codes, const uint8_t* scales, float s_dec,
+                 int64_t rows, int64_t cols, int block2d,
+                 int64_t row_begin, int64_t row_end, double* out) {
+    (void)rows;
+    for (int64_t i = row_begin; i < row_end; ++i)
+        for (int64_t j = 0; j < cols; ++j) {
+            uint8_t byte = codes[i * (cols / 2) + j / 2];
+            int code = (j & 1) ? (byte >> 4) : (byte & 15);
+            uint8_t sb = block2d ? scales[(i / 16) * (cols / 16) + j / 16] : scales[i * (cols / 16) + j / 16];
+            out[(i - row_begin) * cols + j] = orc_e2m1_value(code) * orc_e4m3_value(sb) * (double)s_dec;
+        }
+}
+
+/* O8. C[M, N] = A[M, K] . B[N, K]^T in fp64, plain dot products in k order. */
+void orc_gemm_f64(const double* A, const double* B, int64_t M, int64_t N, int64_t K, double* C) {
+    for (int64_t m = 0; m < M; ++m)
+        for (int64_t n = 0; n < N; ++n) {
+            double s = 0.0;
+            for (int64_t k = 0; k < K; ++k) s += A[m * K + k] * B[n * K + k];
+            C[m * N + n] = s;
+        }
+}
+
+/* ------------------------------------------------------------------------- */
+/* Array forms of the codecs, for the pins that sweep many values.            */
+/* ------------------------------------------------------------------------- */
+void orc_e4m3_encode_array(const float* v, int64_t n, uint8_t* out) {
+    for (int64_t i = 0; i < n; ++i) out[i] = orc_e4m3_encode(v[i]);
+}
+
+void orc_e2m1_encode_rne_array(const float* y, int64_t n, uint8_t* out) {
+    for (int64_t i = 0; i < n; ++i) out[i] = (uint8_t)orc_e2m1_encode_rne(y[i]);
+}
+
+void orc_e2m1_encode_sr_array(const float* y, const uint32_t* r16, int64_t n, uint8_t* out) {
+    for (int64_t i = 0; i < n; ++i) out[i] = (uint8_t)orc_e2m1_encode_sr(y[i], r16[i]);
+}
+
+void orc_sr_bits_array(uint64_t seed, uint32_t stream, uint32_t offset, const uint64_t* idx,
+                       int64_t n, uint32_t* out) {
+    for (int64_t i = 0; i < n; ++i) out[i] = orc_sr_bits(seed, stream, offset, idx[i]);
+}
