@@ -1,0 +1,355 @@
+#!/usr/bin/env python3
+"""Benchmark of the NVFP4 quantized linear layer on one GB300.
+
+A step is one pass of the whole hot path over one batch of the FFN up-projection
+shaped like the 5120-hidden model of the NVFP4 pretraining news page (¶1):
+M = 8192 tokens, K = 5120, N = 20480, bf16 inputs X ~ N(0,1), W ~ N(0,0.02),
+dY ~ N(0,1e-3):
+  quantize W (16x16, RNE, with W^T)            -- weights [page ¶2]
+  Fprop : quantize X (1x16, RNE)     ; Y  = X . W^T     (tcgen05 FP4 GEMM, bf16 out)
+  Dgrad : quantize dY (1x16, SR)     ; dX = dY . W
+  Wgrad : quantize dY^T, X^T (1x16 along M, shared-sign RHT; SR / RNE) ; dW = dY^T . X
+value = 3 * 2MNK / step time (TFLOP/s, quantizers included).  One JSON line.
+
+--impl reference times the CPU oracle (test infrastructure) on a bounded sample of
+the same workload; it is the reference arm because the pages ship no code.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+M, K, N = 8192, 5120, 20480
+METRIC = "NVFP4 GEMM TFLOPS (Fprop/Dgrad/Wgrad at 8192x5120x20480); quantize GB/s"
+WORKLOAD = "ffn_up_8192x5120x20480"
+FP4_PER_BF16 = 13.5 / 2.25          # nominal dense FP4 : BF16 tensor rate on GB300
+
+
+def env_rank():
+    return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), int(os.environ.get("LOCAL_RANK", 0))
+
+
+def measured_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return json.load(f), "measured"
+    except Exception:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms during the timed region."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        self.lines = []
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except Exception:
+                self.proc.kill()
+                out = ""
+            self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for l in getattr(self, "lines", []):
+            f = [x.strip() for x in l.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# --------------------------------------------------------------------------- our arm
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+    import nvfp4_bit_quantized_gb300 as nv
+    from nvfp4_bit_quantized_gb300 import inputs
+
+    rank, world, local = env_rank()
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local)
+    # weak scaling: every rank owns its own token batch (data parallel over M)
+    X, W, dY = inputs.linear_layer(M, K, N, seed=1000 * rank, dtype=torch.bfloat16, device=dev)
+    nv.reset_status()
+    stream = torch.cuda.current_stream()
+
+    names = ["quant_W_2d", "quant_X_row", "gemm_fprop", "quant_dY_row_sr", "gemm_dgrad",
+             "quant_dYt_rht_sr", "quant_Xt_rht", "gemm_wgrad"]
+
+    def step(sr_offset, ev=None):
+        def mark(i):
+            if ev is not None:
+                ev[i].record(stream)
+        mark(0)
+        wq = nv.quantize(W, nv.TILE16, nv.RNE, scales=False, transpose=True)
+        mark(1)
+        xq = nv.quantize(X, nv.ROW, nv.RNE, scales=False)
+        mark(2)
+        Y = nv.gemm(xq, wq, torch.bfloat16)
+        mark(3)
+        dyq = nv.quantize(dY, nv.ROW, nv.SR, sr_seed=7, sr_offset=sr_offset, scales=False)
+        mark(4)
+        dX = nv.gemm(dyq, wq.transposed(), torch.bfloat16)
+        mark(5)
+        dyt = nv.quantize(dY, nv.COL, nv.SR, rht=True, sr_seed=7, sr_offset=sr_offset, rht_seed=11, scales=False)
+        mark(6)
+        xt = nv.quantize(X, nv.COL, nv.RNE, rht=True, rht_seed=11, scales=False)
+        mark(7)
+        dW = nv.gemm(dyt, xt, torch.bfloat16)
+        mark(8)
+        return Y, dX, dW
+
+    launches_per_step = 5 * 2 + 3
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    if nv.status_query() != 0:
+        raise RuntimeError("device status error during warm-up")
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(9)] for _ in range(args.steps)]
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        t0.record(stream)
+        for i in range(args.steps):
+            step(args.warmup + i, evs[i])
+        t1.record(stream)
+        torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    ms_total = t0.elapsed_time(t1)
+    if world > 1:
+        tt = torch.tensor([ms_total], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms_total = float(tt.item())
+    status = nv.status_query()
+    ms_step = ms_total / args.steps
+    flops_step = 3 * 2.0 * M * N * K
+    value = world * flops_step / (ms_step * 1e-3) / 1e12
+
+    per = {n: statistics.mean(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(args.steps))
+           for j, n in enumerate(names)}
+    gemm_ms = statistics.mean([per["gemm_fprop"], per["gemm_dgrad"], per["gemm_wgrad"]])
+    gemm_tflops = {k: 2.0 * M * N * K / (per[k] * 1e-3) / 1e12 for k in ("gemm_fprop", "gemm_dgrad", "gemm_wgrad")}
+    # algorithmic bytes per element: read bf16 twice (amax + encode), write 0.5 B codes + 1/16 B scales;
+    # the 2D weight pass also writes the transposed codes and scales (another 0.5 + 1/16 B)
+    qbytes = {
+        "quant_W_2d": N * K * (2 + 2 + 2 * (0.5 + 1 / 16)),
+        "quant_X_row": M * K * (4 + 0.5 + 1 / 16),
+        "quant_dY_row_sr": M * N * (4 + 0.5 + 1 / 16),
+        "quant_dYt_rht_sr": M * N * (4 + 0.5 + 1 / 16),
+        "quant_Xt_rht": M * K * (4 + 0.5 + 1 / 16),
+    }
+    quant_gbs = {k: qbytes[k] / (per[k] * 1e-3) / 1e9 for k in qbytes}
+    quant_ms = sum(per[k] for k in qbytes)
+    peaks, peak_src = measured_peaks()
+    fp4_peak = peaks["bf16_tflops_sustained"] * FP4_PER_BF16
+    achieved = 2.0 * M * N * K / (gemm_ms * 1e-3) / 1e12
+
+    # end to end through the public API with host buffers: H2D inputs, the step, D2H results
+    hX = X.cpu().pin_memory()
+    hW = W.cpu().pin_memory()
+    hdY = dY.cpu().pin_memory()
+    hY = torch.empty((M, N), dtype=torch.bfloat16).pin_memory()
+    hdX = torch.empty((M, K), dtype=torch.bfloat16).pin_memory()
+    hdW = torch.empty((N, K), dtype=torch.bfloat16).pin_memory()
+    h2d = (hX.numel() + hW.numel() + hdY.numel()) * 2
+    d2h = (hY.numel() + hdX.numel() + hdW.numel()) * 2
+
+    def e2e_step(i):
+        X.copy_(hX, non_blocking=True)
+        W.copy_(hW, non_blocking=True)
+        dY.copy_(hdY, non_blocking=True)
+        Y, dX, dW = step(i)
+        hY.copy_(Y, non_blocking=True)
+        hdX.copy_(dX, non_blocking=True)
+        hdW.copy_(dW, non_blocking=True)
+
+    for i in range(2):
+        e2e_step(i)
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e2e_steps = max(1, min(args.steps, 5))
+    e0.record(stream)
+    for i in range(e2e_steps):
+        e2e_step(i)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    e2e_value = world * flops_step / (e2e_ms * 1e-3) / 1e12
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        cpu = oracle_sample(budget_s=args.cpu_seconds)
+
+    if world > 1:
+        dist.destroy_process_group()
+    if rank != 0:
+        return
+    line = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_step, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "e2m1/e4m3 operands, fp32 accumulate, bf16 in/out",
+        "data": "synthetic (seeded normal; X N(0,1), W N(0,0.02), dY N(0,1e-3))",
+        "config": {"workload": WORKLOAD, "M": M, "K": K, "N": N, "in_dtype": "bf16", "out_dtype": "bf16",
+                   "step": "quantize W(16x16)+X(row)+dY(row,SR)+dY^T,X^T(RHT) + Fprop/Dgrad/Wgrad GEMMs",
+                   "l2": "inputs larger than L2 (the step streams >1 GB; 129 MB L2)",
+                   "parallelism": f"dp{world} (independent token batches, no collective)"},
+        "gemm_tflops": {k: round(v, 1) for k, v in gemm_tflops.items()},
+        "quantize_gbs": {k: round(v, 1) for k, v in quant_gbs.items()},
+        "ms_breakdown": {k: round(v, 4) for k, v in per.items()},
+        "quantize_ms_per_step": round(quant_ms, 4),
+        "roofline": {"bound": "tensor", "achieved": round(achieved, 1), "peak": round(fp4_peak, 1),
+                     "unit": "TFLOP/s", "frac": round(achieved / fp4_peak, 4), "traffic": None,
+                     "kernel": "gemm_nvfp4_kernel",
+                     "peak_source": f"{peak_src} bf16 sustained x {FP4_PER_BF16:g} (nominal dense FP4:BF16)"},
+        "quantize_roofline": {"bound": "hbm", "achieved": round(sum(qbytes.values()) / (quant_ms * 1e-3) / 1e9, 1),
+                              "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                              "frac": round(sum(qbytes.values()) / (quant_ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 4)},
+        "e2e": {"value": round(e2e_value, 2), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 3)},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clk.summary(),
+        "device_status": status,
+        "cpu_baseline": cpu,
+    }
+    print(json.dumps(line))
+
+
+# --------------------------------------------------------------------------- oracle (CPU) arm
+
+def oracle_sample(budget_s: float = 15.0, reps: int | None = None):
+    """Times the CPU oracle on a bounded sample of the step: one output block of
+    each GEMM with the full contraction length of the workload, the oracle
+    quantizing the operand rows that block needs:
+      Fprop  64x128 block of Y,  K = 5120   (X rows 1x16 RNE, W rows 16x16)
+      Dgrad  64x128 block of dX, N = 20480  (dY rows 1x16 SR, W^T rows 16x16)
+      Wgrad 128x64  block of dW, M = 8192   (dY^T, X^T columns with the RHT; SR / RNE)
+    value = sampled GEMM flops / oracle time (single-threaded C)."""
+    import numpy as np
+    import oracle
+    import torch
+    from nvfp4_bit_quantized_gb300 import inputs
+
+    def bits(t):
+        return t.contiguous().view(torch.int16).numpy().view(np.uint16)
+
+    mb, nb = 64, 128
+    xs = bits(inputs.normal((mb, K), 1.0, 0))            # X rows
+    ws = bits(inputs.normal((nb, K), 0.02, 1))           # W rows
+    dys = bits(inputs.normal((mb, N), 1e-3, 2))          # dY rows
+    wts = bits(inputs.normal((nb, N), 0.02, 3))          # W^T rows (= W columns)
+    dyc = bits(inputs.normal((M, nb), 1e-3, 4))          # dY columns
+    xc = bits(inputs.normal((M, mb), 1.0, 5))            # X columns
+    flops_rep = 2.0 * mb * nb * (K + N + M)
+    n, t0 = 0, time.perf_counter()
+    while True:
+        deq, gemm = oracle.dequant, oracle.gemm_f64
+        gemm(deq(oracle.quantize(xs, oracle.ROW)), deq(oracle.quantize(ws, oracle.TILE16)))
+        gemm(deq(oracle.quantize(dys, oracle.ROW, oracle.SR, sr_seed=7)), deq(oracle.quantize(wts, oracle.TILE16)))
+        gemm(deq(oracle.quantize(dyc, oracle.COL, oracle.SR, rht=True, sr_seed=7, rht_seed=11)),
+             deq(oracle.quantize(xc, oracle.COL, oracle.RNE, rht=True, rht_seed=11)))
+        n += 1
+        el = time.perf_counter() - t0
+        if (reps is not None and n >= reps) or (reps is None and el >= budget_s):
+            break
+    return {"value": round(n * flops_rep / el / 1e12, 6), "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
+            "sample": f"{n} x three output blocks (Fprop 64x128 K={K}, Dgrad 64x128 K={N}, Wgrad 128x64 K={M}) "
+                      f"with their operand rows quantized by the oracle; single-threaded C; {el:.1f} s",
+            "flops_per_rep": flops_rep, "seconds": round(el, 3)}
+
+
+def run_reference(args):
+    rank, world, _ = env_rank()
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    for _ in range(args.warmup):
+        oracle_sample(reps=1)
+    t0 = time.perf_counter()
+    r = oracle_sample(reps=args.steps)
+    el = time.perf_counter() - t0
+    value = r["value"]
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(el / args.steps * 1e3, 2),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64 (oracle)",
+            "data": "synthetic", "config": {"workload": WORKLOAD, "M": M, "K": K, "N": N,
+                                            "sample": "per step: one output block of each GEMM, full contraction"},
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": 1, "kind": "oracle", "sample": r["sample"]},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours":
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

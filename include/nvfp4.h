@@ -1,0 +1,213 @@
+/*
+ * nvfp4.h -- C ABI of the GB300 (sm_103a) NVFP4 quantized linear layer.
+ *
+ * The method is the one summarised on the news page "NVIDIA NVFP4 paper: 4-bit
+ * pretrain hits FP8 parity (12B, 10T tokens)" (zubnet.ai), cited as [page ¶n]:
+ *   ¶2: E2M1 elements in 16-element blocks with an E4M3 scale per block and an
+ *       FP32 per-tensor scale; 2D block scaling for weights; a 16x16 Random
+ *       Hadamard Transform with random +-1 signs on the Wgrad inputs only;
+ *       stochastic rounding on gradients only.
+ *   ¶1, ¶3: the GEMMs run on Blackwell tensor cores.
+ * Where the page is silent this library fixes one reading:
+ *   tensor scale   s_enc = 2688 / amax_t (1 if amax_t = 0, clamped to FLT_MAX),
+ *                  s_dec = 1 / s_enc (the stored FP32 per-tensor scale);
+ *   block scale    S_b = e4m3_rne_satfinite((amax_b / 6) * s_enc);
+ *   element        y = x * RN(s_enc / S_b), E2M1 round-to-nearest-even (ties to
+ *                  the even code) or stochastic (round up iff r * 2^-16 < p,
+ *                  r = 16 Philox4x32-10 bits); the sign of x is kept (-0 -> 8);
+ *   RHT            y = (1/4) H16 diag(s) v per 16-chunk along the token axis,
+ *                  stages h = 1, 2, 4, 8, one sign vector s per call
+ *                  (bit j of word 0 of Philox(key = rht_seed, counter = 0));
+ *   SR bits        element i (row-major in the operand's logical [rows, cols])
+ *                  takes 16-bit half (i & 1) of word ((i >> 1) & 3) of
+ *                  Philox(key = sr_seed, counter = (i >> 3, stream, sr_offset)),
+ *                  stream 1 for column quantization, 0 otherwise.
+ *
+ * Conventions for every call below:
+ *   - pointers are DEVICE pointers unless stated; `stream` is a cudaStream_t;
+ *   - every call is asynchronous on `stream`, never allocates, never syncs
+ *     (except nvfp4_status_query);
+ *   - the caller owns every buffer;
+ *   - host-side argument errors return a status and launch nothing;
+ *   - device-side errors (a non-finite tensor, a pipeline wait that timed out)
+ *     are written to *dev_status (a uint32 the caller zeroes once) and read back
+ *     with nvfp4_status_query; after an error the outputs are unspecified.
+ */
+#ifndef NVFP4_GB300_H
+#define NVFP4_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define NVFP4_API __attribute__((visibility("default")))
+#else
+#define NVFP4_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    NVFP4_OK = 0,
+    NVFP4_ERR_INVALID_ARG = 1,   /* null pointer, bad enum, inconsistent operands */
+    NVFP4_ERR_SHAPE = 2,         /* a dimension breaks the block or tile rules */
+    NVFP4_ERR_ALIGNMENT = 3,     /* pointer or pitch not 16-byte aligned */
+    NVFP4_ERR_WORKSPACE = 4,     /* workspace missing or too small */
+    NVFP4_ERR_UNSUPPORTED = 5,   /* valid request this build does not implement */
+    NVFP4_ERR_CUDA = 6,          /* a CUDA runtime call failed (launch, no device) */
+    NVFP4_ERR_NONFINITE = 7,     /* device: the tensor amax was Inf or NaN */
+    NVFP4_ERR_TIMEOUT = 8        /* device: a bounded pipeline wait ran out */
+} nvfp4_status;
+
+typedef enum { NVFP4_F32 = 0, NVFP4_BF16 = 1 } nvfp4_dtype;
+typedef enum { NVFP4_ROUND_RNE = 0, NVFP4_ROUND_SR = 1 } nvfp4_round;
+typedef enum {
+    NVFP4_BLOCK_1X16_ROW = 0,    /* activations / Fprop & Dgrad gradients [page ¶2] */
+    NVFP4_BLOCK_1X16_COL = 1,    /* Wgrad operands: blocks along the token axis */
+    NVFP4_BLOCK_16X16 = 2        /* weights: 2D 16x16 tiles [page ¶2] */
+} nvfp4_block;
+
+/* Quantization parameters.  `rht` is only valid with NVFP4_BLOCK_1X16_COL. */
+typedef struct {
+    int32_t block;               /* nvfp4_block */
+    int32_t round;               /* nvfp4_round */
+    int32_t rht;                 /* 1: apply the 16x16 RHT (Wgrad inputs) */
+    uint32_t sr_offset;          /* Philox counter word 3 for SR */
+    uint64_t sr_seed;            /* Philox key for SR */
+    uint64_t rht_seed;           /* Philox key for the RHT sign vector */
+} nvfp4_qparams;
+
+/*
+ * A quantized operand of logical shape [rows, cols], 16-element blocks along cols.
+ *   codes        [rows, cols/2] bytes, row pitch cols/2: element 2j in the low
+ *                nibble of byte j, element 2j+1 in the high nibble.
+ *   scales       canonical E4M3 block scales, row-major: [rows, cols/16]; for
+ *                NVFP4_BLOCK_16X16 the tile grid [rows/16, cols/16].  May be NULL.
+ *   scales_mma   the same scales in the tensor-core tile layout the GEMM reads:
+ *                ceil(rows/128) x ceil(cols/256) tiles of 2048 bytes, tile
+ *                (rb, kb) at byte ((rb * ceil(cols/256)) + kb) * 2048; inside a
+ *                tile, the scale of row r, scale-column s (s = k/16) sits at
+ *                ((s/4)%4)*512 + (r%32)*16 + ((r%128)/32)*4 + s%4.  Padding rows
+ *                and scale-columns hold 0.  nvfp4_scales_mma_bytes() gives the
+ *                size.  May be NULL (then the operand cannot feed nvfp4_gemm).
+ *   s_dec        one float: the FP32 per-tensor decode scale.  Always written.
+ *   codes_t,     NVFP4_BLOCK_16X16 only (else ignored): the transposed operand
+ *   scales_mma_t [cols, rows/2] codes and its tile-layout scales, so that W and
+ *                W^T share one quantized representation [page ¶2].  NULL: skip.
+ * Dequantized value: e2m1(code) * e4m3(scale) * s_dec.
+ */
+typedef struct {
+    uint8_t* codes;
+    uint8_t* scales;
+    uint8_t* scales_mma;
+    float* s_dec;
+    uint8_t* codes_t;
+    uint8_t* scales_mma_t;
+    int64_t rows;
+    int64_t cols;
+} nvfp4_qtensor;
+
+/* Bytes of a tile-layout scale buffer for an operand of logical [rows, cols]. */
+NVFP4_API size_t nvfp4_scales_mma_bytes(int64_t rows, int64_t cols);
+
+/* Workspace bytes nvfp4_quantize needs (device memory, any contents, 16-byte
+   aligned): the per-CTA partial maxima of the tensor amax pass. */
+NVFP4_API size_t nvfp4_quantize_workspace_bytes(int64_t R, int64_t C, const nvfp4_qparams* params);
+
+/*
+ * nvfp4_quantize -- quantize x [R, C] (row pitch ldx elements, F32 or BF16).
+ *   1X16_ROW : operand x,   out->rows = R, out->cols = C; C % 16 == 0.
+ *   1X16_COL : operand x^T, out->rows = C, out->cols = R; R % 16 == 0, C % 16 == 0;
+ *              with params->rht the RHT runs along R before everything else.
+ *   16X16    : operand x,   out->rows = R, out->cols = C; R, C % 16 == 0.
+ * Two passes over x: the tensor amax (after the RHT where it applies) and the
+ * encode.  x, the output buffers and ldx*sizeof(elem) must be 16-byte aligned.
+ * R == 0 or C == 0 is valid: only s_dec (= 1) is written.
+ */
+NVFP4_API nvfp4_status nvfp4_quantize(const void* x, int32_t x_dtype, int64_t R, int64_t C, int64_t ldx,
+                            const nvfp4_qparams* params, const nvfp4_qtensor* out,
+                            void* workspace, size_t workspace_bytes, uint32_t* dev_status,
+                            void* stream);
+
+/*
+ * nvfp4_gemm -- D[M, N] = s_dec(A) * s_dec(B) * sum_k qA[m,k]*SA[m,k/16] * qB[n,k]*SB[n,k/16]
+ * on the tcgen05 block-scaled FP4 tensor cores (fp32 accumulation in TMEM).
+ *   A: [M, K] quantized along K (codes + scales_mma); B: [N, K] likewise.
+ *   D: F32 or BF16, row pitch ldd elements (ldd >= N).
+ * Rules: A->cols == B->cols == K, K % 32 == 0, M, N >= 1; codes 16-byte aligned.
+ * M and N need not be tile multiples (edges are masked).
+ */
+NVFP4_API nvfp4_status nvfp4_gemm(const nvfp4_qtensor* A, const nvfp4_qtensor* B, void* D, int32_t d_dtype,
+                        int64_t ldd, uint32_t* dev_status, void* stream);
+
+/* Workspace bytes for the three linear-layer calls below with these sizes. */
+NVFP4_API size_t nvfp4_linear_workspace_bytes(int64_t M, int64_t N, int64_t K);
+
+/*
+ * Fprop [page ¶2]: Y[M, N] = X[M, K] . W^T.  X (F32/BF16, pitch ldx) is
+ * quantized 1x16 along K with RNE; Wq is the 16X16-quantized weight ([N, K]).
+ */
+NVFP4_API nvfp4_status nvfp4_linear_fprop(const void* X, int32_t x_dtype, int64_t M, int64_t K, int64_t ldx,
+                                const nvfp4_qtensor* Wq, void* Y, int32_t y_dtype, int64_t ldy,
+                                void* workspace, size_t workspace_bytes, uint32_t* dev_status,
+                                void* stream);
+
+/*
+ * Dgrad [page ¶2]: dX[M, K] = dY[M, N] . W.  dY is quantized 1x16 along N with
+ * stochastic rounding (sr_seed, sr_offset); the weight operand is W^T from the
+ * same 16X16 quantization (Wq->codes_t and Wq->scales_mma_t must be set).
+ */
+NVFP4_API nvfp4_status nvfp4_linear_dgrad(const void* dY, int32_t dy_dtype, int64_t M, int64_t N, int64_t lddy,
+                                const nvfp4_qtensor* Wq, uint64_t sr_seed, uint32_t sr_offset,
+                                void* dX, int32_t dx_dtype, int64_t lddx,
+                                void* workspace, size_t workspace_bytes, uint32_t* dev_status,
+                                void* stream);
+
+/*
+ * Wgrad [page ¶2]: dW[N, K] = dY^T . X.  Both operands are quantized 1x16 along
+ * the token axis M after the 16x16 RHT with one shared sign vector (rht_seed);
+ * dY^T with stochastic rounding (sr_seed, sr_offset), X^T with RNE.  M % 16 == 0.
+ */
+NVFP4_API nvfp4_status nvfp4_linear_wgrad(const void* dY, int32_t dy_dtype, int64_t lddy,
+                                const void* X, int32_t x_dtype, int64_t ldx,
+                                int64_t M, int64_t N, int64_t K,
+                                uint64_t sr_seed, uint32_t sr_offset, uint64_t rht_seed,
+                                void* dW, int32_t dw_dtype, int64_t lddw,
+                                void* workspace, size_t workspace_bytes, uint32_t* dev_status,
+                                void* stream);
+
+/* Synchronises `stream`, reads *dev_status and returns it as a status. */
+NVFP4_API nvfp4_status nvfp4_status_query(const uint32_t* dev_status, void* stream);
+
+/* Static string for a status code. */
+NVFP4_API const char* nvfp4_status_string(int32_t status);
+
+/* Upper bound, in nanoseconds, of every bounded pipeline wait in the GEMM
+   (default 2e9).  Process-wide; for tests that exercise the timeout path. */
+NVFP4_API void nvfp4_set_wait_timeout_ns(uint64_t ns);
+
+/*
+ * Diagnostics (not on the hot path).  They run the exact device routines the
+ * kernels use, so tests can pin them element by element.
+ *   nvfp4_debug_e4m3: out[i] = block-scale cast of v[i] (RNE, saturating).
+ *   nvfp4_debug_e2m1: out[i] = E2M1 code of y[i]; round = RNE or SR (with the
+ *                     16-bit r16[i]); hw = 1 uses the tensor-core format
+ *                     conversion instruction instead of the software rule.
+ *   nvfp4_debug_philox: out[4*i..] = Philox4x32-10(ctr[4*i..], key) words.
+ *   nvfp4_selftest_wait_timeout: one CTA waits on an mbarrier nobody arrives
+ *                     at, bounded by timeout_ns; sets *dev_status to
+ *                     NVFP4_ERR_TIMEOUT and returns normally.
+ */
+NVFP4_API nvfp4_status nvfp4_debug_e4m3(const float* v, int64_t n, uint8_t* out, void* stream);
+NVFP4_API nvfp4_status nvfp4_debug_e2m1(const float* y, const uint32_t* r16, int64_t n, int32_t round, int32_t hw,
+                              uint8_t* out, void* stream);
+NVFP4_API nvfp4_status nvfp4_debug_philox(const uint32_t* ctr, int64_t n, uint64_t key, uint32_t* out, void* stream);
+NVFP4_API nvfp4_status nvfp4_selftest_wait_timeout(uint64_t timeout_ns, uint32_t* dev_status, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* NVFP4_GB300_H */

@@ -1,0 +1,211 @@
+"""Torch-facing wrappers of the C ABI (include/nvfp4.h): argument marshalling only.
+
+Every function takes CUDA tensors, allocates outputs with torch, and launches
+the library's kernels on ``torch.cuda.current_stream()``.  Host-side argument
+errors raise :class:`NVFP4Error` before anything is launched; device-side errors
+(a non-finite tensor, a timed-out pipeline wait) land in the per-device status
+word read by :func:`status_query`.
+"""
+from __future__ import annotations
+
+import ctypes
+from dataclasses import dataclass
+from typing import Optional
+
+import torch
+
+from . import _lib as L
+from ._lib import NVFP4Error
+
+_DT = {torch.float32: L.F32, torch.bfloat16: L.BF16}
+
+
+def _ptr(t: Optional[torch.Tensor]) -> Optional[int]:
+    return None if t is None else t.data_ptr()
+
+
+def _stream() -> int:
+    return torch.cuda.current_stream().cuda_stream
+
+
+def _check_2d(x: torch.Tensor, name: str) -> None:
+    if not x.is_cuda:
+        raise NVFP4Error(L.ERR_INVALID_ARG, f"{name} must be a CUDA tensor")
+    if x.dim() != 2 or (x.shape[1] > 1 and x.stride(1) != 1):
+        raise NVFP4Error(L.ERR_INVALID_ARG, f"{name} must be 2-D with unit column stride")
+    if x.dtype not in _DT:
+        raise NVFP4Error(L.ERR_INVALID_ARG, f"{name} must be float32 or bfloat16")
+
+
+# ----------------------------------------------------------------------------- status
+
+_status: dict = {}
+
+
+def dev_status(device=None) -> torch.Tensor:
+    """The device status word (uint32 stored in an int32 tensor) for ``device``."""
+    dev = torch.device("cuda", torch.cuda.current_device() if device is None else torch.device(device).index)
+    t = _status.get(dev.index)
+    if t is None:
+        t = torch.zeros(4, dtype=torch.int32, device=dev)
+        _status[dev.index] = t
+    return t
+
+
+def reset_status(device=None) -> None:
+    dev_status(device).zero_()
+
+
+def status_query(device=None) -> int:
+    """Synchronises the current stream and returns the device status (0 = ok)."""
+    return int(L.lib().nvfp4_status_query(dev_status(device).data_ptr(), _stream()))
+
+
+# ----------------------------------------------------------------------------- workspace
+
+_ws: dict = {}
+
+
+def _workspace(nbytes: int) -> torch.Tensor:
+    key = (torch.cuda.current_device(), _stream())
+    t = _ws.get(key)
+    if t is None or t.numel() < nbytes:
+        t = torch.empty(max(nbytes, 1 << 16), dtype=torch.uint8, device="cuda")
+        _ws[key] = t
+    return t
+
+
+def scales_mma_bytes(rows: int, cols: int) -> int:
+    return int(L.lib().nvfp4_scales_mma_bytes(rows, cols))
+
+
+# ----------------------------------------------------------------------------- quantized operand
+
+@dataclass
+class QTensor:
+    """A quantized operand of logical shape [rows, cols] (16-element blocks along cols)."""
+    codes: torch.Tensor                       # uint8 [rows, cols/2]
+    scales: Optional[torch.Tensor]            # uint8 [rows, cols/16] (TILE16: [rows/16, cols/16])
+    scales_mma: Optional[torch.Tensor]        # uint8, tensor-core tile layout
+    s_dec: torch.Tensor                       # float32 [4]; element 0 is the tensor decode scale
+    rows: int
+    cols: int
+    block: int
+    codes_t: Optional[torch.Tensor] = None    # TILE16 only: codes of the transpose
+    scales_mma_t: Optional[torch.Tensor] = None
+
+    def c_struct(self) -> L.QTensorC:
+        return L.QTensorC(_ptr(self.codes), _ptr(self.scales), _ptr(self.scales_mma), _ptr(self.s_dec),
+                          _ptr(self.codes_t), _ptr(self.scales_mma_t), self.rows, self.cols)
+
+    def transposed(self) -> "QTensor":
+        """W^T as an operand (TILE16 quantization with the transposed copy)."""
+        if self.codes_t is None or self.scales_mma_t is None:
+            raise NVFP4Error(L.ERR_INVALID_ARG, "no transposed copy was written")
+        return QTensor(self.codes_t, None, self.scales_mma_t, self.s_dec, self.cols, self.rows, self.block)
+
+
+def quantize(x: torch.Tensor, block: int = L.ROW, round: int = L.RNE, rht: bool = False,
+             sr_seed: int = 0, sr_offset: int = 0, rht_seed: int = 0, scales: bool = True,
+             scales_mma: bool = True, transpose: bool = True) -> QTensor:
+    """Quantize x [R, C] (float32 / bfloat16, CUDA) to NVFP4 with the library's kernels."""
+    _check_2d(x, "x")
+    R, C = x.shape
+    rows, cols = (C, R) if block == L.COL else (R, C)
+    dev = x.device
+    codes = torch.empty((rows, cols // 2), dtype=torch.uint8, device=dev)
+    sc = None
+    if scales:
+        shape = (rows // 16, cols // 16) if block == L.TILE16 else (rows, cols // 16)
+        sc = torch.empty(shape, dtype=torch.uint8, device=dev)
+    smma = torch.empty(max(scales_mma_bytes(rows, cols), 16), dtype=torch.uint8, device=dev) if scales_mma else None
+    s_dec = torch.empty(4, dtype=torch.float32, device=dev)
+    codes_t = smma_t = None
+    if block == L.TILE16 and transpose:
+        codes_t = torch.empty((cols, rows // 2), dtype=torch.uint8, device=dev)
+        smma_t = torch.empty(max(scales_mma_bytes(cols, rows), 16), dtype=torch.uint8, device=dev)
+    q = QTensor(codes, sc, smma, s_dec, rows, cols, block, codes_t, smma_t)
+    params = L.QParams(block, round, int(bool(rht)), sr_offset & 0xFFFFFFFF, sr_seed & (2**64 - 1),
+                       rht_seed & (2**64 - 1))
+    qc = q.c_struct()
+    lib = L.lib()
+    ws_bytes = int(lib.nvfp4_quantize_workspace_bytes(R, C, ctypes.byref(params)))
+    ws = _workspace(ws_bytes)
+    ld = x.stride(0) if R > 1 else max(C, 1)
+    st = lib.nvfp4_quantize(_ptr(x), _DT[x.dtype], R, C, ld, ctypes.byref(params), ctypes.byref(qc),
+                            ws.data_ptr(), ws.numel(), dev_status(dev).data_ptr(), _stream())
+    L.check(st, "nvfp4_quantize")
+    return q
+
+
+def quantize_weight(W: torch.Tensor) -> QTensor:
+    """Weights: 16x16 2D blocks, RNE, with the transposed copy for Dgrad [page ¶2]."""
+    return quantize(W, L.TILE16, L.RNE, transpose=True)
+
+
+def gemm(A: QTensor, B: QTensor, out_dtype=torch.bfloat16, out: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """D[M, N] = dequant(A) . dequant(B)^T on the tcgen05 block-scaled FP4 tensor cores."""
+    M, N = A.rows, B.rows
+    if out is None:
+        out = torch.empty((M, N), dtype=out_dtype, device=A.codes.device)
+    _check_2d(out, "out")
+    a, b = A.c_struct(), B.c_struct()
+    st = L.lib().nvfp4_gemm(ctypes.byref(a), ctypes.byref(b), _ptr(out), _DT[out.dtype], out.stride(0),
+                            dev_status(out.device).data_ptr(), _stream())
+    L.check(st, "nvfp4_gemm")
+    return out
+
+
+def _linear_ws(M: int, N: int, K: int) -> torch.Tensor:
+    return _workspace(int(L.lib().nvfp4_linear_workspace_bytes(M, N, K)))
+
+
+def linear_fprop(X: torch.Tensor, Wq: QTensor, out_dtype=torch.bfloat16) -> torch.Tensor:
+    """Y[M, N] = X . W^T; X quantized 1x16 RNE inside the call."""
+    _check_2d(X, "X")
+    M, K = X.shape
+    N = Wq.rows
+    Y = torch.empty((M, N), dtype=out_dtype, device=X.device)
+    ws = _linear_ws(M, N, K)
+    w = Wq.c_struct()
+    st = L.lib().nvfp4_linear_fprop(_ptr(X), _DT[X.dtype], M, K, X.stride(0), ctypes.byref(w), _ptr(Y),
+                                    _DT[out_dtype], Y.stride(0), ws.data_ptr(), ws.numel(),
+                                    dev_status(X.device).data_ptr(), _stream())
+    L.check(st, "nvfp4_linear_fprop")
+    return Y
+
+
+def linear_dgrad(dY: torch.Tensor, Wq: QTensor, sr_seed: int = 0, sr_offset: int = 0,
+                 out_dtype=torch.bfloat16) -> torch.Tensor:
+    """dX[M, K] = dY . W; dY quantized 1x16 with stochastic rounding inside the call."""
+    _check_2d(dY, "dY")
+    M, N = dY.shape
+    K = Wq.cols
+    dX = torch.empty((M, K), dtype=out_dtype, device=dY.device)
+    ws = _linear_ws(M, N, K)
+    w = Wq.c_struct()
+    st = L.lib().nvfp4_linear_dgrad(_ptr(dY), _DT[dY.dtype], M, N, dY.stride(0), ctypes.byref(w),
+                                    sr_seed & (2**64 - 1), sr_offset & 0xFFFFFFFF, _ptr(dX), _DT[out_dtype],
+                                    dX.stride(0), ws.data_ptr(), ws.numel(), dev_status(dY.device).data_ptr(),
+                                    _stream())
+    L.check(st, "nvfp4_linear_dgrad")
+    return dX
+
+
+def linear_wgrad(dY: torch.Tensor, X: torch.Tensor, sr_seed: int = 0, sr_offset: int = 0, rht_seed: int = 0,
+                 out_dtype=torch.bfloat16) -> torch.Tensor:
+    """dW[N, K] = dY^T . X; both quantized 1x16 along M after the shared-sign RHT."""
+    _check_2d(dY, "dY")
+    _check_2d(X, "X")
+    M, N = dY.shape
+    K = X.shape[1]
+    if X.shape[0] != M:
+        raise NVFP4Error(L.ERR_SHAPE, "dY and X disagree on M")
+    dW = torch.empty((N, K), dtype=out_dtype, device=dY.device)
+    ws = _linear_ws(M, N, K)
+    st = L.lib().nvfp4_linear_wgrad(_ptr(dY), _DT[dY.dtype], dY.stride(0), _ptr(X), _DT[X.dtype], X.stride(0),
+                                    M, N, K, sr_seed & (2**64 - 1), sr_offset & 0xFFFFFFFF, rht_seed & (2**64 - 1),
+                                    _ptr(dW), _DT[out_dtype], dW.stride(0), ws.data_ptr(), ws.numel(),
+                                    dev_status(dY.device).data_ptr(), _stream())
+    L.check(st, "nvfp4_linear_wgrad")
+    return dW

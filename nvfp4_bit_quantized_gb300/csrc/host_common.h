@@ -1,0 +1,27 @@
+// host_common.h -- host-side helpers shared by the C-ABI translation units.
+#pragma once
+
+#include <algorithm>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "../../include/nvfp4.h"
+
+namespace nvfp4 {
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Multiprocessor count of `dev`, cached (152 on GB300).
+int sm_count(int dev);
+
+// Process-wide bound of the GEMM's pipeline waits, in ns.
+uint64_t wait_timeout_ns();
+
+nvfp4_status quantize_impl(const void* x, int32_t x_dtype, int64_t R, int64_t C, int64_t ldx,
+                           const nvfp4_qparams* p, const nvfp4_qtensor* out, void* ws, size_t ws_bytes,
+                           uint32_t* dev_status, cudaStream_t stream);
+
+nvfp4_status gemm_impl(const nvfp4_qtensor* A, const nvfp4_qtensor* B, void* D, int32_t d_dtype, int64_t ldd,
+                       uint32_t* dev_status, cudaStream_t stream);
+
+}  // namespace nvfp4

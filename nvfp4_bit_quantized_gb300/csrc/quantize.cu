@@ -1,0 +1,510 @@
+// quantize.cu -- NVFP4 quantizers for sm_103a (HBM-bound, two passes).
+//
+// Pass 1 (amax): per-CTA partial maxima of |x| (of |RHT(x)| for the Wgrad
+// operands), written to the workspace; no atomics, no memset.
+// Pass 2 (encode): every CTA reduces the partials to the tensor amax (an
+// order-free max, so every CTA gets the same value), derives s_enc, then
+// encodes its blocks: block amax -> E4M3 scale -> E2M1 codes -> packed nibbles,
+// canonical and tensor-core-layout scales.
+//
+// Method: news page "NVIDIA NVFP4 paper: 4-bit pretrain hits FP8 parity (12B,
+// 10T tokens)", ¶2 (format, 2D weight blocks, RHT on Wgrad inputs, SR on
+// gradients only).  Readings of what the page leaves open: include/nvfp4.h.
+//
+// Thread mappings (16-byte chunks = 8 bf16 or 4 fp32 values, VEC below):
+//   row kernel  : a warp reads 32 consecutive chunks of one row (512 B, fully
+//                 coalesced); a 16-element block spans 16/VEC lanes.
+//   col / 16x16 : a thread owns a 16-row x VEC-column patch; lane = 8*rg + cc
+//                 (rg: 4 row groups of 16, cc: 8 column chunks), so one warp
+//                 covers 64 rows x 8*VEC columns; every load instruction reads
+//                 4 full 128-byte lines, every transposed store writes full
+//                 32-byte sectors (4 lanes x 8 bytes per output row).
+#include <cuda_runtime.h>
+#include <cstdint>
+#include <cstdio>
+
+#include "device_common.cuh"
+#include "host_common.h"
+
+namespace nvfp4 {
+
+constexpr int kThreads = 256;
+constexpr int kMaxPartials = 4096;
+
+// Byte offset of (row r, scale-column s) in the tensor-core scale layout.
+__device__ __forceinline__ size_t mma_sf_offset(int64_t r, int64_t s, int64_t nkb) {
+    return ((size_t)((r >> 7) * nkb + (s >> 4)) << 11) + (size_t)(((s >> 2) & 3) << 9) +
+           (size_t)((r & 31) << 4) + (size_t)(((r >> 5) & 3) << 2) + (size_t)(s & 3);
+}
+
+// ---------------------------------------------------------------------------
+// Pass 1: amax
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t abs_bits_max(uint4 v, const uint16_t*) {
+    uint32_t m = __vmaxu2(__vmaxu2(v.x & 0x7FFF7FFFu, v.y & 0x7FFF7FFFu),
+                          __vmaxu2(v.z & 0x7FFF7FFFu, v.w & 0x7FFF7FFFu));
+    return max(m >> 16, m & 0xFFFFu) << 16;           // bf16 |x| as fp32 bits
+}
+__device__ __forceinline__ uint32_t abs_bits_max(uint4 v, const float*) {
+    return max(max(v.x & 0x7FFFFFFFu, v.y & 0x7FFFFFFFu), max(v.z & 0x7FFFFFFFu, v.w & 0x7FFFFFFFu));
+}
+
+__device__ __forceinline__ void block_max_store(uint32_t m, uint32_t* partials) {
+    __shared__ uint32_t red[kThreads / 32];
+    m = __reduce_max_sync(0xFFFFFFFFu, m);
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
+    __syncthreads();
+    if (threadIdx.x < 32) {
+        uint32_t v = threadIdx.x < (kThreads / 32) ? red[threadIdx.x] : 0u;
+        v = __reduce_max_sync(0xFFFFFFFFu, v);
+        if (threadIdx.x == 0) partials[blockIdx.x] = v;
+    }
+}
+
+// |x| max, unsigned compare of the magnitude bits (NaN sorts above Inf).
+template <typename T>
+__global__ void __launch_bounds__(kThreads) amax_kernel(const T* __restrict__ x, int64_t R, int64_t C,
+                                                        int64_t ldx, uint32_t* __restrict__ partials) {
+    constexpr int VEC = Vec<T>::N;
+    const int lane = threadIdx.x & 31;
+    const int64_t cpr = C / VEC;
+    const int64_t spr = (cpr + 31) / 32;
+    const int64_t nseg = R * spr;
+    const int64_t warp0 = (int64_t)blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5);
+    const int64_t nwarps = (int64_t)gridDim.x * (kThreads / 32);
+    uint32_t m = 0;
+    constexpr int U = 4;
+    for (int64_t base = warp0; base < nseg; base += nwarps * U) {
+        uint4 v[U];
+        bool ok[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int64_t seg = base + (int64_t)u * nwarps;
+            ok[u] = false;
+            if (seg < nseg) {
+                const int64_t r = seg / spr;
+                const int64_t ch = (seg - r * spr) * 32 + lane;
+                if (ch < cpr) {
+                    v[u] = ld_stream(x + r * ldx + ch * VEC);
+                    ok[u] = true;
+                }
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+            if (ok[u]) m = max(m, abs_bits_max(v[u], (const T*)nullptr));
+    }
+    block_max_store(m, partials);
+}
+
+// Loads the 16-row x VEC-column patch at (r0, c0) into t[col][row] as fp32.
+template <typename T>
+__device__ __forceinline__ void load_patch(const T* __restrict__ x, int64_t ldx, int64_t r0, int64_t c0,
+                                           float (&t)[Vec<T>::N][16]) {
+    constexpr int VEC = Vec<T>::N;
+    uint4 v[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = ld_stream(x + (r0 + i) * ldx + c0);
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        float f[VEC];
+        Vec<T>::unpack(v[i], f);
+#pragma unroll
+        for (int j = 0; j < VEC; ++j) t[j][i] = f[j];
+    }
+}
+
+// amax of RHT(x) along rows: the Wgrad operands' tensor amax after the transform.
+template <typename T>
+__global__ void __launch_bounds__(kThreads) amax_rht_kernel(const T* __restrict__ x, int64_t R, int64_t C,
+                                                            int64_t ldx, uint64_t rht_seed,
+                                                            uint32_t* __restrict__ partials) {
+    constexpr int VEC = Vec<T>::N;
+    const int lane = threadIdx.x & 31, rg = lane >> 3, cc = lane & 7;
+    const int64_t tiles_c = (C + 8 * VEC - 1) / (8 * VEC);
+    const int64_t tiles = ((R + 63) / 64) * tiles_c;
+    const int64_t warp0 = (int64_t)blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5);
+    const int64_t nwarps = (int64_t)gridDim.x * (kThreads / 32);
+    const uint32_t sign_mask = rht_sign_mask(rht_seed);
+    float m = 0.0f;
+    bool bad = false;                                // NaN: fmaxf would drop it
+    for (int64_t tile = warp0; tile < tiles; tile += nwarps) {
+        const int64_t r0 = (tile / tiles_c) * 64 + rg * 16;
+        const int64_t c0 = (tile % tiles_c) * (8 * VEC) + cc * VEC;
+        if (r0 >= R || c0 >= C) continue;
+        float t[VEC][16];
+        load_patch<T>(x, ldx, r0, c0, t);
+#pragma unroll
+        for (int j = 0; j < VEC; ++j) {
+            rht16(t[j], sign_mask);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                const float a = fabsf(t[j][i]);
+                m = fmaxf(m, a);
+                bad |= !(a <= FLT_MAX);
+            }
+        }
+    }
+    block_max_store(bad ? 0x7FC00000u : __float_as_uint(m), partials);
+}
+
+// ---------------------------------------------------------------------------
+// Pass 2 prologue: reduce the partials to s_enc (same value in every CTA).
+// ---------------------------------------------------------------------------
+struct Scales { float s_enc; bool finite; };
+
+__device__ __forceinline__ Scales tensor_scales(const uint32_t* __restrict__ partials, int nparts,
+                                                float* s_dec_out, uint32_t* dev_status) {
+    __shared__ uint32_t red[kThreads / 32];
+    __shared__ uint32_t total;
+    uint32_t m = 0;
+    for (int i = threadIdx.x; i < nparts; i += blockDim.x) m = max(m, partials[i]);
+    m = __reduce_max_sync(0xFFFFFFFFu, m);
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
+    __syncthreads();
+    if (threadIdx.x < 32) {
+        uint32_t v = threadIdx.x < (blockDim.x / 32) ? red[threadIdx.x] : 0u;
+        v = __reduce_max_sync(0xFFFFFFFFu, v);
+        if (threadIdx.x == 0) total = v;
+    }
+    __syncthreads();
+    const uint32_t bits = total;
+    Scales s;
+    s.finite = bits < 0x7F800000u;
+    const float amax_t = s.finite ? __uint_as_float(bits) : 0.0f;
+    s.s_enc = tensor_s_enc(amax_t);
+    if (blockIdx.x == 0 && threadIdx.x == 0) {
+        *s_dec_out = __fdiv_rn(1.0f, s.s_enc);
+        if (!s.finite) set_status(dev_status, NVFP4_ERR_NONFINITE);
+    }
+    return s;
+}
+
+struct QOut {
+    uint8_t* codes;
+    uint8_t* scales;
+    uint8_t* scales_mma;
+    uint8_t* codes_t;
+    uint8_t* scales_mma_t;
+    float* s_dec;
+};
+
+// ---------------------------------------------------------------------------
+// Pass 2, 1x16 blocks along rows.
+// ---------------------------------------------------------------------------
+template <typename T, bool SR>
+__global__ void __launch_bounds__(kThreads) encode_row_kernel(const T* __restrict__ x, int64_t R, int64_t C,
+                                                              int64_t ldx, const uint32_t* __restrict__ partials,
+                                                              int nparts, QOut out, uint64_t sr_seed,
+                                                              uint32_t sr_offset, uint32_t* dev_status) {
+    constexpr int VEC = Vec<T>::N;
+    constexpr int LPB = 16 / VEC;                    // lanes per 16-element block
+    const Scales sc = tensor_scales(partials, nparts, out.s_dec, dev_status);
+    const int lane = threadIdx.x & 31;
+    const int64_t cpr = C / VEC;
+    const int64_t spr = (cpr + 31) / 32;
+    const int64_t nseg = R * spr;
+    const int64_t nkb = (C + 255) / 256;
+    const int64_t warp0 = (int64_t)blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5);
+    const int64_t nwarps = (int64_t)gridDim.x * (kThreads / 32);
+    for (int64_t seg = warp0; seg < nseg; seg += nwarps) {
+        const int64_t r = seg / spr;
+        const int64_t ch = (seg - r * spr) * 32 + lane;
+        const bool valid = ch < cpr;
+        float f[VEC];
+        float amax = 0.0f;
+        if (valid) {
+            const uint4 v = ld_stream(x + r * ldx + ch * VEC);
+            Vec<T>::unpack(v, f);
+#pragma unroll
+            for (int j = 0; j < VEC; ++j) amax = fmaxf(amax, fabsf(f[j]));
+        }
+#pragma unroll
+        for (int o = 1; o < LPB; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
+        const uint32_t sb = valid ? block_scale_code(amax, sc.s_enc) : 0u;
+        const float e_b = block_multiplier(sb, sc.s_enc);
+        const int64_t col = ch * VEC;                // first element of this lane
+        if (valid) {
+            uint32_t packed = 0;
+            if constexpr (SR) {
+                // idx0 % 8 is 0 for bf16 (8-element chunks) and 0 or 4 for fp32
+                const uint64_t idx0 = (uint64_t)(r * C + col);
+                const Philox4 p = sr_philox(sr_seed, 0u, sr_offset, idx0 >> 3);
+                const bool upper = (VEC == 4) && (idx0 & 4);
+#pragma unroll
+                for (int j = 0; j < VEC; ++j)
+                    packed |= e2m1_sr_sw(__fmul_rn(f[j], e_b), upper ? sr_r16(p, 4 + j) : sr_r16(p, j)) << (4 * j);
+            } else {
+#pragma unroll
+                for (int j = 0; j < VEC; ++j) packed |= e2m1_rne_sw(__fmul_rn(f[j], e_b)) << (4 * j);
+            }
+            uint8_t* dst = out.codes + r * (C / 2) + col / 2;
+            if constexpr (VEC == 8) *reinterpret_cast<uint32_t*>(dst) = packed;
+            else *reinterpret_cast<uint16_t*>(dst) = (uint16_t)packed;
+            if ((lane % LPB) == 0) {
+                const int64_t s = col / 16;
+                if (out.scales) out.scales[r * (C / 16) + s] = (uint8_t)sb;
+                if (out.scales_mma) out.scales_mma[mma_sf_offset(r, s, nkb)] = (uint8_t)sb;
+            }
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Pass 2, 1x16 blocks along columns (operand x^T), optional RHT along rows.
+// ---------------------------------------------------------------------------
+template <typename T, bool SR, bool RHT>
+__global__ void __launch_bounds__(kThreads) encode_col_kernel(const T* __restrict__ x, int64_t R, int64_t C,
+                                                              int64_t ldx, const uint32_t* __restrict__ partials,
+                                                              int nparts, QOut out, uint64_t sr_seed,
+                                                              uint32_t sr_offset, uint64_t rht_seed,
+                                                              uint32_t* dev_status) {
+    constexpr int VEC = Vec<T>::N;
+    const uint32_t sign_mask = RHT ? rht_sign_mask(rht_seed) : 0u;
+    const Scales sc = tensor_scales(partials, nparts, out.s_dec, dev_status);
+    const int lane = threadIdx.x & 31, rg = lane >> 3, cc = lane & 7;
+    const int64_t tiles_c = (C + 8 * VEC - 1) / (8 * VEC);
+    const int64_t tiles = ((R + 63) / 64) * tiles_c;
+    const int64_t nkb = (R + 255) / 256;             // operand cols = R
+    const int64_t warp0 = (int64_t)blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5);
+    const int64_t nwarps = (int64_t)gridDim.x * (kThreads / 32);
+    for (int64_t tile = warp0; tile < tiles; tile += nwarps) {
+        const int64_t r0 = (tile / tiles_c) * 64 + rg * 16;
+        const int64_t c0 = (tile % tiles_c) * (8 * VEC) + cc * VEC;
+        if (r0 >= R || c0 >= C) continue;
+        float t[VEC][16];
+        load_patch<T>(x, ldx, r0, c0, t);
+#pragma unroll
+        for (int j = 0; j < VEC; ++j) {
+            if constexpr (RHT) rht16(t[j], sign_mask);
+            float amax = 0.0f;
+#pragma unroll
+            for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(t[j][i]));
+            const uint32_t sb = block_scale_code(amax, sc.s_enc);
+            const float e_b = block_multiplier(sb, sc.s_enc);
+            const int64_t c = c0 + j;                // operand row
+            uint32_t lo = 0, hi = 0;
+            if constexpr (SR) {
+                const uint64_t idx0 = (uint64_t)(c * R + r0);
+                const Philox4 p0 = sr_philox(sr_seed, 1u, sr_offset, idx0 >> 3);
+                const Philox4 p1 = sr_philox(sr_seed, 1u, sr_offset, (idx0 >> 3) + 1);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) lo |= e2m1_sr_sw(__fmul_rn(t[j][i], e_b), sr_r16(p0, i)) << (4 * i);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) hi |= e2m1_sr_sw(__fmul_rn(t[j][8 + i], e_b), sr_r16(p1, i)) << (4 * i);
+            } else {
+#pragma unroll
+                for (int i = 0; i < 8; ++i) lo |= e2m1_rne_sw(__fmul_rn(t[j][i], e_b)) << (4 * i);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) hi |= e2m1_rne_sw(__fmul_rn(t[j][8 + i], e_b)) << (4 * i);
+            }
+            *reinterpret_cast<uint2*>(out.codes + c * (R / 2) + r0 / 2) = make_uint2(lo, hi);
+            const int64_t s = r0 / 16;
+            if (out.scales) out.scales[c * (R / 16) + s] = (uint8_t)sb;
+            if (out.scales_mma) out.scales_mma[mma_sf_offset(c, s, nkb)] = (uint8_t)sb;
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Pass 2, 16x16 tiles (weights): writes W and W^T codes from one tile scale.
+// ---------------------------------------------------------------------------
+template <typename T, bool SR>
+__global__ void __launch_bounds__(kThreads) encode_2d_kernel(const T* __restrict__ x, int64_t R, int64_t C,
+                                                             int64_t ldx, const uint32_t* __restrict__ partials,
+                                                             int nparts, QOut out, uint64_t sr_seed,
+                                                             uint32_t sr_offset, uint32_t* dev_status) {
+    constexpr int VEC = Vec<T>::N;
+    constexpr int LPT = 16 / VEC;                    // lanes per 16-column tile
+    const Scales sc = tensor_scales(partials, nparts, out.s_dec, dev_status);
+    const int lane = threadIdx.x & 31, rg = lane >> 3, cc = lane & 7;
+    const int64_t tiles_c = (C + 8 * VEC - 1) / (8 * VEC);
+    const int64_t tiles = ((R + 63) / 64) * tiles_c;
+    const int64_t nkb = (C + 255) / 256, nkb_t = (R + 255) / 256;
+    const int64_t warp0 = (int64_t)blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5);
+    const int64_t nwarps = (int64_t)gridDim.x * (kThreads / 32);
+    for (int64_t tile = warp0; tile < tiles; tile += nwarps) {
+        const int64_t r0 = (tile / tiles_c) * 64 + rg * 16;
+        const int64_t c0 = (tile % tiles_c) * (8 * VEC) + cc * VEC;
+        // every lane takes part in the shuffles; invalid ones contribute 0
+        const bool valid = (r0 < R) && (c0 < C);
+        float t[VEC][16];
+        float amax = 0.0f;
+        if (valid) {
+            load_patch<T>(x, ldx, r0, c0, t);
+#pragma unroll
+            for (int j = 0; j < VEC; ++j)
+#pragma unroll
+                for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(t[j][i]));
+        }
+#pragma unroll
+        for (int o = 1; o < LPT; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
+        if (!valid) continue;
+        const uint32_t sb = block_scale_code(amax, sc.s_enc);
+        const float e_b = block_multiplier(sb, sc.s_enc);
+        // Encode row by row: W codes go out per row, W^T codes are packed per column.
+        uint32_t lo_t[VEC], hi_t[VEC];
+#pragma unroll
+        for (int j = 0; j < VEC; ++j) { lo_t[j] = 0; hi_t[j] = 0; }
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            uint32_t packed = 0;
+            if constexpr (SR) {
+                const uint64_t idx0 = (uint64_t)((r0 + i) * C + c0);
+                const Philox4 p = sr_philox(sr_seed, 0u, sr_offset, idx0 >> 3);
+                const bool upper = (VEC == 4) && (idx0 & 4);
+#pragma unroll
+                for (int j = 0; j < VEC; ++j) {
+                    const uint32_t cd = e2m1_sr_sw(__fmul_rn(t[j][i], e_b), upper ? sr_r16(p, 4 + j) : sr_r16(p, j));
+                    packed |= cd << (4 * j);
+                    if (i < 8) lo_t[j] |= cd << (4 * i); else hi_t[j] |= cd << (4 * (i - 8));
+                }
+            } else {
+#pragma unroll
+                for (int j = 0; j < VEC; ++j) {
+                    const uint32_t cd = e2m1_rne_sw(__fmul_rn(t[j][i], e_b));
+                    packed |= cd << (4 * j);
+                    if (i < 8) lo_t[j] |= cd << (4 * i); else hi_t[j] |= cd << (4 * (i - 8));
+                }
+            }
+            uint8_t* dst = out.codes + (r0 + i) * (C / 2) + c0 / 2;
+            if constexpr (VEC == 8) *reinterpret_cast<uint32_t*>(dst) = packed;
+            else *reinterpret_cast<uint16_t*>(dst) = (uint16_t)packed;
+        }
+        if (out.codes_t) {
+#pragma unroll
+            for (int j = 0; j < VEC; ++j)
+                *reinterpret_cast<uint2*>(out.codes_t + (c0 + j) * (R / 2) + r0 / 2) = make_uint2(lo_t[j], hi_t[j]);
+        }
+        if ((cc % LPT) == 0) {
+            const int64_t s = c0 / 16, st = r0 / 16;
+            if (out.scales) out.scales[st * (C / 16) + s] = (uint8_t)sb;
+            if (out.scales_mma)
+                for (int i = 0; i < 16; ++i) out.scales_mma[mma_sf_offset(r0 + i, s, nkb)] = (uint8_t)sb;
+            if (out.scales_mma_t)
+                for (int j = 0; j < 16; ++j) out.scales_mma_t[mma_sf_offset(c0 + j, st, nkb_t)] = (uint8_t)sb;
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Host side
+// ---------------------------------------------------------------------------
+}  // namespace nvfp4
+
+using namespace nvfp4;
+
+extern "C" size_t nvfp4_scales_mma_bytes(int64_t rows, int64_t cols) {
+    if (rows <= 0 || cols <= 0) return 0;
+    return (size_t)((rows + 127) / 128) * (size_t)((cols + 255) / 256) * 2048u;
+}
+
+extern "C" size_t nvfp4_quantize_workspace_bytes(int64_t, int64_t, const nvfp4_qparams*) {
+    return (size_t)kMaxPartials * sizeof(uint32_t);
+}
+
+namespace nvfp4 {
+
+nvfp4_status quantize_impl(const void* x, int32_t x_dtype, int64_t R, int64_t C, int64_t ldx,
+                           const nvfp4_qparams* p, const nvfp4_qtensor* out, void* ws, size_t ws_bytes,
+                           uint32_t* dev_status, cudaStream_t stream) {
+    if (!p || !out || !out->s_dec) return NVFP4_ERR_INVALID_ARG;
+    if (x_dtype != NVFP4_F32 && x_dtype != NVFP4_BF16) return NVFP4_ERR_INVALID_ARG;
+    if (p->block < NVFP4_BLOCK_1X16_ROW || p->block > NVFP4_BLOCK_16X16) return NVFP4_ERR_INVALID_ARG;
+    if (p->round != NVFP4_ROUND_RNE && p->round != NVFP4_ROUND_SR) return NVFP4_ERR_INVALID_ARG;
+    if (p->rht && p->block != NVFP4_BLOCK_1X16_COL) return NVFP4_ERR_INVALID_ARG;
+    if (R < 0 || C < 0 || ldx < C) return NVFP4_ERR_SHAPE;
+    const bool col = p->block == NVFP4_BLOCK_1X16_COL;
+    const int64_t rows = col ? C : R, cols = col ? R : C;
+    if (out->rows != rows || out->cols != cols) return NVFP4_ERR_SHAPE;
+    if (C % 16 != 0) return NVFP4_ERR_SHAPE;
+    if ((col || p->block == NVFP4_BLOCK_16X16) && R % 16 != 0) return NVFP4_ERR_SHAPE;
+    const size_t esz = x_dtype == NVFP4_BF16 ? 2 : 4;
+    const bool empty = (R == 0 || C == 0);
+    if (!empty) {
+        if (!x || !out->codes) return NVFP4_ERR_INVALID_ARG;
+        if (!out->scales && !out->scales_mma) return NVFP4_ERR_INVALID_ARG;
+        if (!aligned16(x) || ((size_t)ldx * esz) % 16 != 0 || !aligned16(out->codes)) return NVFP4_ERR_ALIGNMENT;
+        if (p->block == NVFP4_BLOCK_16X16 && out->codes_t && !aligned16(out->codes_t)) return NVFP4_ERR_ALIGNMENT;
+        if ((out->scales_mma && !aligned16(out->scales_mma)) ||
+            (p->block == NVFP4_BLOCK_16X16 && out->scales_mma_t && !aligned16(out->scales_mma_t)))
+            return NVFP4_ERR_ALIGNMENT;
+    }
+    if (!ws || ws_bytes < (size_t)kMaxPartials * sizeof(uint32_t) || !aligned16(ws)) return NVFP4_ERR_WORKSPACE;
+
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return NVFP4_ERR_CUDA;
+    sms = sm_count(dev);
+    if (sms <= 0) return NVFP4_ERR_CUDA;
+
+    uint32_t* partials = static_cast<uint32_t*>(ws);
+    const uint64_t rs = p->rht_seed;
+    const bool is16 = x_dtype == NVFP4_BF16;
+    QOut q{out->codes, out->scales, out->scales_mma,
+           p->block == NVFP4_BLOCK_16X16 ? out->codes_t : nullptr,
+           p->block == NVFP4_BLOCK_16X16 ? out->scales_mma_t : nullptr, out->s_dec};
+
+    // Zero the padding of the tensor-core scale layout (rows to 128, scale columns to 16).
+    if (!empty) {
+        if (q.scales_mma && (rows % 128 != 0 || cols % 256 != 0))
+            if (cudaMemsetAsync(q.scales_mma, 0, nvfp4_scales_mma_bytes(rows, cols), stream) != cudaSuccess)
+                return NVFP4_ERR_CUDA;
+        if (q.scales_mma_t && (cols % 128 != 0 || rows % 256 != 0))
+            if (cudaMemsetAsync(q.scales_mma_t, 0, nvfp4_scales_mma_bytes(cols, rows), stream) != cudaSuccess)
+                return NVFP4_ERR_CUDA;
+    }
+
+    // Pass 1.
+    const int64_t chunks = empty ? 0 : R * (C / (is16 ? 8 : 4));
+    int g1 = (int)std::min<int64_t>((int64_t)sms * 8, std::max<int64_t>(1, (chunks + kThreads * 4 - 1) / (kThreads * 4)));
+    g1 = std::min(g1, kMaxPartials);
+    if (p->rht) {
+        if (is16) amax_rht_kernel<uint16_t><<<g1, kThreads, 0, stream>>>((const uint16_t*)x, R, C, ldx, rs, partials);
+        else amax_rht_kernel<float><<<g1, kThreads, 0, stream>>>((const float*)x, R, C, ldx, rs, partials);
+    } else {
+        if (is16) amax_kernel<uint16_t><<<g1, kThreads, 0, stream>>>((const uint16_t*)x, R, C, ldx, partials);
+        else amax_kernel<float><<<g1, kThreads, 0, stream>>>((const float*)x, R, C, ldx, partials);
+    }
+    if (cudaGetLastError() != cudaSuccess) return NVFP4_ERR_CUDA;
+
+    // Pass 2.
+    const bool sr = p->round == NVFP4_ROUND_SR;
+    const int per_sm = (p->block == NVFP4_BLOCK_1X16_ROW) ? 8 : 4;
+    const int64_t work_warps = (p->block == NVFP4_BLOCK_1X16_ROW)
+        ? (empty ? 0 : R * ((C / (is16 ? 8 : 4) + 31) / 32))
+        : (empty ? 0 : ((R + 63) / 64) * ((C + 8 * (is16 ? 8 : 4) - 1) / (8 * (is16 ? 8 : 4))));
+    const int g2 = (int)std::max<int64_t>(1, std::min<int64_t>((int64_t)sms * per_sm, (work_warps + 7) / 8));
+    const uint64_t ss = p->sr_seed;
+    const uint32_t so = p->sr_offset;
+#define NVFP4_LAUNCH_T(T)                                                                                  \
+    do {                                                                                                   \
+        const T* xt = (const T*)x;                                                                         \
+        if (p->block == NVFP4_BLOCK_1X16_ROW) {                                                            \
+            if (sr) encode_row_kernel<T, true><<<g2, kThreads, 0, stream>>>(xt, R, C, ldx, partials, g1, q, ss, so, dev_status); \
+            else encode_row_kernel<T, false><<<g2, kThreads, 0, stream>>>(xt, R, C, ldx, partials, g1, q, ss, so, dev_status); \
+        } else if (p->block == NVFP4_BLOCK_1X16_COL) {                                                     \
+            if (sr && p->rht) encode_col_kernel<T, true, true><<<g2, kThreads, 0, stream>>>(xt, R, C, ldx, partials, g1, q, ss, so, rs, dev_status); \
+            else if (sr) encode_col_kernel<T, true, false><<<g2, kThreads, 0, stream>>>(xt, R, C, ldx, partials, g1, q, ss, so, rs, dev_status); \
+            else if (p->rht) encode_col_kernel<T, false, true><<<g2, kThreads, 0, stream>>>(xt, R, C, ldx, partials, g1, q, ss, so, rs, dev_status); \
+            else encode_col_kernel<T, false, false><<<g2, kThreads, 0, stream>>>(xt, R, C, ldx, partials, g1, q, ss, so, rs, dev_status); \
+        } else {                                                                                           \
+            if (sr) encode_2d_kernel<T, true><<<g2, kThreads, 0, stream>>>(xt, R, C, ldx, partials, g1, q, ss, so, dev_status); \
+            else encode_2d_kernel<T, false><<<g2, kThreads, 0, stream>>>(xt, R, C, ldx, partials, g1, q, ss, so, dev_status); \
+        }                                                                                                  \
+    } while (0)
+    if (is16) NVFP4_LAUNCH_T(uint16_t);
+    else NVFP4_LAUNCH_T(float);
+#undef NVFP4_LAUNCH_T
+    if (cudaGetLastError() != cudaSuccess) return NVFP4_ERR_CUDA;
+    return NVFP4_OK;
+}
+
+}  // namespace nvfp4
+
+extern "C" nvfp4_status nvfp4_quantize(const void* x, int32_t x_dtype, int64_t R, int64_t C, int64_t ldx,
+                                       const nvfp4_qparams* params, const nvfp4_qtensor* out,
+                                       void* workspace, size_t workspace_bytes, uint32_t* dev_status,
+                                       void* stream) {
+    return nvfp4::quantize_impl(x, x_dtype, R, C, ldx, params, out, workspace, workspace_bytes, dev_status,
+                                static_cast<cudaStream_t>(stream));
+}

@@ -1,0 +1,88 @@
+"""GEMM parity: the tcgen05 block-scaled FP4 kernel against the fp64 oracle GEMM
+over the identical dequantized operands (the codes and scales the GPU wrote)."""
+import numpy as np
+import pytest
+import torch
+
+from helpers import bf16_round, qtensor_to_oracle, rel_fro
+
+pytestmark = pytest.mark.gpu
+
+TOL = 1e-3        # relative Frobenius error
+
+
+@pytest.fixture(scope="module")
+def nv():
+    import __graft_entry__
+    __graft_entry__.build()
+    import nvfp4_bit_quantized_gb300 as nv
+    return nv
+
+
+def _operands(nv, M, N, K, seed, b_block=0):
+    g = torch.Generator(device="cpu").manual_seed(seed)
+    A = torch.randn((M, K), generator=g).to(torch.bfloat16).cuda()
+    B = (torch.randn((N, K), generator=g) * 0.02).to(torch.bfloat16).cuda()
+    qa = nv.quantize(A, nv.ROW, nv.RNE)
+    qb = nv.quantize(B, b_block, nv.RNE)
+    return qa, qb
+
+
+def _ref(oracle_mod, qa, qb, b_block):
+    return oracle_mod.gemm_f64(oracle_mod.dequant(qtensor_to_oracle(qa, 0)),
+                               oracle_mod.dequant(qtensor_to_oracle(qb, b_block)))
+
+
+@pytest.mark.parametrize("M,N,K", [(128, 256, 256), (384, 640, 768), (200, 300, 224), (1, 8, 32),
+                                   (130, 260, 544), (256, 512, 2048)])
+def test_gemm_fp32_out(nv, oracle_mod, M, N, K):
+    qa, qb = _operands(nv, M, N, K, seed=M + N + K)
+    nv.reset_status()
+    D = nv.gemm(qa, qb, torch.float32)
+    assert nv.status_query() == 0
+    ref = _ref(oracle_mod, qa, qb, 0)
+    err = rel_fro(D.cpu().numpy(), ref)
+    assert err <= TOL, err
+
+
+@pytest.mark.parametrize("M,N,K", [(256, 512, 512), (200, 300, 224)])
+def test_gemm_bf16_out(nv, oracle_mod, M, N, K):
+    qa, qb = _operands(nv, M, N, K, seed=7)
+    D = nv.gemm(qa, qb, torch.bfloat16)
+    ref = _ref(oracle_mod, qa, qb, 0)
+    err = rel_fro(D.float().cpu().numpy(), bf16_round(ref))
+    assert err <= TOL, err
+
+
+def test_gemm_with_2d_weight_operand_and_transpose(nv, oracle_mod):
+    M, N, K = 256, 512, 384
+    qa, qw = _operands(nv, M, N, K, seed=11, b_block=2)
+    D = nv.gemm(qa, qw, torch.float32)
+    assert rel_fro(D.cpu().numpy(), _ref(oracle_mod, qa, qw, 2)) <= TOL
+    # W^T as the B operand of a [*, N] x [N, K]^T product
+    g = torch.Generator(device="cpu").manual_seed(12)
+    dY = (torch.randn((M, N), generator=g) * 1e-3).to(torch.bfloat16).cuda()
+    qd = nv.quantize(dY, nv.ROW, nv.SR, sr_seed=5)
+    dX = nv.gemm(qd, qw.transposed(), torch.float32)
+    wt = dict(codes=qw.codes_t.cpu().numpy(), scales=qw.scales.cpu().numpy().T.copy(),
+              s_dec=float(qw.s_dec[0].item()), rows=K, cols=N, block=2)
+    ref = oracle_mod.gemm_f64(oracle_mod.dequant(qtensor_to_oracle(qd, 0)), oracle_mod.dequant(wt))
+    assert rel_fro(dX.cpu().numpy(), ref) <= TOL
+
+
+def test_gemm_strided_output(nv, oracle_mod):
+    M, N, K = 128, 256, 256
+    qa, qb = _operands(nv, M, N, K, seed=13)
+    big = torch.full((M, N + 40), 7.0, dtype=torch.float32, device="cuda")
+    nv.gemm(qa, qb, out=big[:, :N])
+    torch.cuda.synchronize()
+    assert torch.all(big[:, N:] == 7.0)
+    assert rel_fro(big[:, :N].cpu().numpy(), _ref(oracle_mod, qa, qb, 0)) <= TOL
+
+
+def test_gemm_repeat_is_deterministic(nv):
+    qa, qb = _operands(nv, 256, 512, 1024, seed=17)
+    d1 = nv.gemm(qa, qb, torch.float32)
+    d2 = nv.gemm(qa, qb, torch.float32)
+    torch.cuda.synchronize()
+    assert torch.equal(d1, d2)
