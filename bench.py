@@ -98,11 +98,55 @@ class ClockSampler:
 
 # --------------------------------------------------------------------------- our arm
 
+def run_kernel_only(args):
+    """One kernel family alone on the Fprop-shaped operands (for profiling): the
+    GEMM (operands quantized once, untimed) or the five quantizer passes."""
+    import torch
+    import nvfp4_bit_quantized_gb300 as nv
+    from nvfp4_bit_quantized_gb300 import inputs
+
+    torch.cuda.set_device(0)
+    X, W, dY = inputs.linear_layer(M, K, N, seed=0, dtype=torch.bfloat16, device="cuda")
+    nv.reset_status()
+    if args.kernel == "gemm":
+        xq = nv.quantize(X, nv.ROW, nv.RNE, scales=False)
+        wq = nv.quantize(W, nv.TILE16, nv.RNE, scales=False, transpose=False)
+        del dY
+        out = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+        work = lambda: nv.gemm(xq, wq, out=out)
+        unit, per = "TFLOP/s", 2.0 * M * N * K / 1e12
+    else:
+        def work():
+            nv.quantize(W, nv.TILE16, nv.RNE, scales=False, transpose=True)
+            nv.quantize(X, nv.ROW, nv.RNE, scales=False)
+            nv.quantize(dY, nv.ROW, nv.SR, sr_seed=7, scales=False)
+            nv.quantize(dY, nv.COL, nv.SR, rht=True, sr_seed=7, rht_seed=11, scales=False)
+            nv.quantize(X, nv.COL, nv.RNE, rht=True, rht_seed=11, scales=False)
+        unit = "GB/s"
+        per = (N * K * (4 + 2 * 0.5625) + 2 * M * K * 4.5625 + 2 * M * N * 4.5625) / 1e9
+    for _ in range(args.warmup):
+        work()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.steps):
+        work()
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / args.steps
+    print(json.dumps({"kernel": args.kernel, "value": round(per / (ms * 1e-3), 1), "unit": unit,
+                      "ms_per_iter": round(ms, 4), "steps": args.steps, "device_status": nv.status_query(),
+                      "config": {"workload": WORKLOAD, "M": M, "K": K, "N": N}}))
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
     import nvfp4_bit_quantized_gb300 as nv
     from nvfp4_bit_quantized_gb300 import inputs
+
+    if args.kernel != "step":
+        return run_kernel_only(args)
 
     rank, world, local = env_rank()
     torch.cuda.set_device(local)
@@ -209,19 +253,22 @@ def run_ours(args):
         hdX.copy_(dX, non_blocking=True)
         hdW.copy_(dW, non_blocking=True)
 
-    for i in range(2):
-        e2e_step(i)
-    torch.cuda.synchronize()
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e2e_steps = max(1, min(args.steps, 5))
-    e0.record(stream)
-    for i in range(e2e_steps):
-        e2e_step(i)
-    e1.record(stream)
-    torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1) / e2e_steps
-    e2e_value = world * flops_step / (e2e_ms * 1e-3) / 1e12
+    e2e_ms = e2e_value = None
+    if not args.no_e2e:
+        for i in range(2):
+            e2e_step(i)
+        torch.cuda.synchronize()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e2e_steps = max(1, min(args.steps, 5))
+        e0.record(stream)
+        for i in range(e2e_steps):
+            e2e_step(i)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = e0.elapsed_time(e1) / e2e_steps
+        e2e_value = round(world * flops_step / (e2e_ms * 1e-3) / 1e12, 2)
+        e2e_ms = round(e2e_ms, 3)
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
@@ -259,8 +306,8 @@ def run_ours(args):
         "quantize_roofline": {"bound": "hbm", "achieved": round(sum(qbytes.values()) / (quant_ms * 1e-3) / 1e9, 1),
                               "peak": peaks["hbm_gbs"], "unit": "GB/s",
                               "frac": round(sum(qbytes.values()) / (quant_ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 4)},
-        "e2e": {"value": round(e2e_value, 2), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 3)},
+        "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clk.summary(),
         "device_status": status,
@@ -342,6 +389,9 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--kernel", choices=["step", "gemm", "quantize"], default="step",
+                    help="step: the whole hot path (the bench line); gemm / quantize: one kernel family alone")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3

@@ -101,7 +101,9 @@ __device__ __forceinline__ uint32_t e2m1_rne_sw(float y) {
 }
 
 // Hardware conversion of two fp32 values to an E2M1 pair (first source in the
-// high nibble); used only by the diagnostics until it is pinned to the rule above.
+// high nibble).  cvt.rn.satfinite.e2m1x2 rounds to nearest-even, saturates to 6
+// and keeps the sign of zero: exactly the rule above (pinned against the oracle
+// element by element), so the kernels use it.
 __device__ __forceinline__ uint32_t e2m1x2_hw(float hi, float lo) {
     uint32_t out;
     asm("{\n\t.reg .b8 t;\n\t"
@@ -109,6 +111,44 @@ __device__ __forceinline__ uint32_t e2m1x2_hw(float hi, float lo) {
         "cvt.u32.u8 %0, t;\n\t}"
         : "=r"(out) : "f"(hi), "f"(lo));
     return out;
+}
+
+// Eight values -> eight E2M1 codes, element k in nibble k (hardware conversion).
+__device__ __forceinline__ uint32_t e2m1x8_rn(const float (&y)[8]) {
+    uint32_t out;
+    asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 b0, %2, %1;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 b1, %4, %3;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 b2, %6, %5;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 b3, %8, %7;\n\t"
+        "mov.b32 %0, {b0, b1, b2, b3};\n\t}"
+        : "=r"(out)
+        : "f"(y[0]), "f"(y[1]), "f"(y[2]), "f"(y[3]), "f"(y[4]), "f"(y[5]), "f"(y[6]), "f"(y[7]));
+    return out;
+}
+
+// Four values -> four codes in the low 16 bits.
+__device__ __forceinline__ uint32_t e2m1x4_rn(const float (&y)[4]) {
+    uint32_t out;
+    asm("{\n\t.reg .b8 b0, b1;\n\t.reg .b16 h;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 b0, %2, %1;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 b1, %4, %3;\n\t"
+        "mov.b16 h, {b0, b1};\n\t"
+        "cvt.u32.u16 %0, h;\n\t}"
+        : "=r"(out) : "f"(y[0]), "f"(y[1]), "f"(y[2]), "f"(y[3]));
+    return out;
+}
+
+// Stochastic rounding to the E2M1 grid, returned as the (signed) grid value:
+// the conversions above then encode it exactly.
+__device__ __forceinline__ float e2m1_sr_value(float y, uint32_t r16) {
+    float a = fminf(fabsf(y), 6.0f);
+    float sp = a < 2.0f ? 0.5f : (a < 4.0f ? 1.0f : 2.0f);
+    float inv = a < 2.0f ? 2.0f : (a < 4.0f ? 1.0f : 0.5f);
+    float lo = __fmul_rn(floorf(__fmul_rn(a, inv)), sp);
+    float thr = __fmul_rn(__fmul_rn((float)r16, 1.0f / 65536.0f), sp);
+    float v = (__fsub_rn(a, lo) > thr) ? __fadd_rn(lo, sp) : lo;
+    return copysignf(v, y);
 }
 
 // Stochastic rounding: saturate |y| to 6; grid spacing sp is 0.5 below 2, 1 below 4,

@@ -8,6 +8,7 @@
 // The quantized activations and gradients live in the caller's workspace:
 //   [partials 16 KB][slot A: codes, tile scales, s_dec][slot B: same]
 #include <cuda_runtime.h>
+#include <algorithm>
 #include <cstdint>
 
 #include "host_common.h"
@@ -23,6 +24,12 @@ struct Slot { uint8_t* codes; uint8_t* scales_mma; float* s_dec; };
 
 inline size_t slot_bytes(int64_t rows, int64_t cols) {
     return up16((size_t)rows * (size_t)cols / 2) + up16(nvfp4_scales_mma_bytes(rows, cols)) + 16;
+}
+
+// Slot A holds X (Fprop, [M, K]), dY (Dgrad, [M, N]) or dY^T (Wgrad, [N, M]); the
+// tile-layout scales pad rows to 128 and columns to 256, so the orientations differ.
+inline size_t slot_a_bytes(int64_t M, int64_t N, int64_t K) {
+    return std::max(std::max(slot_bytes(M, K), slot_bytes(M, N)), slot_bytes(N, M));
 }
 
 inline Slot carve(uint8_t*& p, int64_t rows, int64_t cols) {
@@ -53,8 +60,7 @@ using namespace nvfp4;
 
 extern "C" size_t nvfp4_linear_workspace_bytes(int64_t M, int64_t N, int64_t K) {
     if (M < 0 || N < 0 || K < 0) return 0;
-    const int64_t big = N > K ? N : K;
-    return kPartialBytes + slot_bytes(M, big) + slot_bytes(K, M) + 64;
+    return kPartialBytes + slot_a_bytes(M, N, K) + slot_bytes(K, M) + 64;
 }
 
 extern "C" nvfp4_status nvfp4_linear_fprop(const void* X, int32_t x_dtype, int64_t M, int64_t K, int64_t ldx,
@@ -115,10 +121,9 @@ extern "C" nvfp4_status nvfp4_linear_wgrad(const void* dY, int32_t dy_dtype, int
     uint8_t* p = static_cast<uint8_t*>(workspace);
     void* partials = p;
     p += kPartialBytes;
-    const int64_t big = N > K ? N : K;
     uint8_t* pa = p;
     const Slot ds = carve(pa, N, M);                 // dY^T: [N, M]
-    p += slot_bytes(M, big);
+    p += slot_a_bytes(M, N, K);
     const Slot xs = carve(p, K, M);                  // X^T: [K, M]
     nvfp4_qtensor dyq = as_q(ds, N, M), xq = as_q(xs, K, M);
     cudaStream_t s = static_cast<cudaStream_t>(stream);

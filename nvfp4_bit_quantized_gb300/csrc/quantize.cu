@@ -153,6 +153,10 @@ __global__ void __launch_bounds__(kThreads) amax_rht_kernel(const T* __restrict_
 // ---------------------------------------------------------------------------
 struct Scales { float s_enc; bool finite; };
 
+// Per-CTA table of the element multiplier e_b = s_enc / S_b for every non-negative
+// E4M3 scale code (one division per code instead of one per block).
+__shared__ float g_eb_table[128];
+
 __device__ __forceinline__ Scales tensor_scales(const uint32_t* __restrict__ partials, int nparts,
                                                 float* s_dec_out, uint32_t* dev_status) {
     __shared__ uint32_t red[kThreads / 32];
@@ -177,6 +181,8 @@ __device__ __forceinline__ Scales tensor_scales(const uint32_t* __restrict__ par
         *s_dec_out = __fdiv_rn(1.0f, s.s_enc);
         if (!s.finite) set_status(dev_status, NVFP4_ERR_NONFINITE);
     }
+    if (threadIdx.x < 128) g_eb_table[threadIdx.x] = block_multiplier(threadIdx.x, s.s_enc);
+    __syncthreads();
     return s;
 }
 
@@ -190,15 +196,53 @@ struct QOut {
 };
 
 // ---------------------------------------------------------------------------
-// Pass 2, 1x16 blocks along rows.
+// Pass 2, 1x16 blocks along rows.  U warp segments per iteration: their loads
+// are all issued before any is used (memory-level parallelism).
 // ---------------------------------------------------------------------------
+template <typename T, bool SR>
+__device__ __forceinline__ void encode_row_chunk(const float (&f)[Vec<T>::N], bool valid, int64_t r, int64_t C,
+                                                 int64_t col, int lane, const Scales& sc, const QOut& out,
+                                                 int64_t nkb, uint64_t sr_seed, uint32_t sr_offset) {
+    constexpr int VEC = Vec<T>::N;
+    constexpr int LPB = 16 / VEC;                    // lanes per 16-element block
+    float amax = 0.0f;
+#pragma unroll
+    for (int j = 0; j < VEC; ++j) amax = fmaxf(amax, fabsf(f[j]));
+#pragma unroll
+    for (int o = 1; o < LPB; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
+    if (!valid) return;
+    const uint32_t sb = block_scale_code(amax, sc.s_enc);
+    const float e_b = g_eb_table[sb];
+    float y[VEC];
+    if constexpr (SR) {
+        // idx0 % 8 is 0 for bf16 (8-element chunks) and 0 or 4 for fp32
+        const uint64_t idx0 = (uint64_t)(r * C + col);
+        const Philox4 p = sr_philox(sr_seed, 0u, sr_offset, idx0 >> 3);
+        const bool upper = (VEC == 4) && (idx0 & 4);
+#pragma unroll
+        for (int j = 0; j < VEC; ++j)
+            y[j] = e2m1_sr_value(__fmul_rn(f[j], e_b), upper ? sr_r16(p, 4 + j) : sr_r16(p, j));
+    } else {
+#pragma unroll
+        for (int j = 0; j < VEC; ++j) y[j] = __fmul_rn(f[j], e_b);
+    }
+    uint8_t* dst = out.codes + r * (C / 2) + col / 2;
+    if constexpr (VEC == 8) *reinterpret_cast<uint32_t*>(dst) = e2m1x8_rn(y);
+    else *reinterpret_cast<uint16_t*>(dst) = (uint16_t)e2m1x4_rn(y);
+    if ((lane % LPB) == 0) {
+        const int64_t s = col / 16;
+        if (out.scales) out.scales[r * (C / 16) + s] = (uint8_t)sb;
+        if (out.scales_mma) out.scales_mma[mma_sf_offset(r, s, nkb)] = (uint8_t)sb;
+    }
+}
+
 template <typename T, bool SR>
 __global__ void __launch_bounds__(kThreads) encode_row_kernel(const T* __restrict__ x, int64_t R, int64_t C,
                                                               int64_t ldx, const uint32_t* __restrict__ partials,
                                                               int nparts, QOut out, uint64_t sr_seed,
                                                               uint32_t sr_offset, uint32_t* dev_status) {
     constexpr int VEC = Vec<T>::N;
-    constexpr int LPB = 16 / VEC;                    // lanes per 16-element block
+    constexpr int U = 4;
     const Scales sc = tensor_scales(partials, nparts, out.s_dec, dev_status);
     const int lane = threadIdx.x & 31;
     const int64_t cpr = C / VEC;
@@ -207,45 +251,28 @@ __global__ void __launch_bounds__(kThreads) encode_row_kernel(const T* __restric
     const int64_t nkb = (C + 255) / 256;
     const int64_t warp0 = (int64_t)blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5);
     const int64_t nwarps = (int64_t)gridDim.x * (kThreads / 32);
-    for (int64_t seg = warp0; seg < nseg; seg += nwarps) {
-        const int64_t r = seg / spr;
-        const int64_t ch = (seg - r * spr) * 32 + lane;
-        const bool valid = ch < cpr;
-        float f[VEC];
-        float amax = 0.0f;
-        if (valid) {
-            const uint4 v = ld_stream(x + r * ldx + ch * VEC);
-            Vec<T>::unpack(v, f);
+    for (int64_t base = warp0; base < nseg; base += nwarps * U) {
+        uint4 v[U];
+        int64_t rr[U], ch[U];
 #pragma unroll
-            for (int j = 0; j < VEC; ++j) amax = fmaxf(amax, fabsf(f[j]));
+        for (int u = 0; u < U; ++u) {
+            const int64_t seg = base + (int64_t)u * nwarps;
+            rr[u] = seg / spr;
+            ch[u] = (seg - rr[u] * spr) * 32 + lane;
+            if (seg < nseg && ch[u] < cpr) v[u] = ld_stream(x + rr[u] * ldx + ch[u] * VEC);
         }
 #pragma unroll
-        for (int o = 1; o < LPB; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
-        const uint32_t sb = valid ? block_scale_code(amax, sc.s_enc) : 0u;
-        const float e_b = block_multiplier(sb, sc.s_enc);
-        const int64_t col = ch * VEC;                // first element of this lane
-        if (valid) {
-            uint32_t packed = 0;
-            if constexpr (SR) {
-                // idx0 % 8 is 0 for bf16 (8-element chunks) and 0 or 4 for fp32
-                const uint64_t idx0 = (uint64_t)(r * C + col);
-                const Philox4 p = sr_philox(sr_seed, 0u, sr_offset, idx0 >> 3);
-                const bool upper = (VEC == 4) && (idx0 & 4);
+        for (int u = 0; u < U; ++u) {
+            const int64_t seg = base + (int64_t)u * nwarps;
+            if (seg >= nseg) break;                      // warp-uniform
+            const bool valid = ch[u] < cpr;
+            float f[VEC];
+            if (valid) Vec<T>::unpack(v[u], f);
+            else {
 #pragma unroll
-                for (int j = 0; j < VEC; ++j)
-                    packed |= e2m1_sr_sw(__fmul_rn(f[j], e_b), upper ? sr_r16(p, 4 + j) : sr_r16(p, j)) << (4 * j);
-            } else {
-#pragma unroll
-                for (int j = 0; j < VEC; ++j) packed |= e2m1_rne_sw(__fmul_rn(f[j], e_b)) << (4 * j);
+                for (int j = 0; j < VEC; ++j) f[j] = 0.0f;
             }
-            uint8_t* dst = out.codes + r * (C / 2) + col / 2;
-            if constexpr (VEC == 8) *reinterpret_cast<uint32_t*>(dst) = packed;
-            else *reinterpret_cast<uint16_t*>(dst) = (uint16_t)packed;
-            if ((lane % LPB) == 0) {
-                const int64_t s = col / 16;
-                if (out.scales) out.scales[r * (C / 16) + s] = (uint8_t)sb;
-                if (out.scales_mma) out.scales_mma[mma_sf_offset(r, s, nkb)] = (uint8_t)sb;
-            }
+            encode_row_chunk<T, SR>(f, valid, rr[u], C, ch[u] * VEC, lane, sc, out, nkb, sr_seed, sr_offset);
         }
     }
 }
@@ -281,24 +308,26 @@ __global__ void __launch_bounds__(kThreads) encode_col_kernel(const T* __restric
 #pragma unroll
             for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(t[j][i]));
             const uint32_t sb = block_scale_code(amax, sc.s_enc);
-            const float e_b = block_multiplier(sb, sc.s_enc);
+            const float e_b = g_eb_table[sb];
             const int64_t c = c0 + j;                // operand row
-            uint32_t lo = 0, hi = 0;
+            float ylo[8], yhi[8];
             if constexpr (SR) {
                 const uint64_t idx0 = (uint64_t)(c * R + r0);
                 const Philox4 p0 = sr_philox(sr_seed, 1u, sr_offset, idx0 >> 3);
                 const Philox4 p1 = sr_philox(sr_seed, 1u, sr_offset, (idx0 >> 3) + 1);
 #pragma unroll
-                for (int i = 0; i < 8; ++i) lo |= e2m1_sr_sw(__fmul_rn(t[j][i], e_b), sr_r16(p0, i)) << (4 * i);
-#pragma unroll
-                for (int i = 0; i < 8; ++i) hi |= e2m1_sr_sw(__fmul_rn(t[j][8 + i], e_b), sr_r16(p1, i)) << (4 * i);
+                for (int i = 0; i < 8; ++i) {
+                    ylo[i] = e2m1_sr_value(__fmul_rn(t[j][i], e_b), sr_r16(p0, i));
+                    yhi[i] = e2m1_sr_value(__fmul_rn(t[j][8 + i], e_b), sr_r16(p1, i));
+                }
             } else {
 #pragma unroll
-                for (int i = 0; i < 8; ++i) lo |= e2m1_rne_sw(__fmul_rn(t[j][i], e_b)) << (4 * i);
-#pragma unroll
-                for (int i = 0; i < 8; ++i) hi |= e2m1_rne_sw(__fmul_rn(t[j][8 + i], e_b)) << (4 * i);
+                for (int i = 0; i < 8; ++i) {
+                    ylo[i] = __fmul_rn(t[j][i], e_b);
+                    yhi[i] = __fmul_rn(t[j][8 + i], e_b);
+                }
             }
-            *reinterpret_cast<uint2*>(out.codes + c * (R / 2) + r0 / 2) = make_uint2(lo, hi);
+            *reinterpret_cast<uint2*>(out.codes + c * (R / 2) + r0 / 2) = make_uint2(e2m1x8_rn(ylo), e2m1x8_rn(yhi));
             const int64_t s = r0 / 16;
             if (out.scales) out.scales[c * (R / 16) + s] = (uint8_t)sb;
             if (out.scales_mma) out.scales_mma[mma_sf_offset(c, s, nkb)] = (uint8_t)sb;
@@ -341,35 +370,37 @@ __global__ void __launch_bounds__(kThreads) encode_2d_kernel(const T* __restrict
         for (int o = 1; o < LPT; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
         if (!valid) continue;
         const uint32_t sb = block_scale_code(amax, sc.s_enc);
-        const float e_b = block_multiplier(sb, sc.s_enc);
-        // Encode row by row: W codes go out per row, W^T codes are packed per column.
+        const float e_b = g_eb_table[sb];
+        // Encode row by row (W); the W^T codes are the same nibbles, transposed in registers.
         uint32_t lo_t[VEC], hi_t[VEC];
 #pragma unroll
-        for (int j = 0; j < VEC; ++j) { lo_t[j] = 0; hi_t[j] = 0; }
+        for (int j = 0; j < VEC; ++j) { lo_t[j] = 0u; hi_t[j] = 0u; }
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-            uint32_t packed = 0;
+            float y[VEC];
             if constexpr (SR) {
                 const uint64_t idx0 = (uint64_t)((r0 + i) * C + c0);
                 const Philox4 p = sr_philox(sr_seed, 0u, sr_offset, idx0 >> 3);
                 const bool upper = (VEC == 4) && (idx0 & 4);
 #pragma unroll
-                for (int j = 0; j < VEC; ++j) {
-                    const uint32_t cd = e2m1_sr_sw(__fmul_rn(t[j][i], e_b), upper ? sr_r16(p, 4 + j) : sr_r16(p, j));
-                    packed |= cd << (4 * j);
-                    if (i < 8) lo_t[j] |= cd << (4 * i); else hi_t[j] |= cd << (4 * (i - 8));
-                }
+                for (int j = 0; j < VEC; ++j)
+                    y[j] = e2m1_sr_value(__fmul_rn(t[j][i], e_b), upper ? sr_r16(p, 4 + j) : sr_r16(p, j));
             } else {
 #pragma unroll
-                for (int j = 0; j < VEC; ++j) {
-                    const uint32_t cd = e2m1_rne_sw(__fmul_rn(t[j][i], e_b));
-                    packed |= cd << (4 * j);
-                    if (i < 8) lo_t[j] |= cd << (4 * i); else hi_t[j] |= cd << (4 * (i - 8));
-                }
+                for (int j = 0; j < VEC; ++j) y[j] = __fmul_rn(t[j][i], e_b);
             }
+            uint32_t packed;
+            if constexpr (VEC == 8) packed = e2m1x8_rn(y);
+            else packed = e2m1x4_rn(y);
             uint8_t* dst = out.codes + (r0 + i) * (C / 2) + c0 / 2;
             if constexpr (VEC == 8) *reinterpret_cast<uint32_t*>(dst) = packed;
             else *reinterpret_cast<uint16_t*>(dst) = (uint16_t)packed;
+#pragma unroll
+            for (int j = 0; j < VEC; ++j) {
+                const uint32_t nib = (packed >> (4 * j)) & 0xFu;
+                if (i < 8) lo_t[j] |= nib << (4 * i);
+                else hi_t[j] |= nib << (4 * (i - 8));
+            }
         }
         if (out.codes_t) {
 #pragma unroll

@@ -52,9 +52,10 @@ def test_single_layer_fp32_config(nv, oracle_mod):
 
 
 def test_layer_bf16_ragged(nv, oracle_mod):
-    """bf16 in/out, M = 272 (not a tile multiple), K = 352, N = 400."""
+    """bf16 in/out, M = 288, K = 352, N = 416: none a tile multiple (each GEMM's
+    contraction length must be a multiple of 32)."""
     from nvfp4_bit_quantized_gb300 import inputs
-    X, W, dY = inputs.linear_layer(272, 352, 400, seed=3, dtype=torch.bfloat16, device="cpu")
+    X, W, dY = inputs.linear_layer(288, 352, 416, seed=3, dtype=torch.bfloat16, device="cpu")
     Xg, Wg, dYg = X.cuda(), W.cuda(), dY.cuda()
     wq = nv.quantize_weight(Wg)
     Y = nv.linear_fprop(Xg, wq)

@@ -104,3 +104,21 @@ def test_product_path_has_no_fallback(monkeypatch, lib):
     monkeypatch.setattr(L, "LIB_PATH", "/nonexistent/libnvfp4_gb300.so")
     with pytest.raises(ImportError):
         L.lib()
+
+
+@pytest.mark.parametrize("M,N,K", [(288, 416, 352), (8192, 20480, 5120), (16384, 14336, 4096), (32, 32, 32),
+                                   (100, 3000, 64), (4096, 96, 5000)])
+def test_linear_workspace_covers_every_operand_orientation(lib, M, N, K):
+    """The linear workspace holds the amax partials plus slot A (X [M,K], dY [M,N] or
+    dY^T [N,M]) and slot B (X^T [K,M]); tile-layout scale padding depends on the
+    orientation, so each must fit."""
+    L = lib.lib()
+
+    def up16(v):
+        return (v + 15) // 16 * 16
+
+    def slot(r, c):
+        return up16(r * c // 2) + up16(L.nvfp4_scales_mma_bytes(r, c)) + 16
+
+    need = 4096 * 4 + max(slot(M, K), slot(M, N), slot(N, M)) + slot(K, M)
+    assert L.nvfp4_linear_workspace_bytes(M, N, K) >= need
