@@ -132,6 +132,31 @@ NVFP4_API nvfp4_status nvfp4_quantize(const void* x, int32_t x_dtype, int64_t R,
                             void* stream);
 
 /*
+ * nvfp4_quantize_noalloc -- nvfp4_quantize without a workspace argument; it
+ * allocates nothing.  The page describes no such call: it exists for callers
+ * that can hand over their input and output buffers but cannot obtain one more
+ * device buffer -- a plug-in that only sees the tensors its host framework
+ * planned, or code running where an allocation would re-enter or break the
+ * caller's allocator.
+ *   Scratch: the amax pass's per-CTA partial maxima live in a static device
+ *   array of 4096 uint32 (16 KB) inside this library, held on every device that
+ *   loads the library until the process exits.  Calls needing more scratch than
+ *   that are rejected with NVFP4_ERR_WORKSPACE (the amax grid is capped at 4096
+ *   CTAs, so no tensor size needs more).
+ *   Set-up: the first call on a device looks up the array's device address
+ *   (cudaGetSymbolAddress) with that device current and caches it; make that
+ *   first call before any stream capture.
+ *   Sharing: every call uses the same array; each amax CTA overwrites its own
+ *   slot before the encode pass reads it, so nothing needs clearing between
+ *   calls, but calls that overlap on the GPU (different streams, concurrently)
+ *   race on the array and give wrong results.
+ * Arguments, layouts, results and errors are otherwise those of nvfp4_quantize.
+ */
+NVFP4_API nvfp4_status nvfp4_quantize_noalloc(const void* x, int32_t x_dtype, int64_t R, int64_t C, int64_t ldx,
+                                              const nvfp4_qparams* params, const nvfp4_qtensor* out,
+                                              uint32_t* dev_status, void* stream);
+
+/*
  * nvfp4_gemm -- D[M, N] = s_dec(A) * s_dec(B) * sum_k qA[m,k]*SA[m,k/16] * qB[n,k]*SB[n,k/16]
  * on the tcgen05 block-scaled FP4 tensor cores (fp32 accumulation in TMEM).
  *   A: [M, K] quantized along K (codes + scales_mma); B: [N, K] likewise.

@@ -22,6 +22,7 @@
 #include <cuda_runtime.h>
 #include <cstdint>
 #include <cstdio>
+#include <mutex>
 
 #include "device_common.cuh"
 #include "host_common.h"
@@ -538,4 +539,55 @@ extern "C" nvfp4_status nvfp4_quantize(const void* x, int32_t x_dtype, int64_t R
                                        void* stream) {
     return nvfp4::quantize_impl(x, x_dtype, R, C, ldx, params, out, workspace, workspace_bytes, dev_status,
                                 static_cast<cudaStream_t>(stream));
+}
+
+// ---------------------------------------------------------------------------
+// Allocation-free quantize.  Same kernels and results as nvfp4_quantize, but
+// the amax pass's partial maxima go to a file-scope device array instead of a
+// caller-provided workspace.  For callers that can pass their input and output
+// buffers but cannot obtain one more device buffer: a plug-in that only sees
+// the tensors its host framework planned, or code that runs where allocating
+// would re-enter or break the caller's allocator.
+// ---------------------------------------------------------------------------
+namespace nvfp4 {
+namespace {
+
+// The scratch: one partial maximum per amax CTA, kMaxPartials (4096) of them,
+// 16 KB.  Every device that loads this library keeps it until the process exits.
+// Host code must not pass the symbol itself to a kernel: on the host it is only
+// a stand-in, so its device address is looked up with cudaGetSymbolAddress.
+static __device__ __align__(256) uint32_t g_noalloc_partials[kMaxPartials];
+
+std::mutex g_noalloc_mutex;
+void* g_noalloc_addr[64] = {nullptr};
+
+// Device address of the scratch on `dev` (which must be the current device);
+// looked up on the first call for that device and cached.
+nvfp4_status noalloc_scratch(int dev, void** addr) {
+    if (dev < 0 || dev >= 64) return NVFP4_ERR_CUDA;
+    std::lock_guard<std::mutex> lk(g_noalloc_mutex);
+    if (!g_noalloc_addr[dev]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_noalloc_partials) != cudaSuccess || !p) return NVFP4_ERR_CUDA;
+        g_noalloc_addr[dev] = p;
+    }
+    *addr = g_noalloc_addr[dev];
+    return NVFP4_OK;
+}
+
+}  // namespace
+}  // namespace nvfp4
+
+extern "C" nvfp4_status nvfp4_quantize_noalloc(const void* x, int32_t x_dtype, int64_t R, int64_t C, int64_t ldx,
+                                               const nvfp4_qparams* params, const nvfp4_qtensor* out,
+                                               uint32_t* dev_status, void* stream) {
+    if (!params) return NVFP4_ERR_INVALID_ARG;
+    if (nvfp4_quantize_workspace_bytes(R, C, params) > sizeof(nvfp4::g_noalloc_partials)) return NVFP4_ERR_WORKSPACE;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return NVFP4_ERR_CUDA;
+    void* scratch = nullptr;
+    const nvfp4_status st = nvfp4::noalloc_scratch(dev, &scratch);
+    if (st != NVFP4_OK) return st;
+    return nvfp4::quantize_impl(x, x_dtype, R, C, ldx, params, out, scratch, sizeof(nvfp4::g_noalloc_partials),
+                                dev_status, static_cast<cudaStream_t>(stream));
 }
