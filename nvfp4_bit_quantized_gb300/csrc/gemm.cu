@@ -12,16 +12,25 @@
 //               swizzle), scale tiles via 1-D cp.async.bulk, into a 4-stage
 //               shared-memory ring guarded by full/empty mbarriers;
 //   warp 1      allocates TMEM (512 columns) and, from one lane, issues
-//               tcgen05.cp (scales -> TMEM) and tcgen05.mma
-//               .kind::mxf4nvf4.block_scale.scale_vec::4X (M=128, N=256, K=64),
-//               accumulating in fp32 in TMEM columns [0, 256);
+//               tcgen05.mma.kind::mxf4nvf4.block_scale.scale_vec::4X
+//               (M=128, N=256, K=64), accumulating in fp32 in TMEM columns [0, 256);
+//   warps 6-9   move each stage's E4M3 scale tiles smem -> registers -> TMEM
+//               (tcgen05.st), off the tensor pipe: copying them with tcgen05.cp
+//               serialised with the MMAs and cost a third of the run time;
 //   warps 2-5   epilogue: tcgen05.ld of their 32-lane quarter, multiply by
-//               alpha = s_dec(A) * s_dec(B), convert, store to global.
+//               alpha = s_dec(A) * s_dec(B), convert.  bf16 output: write a
+//               128B-swizzled shared-memory tile, release the accumulator, then
+//               one lane issues TMA bulk stores (3-stage ring + 64 KB staging);
+//               fp32 or unaligned output: direct stores (4-stage ring).
 // Every wait is bounded (see mbar_wait_bounded): on a timeout the kernel
 // records NVFP4_ERR_TIMEOUT, lets every role leave its loop, waits for its own
 // copies and MMAs in flight, frees TMEM and returns.
 //
 // Shared memory per stage: A 128x128 B | B 256x128 B | SFA 2 KB | SFB 4 KB = 54 KB.
+// The single accumulator is released as soon as the epilogue has it in registers /
+// shared memory, so the next tile's MMAs overlap the global stores.
+// The scale tiles have their own barrier (sf_loaded) so the scale warps start while
+// the codes tiles are still in flight.
 // TMEM: accumulator cols [0,256); scale slots at 256 + 48*stage:
 //   SFA k-step j  -> 4 columns at +4j       (lane r%32, column r/32 = row r)
 //   SFB k-step j  -> 8 columns at +16 + 8j  (two 128-row halves of the N tile)
@@ -41,7 +50,6 @@ namespace gemm {
 
 constexpr int BM = 128, BN = 256, BK = 256;       // BK in E2M1 elements
 constexpr int BKB = BK / 2;                       // 128 bytes per row per stage
-constexpr int STAGES = 4;
 constexpr int A_BYTES = BM * BKB;                 // 16 KB
 constexpr int B_BYTES = BN * BKB;                 // 32 KB
 constexpr int SFA_BYTES = 2048;                   // 128 rows x 16 scales
@@ -51,14 +59,30 @@ constexpr int TMEM_COLS = 512;
 constexpr int ACC_COL = 0;
 constexpr int SF_COL0 = 256;
 constexpr int SF_STAGE_COLS = 48;
-constexpr int NUM_THREADS = 192;
-constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 256;
+constexpr int NUM_THREADS = 320;                 // 10 warps: producer, MMA, 4 epilogue, 4 scale loaders
+// bf16 output staged through shared memory for TMA stores: each epilogue warp owns
+// 32 rows x 256 columns = four 32 x 64 boxes of 4 KB (128-byte swizzle).
+constexpr int BOX_COLS = 64;
+constexpr int BOX_BYTES = 32 * BOX_COLS * 2;
+constexpr int STAGING_BYTES = 4 * 4 * BOX_BYTES;  // 64 KB
+constexpr int BAR_BYTES = 256;
+constexpr int SMEM_LIMIT = 232448;                // 227 KB per CTA on sm_103a
+
+template <bool STAGED> struct Cfg {
+    static constexpr int STAGES = STAGED ? 3 : 4;
+    static constexpr int RING_BYTES = STAGES * STAGE_BYTES;
+    static constexpr int STAGING = STAGED ? STAGING_BYTES : 0;
+    static constexpr int SLACK = STAGED ? (SMEM_LIMIT - RING_BYTES - STAGING_BYTES - BAR_BYTES) : 1024;
+    static constexpr int SMEM_BYTES = RING_BYTES + STAGING + BAR_BYTES + SLACK;
+    static_assert(SMEM_BYTES <= SMEM_LIMIT, "shared memory budget");
+    static_assert(SF_COL0 + STAGES * SF_STAGE_COLS <= TMEM_COLS, "TMEM budget");
+};
 static_assert(STAGE_BYTES % 1024 == 0, "stage tiles must stay 1024-byte aligned for the 128B swizzle");
-static_assert(SF_COL0 + STAGES * SF_STAGE_COLS <= TMEM_COLS, "TMEM budget");
 
 // Instruction descriptor, kind::mxf4nvf4: A and B E2M1 (format 1), both K-major,
 // N>>3 at bit 17, scale format UE4M3 (bit 23 = 0), M>>4 at bit 24.
 constexpr uint32_t IDESC = (1u << 7) | (1u << 10) | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
+static_assert(IDESC == 0x08400480u, "instruction descriptor");
 
 struct Params {
     const uint8_t* sfa;
@@ -88,12 +112,17 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
                  :: "r"(dst), "l"(src), "r"(bytes), "r"(bar) : "memory");
 }
 
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* tm, uint32_t src, int x, int y) {
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];"
+                 :: "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y), "r"(src) : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+__device__ __forceinline__ void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
-
-__device__ __forceinline__ void tc_cp_sf(uint32_t taddr, uint64_t desc) {
-    asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" :: "r"(taddr), "l"(desc) : "memory");
-}
 
 __device__ __forceinline__ void tc_mma(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t sfa,
                                        uint32_t sfb, uint32_t accumulate) {
@@ -122,35 +151,127 @@ __device__ __forceinline__ void tmem_ld_32cols(uint32_t taddr, uint32_t (&v)[32]
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
+// Each thread writes 16 consecutive 32-bit TMEM columns of its lane.
+__device__ __forceinline__ void tmem_st_16cols(uint32_t taddr, const uint32_t (&v)[16]) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};"
+                 :: "r"(taddr), "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
+                    "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]) : "memory");
+}
+__device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
 // Shared-memory matrix descriptor: K-major, 128-byte swizzle, 8-row groups 1024 B apart.
 __device__ __forceinline__ uint64_t desc_sw128(uint32_t saddr) {
     return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)1 << 16) | ((uint64_t)(1024 >> 4) << 32) |
            ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
 }
-// Descriptor of a 32-row x 16-byte scale block (no swizzle, 8-row groups 128 B apart).
-__device__ __forceinline__ uint64_t desc_sf(uint32_t saddr) {
-    return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)(128 >> 4) << 32) | ((uint64_t)1 << 46);
+
+// Epilogue for one 32-row x 256-column slice (one warp): TMEM -> alpha -> global.
+// Direct stores: each lane writes its row (bf16 or fp32), masked at the edges.
+__device__ __forceinline__ void epilogue_direct(const Params& p, uint32_t tmem_row, int row, int n0, float alpha) {
+    for (int c = 0; c < BN / 32; ++c) {
+        const int nb = n0 + c * 32;
+        if (nb >= p.N) break;                        // warp-uniform
+        uint32_t v[32];
+        tmem_ld_32cols(tmem_row + ACC_COL + c * 32, v);
+        if (row >= p.M) continue;
+        const bool full_chunk = (nb + 32 <= p.N) && p.vec_store;
+        if (p.d_bf16) {
+            __nv_bfloat16* drow = reinterpret_cast<__nv_bfloat16*>(p.D) + (int64_t)row * p.ldd + nb;
+            if (full_chunk) {
+                uint32_t w[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    __nv_bfloat162 h = __floats2bfloat162_rn(__fmul_rn(__uint_as_float(v[2 * i]), alpha),
+                                                             __fmul_rn(__uint_as_float(v[2 * i + 1]), alpha));
+                    w[i] = *reinterpret_cast<uint32_t*>(&h);
+                }
+                uint4* d4 = reinterpret_cast<uint4*>(drow);
+#pragma unroll
+                for (int i = 0; i < 4; ++i) d4[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+            } else {
+#pragma unroll
+                for (int i = 0; i < 32; ++i)
+                    if (nb + i < p.N) drow[i] = __float2bfloat16_rn(__fmul_rn(__uint_as_float(v[i]), alpha));
+            }
+        } else {
+            float* drow = reinterpret_cast<float*>(p.D) + (int64_t)row * p.ldd + nb;
+            if (full_chunk) {
+                float4* d4 = reinterpret_cast<float4*>(drow);
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                    d4[i] = make_float4(__fmul_rn(__uint_as_float(v[4 * i]), alpha),
+                                        __fmul_rn(__uint_as_float(v[4 * i + 1]), alpha),
+                                        __fmul_rn(__uint_as_float(v[4 * i + 2]), alpha),
+                                        __fmul_rn(__uint_as_float(v[4 * i + 3]), alpha));
+            } else {
+#pragma unroll
+                for (int i = 0; i < 32; ++i)
+                    if (nb + i < p.N) drow[i] = __fmul_rn(__uint_as_float(v[i]), alpha);
+            }
+        }
+    }
 }
 
+// Staged bf16 epilogue, part 1: TMEM -> alpha -> bf16 -> this warp's four 32 x 64
+// boxes in shared memory, 128-byte swizzled (16-byte chunk c of row r at chunk
+// c ^ (r & 7)), the layout the TMA store expects.  Lane = row within the slice.
+__device__ __forceinline__ void epilogue_to_smem(uint32_t tmem_row, uint8_t* stg, int lane, float alpha) {
+#pragma unroll 1
+    for (int b = 0; b < BN / BOX_COLS; ++b) {
+        uint32_t v[32], u[32];
+        tmem_ld_32cols(tmem_row + ACC_COL + b * BOX_COLS, v);
+        tmem_ld_32cols(tmem_row + ACC_COL + b * BOX_COLS + 32, u);
+        uint32_t w[32];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            __nv_bfloat162 h0 = __floats2bfloat162_rn(__fmul_rn(__uint_as_float(v[2 * i]), alpha),
+                                                      __fmul_rn(__uint_as_float(v[2 * i + 1]), alpha));
+            __nv_bfloat162 h1 = __floats2bfloat162_rn(__fmul_rn(__uint_as_float(u[2 * i]), alpha),
+                                                      __fmul_rn(__uint_as_float(u[2 * i + 1]), alpha));
+            w[i] = *reinterpret_cast<uint32_t*>(&h0);
+            w[16 + i] = *reinterpret_cast<uint32_t*>(&h1);
+        }
+        uint8_t* row = stg + b * BOX_BYTES + lane * 128;
+#pragma unroll
+        for (int c = 0; c < 8; ++c)
+            *reinterpret_cast<uint4*>(row + ((c ^ (lane & 7)) << 4)) =
+                make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
+    }
+}
+
+template <bool STAGED>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
 gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                  const Params p) {
+                  const __grid_constant__ CUtensorMap tmD, const Params p) {
+    using C = Cfg<STAGED>;
+    constexpr int STAGES = C::STAGES;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint64_t* full = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
+    uint8_t* staging = smem + C::RING_BYTES;
+    uint64_t* full = reinterpret_cast<uint64_t*>(staging + C::STAGING);
     uint64_t* empty = full + STAGES;
     uint64_t* acc_full = empty + STAGES;
     uint64_t* acc_empty = acc_full + 1;
     uint64_t* drain = acc_empty + 1;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+    uint64_t* sf_loaded = drain + 1;                     // scale tiles of a stage have landed in smem
+    uint64_t* sf_ready = sf_loaded + STAGES;             // ... and have been written to TMEM
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sf_ready + STAGES);
     volatile uint32_t* abort_flag = tmem_slot + 1;
+    // the carve-out above must fit the dynamic allocation (the base is normally 1024-aligned)
+    const bool layout_ok = (reinterpret_cast<uintptr_t>(tmem_slot + 2) - reinterpret_cast<uintptr_t>(smem_raw)) <=
+                           (uintptr_t)C::SMEM_BYTES;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (!layout_ok) {
+        if (threadIdx.x == 0) set_status(p.dev_status, NVFP4_ERR_UNSUPPORTED);
+        return;
+    }
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) { mbar_init(&full[s], 1); mbar_init(&empty[s], 1); }
         mbar_init(acc_full, 1);
         mbar_init(acc_empty, 4);
         mbar_init(drain, 1);
+        for (int s = 0; s < STAGES; ++s) { mbar_init(&sf_loaded[s], 1); mbar_init(&sf_ready[s], 4); }
         *abort_flag = 0u;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -173,7 +294,7 @@ gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
         for (int tile = blockIdx.x; tile < tiles && ok; tile += gridDim.x) {
             const int mt = tile % p.m_tiles, nt = tile / p.m_tiles;
             const bool second_sfb = (nt * BN + 128) < p.N;
-            const uint32_t bytes = STAGE_BYTES - (second_sfb ? 0 : 2048);
+            const uint32_t sf_bytes = SFA_BYTES + SFB_BYTES - (second_sfb ? 0 : 2048);
             for (int kt = 0; kt < p.nkt; ++kt) {
                 if (!mbar_wait_bounded(&empty[stage], phase ^ 1u, p.timeout_ns, abort_flag, p.dev_status)) {
                     ok = false;
@@ -183,14 +304,16 @@ gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                 uint8_t* sB = sA + A_BYTES;
                 uint8_t* sSFA = sB + B_BYTES;
                 uint8_t* sSFB = sSFA + SFA_BYTES;
+                const uint32_t sbar = smem_addr(&sf_loaded[stage]);
+                mbar_arrive_expect_tx(&sf_loaded[stage], sf_bytes);
+                bulk_load(smem_addr(sSFA), p.sfa + ((size_t)mt * p.nkt + kt) * 2048u, 2048u, sbar);
+                bulk_load(smem_addr(sSFB), p.sfb + ((size_t)(2 * nt) * p.nkt + kt) * 2048u, 2048u, sbar);
+                if (second_sfb)
+                    bulk_load(smem_addr(sSFB + 2048), p.sfb + ((size_t)(2 * nt + 1) * p.nkt + kt) * 2048u, 2048u, sbar);
                 const uint32_t bar = smem_addr(&full[stage]);
-                mbar_arrive_expect_tx(&full[stage], bytes);
+                mbar_arrive_expect_tx(&full[stage], A_BYTES + B_BYTES);
                 tma_load_2d(smem_addr(sA), &tmA, kt * BKB, mt * BM, bar);
                 tma_load_2d(smem_addr(sB), &tmB, kt * BKB, nt * BN, bar);
-                bulk_load(smem_addr(sSFA), p.sfa + ((size_t)mt * p.nkt + kt) * 2048u, 2048u, bar);
-                bulk_load(smem_addr(sSFB), p.sfb + ((size_t)(2 * nt) * p.nkt + kt) * 2048u, 2048u, bar);
-                if (second_sfb)
-                    bulk_load(smem_addr(sSFB + 2048), p.sfb + ((size_t)(2 * nt + 1) * p.nkt + kt) * 2048u, 2048u, bar);
                 issued_mask |= 1u << stage;
                 issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
                 if (++stage == STAGES) { stage = 0; phase ^= 1u; }
@@ -198,8 +321,10 @@ gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
         }
         if (!ok) {   // let every copy this thread started land before the CTA exits
             for (int s = 0; s < STAGES; ++s)
-                if (issued_mask & (1u << s))
+                if (issued_mask & (1u << s)) {
                     mbar_wait_bounded(&full[s], (issued_phase >> s) & 1u, p.timeout_ns, nullptr, p.dev_status);
+                    mbar_wait_bounded(&sf_loaded[s], (issued_phase >> s) & 1u, p.timeout_ns, nullptr, p.dev_status);
+                }
         }
     } else if (warp == 1 && lane == 0) {
         // ------------------------------------------------ MMA issuer
@@ -212,23 +337,15 @@ gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
             }
             tc_fence_after();
             for (int kt = 0; kt < p.nkt; ++kt) {
-                if (!mbar_wait_bounded(&full[stage], phase, p.timeout_ns, abort_flag, p.dev_status)) {
+                if (!mbar_wait_bounded(&full[stage], phase, p.timeout_ns, abort_flag, p.dev_status) ||
+                    !mbar_wait_bounded(&sf_ready[stage], phase, p.timeout_ns, abort_flag, p.dev_status)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
                 const uint32_t sA = smem_addr(smem + stage * STAGE_BYTES);
                 const uint32_t sB = sA + A_BYTES;
-                const uint32_t sSFA = sB + B_BYTES;
-                const uint32_t sSFB = sSFA + SFA_BYTES;
                 const uint32_t tsf = tmem + SF_COL0 + stage * SF_STAGE_COLS;
-#pragma unroll
-                for (int j = 0; j < 4; ++j) tc_cp_sf(tsf + 4 * j, desc_sf(sSFA + 512 * j));
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    tc_cp_sf(tsf + 16 + 8 * j, desc_sf(sSFB + 512 * j));
-                    tc_cp_sf(tsf + 16 + 8 * j + 4, desc_sf(sSFB + 2048 + 512 * j));
-                }
                 const uint64_t da = desc_sw128(sA), db = desc_sw128(sB);
 #pragma unroll
                 for (int j = 0; j < 4; ++j)
@@ -246,63 +363,91 @@ gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
             tc_commit(smem_addr(drain));
             mbar_wait_bounded(drain, 0u, p.timeout_ns, nullptr, p.dev_status);
         }
+    } else if (warp >= 6) {
+        // ------------------------------------------------ scale loaders: smem -> registers -> TMEM
+        // Warp w writes TMEM lanes 32*(w%4)..+31.  Lane i of every warp writes the same
+        // 16-byte rows: row i of each 512-byte scale atom holds the scales of tile rows
+        // i, i+32, i+64, i+96, so TMEM lane i (of every lane quarter), column c gets
+        // row 32c + i -- the operand layout of the block-scaled MMA (M = 128 for A;
+        // two 128-row halves side by side for the 256-row B tile).
+        const int q = warp & 3;
+        const uint32_t tq = tmem + ((uint32_t)(q * 32) << 16);
+        uint32_t stage = 0, phase = 0;
+        bool ok = true;
+        for (int tile = blockIdx.x; tile < tiles && ok; tile += gridDim.x) {
+            for (int kt = 0; kt < p.nkt; ++kt) {
+                // sf_loaded[s] completes only after the producer refilled the stage, which
+                // waited for the MMAs that last read this TMEM slot: the slot is free.
+                if (!mbar_wait_bounded(&sf_loaded[stage], phase, p.timeout_ns, abort_flag, p.dev_status)) {
+                    ok = false;
+                    break;
+                }
+                const uint8_t* sSFA = smem + stage * STAGE_BYTES + A_BYTES + B_BYTES;
+                const uint8_t* sSFB = sSFA + SFA_BYTES;
+                uint32_t va[16], vb0[16], vb1[16];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const uint4 a4 = *reinterpret_cast<const uint4*>(sSFA + 512 * j + 16 * lane);
+                    va[4 * j] = a4.x; va[4 * j + 1] = a4.y; va[4 * j + 2] = a4.z; va[4 * j + 3] = a4.w;
+                }
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+#pragma unroll
+                    for (int nb = 0; nb < 2; ++nb) {
+                        const uint4 b4 = *reinterpret_cast<const uint4*>(sSFB + 2048 * nb + 512 * j + 16 * lane);
+                        const int o = 8 * j + 4 * nb;          // SFB column of this atom, k-step j
+                        uint32_t* dst = o < 16 ? vb0 : vb1;
+                        dst[(o & 15)] = b4.x; dst[(o & 15) + 1] = b4.y; dst[(o & 15) + 2] = b4.z; dst[(o & 15) + 3] = b4.w;
+                    }
+                }
+                const uint32_t tsf = tq + SF_COL0 + stage * SF_STAGE_COLS;
+                tmem_st_16cols(tsf, va);
+                tmem_st_16cols(tsf + 16, vb0);
+                tmem_st_16cols(tsf + 32, vb1);
+                tmem_st_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&sf_ready[stage]);
+                if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+            }
+        }
     } else if (warp >= 2) {
         // ------------------------------------------------ epilogue
         const int q = warp & 3;                          // TMEM lane quarter of this warp
         const float alpha = __fmul_rn(*p.sdec_a, *p.sdec_b);
+        const uint32_t tmem_row = tmem + ((uint32_t)(q * 32) << 16);
+        uint8_t* stg = staging + q * (4 * BOX_BYTES);
         uint32_t acc_phase = 0;
         for (int tile = blockIdx.x; tile < tiles; tile += gridDim.x) {
             const int mt = tile % p.m_tiles, nt = tile / p.m_tiles;
+            const int m0 = mt * BM + q * 32, n0 = nt * BN;
             if (!mbar_wait_bounded(acc_full, acc_phase, p.timeout_ns, abort_flag, p.dev_status)) break;
             tc_fence_after();
-            const int row = mt * BM + q * 32 + lane;
-            const int n0 = nt * BN;
-            for (int c = 0; c < BN / 32; ++c) {
-                const int nb = n0 + c * 32;
-                if (nb >= p.N) break;                    // warp-uniform
-                uint32_t v[32];
-                tmem_ld_32cols(tmem + ((uint32_t)(q * 32) << 16) + ACC_COL + c * 32, v);
-                if (row >= p.M) continue;
-                const bool full_chunk = (nb + 32 <= p.N) && p.vec_store;
-                if (p.d_bf16) {
-                    __nv_bfloat16* drow = reinterpret_cast<__nv_bfloat16*>(p.D) + (int64_t)row * p.ldd + nb;
-                    if (full_chunk) {
-                        uint32_t w[16];
-#pragma unroll
-                        for (int i = 0; i < 16; ++i) {
-                            __nv_bfloat162 h = __floats2bfloat162_rn(__fmul_rn(__uint_as_float(v[2 * i]), alpha),
-                                                                     __fmul_rn(__uint_as_float(v[2 * i + 1]), alpha));
-                            w[i] = *reinterpret_cast<uint32_t*>(&h);
-                        }
-                        uint4* d4 = reinterpret_cast<uint4*>(drow);
-#pragma unroll
-                        for (int i = 0; i < 4; ++i) d4[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
-                    } else {
-#pragma unroll
-                        for (int i = 0; i < 32; ++i)
-                            if (nb + i < p.N) drow[i] = __float2bfloat16_rn(__fmul_rn(__uint_as_float(v[i]), alpha));
-                    }
-                } else {
-                    float* drow = reinterpret_cast<float*>(p.D) + (int64_t)row * p.ldd + nb;
-                    if (full_chunk) {
-                        float4* d4 = reinterpret_cast<float4*>(drow);
-#pragma unroll
-                        for (int i = 0; i < 8; ++i)
-                            d4[i] = make_float4(__fmul_rn(__uint_as_float(v[4 * i]), alpha),
-                                                __fmul_rn(__uint_as_float(v[4 * i + 1]), alpha),
-                                                __fmul_rn(__uint_as_float(v[4 * i + 2]), alpha),
-                                                __fmul_rn(__uint_as_float(v[4 * i + 3]), alpha));
-                    } else {
-#pragma unroll
-                        for (int i = 0; i < 32; ++i)
-                            if (nb + i < p.N) drow[i] = __fmul_rn(__uint_as_float(v[i]), alpha);
-                    }
-                }
+            if constexpr (STAGED) {
+                // the previous tile's stores must have finished reading this warp's boxes
+                if (lane == 0) bulk_wait_read0();
+                __syncwarp();
+                epilogue_to_smem(tmem_row, stg, lane, alpha);
+            } else {
+                epilogue_direct(p, tmem_row, m0 + lane, n0, alpha);
             }
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(acc_empty);
+            if (lane == 0) mbar_arrive(acc_empty);       // the MMA may start the next tile now
+            if constexpr (STAGED) {
+                fence_proxy_async_smem();                // generic-proxy writes -> visible to TMA
+                __syncwarp();
+                if (lane == 0 && m0 < p.M) {
+                    for (int b = 0; b < BN / BOX_COLS; ++b)
+                        if (n0 + b * BOX_COLS < p.N) tma_store_2d(&tmD, smem_addr(stg + b * BOX_BYTES), n0 + b * BOX_COLS, m0);
+                    bulk_commit();
+                }
+            }
             acc_phase ^= 1u;
+        }
+        if constexpr (STAGED) {
+            if (lane == 0) bulk_wait0();
+            __syncwarp();
         }
     }
 
@@ -342,6 +487,33 @@ bool make_codes_map(CUtensorMap* m, const void* codes, int64_t rows, int64_t col
     return r == CUDA_SUCCESS;
 }
 
+// bf16 D [M, N] (pitch ldd elements): 64 x 32 boxes, 128-byte swizzle, for the TMA stores.
+bool make_out_map(CUtensorMap* m, void* D, int64_t M, int64_t N, int64_t ldd) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {(cuuint64_t)N, (cuuint64_t)M};
+    cuuint64_t strides[1] = {(cuuint64_t)(ldd * 2)};
+    cuuint32_t box[2] = {(cuuint32_t)BOX_COLS, 32u};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, D, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+template <bool STAGED>
+cudaError_t launch(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& td, const Params& p, int grid,
+                   cudaStream_t stream) {
+    static std::once_flag once;
+    static cudaError_t attr_err = cudaSuccess;
+    std::call_once(once, [] {
+        attr_err = cudaFuncSetAttribute(gemm_nvfp4_kernel<STAGED>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        Cfg<STAGED>::SMEM_BYTES);
+    });
+    if (attr_err != cudaSuccess) return attr_err;
+    gemm_nvfp4_kernel<STAGED><<<grid, NUM_THREADS, Cfg<STAGED>::SMEM_BYTES, stream>>>(ta, tb, td, p);
+    return cudaGetLastError();
+}
+
 }  // namespace gemm
 
 nvfp4_status gemm_impl(const nvfp4_qtensor* A, const nvfp4_qtensor* B, void* D, int32_t d_dtype, int64_t ldd,
@@ -365,13 +537,6 @@ nvfp4_status gemm_impl(const nvfp4_qtensor* A, const nvfp4_qtensor* B, void* D, 
 
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return NVFP4_ERR_CUDA;
-    static std::once_flag attr_once;
-    static cudaError_t attr_err = cudaSuccess;
-    std::call_once(attr_once, [] {
-        attr_err = cudaFuncSetAttribute(gemm_nvfp4_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
-    });
-    if (attr_err != cudaSuccess) return NVFP4_ERR_CUDA;
-
     Params p;
     p.sfa = A->scales_mma;
     p.sfb = B->scales_mma;
@@ -391,9 +556,12 @@ nvfp4_status gemm_impl(const nvfp4_qtensor* A, const nvfp4_qtensor* B, void* D, 
     p.timeout_ns = wait_timeout_ns();
     const int tiles = p.m_tiles * p.n_tiles;
     const int grid = std::max(1, std::min(tiles, sm_count(dev)));
-    gemm_nvfp4_kernel<<<grid, NUM_THREADS, SMEM_BYTES, stream>>>(ta, tb, p);
-    if (cudaGetLastError() != cudaSuccess) return NVFP4_ERR_CUDA;
-    return NVFP4_OK;
+    // bf16 output with a 16-byte aligned base and pitch goes through the staged TMA-store epilogue
+    CUtensorMap td;
+    const bool staged = p.d_bf16 && p.vec_store && make_out_map(&td, D, M, N, ldd);
+    if (!staged) std::memset(&td, 0, sizeof(td));
+    const cudaError_t e = staged ? launch<true>(ta, tb, td, p, grid, stream) : launch<false>(ta, tb, td, p, grid, stream);
+    return e == cudaSuccess ? NVFP4_OK : NVFP4_ERR_CUDA;
 }
 
 }  // namespace nvfp4
