@@ -37,6 +37,23 @@ def env_rank():
     return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), int(os.environ.get("LOCAL_RANK", 0))
 
 
+def gemm_traffic_bytes():
+    """DRAM bytes per GEMM launch from the committed ncu summary, if it was taken
+    on the current gemm.cu (else None: the counters are stale)."""
+    import hashlib
+    import re
+    try:
+        src = open(os.path.join(ROOT, "nvfp4_bit_quantized_gb300", "csrc", "gemm.cu"), "rb").read()
+        txt = open(os.path.join(ROOT, "profiles", "gemm_nvfp4_ffn_up_8192x5120x20480.md")).read()
+    except OSError:
+        return None
+    sha = re.search(r"source_sha256:\s*([0-9a-f]{64})", txt)
+    tr = re.search(r"traffic_bytes_per_launch:\s*(\d+)", txt)
+    if not sha or not tr or sha.group(1) != hashlib.sha256(src).hexdigest():
+        return None
+    return int(tr.group(1))
+
+
 def measured_peaks():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -300,7 +317,7 @@ def run_ours(args):
         "ms_breakdown": {k: round(v, 4) for k, v in per.items()},
         "quantize_ms_per_step": round(quant_ms, 4),
         "roofline": {"bound": "tensor", "achieved": round(achieved, 1), "peak": round(fp4_peak, 1),
-                     "unit": "TFLOP/s", "frac": round(achieved / fp4_peak, 4), "traffic": None,
+                     "unit": "TFLOP/s", "frac": round(achieved / fp4_peak, 4), "traffic": gemm_traffic_bytes(),
                      "kernel": "gemm_nvfp4_kernel",
                      "peak_source": f"{peak_src} bf16 sustained x {FP4_PER_BF16:g} (nominal dense FP4:BF16)"},
         "quantize_roofline": {"bound": "hbm", "achieved": round(sum(qbytes.values()) / (quant_ms * 1e-3) / 1e9, 1),

@@ -230,6 +230,11 @@ NVFP4_API nvfp4_status nvfp4_debug_e2m1(const float* y, const uint32_t* r16, int
                               uint8_t* out, void* stream);
 NVFP4_API nvfp4_status nvfp4_debug_philox(const uint32_t* ctr, int64_t n, uint64_t key, uint32_t* out, void* stream);
 NVFP4_API nvfp4_status nvfp4_selftest_wait_timeout(uint64_t timeout_ns, uint32_t* dev_status, void* stream);
+/* GEMM kernel choice, process-wide, for tests: 0 = automatic (the CTA-pair
+   kernel for bf16 outputs with at least one 256 x 256 tile per SM pair, else
+   the single-CTA kernel), 1 = always single-CTA, 2 = CTA-pair wherever its
+   epilogue applies (bf16, 16-byte aligned output). */
+NVFP4_API void nvfp4_gemm_force_path(int32_t path);
 
 #ifdef __cplusplus
 }

@@ -459,6 +459,287 @@ gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
     }
 }
 
+// ============================================================================
+// CTA-pair kernel (tcgen05 cta_group::2): one 256 x 256 output tile per pair of
+// SMs.  The leader CTA (cluster rank 0) issues MMAs with M = 256: rows 0-127 of
+// the tile come from the leader's A tile, rows 128-255 from the follower's, and
+// the 256 B rows (N) are split the same way; each CTA's TMEM receives its own
+// 128 rows of the accumulator.  Per CTA and stage the ring holds A 16 KB +
+// B 16 KB + scales 6 KB = 38 KB (instead of 54 KB), so 4 stages fit next to the
+// 64 KB output staging, and each SM pulls a third less from L2.
+// Cross-CTA signals: the leader's MMA commits are multicast to both CTAs' barriers;
+// the follower's scale warps and epilogue warps arrive remotely on the leader's
+// sf_ready / acc_empty barriers.  Codes and scales are loaded CTA-locally.
+// ============================================================================
+constexpr int P_B_BYTES = 128 * BKB;                                   // half of N per CTA
+constexpr int P_STAGE_BYTES = A_BYTES + P_B_BYTES + SFA_BYTES + SFB_BYTES;   // 38 KB
+constexpr int P_STAGES = 4;
+constexpr int P_RING_BYTES = P_STAGES * P_STAGE_BYTES;
+constexpr int P_SLACK = SMEM_LIMIT - P_RING_BYTES - STAGING_BYTES - BAR_BYTES;
+constexpr int P_SMEM_BYTES = P_RING_BYTES + STAGING_BYTES + BAR_BYTES + P_SLACK;
+static_assert(P_STAGE_BYTES % 1024 == 0, "pair stages must stay 1024-byte aligned");
+static_assert(P_SLACK >= 0 && P_SMEM_BYTES <= SMEM_LIMIT, "pair shared memory budget");
+static_assert(SF_COL0 + P_STAGES * SF_STAGE_COLS <= TMEM_COLS, "pair TMEM budget");
+// M = 256 (both CTAs), N = 256
+constexpr uint32_t IDESC_PAIR = (1u << 7) | (1u << 10) | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(256 >> 4) << 24);
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+// Address of the same shared variable in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t map_to_rank(uint32_t saddr, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+    return r;
+}
+// Arrive on a barrier of another CTA of the cluster.  Default (CTA-scope) semantics:
+// what it guards is already complete when it is issued (tcgen05.wait::st for the
+// scale writes, a local TMA barrier for the codes tiles, tcgen05.ld for the
+// accumulator), and a cluster-scope release fence on every k-tile stalled the
+// issuing warps (membar) for most of the run time.
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
+    asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" :: "r"(cluster_addr) : "memory");
+}
+__device__ __forceinline__ void tc_mma_pair(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t sfa,
+                                            uint32_t sfb, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%5], [%6], p;\n\t}"
+        :: "r"(d), "l"(a), "l"(b), "r"(idesc), "r"(accumulate), "r"(sfa), "r"(sfb) : "memory");
+}
+// Arrive on the barrier at this offset in both CTAs of the pair when the MMAs issued so far complete.
+__device__ __forceinline__ void tc_commit_pair(uint32_t bar) {
+    asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;"
+                 :: "r"(bar), "h"((uint16_t)0x3) : "memory");
+}
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
+gemm_nvfp4_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                       const __grid_constant__ CUtensorMap tmD, const Params p) {
+    constexpr int STAGES = P_STAGES;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* staging = smem + P_RING_BYTES;
+    uint64_t* full = reinterpret_cast<uint64_t*>(staging + STAGING_BYTES);   // local A/B landed
+    uint64_t* empty = full + STAGES;                     // both CTAs' stage consumed (leader's commit)
+    uint64_t* sf_loaded = empty + STAGES;                // local scale tiles landed
+    uint64_t* sf_ready = sf_loaded + STAGES;             // leader: 8 warps wrote scales and saw their A/B
+    uint64_t* acc_full = sf_ready + STAGES;              // accumulator complete (leader's commit)
+    uint64_t* acc_empty = acc_full + 1;                  // leader: 8 epilogue warps drained
+    uint64_t* drain = acc_empty + 1;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+    volatile uint32_t* abort_flag = tmem_slot + 1;
+    // identical in both CTAs (same kernel, same dynamic smem base), so layout_ok is uniform
+    const bool layout_ok = (reinterpret_cast<uintptr_t>(tmem_slot + 2) - reinterpret_cast<uintptr_t>(smem_raw)) <=
+                           (uintptr_t)P_SMEM_BYTES;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_rank();
+    const bool leader = rank == 0;
+    if (!layout_ok) {
+        if (threadIdx.x == 0) set_status(p.dev_status, NVFP4_ERR_UNSUPPORTED);
+        return;
+    }
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+            mbar_init(&sf_loaded[s], 1);
+            mbar_init(&sf_ready[s], 8);
+        }
+        mbar_init(acc_full, 1);
+        mbar_init(acc_empty, 8);
+        mbar_init(drain, 1);
+        *abort_flag = 0u;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == 1) {    // one warp in each CTA of the pair allocates collectively
+        asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;"
+                     :: "r"(smem_addr(tmem_slot)), "r"(TMEM_COLS) : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    cluster_sync();                                      // barriers initialised in both CTAs
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const int m_pairs = (p.M + 255) / 256;
+    const int tiles = m_pairs * p.n_tiles;
+    const int cluster = blockIdx.x >> 1, nclusters = gridDim.x >> 1;
+    const uint32_t sf_ready_leader = map_to_rank(smem_addr(&sf_ready[0]), 0);
+    const uint32_t acc_empty_leader = map_to_rank(smem_addr(acc_empty), 0);
+
+    if (warp == 0 && lane == 0) {
+        // ------------------------------------------------ TMA producer (each CTA, its own halves)
+        uint32_t stage = 0, phase = 0;
+        uint32_t issued_mask = 0, issued_phase = 0;
+        bool ok = true;
+        for (int tile = cluster; tile < tiles && ok; tile += nclusters) {
+            const int mp = tile % m_pairs, nt = tile / m_pairs;
+            const int mrow = mp * 256 + (int)rank * 128;          // this CTA's A rows
+            const int nrow = nt * BN + (int)rank * 128;           // this CTA's B rows
+            const bool second_sfb = (nt * BN + 128) < p.N;
+            // rows past M (the follower's half of the last pair tile) have no scale block:
+            // their codes load as zeros and their output rows are never stored
+            const bool has_sfa = mrow < p.M;
+            const uint32_t sf_bytes = (has_sfa ? SFA_BYTES : 0) + SFB_BYTES - (second_sfb ? 0 : 2048);
+            for (int kt = 0; kt < p.nkt; ++kt) {
+                if (!mbar_wait_bounded(&empty[stage], phase ^ 1u, p.timeout_ns, abort_flag, p.dev_status)) {
+                    ok = false;
+                    break;
+                }
+                uint8_t* sA = smem + stage * P_STAGE_BYTES;
+                uint8_t* sB = sA + A_BYTES;
+                uint8_t* sSFA = sB + P_B_BYTES;
+                uint8_t* sSFB = sSFA + SFA_BYTES;
+                const uint32_t sbar = smem_addr(&sf_loaded[stage]);
+                mbar_arrive_expect_tx(&sf_loaded[stage], sf_bytes);
+                if (has_sfa) bulk_load(smem_addr(sSFA), p.sfa + ((size_t)(mrow / 128) * p.nkt + kt) * 2048u, 2048u, sbar);
+                bulk_load(smem_addr(sSFB), p.sfb + ((size_t)(2 * nt) * p.nkt + kt) * 2048u, 2048u, sbar);
+                if (second_sfb)
+                    bulk_load(smem_addr(sSFB + 2048), p.sfb + ((size_t)(2 * nt + 1) * p.nkt + kt) * 2048u, 2048u, sbar);
+                const uint32_t bar = smem_addr(&full[stage]);
+                mbar_arrive_expect_tx(&full[stage], A_BYTES + P_B_BYTES);
+                tma_load_2d(smem_addr(sA), &tmA, kt * BKB, mrow, bar);
+                tma_load_2d(smem_addr(sB), &tmB, kt * BKB, nrow, bar);
+                issued_mask |= 1u << stage;
+                issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
+                if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+            }
+        }
+        if (!ok) {
+            for (int s = 0; s < STAGES; ++s)
+                if (issued_mask & (1u << s)) {
+                    mbar_wait_bounded(&full[s], (issued_phase >> s) & 1u, p.timeout_ns, nullptr, p.dev_status);
+                    mbar_wait_bounded(&sf_loaded[s], (issued_phase >> s) & 1u, p.timeout_ns, nullptr, p.dev_status);
+                }
+        }
+    } else if (warp == 1 && lane == 0 && leader) {
+        // ------------------------------------------------ MMA issuer (leader only)
+        uint32_t stage = 0, phase = 0, acc_phase = 0;
+        bool ok = true, issued = false;
+        for (int tile = cluster; tile < tiles && ok; tile += nclusters) {
+            if (!mbar_wait_bounded(acc_empty, acc_phase ^ 1u, p.timeout_ns, abort_flag, p.dev_status)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            for (int kt = 0; kt < p.nkt; ++kt) {
+                if (!mbar_wait_bounded(&sf_ready[stage], phase, p.timeout_ns, abort_flag, p.dev_status)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t sA = smem_addr(smem + stage * P_STAGE_BYTES);
+                const uint32_t sB = sA + A_BYTES;
+                const uint32_t tsf = tmem + SF_COL0 + stage * SF_STAGE_COLS;
+                const uint64_t da = desc_sw128(sA), db = desc_sw128(sB);
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    tc_mma_pair(tmem + ACC_COL, da + 2 * j, db + 2 * j, IDESC_PAIR, tsf + 4 * j, tsf + 16 + 8 * j,
+                                (kt | j) != 0 ? 1u : 0u);
+                issued = true;
+                tc_commit_pair(smem_addr(&empty[stage]));
+                if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+            }
+            if (!ok) break;
+            tc_commit_pair(smem_addr(acc_full));
+            acc_phase ^= 1u;
+        }
+        if (!ok && issued) {
+            tc_commit_pair(smem_addr(drain));
+            mbar_wait_bounded(drain, 0u, p.timeout_ns, nullptr, p.dev_status);
+        }
+    } else if (warp >= 6) {
+        // ------------------------------------------------ scale loaders (each CTA, its own TMEM)
+        const int q = warp & 3;
+        const uint32_t tq = tmem + ((uint32_t)(q * 32) << 16);
+        uint32_t stage = 0, phase = 0;
+        bool ok = true;
+        for (int tile = cluster; tile < tiles && ok; tile += nclusters) {
+            for (int kt = 0; kt < p.nkt; ++kt) {
+                if (!mbar_wait_bounded(&sf_loaded[stage], phase, p.timeout_ns, abort_flag, p.dev_status)) {
+                    ok = false;
+                    break;
+                }
+                const uint8_t* sSFA = smem + stage * P_STAGE_BYTES + A_BYTES + P_B_BYTES;
+                const uint8_t* sSFB = sSFA + SFA_BYTES;
+                uint32_t va[16], vb0[16], vb1[16];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const uint4 a4 = *reinterpret_cast<const uint4*>(sSFA + 512 * j + 16 * lane);
+                    va[4 * j] = a4.x; va[4 * j + 1] = a4.y; va[4 * j + 2] = a4.z; va[4 * j + 3] = a4.w;
+                }
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+#pragma unroll
+                    for (int nb = 0; nb < 2; ++nb) {
+                        const uint4 b4 = *reinterpret_cast<const uint4*>(sSFB + 2048 * nb + 512 * j + 16 * lane);
+                        const int o = 8 * j + 4 * nb;
+                        uint32_t* dst = o < 16 ? vb0 : vb1;
+                        dst[(o & 15)] = b4.x; dst[(o & 15) + 1] = b4.y; dst[(o & 15) + 2] = b4.z; dst[(o & 15) + 3] = b4.w;
+                    }
+                }
+                const uint32_t tsf = tq + SF_COL0 + stage * SF_STAGE_COLS;
+                tmem_st_16cols(tsf, va);
+                tmem_st_16cols(tsf + 16, vb0);
+                tmem_st_16cols(tsf + 32, vb1);
+                tmem_st_wait();
+                // this CTA's codes tiles must have landed too before the leader may issue
+                if (!mbar_wait_bounded(&full[stage], phase, p.timeout_ns, abort_flag, p.dev_status)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive_cluster(sf_ready_leader + 8u * stage);
+                if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+            }
+        }
+    } else if (warp >= 2) {
+        // ------------------------------------------------ epilogue (each CTA, its 128 rows)
+        const int q = warp & 3;
+        const float alpha = __fmul_rn(*p.sdec_a, *p.sdec_b);
+        const uint32_t tmem_row = tmem + ((uint32_t)(q * 32) << 16);
+        uint8_t* stg = staging + q * (4 * BOX_BYTES);
+        uint32_t acc_phase = 0;
+        for (int tile = cluster; tile < tiles; tile += nclusters) {
+            const int mp = tile % m_pairs, nt = tile / m_pairs;
+            const int m0 = mp * 256 + (int)rank * 128 + q * 32, n0 = nt * BN;
+            if (!mbar_wait_bounded(acc_full, acc_phase, p.timeout_ns, abort_flag, p.dev_status)) break;
+            tc_fence_after();
+            if (lane == 0) bulk_wait_read0();
+            __syncwarp();
+            epilogue_to_smem(tmem_row, stg, lane, alpha);
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cluster(acc_empty_leader);
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0 && m0 < p.M) {
+                for (int b = 0; b < BN / BOX_COLS; ++b)
+                    if (n0 + b * BOX_COLS < p.N) tma_store_2d(&tmD, smem_addr(stg + b * BOX_BYTES), n0 + b * BOX_COLS, m0);
+                bulk_commit();
+            }
+            acc_phase ^= 1u;
+        }
+        if (lane == 0) bulk_wait0();
+        __syncwarp();
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync();                                      // neither CTA leaves while the other may signal it
+    if (warp == 1) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" :: "r"(tmem), "r"(TMEM_COLS) : "memory");
+    }
+}
+
 // ---- host ------------------------------------------------------------------------
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -514,6 +795,31 @@ cudaError_t launch(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorM
     return cudaGetLastError();
 }
 
+cudaError_t launch_pair(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& td, const Params& p,
+                        int pair_tiles, int sms, cudaStream_t stream) {
+    static std::once_flag once;
+    static cudaError_t attr_err = cudaSuccess;
+    static int max_clusters = 0;
+    std::call_once(once, [sms] {
+        attr_err = cudaFuncSetAttribute(gemm_nvfp4_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        P_SMEM_BYTES);
+        if (attr_err != cudaSuccess) return;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(2 * (sms / 2), 1, 1);
+        cfg.blockDim = dim3(NUM_THREADS, 1, 1);
+        cfg.dynamicSmemBytes = P_SMEM_BYTES;
+        int n = 0;
+        if (cudaOccupancyMaxActiveClusters(&n, gemm_nvfp4_pair_kernel, &cfg) != cudaSuccess || n <= 0) n = sms / 2;
+        max_clusters = n;
+    });
+    if (attr_err != cudaSuccess) return attr_err;
+    const int clusters = std::max(1, std::min(pair_tiles, max_clusters));
+    gemm_nvfp4_pair_kernel<<<2 * clusters, NUM_THREADS, P_SMEM_BYTES, stream>>>(ta, tb, td, p);
+    return cudaGetLastError();
+}
+
+int g_force_path = 0;      // 0: automatic, 1: single-CTA kernel, 2: CTA-pair kernel (tests)
+
 }  // namespace gemm
 
 nvfp4_status gemm_impl(const nvfp4_qtensor* A, const nvfp4_qtensor* B, void* D, int32_t d_dtype, int64_t ldd,
@@ -560,11 +866,26 @@ nvfp4_status gemm_impl(const nvfp4_qtensor* A, const nvfp4_qtensor* B, void* D, 
     CUtensorMap td;
     const bool staged = p.d_bf16 && p.vec_store && make_out_map(&td, D, M, N, ldd);
     if (!staged) std::memset(&td, 0, sizeof(td));
-    const cudaError_t e = staged ? launch<true>(ta, tb, td, p, grid, stream) : launch<false>(ta, tb, td, p, grid, stream);
+    // The CTA-pair kernel needs the staged bf16 epilogue and enough 256 x 256 tiles to fill the SMs.
+    const int pair_tiles = (int)((M + 255) / 256) * p.n_tiles;
+    bool pair = staged && (pair_tiles * 2 >= sm_count(dev) || g_force_path == 2);
+    if (g_force_path == 1) pair = false;
+    cudaError_t e;
+    if (pair) {
+        CUtensorMap tb2;      // B boxes of 128 rows (each CTA loads its half of the N tile)
+        if (!make_codes_map(&tb2, B->codes, N, K, 128)) return NVFP4_ERR_CUDA;
+        e = launch_pair(ta, tb2, td, p, pair_tiles, sm_count(dev), stream);
+    } else {
+        e = staged ? launch<true>(ta, tb, td, p, grid, stream) : launch<false>(ta, tb, td, p, grid, stream);
+    }
     return e == cudaSuccess ? NVFP4_OK : NVFP4_ERR_CUDA;
 }
 
 }  // namespace nvfp4
+
+// Test hook: 0 chooses the kernel automatically, 1 forces the single-CTA kernel,
+// 2 forces the CTA-pair kernel where its epilogue applies (bf16, aligned output).
+extern "C" void nvfp4_gemm_force_path(int32_t path) { nvfp4::gemm::g_force_path = (path >= 0 && path <= 2) ? path : 0; }
 
 extern "C" nvfp4_status nvfp4_gemm(const nvfp4_qtensor* A, const nvfp4_qtensor* B, void* D, int32_t d_dtype,
                                    int64_t ldd, uint32_t* dev_status, void* stream) {

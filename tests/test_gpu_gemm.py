@@ -86,3 +86,29 @@ def test_gemm_repeat_is_deterministic(nv):
     d2 = nv.gemm(qa, qb, torch.float32)
     torch.cuda.synchronize()
     assert torch.equal(d1, d2)
+
+
+@pytest.fixture
+def force_path():
+    from nvfp4_bit_quantized_gb300 import _lib as L
+    yield lambda path: L.lib().nvfp4_gemm_force_path(path)
+    L.lib().nvfp4_gemm_force_path(0)
+
+
+@pytest.mark.parametrize("M,N,K", [(256, 256, 256), (512, 768, 1024), (300, 520, 352), (1000, 300, 224),
+                                   (128, 256, 512), (2048, 2048, 2048)])
+def test_single_cta_and_cta_pair_kernels_agree_with_oracle(nv, oracle_mod, force_path, M, N, K):
+    """bf16 output through both GEMM kernels: the single-CTA tcgen05 kernel and the
+    CTA-pair (cta_group::2, M = 256) kernel, ragged edges included."""
+    qa, qb = _operands(nv, M, N, K, seed=M * 7 + N)
+    ref = bf16_round(_ref(oracle_mod, qa, qb, 0))
+    outs = {}
+    for path in (1, 2):
+        force_path(path)
+        nv.reset_status()
+        D = nv.gemm(qa, qb, torch.bfloat16)
+        assert nv.status_query() == 0
+        outs[path] = D.float().cpu().numpy()
+        err = rel_fro(outs[path], ref)
+        assert err <= TOL, (path, err)
+    assert np.array_equal(outs[1], outs[2]) or rel_fro(outs[2], outs[1]) <= 1e-6
