@@ -37,6 +37,13 @@ __device__ __forceinline__ uint4 ld_stream(const void* p) {
     return v;
 }
 
+// 32-byte streaming load (the address must be 32-byte aligned).
+__device__ __forceinline__ void ld_stream32(const void* p, uint32_t (&w)[8]) {
+    asm volatile("ld.global.nc.L1::no_allocate.v8.u32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+                 : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3]), "=r"(w[4]), "=r"(w[5]), "=r"(w[6]), "=r"(w[7])
+                 : "l"(p));
+}
+
 template <typename T> struct Vec;
 template <> struct Vec<uint16_t> {           // bf16 bits
     static constexpr int N = 8;
@@ -139,31 +146,29 @@ __device__ __forceinline__ uint32_t e2m1x4_rn(const float (&y)[4]) {
     return out;
 }
 
-// Stochastic rounding to the E2M1 grid, returned as the (signed) grid value:
-// the conversions above then encode it exactly.
+// Stochastic rounding to the E2M1 grid, returned as the (signed) grid value; the
+// conversions above then encode it exactly (values >= 6 saturate to code 7 there).
+// Decision: round up iff r * 2^-16 < p, p = (a - lo) / (hi - lo), a = |y|.  It is
+// taken on fp32 bit patterns, exactly:
+//   a >= 4   : the grid step is 2 = bit 22 of the fp32 mantissa in [4, 8) (also
+//              right above 6, where both neighbours saturate to 6): up iff the low
+//              22 bits exceed r << 6, i.e. iff bits + 0x3FFFFF - (r << 6) carries
+//              into bit 22; clearing the low 22 bits leaves lo or hi.
+//   a < 4    : a' = a + 2 rounded upward lands in [2, 6), where the grid steps
+//              (0.5 below 2, 1 in [2, 4)) are exactly bit 21 of the mantissa; up
+//              iff the low 21 bits exceed r << 5.  The thresholds lo + r*2^-16*step
+//              lie on a' 's 2^-21 (or 2^-22) grid, so rounding the sum upward keeps
+//              every comparison exact; subtracting 2 afterwards is exact.
+// All integer and fp32 steps are full-rate; this runs ALU-bound, per element.
 __device__ __forceinline__ float e2m1_sr_value(float y, uint32_t r16) {
-    float a = fminf(fabsf(y), 6.0f);
-    float sp = a < 2.0f ? 0.5f : (a < 4.0f ? 1.0f : 2.0f);
-    float inv = a < 2.0f ? 2.0f : (a < 4.0f ? 1.0f : 0.5f);
-    float lo = __fmul_rn(floorf(__fmul_rn(a, inv)), sp);
-    float thr = __fmul_rn(__fmul_rn((float)r16, 1.0f / 65536.0f), sp);
-    float v = (__fsub_rn(a, lo) > thr) ? __fadd_rn(lo, sp) : lo;
-    return copysignf(v, y);
-}
-
-// Stochastic rounding: saturate |y| to 6; grid spacing sp is 0.5 below 2, 1 below 4,
-// 2 above; lo = floor(|y|/sp)*sp; round up iff (|y| - lo) > r * 2^-16 * sp, which is
-// r * 2^-16 < p with p = (|y| - lo)/sp, every step exact in fp32.
-__device__ __forceinline__ uint32_t e2m1_sr_sw(float y, uint32_t r16) {
-    float a = fminf(fabsf(y), 6.0f);
-    float sp = a < 2.0f ? 0.5f : (a < 4.0f ? 1.0f : 2.0f);
-    float inv = a < 2.0f ? 2.0f : (a < 4.0f ? 1.0f : 0.5f);
-    float lo = __fmul_rn(floorf(__fmul_rn(a, inv)), sp);
-    float thr = __fmul_rn(__fmul_rn((float)r16, 1.0f / 65536.0f), sp);
-    float v = (__fsub_rn(a, lo) > thr) ? __fadd_rn(lo, sp) : lo;   // exact grid value
-    uint32_t c = (v > 0.25f) + (v >= 0.75f) + (v > 1.25f) + (v >= 1.75f) +
-                 (v > 2.5f) + (v >= 3.5f) + (v > 5.0f);
-    return c | ((__float_as_uint(y) >> 28) & 8u);
+    const float a = fabsf(y);
+    const bool big = a >= 4.0f;
+    const float ap = big ? a : __fadd_ru(a, 2.0f);
+    const uint32_t mask = big ? 0x003FFFFFu : 0x001FFFFFu;
+    const uint32_t rs = big ? (r16 << 6) : (r16 << 5);
+    const uint32_t t = (__float_as_uint(ap) + mask - rs) & ~mask;
+    const float v = __fsub_rn(__uint_as_float(t), big ? 0.0f : 2.0f);
+    return __uint_as_float(__float_as_uint(v) | (__float_as_uint(y) & 0x80000000u));
 }
 
 // ----------------------------------------------------------------------------
@@ -173,26 +178,40 @@ __device__ __forceinline__ uint32_t e2m1_sr_sw(float y, uint32_t r16) {
 // ----------------------------------------------------------------------------
 struct Philox4 { uint32_t w[4]; };
 
+// The ten round keys, computed once per thread (the key is a launch parameter).
+struct PhiloxKey { uint32_t k0[10], k1[10]; };
+
+__device__ __forceinline__ PhiloxKey philox_key(uint64_t seed) {
+    PhiloxKey k;
+    uint32_t a = (uint32_t)seed, b = (uint32_t)(seed >> 32);
+#pragma unroll
+    for (int i = 0; i < 10; ++i) { k.k0[i] = a; k.k1[i] = b; a += 0x9E3779B9u; b += 0xBB67AE85u; }
+    return k;
+}
+
 __device__ __forceinline__ Philox4 philox4x32_10(uint32_t c0, uint32_t c1, uint32_t c2, uint32_t c3,
-                                                 uint32_t k0, uint32_t k1) {
+                                                 const PhiloxKey& key) {
 #pragma unroll
     for (int i = 0; i < 10; ++i) {
         const uint32_t hi_a = __umulhi(0xD2511F53u, c0), lo_a = 0xD2511F53u * c0;
         const uint32_t hi_b = __umulhi(0xCD9E8D57u, c2), lo_b = 0xCD9E8D57u * c2;
-        const uint32_t n0 = hi_b ^ c1 ^ k0;
-        const uint32_t n2 = hi_a ^ c3 ^ k1;
+        const uint32_t n0 = hi_b ^ c1 ^ key.k0[i];
+        const uint32_t n2 = hi_a ^ c3 ^ key.k1[i];
         c0 = n0; c1 = lo_b; c2 = n2; c3 = lo_a;
-        k0 += 0x9E3779B9u; k1 += 0xBB67AE85u;
     }
     Philox4 r;
     r.w[0] = c0; r.w[1] = c1; r.w[2] = c2; r.w[3] = c3;
     return r;
 }
 
+__device__ __forceinline__ Philox4 philox4x32_10(uint32_t c0, uint32_t c1, uint32_t c2, uint32_t c3,
+                                                 uint32_t k0, uint32_t k1) {
+    return philox4x32_10(c0, c1, c2, c3, philox_key(((uint64_t)k1 << 32) | k0));
+}
+
 // The 16 random bits of element `idx` come from call idx>>3: half (idx&1) of word (idx>>1)&3.
-__device__ __forceinline__ Philox4 sr_philox(uint64_t seed, uint32_t stream, uint32_t offset, uint64_t group) {
-    return philox4x32_10((uint32_t)group, (uint32_t)(group >> 32), stream, offset,
-                         (uint32_t)seed, (uint32_t)(seed >> 32));
+__device__ __forceinline__ Philox4 sr_philox(const PhiloxKey& key, uint32_t stream, uint32_t offset, uint64_t group) {
+    return philox4x32_10((uint32_t)group, (uint32_t)(group >> 32), stream, offset, key);
 }
 __device__ __forceinline__ uint32_t sr_r16(const Philox4& p, int j) {   // j = idx & 7
     const uint32_t w = p.w[(j >> 1) & 3];

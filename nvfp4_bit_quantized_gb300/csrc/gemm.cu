@@ -138,6 +138,32 @@ __device__ __forceinline__ void tc_commit(uint32_t bar) {
                  :: "r"(bar) : "memory");
 }
 
+__device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// Ties 32 registers written by an asynchronous tcgen05.ld to a point after the
+// tcgen05.wait::ld that precedes it: the compiler sees them modified here, so no
+// use of them can be scheduled before the wait.
+__device__ __forceinline__ void reg_fence32(uint32_t (&v)[32]) {
+    asm volatile(""
+                 : "+r"(v[0]), "+r"(v[1]), "+r"(v[2]), "+r"(v[3]), "+r"(v[4]), "+r"(v[5]), "+r"(v[6]), "+r"(v[7]),
+                   "+r"(v[8]), "+r"(v[9]), "+r"(v[10]), "+r"(v[11]), "+r"(v[12]), "+r"(v[13]), "+r"(v[14]),
+                   "+r"(v[15]), "+r"(v[16]), "+r"(v[17]), "+r"(v[18]), "+r"(v[19]), "+r"(v[20]), "+r"(v[21]),
+                   "+r"(v[22]), "+r"(v[23]), "+r"(v[24]), "+r"(v[25]), "+r"(v[26]), "+r"(v[27]), "+r"(v[28]),
+                   "+r"(v[29]), "+r"(v[30]), "+r"(v[31]));
+}
+
+__device__ __forceinline__ void tmem_ld_32cols_nowait(uint32_t taddr, uint32_t (&v)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+        : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]),
+          "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15]),
+          "=r"(v[16]), "=r"(v[17]), "=r"(v[18]), "=r"(v[19]), "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]),
+          "=r"(v[24]), "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]), "=r"(v[31])
+        : "r"(taddr) : "memory");
+}
+
 __device__ __forceinline__ void tmem_ld_32cols(uint32_t taddr, uint32_t (&v)[32]) {
     asm volatile(
         "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
@@ -149,6 +175,7 @@ __device__ __forceinline__ void tmem_ld_32cols(uint32_t taddr, uint32_t (&v)[32]
           "=r"(v[24]), "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]), "=r"(v[31])
         : "r"(taddr));
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+    reg_fence32(v);
 }
 
 // Each thread writes 16 consecutive 32-bit TMEM columns of its lane.
@@ -212,31 +239,57 @@ __device__ __forceinline__ void epilogue_direct(const Params& p, uint32_t tmem_r
     }
 }
 
-// Staged bf16 epilogue, part 1: TMEM -> alpha -> bf16 -> this warp's four 32 x 64
-// boxes in shared memory, 128-byte swizzled (16-byte chunk c of row r at chunk
-// c ^ (r & 7)), the layout the TMA store expects.  Lane = row within the slice.
-__device__ __forceinline__ void epilogue_to_smem(uint32_t tmem_row, uint8_t* stg, int lane, float alpha) {
-#pragma unroll 1
-    for (int b = 0; b < BN / BOX_COLS; ++b) {
-        uint32_t v[32], u[32];
-        tmem_ld_32cols(tmem_row + ACC_COL + b * BOX_COLS, v);
-        tmem_ld_32cols(tmem_row + ACC_COL + b * BOX_COLS + 32, u);
-        uint32_t w[32];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-            __nv_bfloat162 h0 = __floats2bfloat162_rn(__fmul_rn(__uint_as_float(v[2 * i]), alpha),
-                                                      __fmul_rn(__uint_as_float(v[2 * i + 1]), alpha));
-            __nv_bfloat162 h1 = __floats2bfloat162_rn(__fmul_rn(__uint_as_float(u[2 * i]), alpha),
-                                                      __fmul_rn(__uint_as_float(u[2 * i + 1]), alpha));
-            w[i] = *reinterpret_cast<uint32_t*>(&h0);
-            w[16 + i] = *reinterpret_cast<uint32_t*>(&h1);
-        }
+// Staged bf16 epilogue: TMEM -> alpha -> bf16 -> this warp's four 32 x 64 boxes in
+// shared memory, 128-byte swizzled (16-byte chunk c of row r at chunk c ^ (r & 7)),
+// the layout the TMA store expects.  Lane = row within the slice.  The TMEM load of
+// box b+1 is in flight while box b is converted, and `release` runs as soon as the
+// last load has completed (before the last box is converted), so the MMA warp can
+// start the next tile early.
+template <typename Release>
+__device__ __forceinline__ void epilogue_to_smem(uint32_t tmem_row, uint8_t* stg, int lane, float alpha,
+                                                 Release&& release) {
+    uint32_t va[64], vb[64];
+    auto ld64 = [&](uint32_t (&v)[64], int b) {
+        uint32_t (&lo)[32] = *reinterpret_cast<uint32_t (*)[32]>(&v[0]);
+        uint32_t (&hi)[32] = *reinterpret_cast<uint32_t (*)[32]>(&v[32]);
+        tmem_ld_32cols_nowait(tmem_row + ACC_COL + b * BOX_COLS, lo);
+        tmem_ld_32cols_nowait(tmem_row + ACC_COL + b * BOX_COLS + 32, hi);
+    };
+    auto fence64 = [&](uint32_t (&v)[64]) {
+        reg_fence32(*reinterpret_cast<uint32_t (*)[32]>(&v[0]));
+        reg_fence32(*reinterpret_cast<uint32_t (*)[32]>(&v[32]));
+    };
+    auto store_box = [&](const uint32_t (&v)[64], int b) {
         uint8_t* row = stg + b * BOX_BYTES + lane * 128;
 #pragma unroll
-        for (int c = 0; c < 8; ++c)
-            *reinterpret_cast<uint4*>(row + ((c ^ (lane & 7)) << 4)) =
-                make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
-    }
+        for (int c = 0; c < 8; ++c) {
+            uint32_t w[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                __nv_bfloat162 h = __floats2bfloat162_rn(__fmul_rn(__uint_as_float(v[8 * c + 2 * i]), alpha),
+                                                         __fmul_rn(__uint_as_float(v[8 * c + 2 * i + 1]), alpha));
+                w[i] = *reinterpret_cast<uint32_t*>(&h);
+            }
+            *reinterpret_cast<uint4*>(row + ((c ^ (lane & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+    };
+    ld64(va, 0);
+    tmem_ld_wait();
+    fence64(va);
+    ld64(vb, 1);
+    store_box(va, 0);
+    tmem_ld_wait();
+    fence64(vb);
+    ld64(va, 2);
+    store_box(vb, 1);
+    tmem_ld_wait();
+    fence64(va);
+    ld64(vb, 3);
+    store_box(va, 2);
+    tmem_ld_wait();
+    fence64(vb);
+    release();
+    store_box(vb, 3);
 }
 
 template <bool STAGED>
@@ -427,13 +480,17 @@ gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                 // the previous tile's stores must have finished reading this warp's boxes
                 if (lane == 0) bulk_wait_read0();
                 __syncwarp();
-                epilogue_to_smem(tmem_row, stg, lane, alpha);
+                epilogue_to_smem(tmem_row, stg, lane, alpha, [&] {
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(acc_empty);   // the MMA may start the next tile now
+                });
             } else {
                 epilogue_direct(p, tmem_row, m0 + lane, n0, alpha);
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(acc_empty);
             }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(acc_empty);       // the MMA may start the next tile now
             if constexpr (STAGED) {
                 fence_proxy_async_smem();                // generic-proxy writes -> visible to TMA
                 __syncwarp();
@@ -714,10 +771,11 @@ gemm_nvfp4_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_con
             tc_fence_after();
             if (lane == 0) bulk_wait_read0();
             __syncwarp();
-            epilogue_to_smem(tmem_row, stg, lane, alpha);
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive_cluster(acc_empty_leader);
+            epilogue_to_smem(tmem_row, stg, lane, alpha, [&] {
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive_cluster(acc_empty_leader);
+            });
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0 && m0 < p.M) {

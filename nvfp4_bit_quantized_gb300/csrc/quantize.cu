@@ -38,6 +38,21 @@ __device__ __forceinline__ size_t mma_sf_offset(int64_t r, int64_t s, int64_t nk
            (size_t)((r & 31) << 4) + (size_t)(((r >> 5) & 3) << 2) + (size_t)(s & 3);
 }
 
+// Walks the sequence k = start, start + step, ... as (k / width, k % width) without a
+// division per step (a 64-bit division costs tens of ALU instructions, which
+// these ALU-bound kernels cannot afford per 16-byte chunk).
+struct Walk2D {
+    int64_t row, col;              // current position
+    int64_t drow, dcol, width;     // step = drow * width + dcol, 0 <= dcol < width
+    __device__ __forceinline__ Walk2D(int64_t start, int64_t step, int64_t w)
+        : row(start / w), col(start % w), drow(step / w), dcol(step % w), width(w) {}
+    __device__ __forceinline__ void advance() {
+        row += drow;
+        col += dcol;
+        if (col >= width) { col -= width; ++row; }
+    }
+};
+
 // ---------------------------------------------------------------------------
 // Pass 1: amax
 // ---------------------------------------------------------------------------
@@ -75,6 +90,8 @@ __global__ void __launch_bounds__(kThreads) amax_kernel(const T* __restrict__ x,
     const int64_t nwarps = (int64_t)gridDim.x * (kThreads / 32);
     uint32_t m = 0;
     constexpr int U = 4;
+    if (nseg == 0) { block_max_store(0u, partials); return; }
+    Walk2D w(warp0, nwarps, spr);
     for (int64_t base = warp0; base < nseg; base += nwarps * U) {
         uint4 v[U];
         bool ok[U];
@@ -83,13 +100,13 @@ __global__ void __launch_bounds__(kThreads) amax_kernel(const T* __restrict__ x,
             const int64_t seg = base + (int64_t)u * nwarps;
             ok[u] = false;
             if (seg < nseg) {
-                const int64_t r = seg / spr;
-                const int64_t ch = (seg - r * spr) * 32 + lane;
+                const int64_t ch = w.col * 32 + lane;
                 if (ch < cpr) {
-                    v[u] = ld_stream(x + r * ldx + ch * VEC);
+                    v[u] = ld_stream(x + w.row * ldx + ch * VEC);
                     ok[u] = true;
                 }
             }
+            w.advance();
         }
 #pragma unroll
         for (int u = 0; u < U; ++u)
@@ -129,9 +146,10 @@ __global__ void __launch_bounds__(kThreads) amax_rht_kernel(const T* __restrict_
     const uint32_t sign_mask = rht_sign_mask(rht_seed);
     float m = 0.0f;
     bool bad = false;                                // NaN: fmaxf would drop it
-    for (int64_t tile = warp0; tile < tiles; tile += nwarps) {
-        const int64_t r0 = (tile / tiles_c) * 64 + rg * 16;
-        const int64_t c0 = (tile % tiles_c) * (8 * VEC) + cc * VEC;
+    Walk2D w(warp0, nwarps, tiles_c > 0 ? tiles_c : 1);
+    for (int64_t tile = warp0; tile < tiles; tile += nwarps, w.advance()) {
+        const int64_t r0 = w.row * 64 + rg * 16;
+        const int64_t c0 = w.col * (8 * VEC) + cc * VEC;
         if (r0 >= R || c0 >= C) continue;
         float t[VEC][16];
         load_patch<T>(x, ldx, r0, c0, t);
@@ -197,83 +215,109 @@ struct QOut {
 };
 
 // ---------------------------------------------------------------------------
-// Pass 2, 1x16 blocks along rows.  U warp segments per iteration: their loads
-// are all issued before any is used (memory-level parallelism).
+// Pass 2, 1x16 blocks along rows.  One 16-element block per lane (a warp covers 32
+// consecutive blocks of one row: 1 KB of bf16, fully coalesced), so the block amax,
+// the scale and its stores need no cross-lane traffic.  U warp segments per
+// iteration issue all their loads before any is used.
 // ---------------------------------------------------------------------------
-template <typename T, bool SR>
-__device__ __forceinline__ void encode_row_chunk(const float (&f)[Vec<T>::N], bool valid, int64_t r, int64_t C,
-                                                 int64_t col, int lane, const Scales& sc, const QOut& out,
-                                                 int64_t nkb, uint64_t sr_seed, uint32_t sr_offset) {
-    constexpr int VEC = Vec<T>::N;
-    constexpr int LPB = 16 / VEC;                    // lanes per 16-element block
-    float amax = 0.0f;
-#pragma unroll
-    for (int j = 0; j < VEC; ++j) amax = fmaxf(amax, fabsf(f[j]));
-#pragma unroll
-    for (int o = 1; o < LPB; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
-    if (!valid) return;
-    const uint32_t sb = block_scale_code(amax, sc.s_enc);
-    const float e_b = g_eb_table[sb];
-    float y[VEC];
-    if constexpr (SR) {
-        // idx0 % 8 is 0 for bf16 (8-element chunks) and 0 or 4 for fp32
-        const uint64_t idx0 = (uint64_t)(r * C + col);
-        const Philox4 p = sr_philox(sr_seed, 0u, sr_offset, idx0 >> 3);
-        const bool upper = (VEC == 4) && (idx0 & 4);
-#pragma unroll
-        for (int j = 0; j < VEC; ++j)
-            y[j] = e2m1_sr_value(__fmul_rn(f[j], e_b), upper ? sr_r16(p, 4 + j) : sr_r16(p, j));
-    } else {
-#pragma unroll
-        for (int j = 0; j < VEC; ++j) y[j] = __fmul_rn(f[j], e_b);
+template <typename T> struct Block16;
+template <> struct Block16<uint16_t> {            // 32 bytes
+    static constexpr int WORDS = 8;
+    __device__ __forceinline__ static void load(const uint16_t* p, bool v8, uint32_t (&w)[8]) {
+        if (v8) {
+            ld_stream32(p, w);
+        } else {
+            const uint4 a = ld_stream(p), b = ld_stream(p + 8);
+            w[0] = a.x; w[1] = a.y; w[2] = a.z; w[3] = a.w; w[4] = b.x; w[5] = b.y; w[6] = b.z; w[7] = b.w;
+        }
     }
-    uint8_t* dst = out.codes + r * (C / 2) + col / 2;
-    if constexpr (VEC == 8) *reinterpret_cast<uint32_t*>(dst) = e2m1x8_rn(y);
-    else *reinterpret_cast<uint16_t*>(dst) = (uint16_t)e2m1x4_rn(y);
-    if ((lane % LPB) == 0) {
-        const int64_t s = col / 16;
-        if (out.scales) out.scales[r * (C / 16) + s] = (uint8_t)sb;
-        if (out.scales_mma) out.scales_mma[mma_sf_offset(r, s, nkb)] = (uint8_t)sb;
+    __device__ __forceinline__ static void unpack(const uint32_t (&w)[8], float (&f)[16]) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) { f[2 * i] = bf16_lo(w[i]); f[2 * i + 1] = bf16_hi(w[i]); }
     }
-}
+};
+template <> struct Block16<float> {               // 64 bytes
+    static constexpr int WORDS = 16;
+    __device__ __forceinline__ static void load(const float* p, bool v8, uint32_t (&w)[16]) {
+        if (v8) {
+            uint32_t a[8], b[8];
+            ld_stream32(p, a);
+            ld_stream32(p + 8, b);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) { w[i] = a[i]; w[8 + i] = b[i]; }
+        } else {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const uint4 a = ld_stream(p + 4 * q);
+                w[4 * q] = a.x; w[4 * q + 1] = a.y; w[4 * q + 2] = a.z; w[4 * q + 3] = a.w;
+            }
+        }
+    }
+    __device__ __forceinline__ static void unpack(const uint32_t (&w)[16], float (&f)[16]) {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) f[i] = __uint_as_float(w[i]);
+    }
+};
 
 template <typename T, bool SR>
 __global__ void __launch_bounds__(kThreads) encode_row_kernel(const T* __restrict__ x, int64_t R, int64_t C,
                                                               int64_t ldx, const uint32_t* __restrict__ partials,
                                                               int nparts, QOut out, uint64_t sr_seed,
-                                                              uint32_t sr_offset, uint32_t* dev_status) {
-    constexpr int VEC = Vec<T>::N;
-    constexpr int U = 4;
+                                                              uint32_t sr_offset, int v8, uint32_t* dev_status) {
+    using B = Block16<T>;
+    constexpr int U = 2;
     const Scales sc = tensor_scales(partials, nparts, out.s_dec, dev_status);
+    const PhiloxKey key = philox_key(sr_seed);
     const int lane = threadIdx.x & 31;
-    const int64_t cpr = C / VEC;
-    const int64_t spr = (cpr + 31) / 32;
+    const int64_t bpr = C / 16;                      // blocks per row
+    const int64_t spr = (bpr + 31) / 32;             // warp segments per row
     const int64_t nseg = R * spr;
     const int64_t nkb = (C + 255) / 256;
     const int64_t warp0 = (int64_t)blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5);
     const int64_t nwarps = (int64_t)gridDim.x * (kThreads / 32);
+    if (nseg == 0) return;
+    Walk2D w(warp0, nwarps, spr);
     for (int64_t base = warp0; base < nseg; base += nwarps * U) {
-        uint4 v[U];
-        int64_t rr[U], ch[U];
+        uint32_t raw[U][B::WORDS];
+        int64_t rr[U], blk[U];
+        bool valid[U];
 #pragma unroll
         for (int u = 0; u < U; ++u) {
             const int64_t seg = base + (int64_t)u * nwarps;
-            rr[u] = seg / spr;
-            ch[u] = (seg - rr[u] * spr) * 32 + lane;
-            if (seg < nseg && ch[u] < cpr) v[u] = ld_stream(x + rr[u] * ldx + ch[u] * VEC);
+            rr[u] = w.row;
+            blk[u] = w.col * 32 + lane;
+            valid[u] = seg < nseg && blk[u] < bpr;
+            if (valid[u]) B::load(x + rr[u] * ldx + blk[u] * 16, v8 != 0, raw[u]);
+            w.advance();
         }
 #pragma unroll
         for (int u = 0; u < U; ++u) {
-            const int64_t seg = base + (int64_t)u * nwarps;
-            if (seg >= nseg) break;                      // warp-uniform
-            const bool valid = ch[u] < cpr;
-            float f[VEC];
-            if (valid) Vec<T>::unpack(v[u], f);
-            else {
+            if (!valid[u]) continue;
+            float f[16];
+            B::unpack(raw[u], f);
+            float amax = 0.0f;
 #pragma unroll
-                for (int j = 0; j < VEC; ++j) f[j] = 0.0f;
+            for (int j = 0; j < 16; ++j) amax = fmaxf(amax, fabsf(f[j]));
+            const uint32_t sb = block_scale_code(amax, sc.s_enc);
+            const float e_b = g_eb_table[sb];
+            const int64_t r = rr[u], col = blk[u] * 16;
+            float ylo[8], yhi[8];
+            if constexpr (SR) {
+                const uint64_t g0 = (uint64_t)(r * C + col) >> 3;     // C % 16 == 0: 8-aligned
+                const Philox4 p0 = sr_philox(key, 0u, sr_offset, g0);
+                const Philox4 p1 = sr_philox(key, 0u, sr_offset, g0 + 1);
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    ylo[j] = e2m1_sr_value(__fmul_rn(f[j], e_b), sr_r16(p0, j));
+                    yhi[j] = e2m1_sr_value(__fmul_rn(f[8 + j], e_b), sr_r16(p1, j));
+                }
+            } else {
+#pragma unroll
+                for (int j = 0; j < 8; ++j) { ylo[j] = __fmul_rn(f[j], e_b); yhi[j] = __fmul_rn(f[8 + j], e_b); }
             }
-            encode_row_chunk<T, SR>(f, valid, rr[u], C, ch[u] * VEC, lane, sc, out, nkb, sr_seed, sr_offset);
+            *reinterpret_cast<uint2*>(out.codes + r * (C / 2) + col / 2) = make_uint2(e2m1x8_rn(ylo), e2m1x8_rn(yhi));
+            if (out.scales) out.scales[r * bpr + blk[u]] = (uint8_t)sb;
+            if (out.scales_mma) out.scales_mma[mma_sf_offset(r, blk[u], nkb)] = (uint8_t)sb;
         }
     }
 }
@@ -290,15 +334,17 @@ __global__ void __launch_bounds__(kThreads) encode_col_kernel(const T* __restric
     constexpr int VEC = Vec<T>::N;
     const uint32_t sign_mask = RHT ? rht_sign_mask(rht_seed) : 0u;
     const Scales sc = tensor_scales(partials, nparts, out.s_dec, dev_status);
+    const PhiloxKey key = philox_key(sr_seed);
     const int lane = threadIdx.x & 31, rg = lane >> 3, cc = lane & 7;
     const int64_t tiles_c = (C + 8 * VEC - 1) / (8 * VEC);
     const int64_t tiles = ((R + 63) / 64) * tiles_c;
     const int64_t nkb = (R + 255) / 256;             // operand cols = R
     const int64_t warp0 = (int64_t)blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5);
     const int64_t nwarps = (int64_t)gridDim.x * (kThreads / 32);
-    for (int64_t tile = warp0; tile < tiles; tile += nwarps) {
-        const int64_t r0 = (tile / tiles_c) * 64 + rg * 16;
-        const int64_t c0 = (tile % tiles_c) * (8 * VEC) + cc * VEC;
+    Walk2D w(warp0, nwarps, tiles_c > 0 ? tiles_c : 1);
+    for (int64_t tile = warp0; tile < tiles; tile += nwarps, w.advance()) {
+        const int64_t r0 = w.row * 64 + rg * 16;
+        const int64_t c0 = w.col * (8 * VEC) + cc * VEC;
         if (r0 >= R || c0 >= C) continue;
         float t[VEC][16];
         load_patch<T>(x, ldx, r0, c0, t);
@@ -314,8 +360,8 @@ __global__ void __launch_bounds__(kThreads) encode_col_kernel(const T* __restric
             float ylo[8], yhi[8];
             if constexpr (SR) {
                 const uint64_t idx0 = (uint64_t)(c * R + r0);
-                const Philox4 p0 = sr_philox(sr_seed, 1u, sr_offset, idx0 >> 3);
-                const Philox4 p1 = sr_philox(sr_seed, 1u, sr_offset, (idx0 >> 3) + 1);
+                const Philox4 p0 = sr_philox(key, 1u, sr_offset, idx0 >> 3);
+                const Philox4 p1 = sr_philox(key, 1u, sr_offset, (idx0 >> 3) + 1);
 #pragma unroll
                 for (int i = 0; i < 8; ++i) {
                     ylo[i] = e2m1_sr_value(__fmul_rn(t[j][i], e_b), sr_r16(p0, i));
@@ -347,15 +393,17 @@ __global__ void __launch_bounds__(kThreads) encode_2d_kernel(const T* __restrict
     constexpr int VEC = Vec<T>::N;
     constexpr int LPT = 16 / VEC;                    // lanes per 16-column tile
     const Scales sc = tensor_scales(partials, nparts, out.s_dec, dev_status);
+    const PhiloxKey key = philox_key(sr_seed);
     const int lane = threadIdx.x & 31, rg = lane >> 3, cc = lane & 7;
     const int64_t tiles_c = (C + 8 * VEC - 1) / (8 * VEC);
     const int64_t tiles = ((R + 63) / 64) * tiles_c;
     const int64_t nkb = (C + 255) / 256, nkb_t = (R + 255) / 256;
     const int64_t warp0 = (int64_t)blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5);
     const int64_t nwarps = (int64_t)gridDim.x * (kThreads / 32);
-    for (int64_t tile = warp0; tile < tiles; tile += nwarps) {
-        const int64_t r0 = (tile / tiles_c) * 64 + rg * 16;
-        const int64_t c0 = (tile % tiles_c) * (8 * VEC) + cc * VEC;
+    Walk2D w(warp0, nwarps, tiles_c > 0 ? tiles_c : 1);
+    for (int64_t tile = warp0; tile < tiles; tile += nwarps, w.advance()) {
+        const int64_t r0 = w.row * 64 + rg * 16;
+        const int64_t c0 = w.col * (8 * VEC) + cc * VEC;
         // every lane takes part in the shuffles; invalid ones contribute 0
         const bool valid = (r0 < R) && (c0 < C);
         float t[VEC][16];
@@ -381,7 +429,7 @@ __global__ void __launch_bounds__(kThreads) encode_2d_kernel(const T* __restrict
             float y[VEC];
             if constexpr (SR) {
                 const uint64_t idx0 = (uint64_t)((r0 + i) * C + c0);
-                const Philox4 p = sr_philox(sr_seed, 0u, sr_offset, idx0 >> 3);
+                const Philox4 p = sr_philox(key, 0u, sr_offset, idx0 >> 3);
                 const bool upper = (VEC == 4) && (idx0 & 4);
 #pragma unroll
                 for (int j = 0; j < VEC; ++j)
@@ -503,17 +551,19 @@ nvfp4_status quantize_impl(const void* x, int32_t x_dtype, int64_t R, int64_t C,
     const bool sr = p->round == NVFP4_ROUND_SR;
     const int per_sm = (p->block == NVFP4_BLOCK_1X16_ROW) ? 8 : 4;
     const int64_t work_warps = (p->block == NVFP4_BLOCK_1X16_ROW)
-        ? (empty ? 0 : R * ((C / (is16 ? 8 : 4) + 31) / 32))
+        ? (empty ? 0 : R * ((C / 16 + 31) / 32))
         : (empty ? 0 : ((R + 63) / 64) * ((C + 8 * (is16 ? 8 : 4) - 1) / (8 * (is16 ? 8 : 4))));
     const int g2 = (int)std::max<int64_t>(1, std::min<int64_t>((int64_t)sms * per_sm, (work_warps + 7) / 8));
+    // 32-byte loads when every 16-element block starts on a 32-byte boundary
+    const int v8 = ((reinterpret_cast<uintptr_t>(x) & 31u) == 0 && ((size_t)ldx * esz) % 32 == 0) ? 1 : 0;
     const uint64_t ss = p->sr_seed;
     const uint32_t so = p->sr_offset;
 #define NVFP4_LAUNCH_T(T)                                                                                  \
     do {                                                                                                   \
         const T* xt = (const T*)x;                                                                         \
         if (p->block == NVFP4_BLOCK_1X16_ROW) {                                                            \
-            if (sr) encode_row_kernel<T, true><<<g2, kThreads, 0, stream>>>(xt, R, C, ldx, partials, g1, q, ss, so, dev_status); \
-            else encode_row_kernel<T, false><<<g2, kThreads, 0, stream>>>(xt, R, C, ldx, partials, g1, q, ss, so, dev_status); \
+            if (sr) encode_row_kernel<T, true><<<g2, kThreads, 0, stream>>>(xt, R, C, ldx, partials, g1, q, ss, so, v8, dev_status); \
+            else encode_row_kernel<T, false><<<g2, kThreads, 0, stream>>>(xt, R, C, ldx, partials, g1, q, ss, so, v8, dev_status); \
         } else if (p->block == NVFP4_BLOCK_1X16_COL) {                                                     \
             if (sr && p->rht) encode_col_kernel<T, true, true><<<g2, kThreads, 0, stream>>>(xt, R, C, ldx, partials, g1, q, ss, so, rs, dev_status); \
             else if (sr) encode_col_kernel<T, true, false><<<g2, kThreads, 0, stream>>>(xt, R, C, ldx, partials, g1, q, ss, so, rs, dev_status); \

@@ -128,3 +128,15 @@ def test_sr_seed_and_offset_change_only_codes(nv):
     torch.cuda.synchronize()
     assert torch.equal(a.codes, b.codes) and not torch.equal(a.codes, c.codes)
     assert torch.equal(a.scales, c.scales)
+
+
+@pytest.mark.parametrize("mode", ["row_rne", "row_sr"])
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+def test_row_mode_16_byte_aligned_input(nv, oracle_mod, mode, dtype):
+    """Inputs whose blocks start 16 (not 32) bytes apart from a 32-byte boundary take
+    the 16-byte load path of the row kernel."""
+    base = _input((40, 8 + 16 * 20), dtype, seed=6).cuda()
+    off = 8 if dtype == torch.bfloat16 else 4           # 16 bytes
+    x = base[:, off:off + 16 * 20]
+    assert (x.data_ptr() % 32) == 16
+    check_against_oracle(nv, oracle_mod, x, mode, sr_seed=4)
