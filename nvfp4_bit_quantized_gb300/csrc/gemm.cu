@@ -96,9 +96,19 @@ struct Params {
     int vec_store;
     int nkt;                     // ceil(K / 256): k tiles, also the scale layout's tiles per row block
     int m_tiles, n_tiles;
+    int n_fastest;               // tile order: 1 = consecutive tiles walk N (A tile reused), 0 = walk M
     uint32_t* dev_status;
     uint64_t timeout_ns;
 };
+
+// Tile order.  Consecutive persistent CTAs (clusters) take consecutive tiles, so the
+// operand indexed by the slow coordinate is shared by the CTAs running together
+// and read about once, while the other is swept once per slow step.  The host
+// picks the order that re-sweeps the smaller operand (it stays in L2).
+__device__ __forceinline__ void tile_coords(const Params& p, int tile, int m_count, int& m, int& n) {
+    if (p.n_fastest) { n = tile % p.n_tiles; m = tile / p.n_tiles; }
+    else { m = tile % m_count; n = tile / m_count; }
+}
 
 // ---- PTX wrappers ---------------------------------------------------------------
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* tm, int x, int y, uint32_t bar) {
@@ -345,7 +355,8 @@ gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
         uint32_t issued_mask = 0, issued_phase = 0;      // per stage: ever issued / parity of last issue
         bool ok = true;
         for (int tile = blockIdx.x; tile < tiles && ok; tile += gridDim.x) {
-            const int mt = tile % p.m_tiles, nt = tile / p.m_tiles;
+            int mt, nt;
+            tile_coords(p, tile, p.m_tiles, mt, nt);
             const bool second_sfb = (nt * BN + 128) < p.N;
             const uint32_t sf_bytes = SFA_BYTES + SFB_BYTES - (second_sfb ? 0 : 2048);
             for (int kt = 0; kt < p.nkt; ++kt) {
@@ -472,7 +483,8 @@ gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
         uint8_t* stg = staging + q * (4 * BOX_BYTES);
         uint32_t acc_phase = 0;
         for (int tile = blockIdx.x; tile < tiles; tile += gridDim.x) {
-            const int mt = tile % p.m_tiles, nt = tile / p.m_tiles;
+            int mt, nt;
+            tile_coords(p, tile, p.m_tiles, mt, nt);
             const int m0 = mt * BM + q * 32, n0 = nt * BN;
             if (!mbar_wait_bounded(acc_full, acc_phase, p.timeout_ns, abort_flag, p.dev_status)) break;
             tc_fence_after();
@@ -636,7 +648,8 @@ gemm_nvfp4_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_con
         uint32_t issued_mask = 0, issued_phase = 0;
         bool ok = true;
         for (int tile = cluster; tile < tiles && ok; tile += nclusters) {
-            const int mp = tile % m_pairs, nt = tile / m_pairs;
+            int mp, nt;
+            tile_coords(p, tile, m_pairs, mp, nt);
             const int mrow = mp * 256 + (int)rank * 128;          // this CTA's A rows
             const int nrow = nt * BN + (int)rank * 128;           // this CTA's B rows
             const bool second_sfb = (nt * BN + 128) < p.N;
@@ -765,7 +778,8 @@ gemm_nvfp4_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_con
         uint8_t* stg = staging + q * (4 * BOX_BYTES);
         uint32_t acc_phase = 0;
         for (int tile = cluster; tile < tiles; tile += nclusters) {
-            const int mp = tile % m_pairs, nt = tile / m_pairs;
+            int mp, nt;
+            tile_coords(p, tile, m_pairs, mp, nt);
             const int m0 = mp * 256 + (int)rank * 128 + q * 32, n0 = nt * BN;
             if (!mbar_wait_bounded(acc_full, acc_phase, p.timeout_ns, abort_flag, p.dev_status)) break;
             tc_fence_after();
@@ -916,6 +930,8 @@ nvfp4_status gemm_impl(const nvfp4_qtensor* A, const nvfp4_qtensor* B, void* D, 
     p.nkt = (int)((K + BK - 1) / BK);
     p.m_tiles = (int)((M + BM - 1) / BM);
     p.n_tiles = (int)((N + BN - 1) / BN);
+    // re-sweep the smaller operand: walk N fastest when A is the larger one
+    p.n_fastest = (M > N) ? 1 : 0;
     p.dev_status = dev_status;
     p.timeout_ns = wait_timeout_ns();
     const int tiles = p.m_tiles * p.n_tiles;
