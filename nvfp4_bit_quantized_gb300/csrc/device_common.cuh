@@ -193,11 +193,12 @@ __device__ __forceinline__ Philox4 philox4x32_10(uint32_t c0, uint32_t c1, uint3
                                                  const PhiloxKey& key) {
 #pragma unroll
     for (int i = 0; i < 10; ++i) {
-        const uint32_t hi_a = __umulhi(0xD2511F53u, c0), lo_a = 0xD2511F53u * c0;
-        const uint32_t hi_b = __umulhi(0xCD9E8D57u, c2), lo_b = 0xCD9E8D57u * c2;
-        const uint32_t n0 = hi_b ^ c1 ^ key.k0[i];
-        const uint32_t n2 = hi_a ^ c3 ^ key.k1[i];
-        c0 = n0; c1 = lo_b; c2 = n2; c3 = lo_a;
+        // one 32x32->64 multiply each (both halves from one instruction)
+        const uint64_t pa = (uint64_t)0xD2511F53u * c0;
+        const uint64_t pb = (uint64_t)0xCD9E8D57u * c2;
+        const uint32_t n0 = (uint32_t)(pb >> 32) ^ c1 ^ key.k0[i];
+        const uint32_t n2 = (uint32_t)(pa >> 32) ^ c3 ^ key.k1[i];
+        c0 = n0; c1 = (uint32_t)pb; c2 = n2; c3 = (uint32_t)pa;
     }
     Philox4 r;
     r.w[0] = c0; r.w[1] = c1; r.w[2] = c2; r.w[3] = c3;

@@ -115,6 +115,27 @@ __global__ void __launch_bounds__(kThreads) amax_kernel(const T* __restrict__ x,
     block_max_store(m, partials);
 }
 
+// |x| max over a contiguous tensor (row pitch == C) as one flat array of 16-byte
+// chunks: no 2D index arithmetic per chunk.
+template <typename T>
+__global__ void __launch_bounds__(kThreads) amax_flat_kernel(const T* __restrict__ x, int64_t nchunks,
+                                                             uint32_t* __restrict__ partials) {
+    constexpr int VEC = Vec<T>::N;
+    constexpr int U = 8;
+    const int64_t stride = (int64_t)gridDim.x * kThreads;
+    uint32_t m = 0;
+    for (int64_t base = (int64_t)blockIdx.x * kThreads + threadIdx.x; base < nchunks; base += stride * U) {
+        uint4 v[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+            if (base + u * stride < nchunks) v[u] = ld_stream(x + (base + u * stride) * VEC);
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+            if (base + u * stride < nchunks) m = max(m, abs_bits_max(v[u], (const T*)nullptr));
+    }
+    block_max_store(m, partials);
+}
+
 // Loads the 16-row x VEC-column patch at (r0, c0) into t[col][row] as fp32.
 template <typename T>
 __device__ __forceinline__ void load_patch(const T* __restrict__ x, int64_t ldx, int64_t r0, int64_t c0,
@@ -541,6 +562,10 @@ nvfp4_status quantize_impl(const void* x, int32_t x_dtype, int64_t R, int64_t C,
     if (p->rht) {
         if (is16) amax_rht_kernel<uint16_t><<<g1, kThreads, 0, stream>>>((const uint16_t*)x, R, C, ldx, rs, partials);
         else amax_rht_kernel<float><<<g1, kThreads, 0, stream>>>((const float*)x, R, C, ldx, rs, partials);
+    } else if (ldx == C) {
+        const int64_t n = chunks;
+        if (is16) amax_flat_kernel<uint16_t><<<g1, kThreads, 0, stream>>>((const uint16_t*)x, n, partials);
+        else amax_flat_kernel<float><<<g1, kThreads, 0, stream>>>((const float*)x, n, partials);
     } else {
         if (is16) amax_kernel<uint16_t><<<g1, kThreads, 0, stream>>>((const uint16_t*)x, R, C, ldx, partials);
         else amax_kernel<float><<<g1, kThreads, 0, stream>>>((const float*)x, R, C, ldx, partials);
