@@ -135,12 +135,10 @@ def run_kernel_only(args):
     else:
         def work():
             nv.quantize(W, nv.TILE16, nv.RNE, scales=False, transpose=True)
-            nv.quantize(X, nv.ROW, nv.RNE, scales=False)
-            nv.quantize(dY, nv.ROW, nv.SR, sr_seed=7, scales=False)
-            nv.quantize(dY, nv.COL, nv.SR, rht=True, sr_seed=7, rht_seed=11, scales=False)
-            nv.quantize(X, nv.COL, nv.RNE, rht=True, rht_seed=11, scales=False)
+            nv.quantize_dual(X, nv.RNE, nv.RNE, rht=True, rht_seed=11, scales=False)
+            nv.quantize_dual(dY, nv.SR, nv.SR, rht=True, sr_seed=7, rht_seed=11, scales=False)
         unit = "GB/s"
-        per = (N * K * (4 + 2 * 0.5625) + 2 * M * K * 4.5625 + 2 * M * N * 4.5625) / 1e9
+        per = (N * K * (4 + 2 * 0.5625) + (M * K + M * N) * (6 + 2 * 0.5625)) / 1e9
     for _ in range(args.warmup):
         work()
     torch.cuda.synchronize()
@@ -175,40 +173,38 @@ def run_ours(args):
     nv.reset_status()
     stream = torch.cuda.current_stream()
 
-    names = ["quant_W_2d", "quant_X_row", "gemm_fprop", "quant_dY_row_sr", "gemm_dgrad",
-             "quant_dYt_rht_sr", "quant_Xt_rht", "gemm_wgrad"]
+    names = ["quant_W_2d", "quant_X_dual", "gemm_fprop", "quant_dY_dual_sr", "gemm_dgrad", "gemm_wgrad"]
 
     def step(sr_offset, ev=None):
+        # forward: W (16x16, with W^T) and X (1x16 rows for Fprop + RHT columns kept for Wgrad);
+        # backward: dY (1x16 rows for Dgrad + RHT columns for Wgrad), stochastic rounding
         def mark(i):
             if ev is not None:
                 ev[i].record(stream)
         mark(0)
         wq = nv.quantize(W, nv.TILE16, nv.RNE, scales=False, transpose=True)
         mark(1)
-        xq = nv.quantize(X, nv.ROW, nv.RNE, scales=False)
+        xq, xt = nv.quantize_dual(X, nv.RNE, nv.RNE, rht=True, rht_seed=11, scales=False)
         mark(2)
         Y = nv.gemm(xq, wq, torch.bfloat16)
         mark(3)
-        dyq = nv.quantize(dY, nv.ROW, nv.SR, sr_seed=7, sr_offset=sr_offset, scales=False)
+        dyq, dyt = nv.quantize_dual(dY, nv.SR, nv.SR, rht=True, sr_seed=7, sr_offset=sr_offset, rht_seed=11,
+                                    scales=False)
         mark(4)
         dX = nv.gemm(dyq, wq.transposed(), torch.bfloat16)
         mark(5)
-        dyt = nv.quantize(dY, nv.COL, nv.SR, rht=True, sr_seed=7, sr_offset=sr_offset, rht_seed=11, scales=False)
-        mark(6)
-        xt = nv.quantize(X, nv.COL, nv.RNE, rht=True, rht_seed=11, scales=False)
-        mark(7)
         dW = nv.gemm(dyt, xt, torch.bfloat16)
-        mark(8)
+        mark(6)
         return Y, dX, dW
 
-    launches_per_step = 5 * 2 + 3
+    launches_per_step = 2 + 3 + 3 + 3
     for i in range(args.warmup):
         step(i)
     torch.cuda.synchronize()
     if nv.status_query() != 0:
         raise RuntimeError("device status error during warm-up")
 
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(9)] for _ in range(args.steps)]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(names) + 1)] for _ in range(args.steps)]
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
     if world > 1:
@@ -236,14 +232,13 @@ def run_ours(args):
            for j, n in enumerate(names)}
     gemm_ms = statistics.mean([per["gemm_fprop"], per["gemm_dgrad"], per["gemm_wgrad"]])
     gemm_tflops = {k: 2.0 * M * N * K / (per[k] * 1e-3) / 1e12 for k in ("gemm_fprop", "gemm_dgrad", "gemm_wgrad")}
-    # algorithmic bytes per element: read bf16 twice (amax + encode), write 0.5 B codes + 1/16 B scales;
-    # the 2D weight pass also writes the transposed codes and scales (another 0.5 + 1/16 B)
+    # algorithmic bytes per element: the 2D weight pass reads bf16 twice (amax + encode) and writes
+    # W and W^T codes + scales (2 x (0.5 + 1/16) B); a dual pass reads bf16 three times (one amax
+    # read for both operands, one encode read per operand) and writes two operands' codes + scales
     qbytes = {
         "quant_W_2d": N * K * (2 + 2 + 2 * (0.5 + 1 / 16)),
-        "quant_X_row": M * K * (4 + 0.5 + 1 / 16),
-        "quant_dY_row_sr": M * N * (4 + 0.5 + 1 / 16),
-        "quant_dYt_rht_sr": M * N * (4 + 0.5 + 1 / 16),
-        "quant_Xt_rht": M * K * (4 + 0.5 + 1 / 16),
+        "quant_X_dual": M * K * (2 + 2 * 2 + 2 * (0.5 + 1 / 16)),
+        "quant_dY_dual_sr": M * N * (2 + 2 * 2 + 2 * (0.5 + 1 / 16)),
     }
     quant_gbs = {k: qbytes[k] / (per[k] * 1e-3) / 1e9 for k in qbytes}
     quant_ms = sum(per[k] for k in qbytes)
@@ -309,7 +304,7 @@ def run_ours(args):
         "dtype": "e2m1/e4m3 operands, fp32 accumulate, bf16 in/out",
         "data": "synthetic (seeded normal; X N(0,1), W N(0,0.02), dY N(0,1e-3))",
         "config": {"workload": WORKLOAD, "M": M, "K": K, "N": N, "in_dtype": "bf16", "out_dtype": "bf16",
-                   "step": "quantize W(16x16)+X(row)+dY(row,SR)+dY^T,X^T(RHT) + Fprop/Dgrad/Wgrad GEMMs",
+                   "step": "quantize W (16x16, +W^T), X dual (1x16 rows + RHT columns), dY dual (SR) + Fprop/Dgrad/Wgrad GEMMs",
                    "l2": "inputs larger than L2 (the step streams >1 GB; 129 MB L2)",
                    "parallelism": f"dp{world} (independent token batches, no collective)"},
         "gemm_tflops": {k: round(v, 1) for k, v in gemm_tflops.items()},

@@ -131,6 +131,24 @@ NVFP4_API nvfp4_status nvfp4_quantize(const void* x, int32_t x_dtype, int64_t R,
                             void* workspace, size_t workspace_bytes, uint32_t* dev_status,
                             void* stream);
 
+/* Workspace bytes nvfp4_quantize_dual needs (two sets of amax partial maxima). */
+NVFP4_API size_t nvfp4_quantize_dual_workspace_bytes(int64_t R, int64_t C);
+
+/*
+ * nvfp4_quantize_dual -- both quantizations a tensor needs in training, from
+ * one amax read: the 1X16_ROW operand (params_row, out_row: [R, C]) and the
+ * 1X16_COL operand (params_col, out_col: [C, R], with or without the RHT).  With
+ * the RHT the single amax pass computes |x| and |RHT(x)| maxima together;
+ * results are identical to two nvfp4_quantize calls with the same parameters.
+ * Used for X (Fprop operand + the Wgrad operand saved for the backward pass) and
+ * for dY (Dgrad + Wgrad operands).  Same argument rules as nvfp4_quantize.
+ */
+NVFP4_API nvfp4_status nvfp4_quantize_dual(const void* x, int32_t x_dtype, int64_t R, int64_t C, int64_t ldx,
+                                           const nvfp4_qparams* params_row, const nvfp4_qtensor* out_row,
+                                           const nvfp4_qparams* params_col, const nvfp4_qtensor* out_col,
+                                           void* workspace, size_t workspace_bytes, uint32_t* dev_status,
+                                           void* stream);
+
 /*
  * nvfp4_quantize_noalloc -- nvfp4_quantize without a workspace argument; it
  * allocates nothing.  The page describes no such call: it exists for callers

@@ -12,10 +12,10 @@ inputs; stochastic rounding on gradients only.
 """
 from __future__ import annotations
 
-from .api import (QTensor, quantize, gemm, linear_fprop, linear_dgrad, linear_wgrad, quantize_weight,
+from .api import (QTensor, quantize, quantize_dual, gemm, linear_fprop, linear_dgrad, linear_wgrad, quantize_weight,
                   status_query, dev_status, reset_status, scales_mma_bytes, NVFP4Error)
 from ._lib import F32, BF16, RNE, SR, ROW, COL, TILE16, EXPORTS, LIB_PATH
 
-__all__ = ["QTensor", "quantize", "gemm", "linear_fprop", "linear_dgrad", "linear_wgrad", "quantize_weight",
+__all__ = ["QTensor", "quantize", "quantize_dual", "gemm", "linear_fprop", "linear_dgrad", "linear_wgrad", "quantize_weight",
            "status_query", "dev_status", "reset_status", "scales_mma_bytes", "NVFP4Error",
            "F32", "BF16", "RNE", "SR", "ROW", "COL", "TILE16", "EXPORTS", "LIB_PATH"]

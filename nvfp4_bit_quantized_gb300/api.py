@@ -105,14 +105,8 @@ class QTensor:
         return QTensor(self.codes_t, None, self.scales_mma_t, self.s_dec, self.cols, self.rows, self.block)
 
 
-def quantize(x: torch.Tensor, block: int = L.ROW, round: int = L.RNE, rht: bool = False,
-             sr_seed: int = 0, sr_offset: int = 0, rht_seed: int = 0, scales: bool = True,
-             scales_mma: bool = True, transpose: bool = True) -> QTensor:
-    """Quantize x [R, C] (float32 / bfloat16, CUDA) to NVFP4 with the library's kernels."""
-    _check_2d(x, "x")
-    R, C = x.shape
+def _alloc_q(R: int, C: int, block: int, dev, scales: bool, scales_mma: bool, transpose: bool) -> QTensor:
     rows, cols = (C, R) if block == L.COL else (R, C)
-    dev = x.device
     codes = torch.empty((rows, cols // 2), dtype=torch.uint8, device=dev)
     sc = None
     if scales:
@@ -124,18 +118,54 @@ def quantize(x: torch.Tensor, block: int = L.ROW, round: int = L.RNE, rht: bool 
     if block == L.TILE16 and transpose:
         codes_t = torch.empty((cols, rows // 2), dtype=torch.uint8, device=dev)
         smma_t = torch.empty(max(scales_mma_bytes(cols, rows), 16), dtype=torch.uint8, device=dev)
-    q = QTensor(codes, sc, smma, s_dec, rows, cols, block, codes_t, smma_t)
-    params = L.QParams(block, round, int(bool(rht)), sr_offset & 0xFFFFFFFF, sr_seed & (2**64 - 1),
-                       rht_seed & (2**64 - 1))
+    return QTensor(codes, sc, smma, s_dec, rows, cols, block, codes_t, smma_t)
+
+
+def _params(block, round, rht, sr_seed, sr_offset, rht_seed) -> L.QParams:
+    return L.QParams(block, round, int(bool(rht)), sr_offset & 0xFFFFFFFF, sr_seed & (2**64 - 1),
+                     rht_seed & (2**64 - 1))
+
+
+def quantize(x: torch.Tensor, block: int = L.ROW, round: int = L.RNE, rht: bool = False,
+             sr_seed: int = 0, sr_offset: int = 0, rht_seed: int = 0, scales: bool = True,
+             scales_mma: bool = True, transpose: bool = True) -> QTensor:
+    """Quantize x [R, C] (float32 / bfloat16, CUDA) to NVFP4 with the library's kernels."""
+    _check_2d(x, "x")
+    R, C = x.shape
+    q = _alloc_q(R, C, block, x.device, scales, scales_mma, transpose)
+    params = _params(block, round, rht, sr_seed, sr_offset, rht_seed)
     qc = q.c_struct()
     lib = L.lib()
     ws_bytes = int(lib.nvfp4_quantize_workspace_bytes(R, C, ctypes.byref(params)))
     ws = _workspace(ws_bytes)
     ld = x.stride(0) if R > 1 else max(C, 1)
     st = lib.nvfp4_quantize(_ptr(x), _DT[x.dtype], R, C, ld, ctypes.byref(params), ctypes.byref(qc),
-                            ws.data_ptr(), ws.numel(), dev_status(dev).data_ptr(), _stream())
+                            ws.data_ptr(), ws.numel(), dev_status(x.device).data_ptr(), _stream())
     L.check(st, "nvfp4_quantize")
     return q
+
+
+def quantize_dual(x: torch.Tensor, row_round: int = L.RNE, col_round: int = L.RNE, rht: bool = True,
+                  sr_seed: int = 0, sr_offset: int = 0, rht_seed: int = 0, scales: bool = True,
+                  scales_mma: bool = True):
+    """Both training quantizations of x [R, C] from one amax read: the 1x16 row
+    operand [R, C] and the 1x16 column operand [C, R] (RHT along R when ``rht``).
+    Identical to two ``quantize`` calls with the same parameters."""
+    _check_2d(x, "x")
+    R, C = x.shape
+    qr = _alloc_q(R, C, L.ROW, x.device, scales, scales_mma, False)
+    qc = _alloc_q(R, C, L.COL, x.device, scales, scales_mma, False)
+    pr = _params(L.ROW, row_round, False, sr_seed, sr_offset, rht_seed)
+    pc = _params(L.COL, col_round, rht, sr_seed, sr_offset, rht_seed)
+    a, b = qr.c_struct(), qc.c_struct()
+    lib = L.lib()
+    ws = _workspace(int(lib.nvfp4_quantize_dual_workspace_bytes(R, C)))
+    ld = x.stride(0) if R > 1 else max(C, 1)
+    st = lib.nvfp4_quantize_dual(_ptr(x), _DT[x.dtype], R, C, ld, ctypes.byref(pr), ctypes.byref(a),
+                                 ctypes.byref(pc), ctypes.byref(b), ws.data_ptr(), ws.numel(),
+                                 dev_status(x.device).data_ptr(), _stream())
+    L.check(st, "nvfp4_quantize_dual")
+    return qr, qc
 
 
 def quantize_weight(W: torch.Tensor) -> QTensor:

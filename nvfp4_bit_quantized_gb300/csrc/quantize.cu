@@ -188,6 +188,62 @@ __global__ void __launch_bounds__(kThreads) amax_rht_kernel(const T* __restrict_
     block_max_store(bad ? 0x7FC00000u : __float_as_uint(m), partials);
 }
 
+// Both tensor amaxes of a dual quantization in one read: |x| (row operand) and
+// |RHT(x)| along rows (column operand).
+template <typename T>
+__global__ void __launch_bounds__(kThreads) amax_dual_kernel(const T* __restrict__ x, int64_t R, int64_t C,
+                                                             int64_t ldx, uint64_t rht_seed,
+                                                             uint32_t* __restrict__ partials_plain,
+                                                             uint32_t* __restrict__ partials_rht) {
+    constexpr int VEC = Vec<T>::N;
+    const int lane = threadIdx.x & 31, rg = lane >> 3, cc = lane & 7;
+    const int64_t tiles_c = (C + 8 * VEC - 1) / (8 * VEC);
+    const int64_t tiles = ((R + 63) / 64) * tiles_c;
+    const int64_t warp0 = (int64_t)blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5);
+    const int64_t nwarps = (int64_t)gridDim.x * (kThreads / 32);
+    const uint32_t sign_mask = rht_sign_mask(rht_seed);
+    float mp = 0.0f, mr = 0.0f;
+    bool bad = false;
+    Walk2D w(warp0, nwarps, tiles_c > 0 ? tiles_c : 1);
+    for (int64_t tile = warp0; tile < tiles; tile += nwarps, w.advance()) {
+        const int64_t r0 = w.row * 64 + rg * 16;
+        const int64_t c0 = w.col * (8 * VEC) + cc * VEC;
+        if (r0 >= R || c0 >= C) continue;
+        float t[VEC][16];
+        load_patch<T>(x, ldx, r0, c0, t);
+#pragma unroll
+        for (int j = 0; j < VEC; ++j) {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                const float a = fabsf(t[j][i]);
+                mp = fmaxf(mp, a);
+                bad |= !(a <= FLT_MAX);
+            }
+            rht16(t[j], sign_mask);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                const float a = fabsf(t[j][i]);
+                mr = fmaxf(mr, a);
+                bad |= !(a <= FLT_MAX);
+            }
+        }
+    }
+    __shared__ uint32_t red[2][kThreads / 32];
+    uint32_t vp = bad ? 0x7FC00000u : __float_as_uint(mp);
+    uint32_t vr = bad ? 0x7FC00000u : __float_as_uint(mr);
+    vp = __reduce_max_sync(0xFFFFFFFFu, vp);
+    vr = __reduce_max_sync(0xFFFFFFFFu, vr);
+    if ((threadIdx.x & 31) == 0) { red[0][threadIdx.x >> 5] = vp; red[1][threadIdx.x >> 5] = vr; }
+    __syncthreads();
+    if (threadIdx.x < 32) {
+        uint32_t a = threadIdx.x < (kThreads / 32) ? red[0][threadIdx.x] : 0u;
+        uint32_t b = threadIdx.x < (kThreads / 32) ? red[1][threadIdx.x] : 0u;
+        a = __reduce_max_sync(0xFFFFFFFFu, a);
+        b = __reduce_max_sync(0xFFFFFFFFu, b);
+        if (threadIdx.x == 0) { partials_plain[blockIdx.x] = a; partials_rht[blockIdx.x] = b; }
+    }
+}
+
 // ---------------------------------------------------------------------------
 // Pass 2 prologue: reduce the partials to s_enc (same value in every CTA).
 // ---------------------------------------------------------------------------
@@ -506,9 +562,11 @@ extern "C" size_t nvfp4_quantize_workspace_bytes(int64_t, int64_t, const nvfp4_q
 
 namespace nvfp4 {
 
-nvfp4_status quantize_impl(const void* x, int32_t x_dtype, int64_t R, int64_t C, int64_t ldx,
-                           const nvfp4_qparams* p, const nvfp4_qtensor* out, void* ws, size_t ws_bytes,
-                           uint32_t* dev_status, cudaStream_t stream) {
+namespace {
+
+// Host-side argument checks shared by the single and the dual quantization.
+nvfp4_status check_quantize_args(const void* x, int32_t x_dtype, int64_t R, int64_t C, int64_t ldx,
+                                 const nvfp4_qparams* p, const nvfp4_qtensor* out) {
     if (!p || !out || !out->s_dec) return NVFP4_ERR_INVALID_ARG;
     if (x_dtype != NVFP4_F32 && x_dtype != NVFP4_BF16) return NVFP4_ERR_INVALID_ARG;
     if (p->block < NVFP4_BLOCK_1X16_ROW || p->block > NVFP4_BLOCK_16X16) return NVFP4_ERR_INVALID_ARG;
@@ -531,16 +589,42 @@ nvfp4_status quantize_impl(const void* x, int32_t x_dtype, int64_t R, int64_t C,
             (p->block == NVFP4_BLOCK_16X16 && out->scales_mma_t && !aligned16(out->scales_mma_t)))
             return NVFP4_ERR_ALIGNMENT;
     }
-    if (!ws || ws_bytes < (size_t)kMaxPartials * sizeof(uint32_t) || !aligned16(ws)) return NVFP4_ERR_WORKSPACE;
+    return NVFP4_OK;
+}
 
-    int dev = 0, sms = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return NVFP4_ERR_CUDA;
-    sms = sm_count(dev);
-    if (sms <= 0) return NVFP4_ERR_CUDA;
+int amax_grid(int sms, int64_t R, int64_t C, bool is16) {
+    const int64_t chunks = (R == 0 || C == 0) ? 0 : R * (C / (is16 ? 8 : 4));
+    const int g = (int)std::min<int64_t>((int64_t)sms * 8, std::max<int64_t>(1, (chunks + kThreads * 4 - 1) / (kThreads * 4)));
+    return std::min(g, kMaxPartials);
+}
 
-    uint32_t* partials = static_cast<uint32_t*>(ws);
-    const uint64_t rs = p->rht_seed;
+// Pass 1 for one quantization: per-CTA partial maxima of |x| or |RHT(x)|.
+cudaError_t amax_pass(const void* x, bool is16, int64_t R, int64_t C, int64_t ldx, bool rht, uint64_t rht_seed,
+                      uint32_t* partials, int g1, cudaStream_t stream) {
+    const int64_t chunks = (R == 0 || C == 0) ? 0 : R * (C / (is16 ? 8 : 4));
+    if (rht) {
+        if (is16) amax_rht_kernel<uint16_t><<<g1, kThreads, 0, stream>>>((const uint16_t*)x, R, C, ldx, rht_seed, partials);
+        else amax_rht_kernel<float><<<g1, kThreads, 0, stream>>>((const float*)x, R, C, ldx, rht_seed, partials);
+    } else if (ldx == C) {
+        if (is16) amax_flat_kernel<uint16_t><<<g1, kThreads, 0, stream>>>((const uint16_t*)x, chunks, partials);
+        else amax_flat_kernel<float><<<g1, kThreads, 0, stream>>>((const float*)x, chunks, partials);
+    } else {
+        if (is16) amax_kernel<uint16_t><<<g1, kThreads, 0, stream>>>((const uint16_t*)x, R, C, ldx, partials);
+        else amax_kernel<float><<<g1, kThreads, 0, stream>>>((const float*)x, R, C, ldx, partials);
+    }
+    return cudaGetLastError();
+}
+
+// Pass 2 for one quantization, given the pass-1 partials (g1 of them).
+nvfp4_status encode_pass(const void* x, int32_t x_dtype, int64_t R, int64_t C, int64_t ldx, const nvfp4_qparams* p,
+                         const nvfp4_qtensor* out, const uint32_t* partials, int g1, int sms, uint32_t* dev_status,
+                         cudaStream_t stream) {
+    const bool col = p->block == NVFP4_BLOCK_1X16_COL;
+    const int64_t rows = col ? C : R, cols = col ? R : C;
+    const bool empty = (R == 0 || C == 0);
     const bool is16 = x_dtype == NVFP4_BF16;
+    const size_t esz = is16 ? 2 : 4;
+    const uint64_t rs = p->rht_seed;
     QOut q{out->codes, out->scales, out->scales_mma,
            p->block == NVFP4_BLOCK_16X16 ? out->codes_t : nullptr,
            p->block == NVFP4_BLOCK_16X16 ? out->scales_mma_t : nullptr, out->s_dec};
@@ -555,24 +639,6 @@ nvfp4_status quantize_impl(const void* x, int32_t x_dtype, int64_t R, int64_t C,
                 return NVFP4_ERR_CUDA;
     }
 
-    // Pass 1.
-    const int64_t chunks = empty ? 0 : R * (C / (is16 ? 8 : 4));
-    int g1 = (int)std::min<int64_t>((int64_t)sms * 8, std::max<int64_t>(1, (chunks + kThreads * 4 - 1) / (kThreads * 4)));
-    g1 = std::min(g1, kMaxPartials);
-    if (p->rht) {
-        if (is16) amax_rht_kernel<uint16_t><<<g1, kThreads, 0, stream>>>((const uint16_t*)x, R, C, ldx, rs, partials);
-        else amax_rht_kernel<float><<<g1, kThreads, 0, stream>>>((const float*)x, R, C, ldx, rs, partials);
-    } else if (ldx == C) {
-        const int64_t n = chunks;
-        if (is16) amax_flat_kernel<uint16_t><<<g1, kThreads, 0, stream>>>((const uint16_t*)x, n, partials);
-        else amax_flat_kernel<float><<<g1, kThreads, 0, stream>>>((const float*)x, n, partials);
-    } else {
-        if (is16) amax_kernel<uint16_t><<<g1, kThreads, 0, stream>>>((const uint16_t*)x, R, C, ldx, partials);
-        else amax_kernel<float><<<g1, kThreads, 0, stream>>>((const float*)x, R, C, ldx, partials);
-    }
-    if (cudaGetLastError() != cudaSuccess) return NVFP4_ERR_CUDA;
-
-    // Pass 2.
     const bool sr = p->round == NVFP4_ROUND_SR;
     const int per_sm = (p->block == NVFP4_BLOCK_1X16_ROW) ? 8 : 4;
     const int64_t work_warps = (p->block == NVFP4_BLOCK_1X16_ROW)
@@ -606,6 +672,60 @@ nvfp4_status quantize_impl(const void* x, int32_t x_dtype, int64_t R, int64_t C,
     return NVFP4_OK;
 }
 
+}  // namespace
+
+nvfp4_status quantize_impl(const void* x, int32_t x_dtype, int64_t R, int64_t C, int64_t ldx,
+                           const nvfp4_qparams* p, const nvfp4_qtensor* out, void* ws, size_t ws_bytes,
+                           uint32_t* dev_status, cudaStream_t stream) {
+    nvfp4_status st = check_quantize_args(x, x_dtype, R, C, ldx, p, out);
+    if (st != NVFP4_OK) return st;
+    if (!ws || ws_bytes < (size_t)kMaxPartials * sizeof(uint32_t) || !aligned16(ws)) return NVFP4_ERR_WORKSPACE;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return NVFP4_ERR_CUDA;
+    const int sms = sm_count(dev);
+    if (sms <= 0) return NVFP4_ERR_CUDA;
+    const bool is16 = x_dtype == NVFP4_BF16;
+    uint32_t* partials = static_cast<uint32_t*>(ws);
+    const int g1 = amax_grid(sms, R, C, is16);
+    if (amax_pass(x, is16, R, C, ldx, p->rht != 0, p->rht_seed, partials, g1, stream) != cudaSuccess)
+        return NVFP4_ERR_CUDA;
+    return encode_pass(x, x_dtype, R, C, ldx, p, out, partials, g1, sms, dev_status, stream);
+}
+
+nvfp4_status quantize_dual_impl(const void* x, int32_t x_dtype, int64_t R, int64_t C, int64_t ldx,
+                                const nvfp4_qparams* p_row, const nvfp4_qtensor* out_row,
+                                const nvfp4_qparams* p_col, const nvfp4_qtensor* out_col, void* ws,
+                                size_t ws_bytes, uint32_t* dev_status, cudaStream_t stream) {
+    if (!p_row || !p_col) return NVFP4_ERR_INVALID_ARG;
+    if (p_row->block != NVFP4_BLOCK_1X16_ROW || p_col->block != NVFP4_BLOCK_1X16_COL) return NVFP4_ERR_INVALID_ARG;
+    nvfp4_status st = check_quantize_args(x, x_dtype, R, C, ldx, p_row, out_row);
+    if (st != NVFP4_OK) return st;
+    st = check_quantize_args(x, x_dtype, R, C, ldx, p_col, out_col);
+    if (st != NVFP4_OK) return st;
+    if (!ws || ws_bytes < 2 * (size_t)kMaxPartials * sizeof(uint32_t) || !aligned16(ws)) return NVFP4_ERR_WORKSPACE;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return NVFP4_ERR_CUDA;
+    const int sms = sm_count(dev);
+    if (sms <= 0) return NVFP4_ERR_CUDA;
+    const bool is16 = x_dtype == NVFP4_BF16;
+    uint32_t* part_plain = static_cast<uint32_t*>(ws);
+    uint32_t* part_col = part_plain + kMaxPartials;
+    const int g1 = amax_grid(sms, R, C, is16);
+    if (p_col->rht) {
+        // one read of x for both tensor amaxes
+        if (is16) amax_dual_kernel<uint16_t><<<g1, kThreads, 0, stream>>>((const uint16_t*)x, R, C, ldx, p_col->rht_seed, part_plain, part_col);
+        else amax_dual_kernel<float><<<g1, kThreads, 0, stream>>>((const float*)x, R, C, ldx, p_col->rht_seed, part_plain, part_col);
+        if (cudaGetLastError() != cudaSuccess) return NVFP4_ERR_CUDA;
+    } else {
+        // without the RHT both operands share the plain amax
+        if (amax_pass(x, is16, R, C, ldx, false, 0, part_plain, g1, stream) != cudaSuccess) return NVFP4_ERR_CUDA;
+        part_col = part_plain;
+    }
+    st = encode_pass(x, x_dtype, R, C, ldx, p_row, out_row, part_plain, g1, sms, dev_status, stream);
+    if (st != NVFP4_OK) return st;
+    return encode_pass(x, x_dtype, R, C, ldx, p_col, out_col, part_col, g1, sms, dev_status, stream);
+}
+
 }  // namespace nvfp4
 
 extern "C" nvfp4_status nvfp4_quantize(const void* x, int32_t x_dtype, int64_t R, int64_t C, int64_t ldx,
@@ -614,6 +734,19 @@ extern "C" nvfp4_status nvfp4_quantize(const void* x, int32_t x_dtype, int64_t R
                                        void* stream) {
     return nvfp4::quantize_impl(x, x_dtype, R, C, ldx, params, out, workspace, workspace_bytes, dev_status,
                                 static_cast<cudaStream_t>(stream));
+}
+
+extern "C" size_t nvfp4_quantize_dual_workspace_bytes(int64_t, int64_t) {
+    return 2 * (size_t)kMaxPartials * sizeof(uint32_t);
+}
+
+extern "C" nvfp4_status nvfp4_quantize_dual(const void* x, int32_t x_dtype, int64_t R, int64_t C, int64_t ldx,
+                                            const nvfp4_qparams* params_row, const nvfp4_qtensor* out_row,
+                                            const nvfp4_qparams* params_col, const nvfp4_qtensor* out_col,
+                                            void* workspace, size_t workspace_bytes, uint32_t* dev_status,
+                                            void* stream) {
+    return nvfp4::quantize_dual_impl(x, x_dtype, R, C, ldx, params_row, out_row, params_col, out_col, workspace,
+                                     workspace_bytes, dev_status, static_cast<cudaStream_t>(stream));
 }
 
 // ---------------------------------------------------------------------------

@@ -140,3 +140,23 @@ def test_row_mode_16_byte_aligned_input(nv, oracle_mod, mode, dtype):
     x = base[:, off:off + 16 * 20]
     assert (x.data_ptr() % 32) == 16
     check_against_oracle(nv, oracle_mod, x, mode, sr_seed=4)
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+@pytest.mark.parametrize("shape", [(208, 336), (1024, 512), (64, 4096)])
+@pytest.mark.parametrize("rnd,rht", [(0, True), (1, True), (0, False), (1, False)])
+def test_dual_quantization_matches_two_single_calls(nv, oracle_mod, dtype, shape, rnd, rht):
+    """nvfp4_quantize_dual (one amax read for both operands) == two nvfp4_quantize calls,
+    and both operands equal the oracle."""
+    x = _input(shape, dtype, seed=sum(shape) + rnd).cuda()
+    qr, qc = nv.quantize_dual(x, rnd, rnd, rht=rht, sr_seed=31, sr_offset=2, rht_seed=8)
+    ar = nv.quantize(x, nv.ROW, rnd, sr_seed=31, sr_offset=2)
+    ac = nv.quantize(x, nv.COL, rnd, rht=rht, sr_seed=31, sr_offset=2, rht_seed=8)
+    torch.cuda.synchronize()
+    for d, s in ((qr, ar), (qc, ac)):
+        assert torch.equal(d.codes, s.codes) and torch.equal(d.scales, s.scales)
+        assert torch.equal(d.scales_mma, s.scales_mma) and torch.equal(d.s_dec[:1], s.s_dec[:1])
+    xh = host_input(x)
+    r = oracle_mod.quantize(xh, oracle_mod.ROW, rnd, sr_seed=31, sr_offset=2)
+    c = oracle_mod.quantize(xh, oracle_mod.COL, rnd, rht=rht, sr_seed=31, sr_offset=2, rht_seed=8)
+    assert np.array_equal(qr.codes.cpu().numpy(), r["codes"]) and np.array_equal(qc.codes.cpu().numpy(), c["codes"])
