@@ -37,6 +37,27 @@ def env_rank():
     return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), int(os.environ.get("LOCAL_RANK", 0))
 
 
+def rank_seed(rank: int) -> int:
+    """Data seed of a rank's token batch (data parallel over M: every rank owns its batch)."""
+    return 1000 * rank
+
+
+def max_over_ranks(ms: float, world: int, device="cpu") -> float:
+    """The slowest rank's time (the job's time) via an all-reduce MAX; no-op on one rank."""
+    if world <= 1:
+        return ms
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(flops_per_rank_step: float, ms_per_step: float, world: int) -> float:
+    """Whole-job TFLOP/s: the units all ranks processed / the slowest rank's time."""
+    return world * flops_per_rank_step / (ms_per_step * 1e-3) / 1e12
+
+
 def gemm_traffic_bytes():
     """DRAM bytes per GEMM launch from the committed ncu summary, if it was taken
     on the current gemm.cu (else None: the counters are stale)."""
@@ -154,6 +175,146 @@ def run_kernel_only(args):
                       "config": {"workload": WORKLOAD, "M": M, "K": K, "N": N}}))
 
 
+def _timed(fn, steps: int, warmup: int) -> float:
+    """ms per call of fn (CUDA events on the current stream, after warm-up)."""
+    import torch
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(steps):
+        fn()
+    e1.record()
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / steps
+
+
+def run_sweep(args):
+    """Quantizer bandwidth sweep: bf16 [R, C], R*C ~ 2^p, C in {5120, 20480}, 0.1% outlier
+    columns x100; four modes.  One JSON line per case (GB/s of algorithmic bytes)."""
+    import torch
+    import nvfp4_bit_quantized_gb300 as nv
+    from nvfp4_bit_quantized_gb300 import inputs
+    peaks, src = measured_peaks()
+    modes = [("row_rne", nv.ROW, nv.RNE, False, 4.5625), ("row_sr", nv.ROW, nv.SR, False, 4.5625),
+             ("tile16_rne_with_transpose", nv.TILE16, nv.RNE, False, 5.125),
+             ("col_rht_sr", nv.COL, nv.SR, True, 4.5625)]
+    for C in (5120, 20480):
+        for p in range(args.sweep_min, args.sweep_max + 1):
+            R = inputs.sweep_rows(p, C)
+            x = inputs.sweep_tensor(R, C, seed=p, device="cuda")
+            for name, block, rnd, rht, bpe in modes:
+                fn = lambda: nv.quantize(x, block, rnd, rht=rht, sr_seed=1, rht_seed=2, scales=False,
+                                         transpose=(block == nv.TILE16))
+                ms = _timed(fn, max(3, args.steps), args.warmup)
+                gbs = R * C * bpe / (ms * 1e-3) / 1e9
+                print(json.dumps({"config": "quantizer_sweep", "mode": name, "R": R, "C": C, "elements": R * C,
+                                  "log2_elements": p, "ms": round(ms, 4), "GB/s": round(gbs, 1),
+                                  "hbm_frac": round(gbs / peaks["hbm_gbs"], 3), "peak_source": src,
+                                  "bytes_per_element": bpe, "inputs_exceed_l2": R * C * 2 > 129e6}))
+            del x
+            torch.cuda.empty_cache()
+
+
+def run_mlp(args):
+    """One dense MLP block step (5120 -> 20480 -> 5120, squared-ReLU, 16384 tokens), all six
+    GEMMs in NVFP4 with re-quantization between them: step time and per-GEMM TFLOP/s."""
+    import torch
+    import nvfp4_bit_quantized_gb300 as nv
+    from nvfp4_bit_quantized_gb300 import inputs
+    T, d, f = 16384, 5120, 20480
+    X = inputs.normal((T, d), 1.0, 10, device="cuda")
+    W1 = inputs.normal((f, d), 0.02, 11, device="cuda")
+    W2 = inputs.normal((d, f), 0.02, 12, device="cuda")
+    dY = inputs.normal((T, d), 1e-3, 13, device="cuda")
+    stream = torch.cuda.current_stream()
+    names = ["fwd1", "fwd2", "dgrad2", "wgrad2", "dgrad1", "wgrad1"]
+
+    def step(i, ev=None):
+        g = []
+        w1q, w2q = nv.quantize_weight(W1), nv.quantize_weight(W2)
+        xq, xt = nv.quantize_dual(X, nv.RNE, nv.RNE, rht=True, rht_seed=9, scales=False)
+
+        def gemm(a, b, k):
+            if ev is not None:
+                ev[k][0].record(stream)
+            out = nv.gemm(a, b, torch.bfloat16)
+            if ev is not None:
+                ev[k][1].record(stream)
+            return out
+        H = gemm(xq, w1q, 0)
+        A = nv.sqrelu_forward(H)
+        aq, at = nv.quantize_dual(A, nv.RNE, nv.RNE, rht=True, rht_seed=9, scales=False)
+        gemm(aq, w2q, 1)
+        dyq, dyt = nv.quantize_dual(dY, nv.SR, nv.SR, rht=True, sr_seed=5, sr_offset=2 * i, rht_seed=9, scales=False)
+        dA = gemm(dyq, w2q.transposed(), 2)
+        gemm(dyt, at, 3)
+        dH = nv.sqrelu_backward(H, dA)
+        dhq, dht = nv.quantize_dual(dH, nv.SR, nv.SR, rht=True, sr_seed=5, sr_offset=2 * i + 1, rht_seed=9,
+                                    scales=False)
+        gemm(dhq, w1q.transposed(), 4)
+        gemm(dht, xt, 5)
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    evs = [[[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in names] for _ in range(args.steps)]
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(args.steps):
+        step(args.warmup + i, evs[i])
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / args.steps
+    flop = 2.0 * T * d * f
+    per = {n: flop / (statistics.mean(evs[i][k][0].elapsed_time(evs[i][k][1]) for i in range(args.steps)) * 1e-3) / 1e12
+           for k, n in enumerate(names)}
+    print(json.dumps({"config": "mlp_block_16384x5120x20480_sqrelu", "ms_per_step": round(ms, 4),
+                      "tflops_step": round(6 * flop / (ms * 1e-3) / 1e12, 1),
+                      "gemm_tflops": {k: round(v, 1) for k, v in per.items()},
+                      "launches_per_step": 2 * 2 + 4 * 3 + 6 + 2, "device_status": nv.status_query()}))
+
+
+def run_heavy(args):
+    """Heavy-tailed layer (M=16384, K=4096, N=14336; Student-t inputs, outlier channels):
+    the NVFP4 step against the same three GEMMs in BF16 on cuBLAS (torch.matmul): speedup
+    (GEMM-only and with quantization) and the NVFP4 error relative to BF16."""
+    import torch
+    import nvfp4_bit_quantized_gb300 as nv
+    from nvfp4_bit_quantized_gb300 import inputs
+    Mh, Kh, Nh = 16384, 4096, 14336
+    X, W, dY = inputs.heavy_tailed_layer(Mh, Kh, Nh, seed=0, device="cuda")
+    wq = nv.quantize(W, nv.TILE16, nv.RNE, scales=False, transpose=True)
+    xq, xt = nv.quantize_dual(X, nv.RNE, nv.RNE, rht=True, rht_seed=11, scales=False)
+    dyq, dyt = nv.quantize_dual(dY, nv.SR, nv.SR, rht=True, sr_seed=7, rht_seed=11, scales=False)
+
+    def gemms():
+        return (nv.gemm(xq, wq, torch.bfloat16), nv.gemm(dyq, wq.transposed(), torch.bfloat16),
+                nv.gemm(dyt, xt, torch.bfloat16))
+
+    def full():
+        w = nv.quantize(W, nv.TILE16, nv.RNE, scales=False, transpose=True)
+        a, at = nv.quantize_dual(X, nv.RNE, nv.RNE, rht=True, rht_seed=11, scales=False)
+        g, gt = nv.quantize_dual(dY, nv.SR, nv.SR, rht=True, sr_seed=7, rht_seed=11, scales=False)
+        return nv.gemm(a, w, torch.bfloat16), nv.gemm(g, w.transposed(), torch.bfloat16), nv.gemm(gt, at, torch.bfloat16)
+
+    def bf16():
+        return X @ W.t(), dY @ W, dY.t() @ X
+
+    t_g, t_f, t_b = (_timed(fn, args.steps, args.warmup) for fn in (gemms, full, bf16))
+    fp4, ref = full(), bf16()
+    err = {n: round(((a.float() - b.float()).norm() / b.float().norm()).item(), 4)
+           for n, a, b in zip(("fprop", "dgrad", "wgrad"), fp4, ref)}
+    flop = 3 * 2.0 * Mh * Kh * Nh
+    print(json.dumps({"config": "heavy_tailed_16384x4096x14336", "nvfp4_gemm_ms": round(t_g, 4),
+                      "nvfp4_step_ms": round(t_f, 4), "bf16_cublas_ms": round(t_b, 4),
+                      "speedup_gemm_only": round(t_b / t_g, 2), "speedup_with_quantization": round(t_b / t_f, 2),
+                      "nvfp4_tflops_gemm": round(flop / (t_g * 1e-3) / 1e12, 1),
+                      "bf16_tflops": round(flop / (t_b * 1e-3) / 1e12, 1),
+                      "rel_error_vs_bf16": err, "device_status": nv.status_query()}))
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
@@ -162,6 +323,9 @@ def run_ours(args):
 
     if args.kernel != "step":
         return run_kernel_only(args)
+    if args.config != "ffn_up":
+        torch.cuda.set_device(0)
+        return {"sweep": run_sweep, "mlp": run_mlp, "heavy": run_heavy}[args.config](args)
 
     rank, world, local = env_rank()
     torch.cuda.set_device(local)
@@ -169,7 +333,7 @@ def run_ours(args):
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
     dev = torch.device("cuda", local)
     # weak scaling: every rank owns its own token batch (data parallel over M)
-    X, W, dY = inputs.linear_layer(M, K, N, seed=1000 * rank, dtype=torch.bfloat16, device=dev)
+    X, W, dY = inputs.linear_layer(M, K, N, seed=rank_seed(rank), dtype=torch.bfloat16, device=dev)
     nv.reset_status()
     stream = torch.cuda.current_stream()
 
@@ -218,15 +382,11 @@ def run_ours(args):
         torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
-    ms_total = t0.elapsed_time(t1)
-    if world > 1:
-        tt = torch.tensor([ms_total], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms_total = float(tt.item())
+    ms_total = max_over_ranks(t0.elapsed_time(t1), world, dev)
     status = nv.status_query()
     ms_step = ms_total / args.steps
     flops_step = 3 * 2.0 * M * N * K
-    value = world * flops_step / (ms_step * 1e-3) / 1e12
+    value = job_throughput(flops_step, ms_step, world)
 
     per = {n: statistics.mean(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(args.steps))
            for j, n in enumerate(names)}
@@ -279,7 +439,7 @@ def run_ours(args):
         e1.record(stream)
         torch.cuda.synchronize()
         e2e_ms = e0.elapsed_time(e1) / e2e_steps
-        e2e_value = round(world * flops_step / (e2e_ms * 1e-3) / 1e12, 2)
+        e2e_value = round(job_throughput(flops_step, e2e_ms, world), 2)
         e2e_ms = round(e2e_ms, 3)
 
     cpu = None
@@ -404,6 +564,11 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--kernel", choices=["step", "gemm", "quantize"], default="step",
                     help="step: the whole hot path (the bench line); gemm / quantize: one kernel family alone")
+    ap.add_argument("--config", choices=["ffn_up", "mlp", "sweep", "heavy"], default="ffn_up",
+                    help="ffn_up: the headline workload (default); mlp / sweep / heavy: the other workloads, "
+                         "one JSON line each (not the headline metric)")
+    ap.add_argument("--sweep-min", type=int, default=20)
+    ap.add_argument("--sweep-max", type=int, default=28)
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3

@@ -221,6 +221,15 @@ NVFP4_API nvfp4_status nvfp4_linear_wgrad(const void* dY, int32_t dy_dtype, int6
                                 void* workspace, size_t workspace_bytes, uint32_t* dev_status,
                                 void* stream);
 
+/*
+ * Squared-ReLU of the dense MLP block the NVFP4 linear layers sit in (the page's
+ * model is a hybrid; the MLP block around them is the plain dense case).  bf16
+ * [n] contiguous buffers, n % 8 == 0, 16-byte aligned; fp32 arithmetic rounded
+ * to nearest-even bf16:  a = relu(h)^2;  dh = da * (2 * relu(h)).
+ */
+NVFP4_API nvfp4_status nvfp4_sqrelu_forward(const void* h, void* a, int64_t n, void* stream);
+NVFP4_API nvfp4_status nvfp4_sqrelu_backward(const void* h, const void* da, void* dh, int64_t n, void* stream);
+
 /* Synchronises `stream`, reads *dev_status and returns it as a status. */
 NVFP4_API nvfp4_status nvfp4_status_query(const uint32_t* dev_status, void* stream);
 

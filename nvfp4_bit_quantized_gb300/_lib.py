@@ -21,6 +21,7 @@ EXPORTS = [
     "nvfp4_linear_workspace_bytes", "nvfp4_linear_fprop", "nvfp4_linear_dgrad", "nvfp4_linear_wgrad",
     "nvfp4_status_query", "nvfp4_status_string", "nvfp4_set_wait_timeout_ns", "nvfp4_debug_e4m3",
     "nvfp4_debug_e2m1", "nvfp4_debug_philox", "nvfp4_selftest_wait_timeout", "nvfp4_gemm_force_path",
+    "nvfp4_sqrelu_forward", "nvfp4_sqrelu_backward",
 ]
 
 
@@ -81,6 +82,8 @@ def lib():
             "nvfp4_debug_philox": (I32, [P, I64, U64, P, P]),
             "nvfp4_selftest_wait_timeout": (I32, [U64, P, P]),
             "nvfp4_gemm_force_path": (None, [I32]),
+            "nvfp4_sqrelu_forward": (I32, [P, P, I64, P]),
+            "nvfp4_sqrelu_backward": (I32, [P, P, P, I64, P]),
         }
         for name, (res, args) in sigs.items():
             fn = getattr(L, name)

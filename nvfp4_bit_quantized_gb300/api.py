@@ -239,3 +239,25 @@ def linear_wgrad(dY: torch.Tensor, X: torch.Tensor, sr_seed: int = 0, sr_offset:
                                     dev_status(dY.device).data_ptr(), _stream())
     L.check(st, "nvfp4_linear_wgrad")
     return dW
+
+
+def sqrelu_forward(h: torch.Tensor) -> torch.Tensor:
+    """a = relu(h)^2 (bf16, contiguous)."""
+    if h.dtype != torch.bfloat16 or not h.is_contiguous() or not h.is_cuda:
+        raise NVFP4Error(L.ERR_INVALID_ARG, "h must be a contiguous CUDA bf16 tensor")
+    a = torch.empty_like(h)
+    L.check(L.lib().nvfp4_sqrelu_forward(h.data_ptr(), a.data_ptr(), h.numel(), _stream()), "nvfp4_sqrelu_forward")
+    return a
+
+
+def sqrelu_backward(h: torch.Tensor, da: torch.Tensor) -> torch.Tensor:
+    """dh = da * 2 relu(h) (bf16, contiguous)."""
+    for t, n in ((h, "h"), (da, "da")):
+        if t.dtype != torch.bfloat16 or not t.is_contiguous() or not t.is_cuda:
+            raise NVFP4Error(L.ERR_INVALID_ARG, f"{n} must be a contiguous CUDA bf16 tensor")
+    if h.shape != da.shape:
+        raise NVFP4Error(L.ERR_SHAPE, "h and da differ in shape")
+    dh = torch.empty_like(h)
+    L.check(L.lib().nvfp4_sqrelu_backward(h.data_ptr(), da.data_ptr(), dh.data_ptr(), h.numel(), _stream()),
+            "nvfp4_sqrelu_backward")
+    return dh

@@ -213,3 +213,30 @@ def gemm_f64(A: np.ndarray, B: np.ndarray) -> np.ndarray:
     C = np.empty((M, N), dtype=np.float64)
     _load().orc_gemm_f64(_ptr(A), _ptr(B), M, N, K, _ptr(C))
     return C
+
+
+# --- squared ReLU of the dense MLP block (plain numpy float32) -------------------------
+
+def _bf16_to_f32(bits: np.ndarray) -> np.ndarray:
+    return (np.asarray(bits, dtype=np.uint16).astype(np.uint32) << np.uint32(16)).view(np.float32)
+
+
+def _f32_to_bf16(x: np.ndarray) -> np.ndarray:
+    """Round-to-nearest-even fp32 -> bf16 bits (finite inputs)."""
+    u = np.asarray(x, dtype=np.float32).view(np.uint32).astype(np.uint64)
+    return ((u + 0x7FFF + ((u >> 16) & 1)) >> 16).astype(np.uint16)
+
+
+def sqrelu_forward(h_bits: np.ndarray) -> np.ndarray:
+    """a = relu(h)^2 with relu(h) = h if h > 0 else +0; bf16 bits in and out."""
+    h = _bf16_to_f32(h_bits)
+    r = np.where(h > 0, h, np.float32(0)).astype(np.float32)
+    return _f32_to_bf16((r * r).astype(np.float32))
+
+
+def sqrelu_backward(h_bits: np.ndarray, da_bits: np.ndarray) -> np.ndarray:
+    """dh = da * (2 relu(h)); bf16 bits in and out."""
+    h = _bf16_to_f32(h_bits)
+    da = _bf16_to_f32(da_bits)
+    t = np.where(h > 0, (np.float32(2) * h).astype(np.float32), np.float32(0)).astype(np.float32)
+    return _f32_to_bf16((da * t).astype(np.float32))

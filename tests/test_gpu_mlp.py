@@ -1,0 +1,142 @@
+"""The dense MLP block (d -> f -> d, squared-ReLU) with all six GEMMs in NVFP4 and
+re-quantization between them: each stage checked against the oracle on the
+GPU's own inputs to that stage (bit for bit for the activation and every
+quantization, within 1e-3 for the GEMMs on identical dequantized operands)."""
+import numpy as np
+import pytest
+import torch
+
+from helpers import bf16_round, host_input, qtensor_to_oracle, rel_fro
+
+pytestmark = pytest.mark.gpu
+TOL = 1e-3
+
+
+@pytest.fixture(scope="module")
+def nv():
+    import __graft_entry__
+    __graft_entry__.build()
+    import nvfp4_bit_quantized_gb300 as nv
+    return nv
+
+
+def mlp_step(nv, X, W1, W2, dY, sr_seed=5, rht_seed=9):
+    """Forward and backward of one MLP block, every GEMM in NVFP4 (bf16 out)."""
+    out = {}
+    out["w1q"] = nv.quantize_weight(W1)
+    out["w2q"] = nv.quantize_weight(W2)
+    out["xq"], out["xt"] = nv.quantize_dual(X, nv.RNE, nv.RNE, rht=True, rht_seed=rht_seed)
+    out["H"] = nv.gemm(out["xq"], out["w1q"], torch.bfloat16)
+    out["A"] = nv.sqrelu_forward(out["H"])
+    out["aq"], out["at"] = nv.quantize_dual(out["A"], nv.RNE, nv.RNE, rht=True, rht_seed=rht_seed)
+    out["Y"] = nv.gemm(out["aq"], out["w2q"], torch.bfloat16)
+    out["dyq"], out["dyt"] = nv.quantize_dual(dY, nv.SR, nv.SR, rht=True, sr_seed=sr_seed, sr_offset=0,
+                                              rht_seed=rht_seed)
+    out["dA"] = nv.gemm(out["dyq"], out["w2q"].transposed(), torch.bfloat16)
+    out["dW2"] = nv.gemm(out["dyt"], out["at"], torch.bfloat16)
+    out["dH"] = nv.sqrelu_backward(out["H"], out["dA"])
+    out["dhq"], out["dht"] = nv.quantize_dual(out["dH"], nv.SR, nv.SR, rht=True, sr_seed=sr_seed, sr_offset=1,
+                                              rht_seed=rht_seed)
+    out["dX"] = nv.gemm(out["dhq"], out["w1q"].transposed(), torch.bfloat16)
+    out["dW1"] = nv.gemm(out["dht"], out["xt"], torch.bfloat16)
+    return out
+
+
+def _wt(q, rows, cols):
+    return dict(codes=q.codes_t.cpu().numpy(), scales=q.scales.cpu().numpy().T.copy(),
+                s_dec=float(q.s_dec[0].item()), rows=rows, cols=cols, block=2)
+
+
+def test_sqrelu_matches_oracle(nv, oracle_mod):
+    g = torch.Generator().manual_seed(3)
+    h = (torch.randn(4096, generator=g) * 3).to(torch.bfloat16)
+    h[:4] = torch.tensor([0.0, -0.0, 1e-30, -1e-30])
+    da = (torch.randn(4096, generator=g) * 1e-3).to(torch.bfloat16)
+    hg, dag = h.cuda(), da.cuda()
+    a = nv.sqrelu_forward(hg)
+    dh = nv.sqrelu_backward(hg, dag)
+    torch.cuda.synchronize()
+    hb, db = host_input(h), host_input(da)
+    assert np.array_equal(host_input(a.cpu()), oracle_mod.sqrelu_forward(hb))
+    assert np.array_equal(host_input(dh.cpu()), oracle_mod.sqrelu_backward(hb, db))
+
+
+def test_mlp_block_small_full_oracle(nv, oracle_mod):
+    """256 tokens, 256 -> 1024 -> 256: every stage against the oracle."""
+    from nvfp4_bit_quantized_gb300 import inputs
+    T, d, f = 256, 256, 1024
+    X = inputs.normal((T, d), 1.0, 0, device="cuda")
+    W1 = inputs.normal((f, d), 0.02, 1, device="cuda")
+    W2 = inputs.normal((d, f), 0.02, 2, device="cuda")
+    dY = inputs.normal((T, d), 1e-3, 3, device="cuda")
+    nv.reset_status()
+    o = mlp_step(nv, X, W1, W2, dY)
+    assert nv.status_query() == 0
+    om = oracle_mod
+
+    def same_q(q, x_bits, block, rnd, rht=False, sr_offset=0):
+        r = om.quantize(x_bits, block, rnd, rht=rht, sr_seed=5, sr_offset=sr_offset, rht_seed=9)
+        assert np.array_equal(q.codes.cpu().numpy(), r["codes"])
+        assert np.array_equal(q.scales.cpu().numpy(), r["scales"])
+        return r
+
+    x, w1, w2, dy = host_input(X), host_input(W1), host_input(W2), host_input(dY)
+    rx, rxt = same_q(o["xq"], x, om.ROW, om.RNE), same_q(o["xt"], x, om.COL, om.RNE, rht=True)
+    rw1, rw2 = same_q(o["w1q"], w1, om.TILE16, om.RNE), same_q(o["w2q"], w2, om.TILE16, om.RNE)
+    deq, gemm = om.dequant, om.gemm_f64
+    assert rel_fro(o["H"].float().cpu().numpy(), bf16_round(gemm(deq(rx), deq(rw1)))) <= TOL
+    h = host_input(o["H"])
+    assert np.array_equal(host_input(o["A"]), om.sqrelu_forward(h))
+    a = host_input(o["A"])
+    ra, rat = same_q(o["aq"], a, om.ROW, om.RNE), same_q(o["at"], a, om.COL, om.RNE, rht=True)
+    assert rel_fro(o["Y"].float().cpu().numpy(), bf16_round(gemm(deq(ra), deq(rw2)))) <= TOL
+    rdy, rdyt = same_q(o["dyq"], dy, om.ROW, om.SR), same_q(o["dyt"], dy, om.COL, om.SR, rht=True)
+    rw2t = om.quantize(np.ascontiguousarray(w2.T), om.TILE16)
+    assert np.array_equal(o["w2q"].codes_t.cpu().numpy(), rw2t["codes"])
+    assert rel_fro(o["dA"].float().cpu().numpy(), bf16_round(gemm(deq(rdy), deq(rw2t)))) <= TOL
+    assert rel_fro(o["dW2"].float().cpu().numpy(), bf16_round(gemm(deq(rdyt), deq(rat)))) <= TOL
+    assert np.array_equal(host_input(o["dH"]), om.sqrelu_backward(h, host_input(o["dA"])))
+    dh = host_input(o["dH"])
+    rdh = same_q(o["dhq"], dh, om.ROW, om.SR, sr_offset=1)
+    rdht = same_q(o["dht"], dh, om.COL, om.SR, rht=True, sr_offset=1)
+    rw1t = om.quantize(np.ascontiguousarray(w1.T), om.TILE16)
+    assert rel_fro(o["dX"].float().cpu().numpy(), bf16_round(gemm(deq(rdh), deq(rw1t)))) <= TOL
+    assert rel_fro(o["dW1"].float().cpu().numpy(), bf16_round(gemm(deq(rdht), deq(rxt)))) <= TOL
+
+
+def test_mlp_block_full_size_sampled(nv, oracle_mod):
+    """16384 tokens, 5120 -> 20480 -> 5120 (the MLP block workload): the activation
+    bit for bit on sampled rows, each GEMM on sampled output blocks."""
+    from nvfp4_bit_quantized_gb300 import inputs
+    T, d, f = 16384, 5120, 20480
+    X = inputs.normal((T, d), 1.0, 10, device="cuda")
+    W1 = inputs.normal((f, d), 0.02, 11, device="cuda")
+    W2 = inputs.normal((d, f), 0.02, 12, device="cuda")
+    dY = inputs.normal((T, d), 1e-3, 13, device="cuda")
+    nv.reset_status()
+    o = mlp_step(nv, X, W1, W2, dY)
+    assert nv.status_query() == 0
+    rng = np.random.default_rng(4)
+    om = oracle_mod
+    rows = [0, int(rng.integers(1, T - 1)), T - 1]
+    h = o["H"][rows].cpu()
+    assert np.array_equal(host_input(o["A"][rows].cpu()), om.sqrelu_forward(host_input(h)))
+    assert np.array_equal(host_input(o["dH"][rows].cpu()),
+                          om.sqrelu_backward(host_input(h), host_input(o["dA"][rows].cpu())))
+
+    def check(qa, qb, D, b_tile=False, a_dict=None, b_dict=None):
+        A = a_dict or qtensor_to_oracle(qa, 0)
+        B = b_dict or qtensor_to_oracle(qb, 2 if b_tile else 0)
+        Mr, Nr = D.shape
+        Dh = D
+        for m, n in ((0, 0), (Mr - 64, Nr - 64), (int(rng.integers(0, Mr // 64)) * 64, int(rng.integers(0, Nr // 64)) * 64)):
+            ref = om.gemm_f64(om.dequant(A, m, m + 64), om.dequant(B, n, n + 64))
+            got = Dh[m:m + 64, n:n + 64].float().cpu().numpy()
+            assert rel_fro(got, bf16_round(ref)) <= TOL, (m, n)
+
+    check(o["xq"], o["w1q"], o["H"], b_tile=True)
+    check(o["aq"], o["w2q"], o["Y"], b_tile=True)
+    check(o["dyq"], None, o["dA"], b_dict=_wt(o["w2q"], f, d))
+    check(o["dyt"], o["at"], o["dW2"])
+    check(o["dhq"], None, o["dX"], b_dict=_wt(o["w1q"], d, f))
+    check(o["dht"], o["xt"], o["dW1"])

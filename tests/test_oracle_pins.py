@@ -469,3 +469,12 @@ def test_gemm_f64_against_exact_integer_arithmetic(oracle_mod, M, N, K):
             exact = sum(terms) * sd
             mag = sum(abs(t) for t in terms) * sd
             assert abs(Fraction(C[m, n]) - exact) <= mag * Fraction(K + 2, 2 ** 52), (m, n)
+
+
+def test_bf16_rounding_helper_matches_torch(oracle_mod):
+    """The oracle's fp32 -> bf16 rounding (used by the MLP activation) equals torch's cast."""
+    rng = np.random.default_rng(21)
+    x = np.concatenate([rng.standard_normal(100000) * 10.0 ** rng.uniform(-5, 5, 100000),
+                        np.array([0.0, -0.0, 1.0, 3.0e38])]).astype(np.float32)
+    ref = torch.from_numpy(x).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(oracle_mod._f32_to_bf16(x), ref)
