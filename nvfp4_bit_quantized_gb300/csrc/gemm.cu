@@ -530,24 +530,38 @@ gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
 
 // ============================================================================
 // CTA-pair kernel (tcgen05 cta_group::2): one 256 x 256 output tile per pair of
-// SMs.  The leader CTA (cluster rank 0) issues MMAs with M = 256: rows 0-127 of
-// the tile come from the leader's A tile, rows 128-255 from the follower's, and
-// the 256 B rows (N) are split the same way; each CTA's TMEM receives its own
-// 128 rows of the accumulator.  Per CTA and stage the ring holds A 16 KB +
-// B 16 KB + scales 6 KB = 38 KB (instead of 54 KB), so 4 stages fit next to the
-// 64 KB output staging, and each SM pulls a third less from L2.
-// Cross-CTA signals: the leader's MMA commits are multicast to both CTAs' barriers;
-// the follower's scale warps and epilogue warps arrive remotely on the leader's
-// sf_ready / acc_empty barriers.  Codes and scales are loaded CTA-locally.
+// SMs, persistent.  The leader CTA (cluster rank 0) issues MMAs with M = 256:
+// rows 0-127 of the tile come from the leader's A tile, rows 128-255 from the
+// follower's, and the 256 B rows (N) are split the same way; each CTA's TMEM
+// receives its own 128 rows of the accumulator.  Per CTA and stage the ring
+// holds A 16 KB + B 16 KB + scales 6 KB = 38 KB, five stages deep.
+//
+//   warp 0      TMA producer of the codes tiles (two tensor copies per K tile);
+//   warp 10     producer of the scale tiles (three 2 KB bulk copies per K tile).
+//               Issuing a TMA copy occupies the issuing thread for about 100
+//               cycles, so with one thread issuing all five the codes tiles of a
+//               freed stage started late;
+//   warp 1      (leader) one lane issues the MMAs and commits them to both CTAs;
+//   warps 6-9   scale warps: shared memory -> registers -> TMEM (tcgen05.st), then
+//               tell the leader that this CTA's scales and codes tiles are ready;
+//   warps 2-5   epilogue: tcgen05.ld of the 32-lane quarter, x alpha (packed
+//               multiplies), bf16, 128-byte swizzled 32 x 64 boxes, TMA stores.
+//               Each warp has two box slots (32 KB in all): it converts two boxes
+//               while the rest of the accumulator is loaded, hands the accumulator
+//               back, and only then issues the stores and converts the last two.
+// Cross-CTA signals: the leader's MMA commits are multicast to both CTAs'
+// barriers; the follower's scale and epilogue warps arrive remotely on the
+// leader's sf_ready / acc_empty barriers.
 // ============================================================================
+constexpr int P_THREADS = 352;                                         // 11 warps
 constexpr int P_B_BYTES = 128 * BKB;                                   // half of N per CTA
 constexpr int P_STAGE_BYTES = A_BYTES + P_B_BYTES + SFA_BYTES + SFB_BYTES;   // 38 KB
-constexpr int P_STAGES = 4;
+constexpr int P_STAGES = 5;
+constexpr int P_STAGING_BYTES = 4 * 2 * BOX_BYTES;                     // two boxes per epilogue warp
 constexpr int P_RING_BYTES = P_STAGES * P_STAGE_BYTES;
-constexpr int P_SLACK = SMEM_LIMIT - P_RING_BYTES - STAGING_BYTES - BAR_BYTES;
-constexpr int P_SMEM_BYTES = P_RING_BYTES + STAGING_BYTES + BAR_BYTES + P_SLACK;
+constexpr int P_SMEM_BYTES = P_RING_BYTES + P_STAGING_BYTES + BAR_BYTES + 1024;   // + base alignment
 static_assert(P_STAGE_BYTES % 1024 == 0, "pair stages must stay 1024-byte aligned");
-static_assert(P_SLACK >= 0 && P_SMEM_BYTES <= SMEM_LIMIT, "pair shared memory budget");
+static_assert(P_SMEM_BYTES <= SMEM_LIMIT, "pair shared memory budget");
 static_assert(SF_COL0 + P_STAGES * SF_STAGE_COLS <= TMEM_COLS, "pair TMEM budget");
 // M = 256 (both CTAs), N = 256
 constexpr uint32_t IDESC_PAIR = (1u << 7) | (1u << 10) | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(256 >> 4) << 24);
@@ -588,17 +602,46 @@ __device__ __forceinline__ void cluster_sync() {
     asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
+// 64 fp32 accumulator columns -> x alpha (packed multiplies) -> bf16 -> one 32 x 64
+// box in shared memory, 128-byte swizzled (16-byte chunk c of row r at chunk
+// c ^ (r & 7)), the layout the TMA store expects.  Lane = row.
+__device__ __forceinline__ void box_to_smem(const uint32_t (&v)[64], uint8_t* box, int lane, float alpha) {
+    uint8_t* row = box + lane * 128;
+    const float2 al = make_float2(alpha, alpha);
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+        uint32_t w[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float2 s = __fmul2_rn(make_float2(__uint_as_float(v[8 * c + 2 * i]),
+                                                    __uint_as_float(v[8 * c + 2 * i + 1])), al);
+            const __nv_bfloat162 h = __float22bfloat162_rn(s);
+            w[i] = *reinterpret_cast<const uint32_t*>(&h);
+        }
+        *reinterpret_cast<uint4*>(row + ((c ^ (lane & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+}
+
+__device__ __forceinline__ void tmem_ld_64cols(uint32_t taddr, uint32_t (&v)[64]) {
+    tmem_ld_32cols_nowait(taddr, *reinterpret_cast<uint32_t (*)[32]>(&v[0]));
+    tmem_ld_32cols_nowait(taddr + 32, *reinterpret_cast<uint32_t (*)[32]>(&v[32]));
+}
+__device__ __forceinline__ void reg_fence64(uint32_t (&v)[64]) {
+    reg_fence32(*reinterpret_cast<uint32_t (*)[32]>(&v[0]));
+    reg_fence32(*reinterpret_cast<uint32_t (*)[32]>(&v[32]));
+}
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
 gemm_nvfp4_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                        const __grid_constant__ CUtensorMap tmD, const Params p) {
     constexpr int STAGES = P_STAGES;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* staging = smem + P_RING_BYTES;
-    uint64_t* full = reinterpret_cast<uint64_t*>(staging + STAGING_BYTES);   // local A/B landed
-    uint64_t* empty = full + STAGES;                     // both CTAs' stage consumed (leader's commit)
+    uint64_t* full = reinterpret_cast<uint64_t*>(staging + P_STAGING_BYTES);   // local A/B landed
+    uint64_t* empty = full + STAGES;                     // the stage's MMAs completed (leader's commit, both CTAs)
     uint64_t* sf_loaded = empty + STAGES;                // local scale tiles landed
-    uint64_t* sf_ready = sf_loaded + STAGES;             // leader: 8 warps wrote scales and saw their A/B
+    uint64_t* sf_ready = sf_loaded + STAGES;             // leader: 8 scale warps wrote TMEM and saw their A/B
     uint64_t* acc_full = sf_ready + STAGES;              // accumulator complete (leader's commit)
     uint64_t* acc_empty = acc_full + 1;                  // leader: 8 epilogue warps drained
     uint64_t* drain = acc_empty + 1;
@@ -642,90 +685,97 @@ gemm_nvfp4_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_con
     const uint32_t sf_ready_leader = map_to_rank(smem_addr(&sf_ready[0]), 0);
     const uint32_t acc_empty_leader = map_to_rank(smem_addr(acc_empty), 0);
 
-    if (warp == 0 && lane == 0) {
-        // ------------------------------------------------ TMA producer (each CTA, its own halves)
-        uint32_t stage = 0, phase = 0;
-        uint32_t issued_mask = 0, issued_phase = 0;
-        bool ok = true;
-        for (int tile = cluster; tile < tiles && ok; tile += nclusters) {
-            int mp, nt;
-            tile_coords(p, tile, m_pairs, mp, nt);
-            const int mrow = mp * 256 + (int)rank * 128;          // this CTA's A rows
-            const int nrow = nt * BN + (int)rank * 128;           // this CTA's B rows
-            const bool second_sfb = (nt * BN + 128) < p.N;
-            // rows past M (the follower's half of the last pair tile) have no scale block:
-            // their codes load as zeros and their output rows are never stored
-            const bool has_sfa = mrow < p.M;
-            const uint32_t sf_bytes = (has_sfa ? SFA_BYTES : 0) + SFB_BYTES - (second_sfb ? 0 : 2048);
-            for (int kt = 0; kt < p.nkt; ++kt) {
-                if (!mbar_wait_bounded(&empty[stage], phase ^ 1u, p.timeout_ns, abort_flag, p.dev_status)) {
-                    ok = false;
-                    break;
+    if (warp == 0 || warp == 10) {
+        // ------------------------------------------------ producers (each CTA, its own halves):
+        // warp 0 the codes tiles, warp 10 the scale tiles, both over the same ring
+        if (lane == 0) {
+            const bool codes = warp == 0;
+            uint64_t* landed = codes ? full : sf_loaded;
+            uint32_t stage = 0, phase = 0;
+            uint32_t issued_mask = 0, issued_phase = 0;
+            bool ok = true;
+            for (int tile = cluster; tile < tiles && ok; tile += nclusters) {
+                int mp, nt;
+                tile_coords(p, tile, m_pairs, mp, nt);
+                const int mrow = mp * 256 + (int)rank * 128;      // this CTA's A rows
+                const int nrow = nt * BN + (int)rank * 128;       // this CTA's B rows
+                const bool second_sfb = (nt * BN + 128) < p.N;
+                // rows past M (the follower's half of the last pair tile) have no scale block:
+                // their codes load as zeros and their output rows are never stored
+                const bool has_sfa = mrow < p.M;
+                const uint32_t sf_bytes = (has_sfa ? SFA_BYTES : 0) + SFB_BYTES - (second_sfb ? 0 : 2048);
+                for (int kt = 0; kt < p.nkt; ++kt) {
+                    if (!mbar_wait_bounded(&empty[stage], phase ^ 1u, p.timeout_ns, abort_flag, p.dev_status)) {
+                        ok = false;
+                        break;
+                    }
+                    uint8_t* sA = smem + stage * P_STAGE_BYTES;
+                    const uint32_t bar = smem_addr(&landed[stage]);
+                    if (codes) {
+                        mbar_arrive_expect_tx(&full[stage], A_BYTES + P_B_BYTES);
+                        tma_load_2d(smem_addr(sA), &tmA, kt * BKB, mrow, bar);
+                        tma_load_2d(smem_addr(sA + A_BYTES), &tmB, kt * BKB, nrow, bar);
+                    } else {
+                        uint8_t* sSFA = sA + A_BYTES + P_B_BYTES;
+                        uint8_t* sSFB = sSFA + SFA_BYTES;
+                        mbar_arrive_expect_tx(&sf_loaded[stage], sf_bytes);
+                        if (has_sfa)
+                            bulk_load(smem_addr(sSFA), p.sfa + ((size_t)(mrow / 128) * p.nkt + kt) * 2048u, 2048u, bar);
+                        bulk_load(smem_addr(sSFB), p.sfb + ((size_t)(2 * nt) * p.nkt + kt) * 2048u, 2048u, bar);
+                        if (second_sfb)
+                            bulk_load(smem_addr(sSFB + 2048), p.sfb + ((size_t)(2 * nt + 1) * p.nkt + kt) * 2048u,
+                                      2048u, bar);
+                    }
+                    issued_mask |= 1u << stage;
+                    issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
+                    if (++stage == STAGES) { stage = 0; phase ^= 1u; }
                 }
-                uint8_t* sA = smem + stage * P_STAGE_BYTES;
-                uint8_t* sB = sA + A_BYTES;
-                uint8_t* sSFA = sB + P_B_BYTES;
-                uint8_t* sSFB = sSFA + SFA_BYTES;
-                const uint32_t sbar = smem_addr(&sf_loaded[stage]);
-                mbar_arrive_expect_tx(&sf_loaded[stage], sf_bytes);
-                if (has_sfa) bulk_load(smem_addr(sSFA), p.sfa + ((size_t)(mrow / 128) * p.nkt + kt) * 2048u, 2048u, sbar);
-                bulk_load(smem_addr(sSFB), p.sfb + ((size_t)(2 * nt) * p.nkt + kt) * 2048u, 2048u, sbar);
-                if (second_sfb)
-                    bulk_load(smem_addr(sSFB + 2048), p.sfb + ((size_t)(2 * nt + 1) * p.nkt + kt) * 2048u, 2048u, sbar);
-                const uint32_t bar = smem_addr(&full[stage]);
-                mbar_arrive_expect_tx(&full[stage], A_BYTES + P_B_BYTES);
-                tma_load_2d(smem_addr(sA), &tmA, kt * BKB, mrow, bar);
-                tma_load_2d(smem_addr(sB), &tmB, kt * BKB, nrow, bar);
-                issued_mask |= 1u << stage;
-                issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
-                if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+            }
+            if (!ok) {   // let every copy this thread started land before the CTA exits
+                for (int s = 0; s < STAGES; ++s)
+                    if (issued_mask & (1u << s))
+                        mbar_wait_bounded(&landed[s], (issued_phase >> s) & 1u, p.timeout_ns, nullptr, p.dev_status);
             }
         }
-        if (!ok) {
-            for (int s = 0; s < STAGES; ++s)
-                if (issued_mask & (1u << s)) {
-                    mbar_wait_bounded(&full[s], (issued_phase >> s) & 1u, p.timeout_ns, nullptr, p.dev_status);
-                    mbar_wait_bounded(&sf_loaded[s], (issued_phase >> s) & 1u, p.timeout_ns, nullptr, p.dev_status);
-                }
-        }
-    } else if (warp == 1 && lane == 0 && leader) {
+    } else if (warp == 1) {
         // ------------------------------------------------ MMA issuer (leader only)
-        uint32_t stage = 0, phase = 0, acc_phase = 0;
-        bool ok = true, issued = false;
-        for (int tile = cluster; tile < tiles && ok; tile += nclusters) {
-            if (!mbar_wait_bounded(acc_empty, acc_phase ^ 1u, p.timeout_ns, abort_flag, p.dev_status)) {
-                ok = false;
-                break;
-            }
-            tc_fence_after();
-            for (int kt = 0; kt < p.nkt; ++kt) {
-                if (!mbar_wait_bounded(&sf_ready[stage], phase, p.timeout_ns, abort_flag, p.dev_status)) {
+        if (lane == 0 && leader) {
+            uint32_t stage = 0, phase = 0, acc_phase = 0;
+            bool ok = true, issued = false;
+            for (int tile = cluster; tile < tiles && ok; tile += nclusters) {
+                if (!mbar_wait_bounded(acc_empty, acc_phase ^ 1u, p.timeout_ns, abort_flag, p.dev_status)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                const uint32_t sA = smem_addr(smem + stage * P_STAGE_BYTES);
-                const uint32_t sB = sA + A_BYTES;
-                const uint32_t tsf = tmem + SF_COL0 + stage * SF_STAGE_COLS;
-                const uint64_t da = desc_sw128(sA), db = desc_sw128(sB);
+                for (int kt = 0; kt < p.nkt; ++kt) {
+                    if (!mbar_wait_bounded(&sf_ready[stage], phase, p.timeout_ns, abort_flag, p.dev_status)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t sA = smem_addr(smem + stage * P_STAGE_BYTES);
+                    const uint64_t da = desc_sw128(sA), db = desc_sw128(sA + A_BYTES);
+                    const uint32_t tsf = tmem + SF_COL0 + stage * SF_STAGE_COLS;
 #pragma unroll
-                for (int j = 0; j < 4; ++j)
-                    tc_mma_pair(tmem + ACC_COL, da + 2 * j, db + 2 * j, IDESC_PAIR, tsf + 4 * j, tsf + 16 + 8 * j,
-                                (kt | j) != 0 ? 1u : 0u);
-                issued = true;
-                tc_commit_pair(smem_addr(&empty[stage]));
-                if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+                    for (int j = 0; j < 4; ++j)
+                        tc_mma_pair(tmem + ACC_COL, da + 2 * j, db + 2 * j, IDESC_PAIR, tsf + 4 * j, tsf + 16 + 8 * j,
+                                    (kt | j) != 0 ? 1u : 0u);
+                    issued = true;
+                    tc_commit_pair(smem_addr(&empty[stage]));
+                    if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+                }
+                if (!ok) break;
+                tc_commit_pair(smem_addr(acc_full));
+                acc_phase ^= 1u;
             }
-            if (!ok) break;
-            tc_commit_pair(smem_addr(acc_full));
-            acc_phase ^= 1u;
-        }
-        if (!ok && issued) {
-            tc_commit_pair(smem_addr(drain));
-            mbar_wait_bounded(drain, 0u, p.timeout_ns, nullptr, p.dev_status);
+            if (!ok && issued) {
+                tc_commit_pair(smem_addr(drain));
+                mbar_wait_bounded(drain, 0u, p.timeout_ns, nullptr, p.dev_status);
+            }
         }
     } else if (warp >= 6) {
-        // ------------------------------------------------ scale loaders (each CTA, its own TMEM)
+        // ------------------------------------------------ scale warps 6-9 (each CTA, its own TMEM)
         const int q = warp & 3;
         const uint32_t tq = tmem + ((uint32_t)(q * 32) << 16);
         uint32_t stage = 0, phase = 0;
@@ -770,33 +820,55 @@ gemm_nvfp4_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_con
                 if (++stage == STAGES) { stage = 0; phase ^= 1u; }
             }
         }
-    } else if (warp >= 2) {
-        // ------------------------------------------------ epilogue (each CTA, its 128 rows)
+    } else {
+        // ------------------------------------------------ epilogue (warps 2-5, each CTA, its 128 rows)
         const int q = warp & 3;
         const float alpha = __fmul_rn(*p.sdec_a, *p.sdec_b);
         const uint32_t tmem_row = tmem + ((uint32_t)(q * 32) << 16);
-        uint8_t* stg = staging + q * (4 * BOX_BYTES);
+        uint8_t* stg = staging + q * (2 * BOX_BYTES);
         uint32_t acc_phase = 0;
         for (int tile = cluster; tile < tiles; tile += nclusters) {
             int mp, nt;
             tile_coords(p, tile, m_pairs, mp, nt);
             const int m0 = mp * 256 + (int)rank * 128 + q * 32, n0 = nt * BN;
+            if (lane == 0) bulk_wait_read0();            // the previous tile's stores have left the slots
+            __syncwarp();
             if (!mbar_wait_bounded(acc_full, acc_phase, p.timeout_ns, abort_flag, p.dev_status)) break;
             tc_fence_after();
+            auto store2 = [&](int b0) {                  // TMA-store boxes b0, b0+1 from the two slots
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0 && m0 < p.M) {
+                    for (int b = 0; b < 2; ++b)
+                        if (n0 + (b0 + b) * BOX_COLS < p.N)
+                            tma_store_2d(&tmD, smem_addr(stg + b * BOX_BYTES), n0 + (b0 + b) * BOX_COLS, m0);
+                    bulk_commit();
+                }
+            };
+            uint32_t va[64], vb[64];
+            tmem_ld_64cols(tmem_row + ACC_COL, va);
+            tmem_ld_64cols(tmem_row + ACC_COL + 64, vb);
+            tmem_ld_wait();
+            reg_fence64(va);
+            reg_fence64(vb);
+            box_to_smem(va, stg, lane, alpha);
+            tmem_ld_64cols(tmem_row + ACC_COL + 128, va);
+            box_to_smem(vb, stg + BOX_BYTES, lane, alpha);
+            tmem_ld_wait();
+            reg_fence64(va);
+            tmem_ld_64cols(tmem_row + ACC_COL + 192, vb);
+            tmem_ld_wait();
+            reg_fence64(vb);
+            // the whole accumulator is in registers or shared memory: hand it back
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cluster(acc_empty_leader);
+            store2(0);
             if (lane == 0) bulk_wait_read0();
             __syncwarp();
-            epilogue_to_smem(tmem_row, stg, lane, alpha, [&] {
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive_cluster(acc_empty_leader);
-            });
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0 && m0 < p.M) {
-                for (int b = 0; b < BN / BOX_COLS; ++b)
-                    if (n0 + b * BOX_COLS < p.N) tma_store_2d(&tmD, smem_addr(stg + b * BOX_BYTES), n0 + b * BOX_COLS, m0);
-                bulk_commit();
-            }
+            box_to_smem(va, stg, lane, alpha);
+            box_to_smem(vb, stg + BOX_BYTES, lane, alpha);
+            store2(2);
             acc_phase ^= 1u;
         }
         if (lane == 0) bulk_wait0();
@@ -878,7 +950,7 @@ cudaError_t launch_pair(const CUtensorMap& ta, const CUtensorMap& tb, const CUte
         if (attr_err != cudaSuccess) return;
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(2 * (sms / 2), 1, 1);
-        cfg.blockDim = dim3(NUM_THREADS, 1, 1);
+        cfg.blockDim = dim3(P_THREADS, 1, 1);
         cfg.dynamicSmemBytes = P_SMEM_BYTES;
         int n = 0;
         if (cudaOccupancyMaxActiveClusters(&n, gemm_nvfp4_pair_kernel, &cfg) != cudaSuccess || n <= 0) n = sms / 2;
@@ -886,7 +958,7 @@ cudaError_t launch_pair(const CUtensorMap& ta, const CUtensorMap& tb, const CUte
     });
     if (attr_err != cudaSuccess) return attr_err;
     const int clusters = std::max(1, std::min(pair_tiles, max_clusters));
-    gemm_nvfp4_pair_kernel<<<2 * clusters, NUM_THREADS, P_SMEM_BYTES, stream>>>(ta, tb, td, p);
+    gemm_nvfp4_pair_kernel<<<2 * clusters, P_THREADS, P_SMEM_BYTES, stream>>>(ta, tb, td, p);
     return cudaGetLastError();
 }
 
