@@ -127,7 +127,9 @@ def test_e2m1_rne_brute_force(oracle_mod):
 # ---------------------------------------------------------------- SR --------------
 
 def test_sr_exact_expectation_by_enumeration(oracle_mod):
-    """E[value] over all 2^16 random values equals lo + (hi-lo) * ceil(p * 2^16) / 2^16."""
+    """E[value] over all 2^16 random values equals lo + (hi-lo) * floor(p * 2^16) / 2^16:
+    adding a uniform 16-bit fraction of the spacing and truncating rounds up for
+    exactly floor(p * 2^16) of the 2^16 values."""
     grid = [0, .5, 1, 1.5, 2, 3, 4, 6]
     r = np.arange(65536, dtype=np.uint32)
     for a in [0.0, 0.1, 0.25, 0.3, 0.5, 0.77, 1.0, 1.2345, 1.99, 2.5, 3.001, 4.0, 4.2, 5.9, 6.0, 7.5]:
@@ -141,7 +143,7 @@ def test_sr_exact_expectation_by_enumeration(oracle_mod):
         hi = min(g for g in grid if g > a32)
         p = Fraction(a32) - Fraction(lo)
         p /= Fraction(hi) - Fraction(lo)
-        n_up = math.ceil(p * 65536)
+        n_up = math.floor(p * 65536)
         expect = Fraction(lo) + (Fraction(hi) - Fraction(lo)) * Fraction(n_up, 65536)
         assert Fraction(int(np.sum(vals * 2)), 2 * 65536) == expect, a
         assert set(np.unique(vals)).issubset({lo, hi})
@@ -221,13 +223,38 @@ def test_sr_bits_uniform_chi_square(oracle_mod):
 
 
 def test_sr_bits_layout_in_philox_words(oracle_mod):
+    """One Philox call per 16 elements; elements 4k..4k+3 split word k into
+    A = bytes (2, 0), A reversed, B = bytes (3, 1), B reversed."""
     seed = 0x0123456789ABCDEF
-    idx = np.arange(64, dtype=np.uint64)
+    idx = np.arange(96, dtype=np.uint64)
     got = oracle_mod.sr_bits(seed, 1, 5, idx)
-    for i in range(64):
-        w = oracle_mod.philox4x32_10([i >> 3, 0, 1, 5], [seed & 0xFFFFFFFF, seed >> 32])
-        word = int(w[(i >> 1) & 3])
-        assert got[i] == ((word >> 16) if i & 1 else (word & 0xFFFF))
+
+    def rev16(v):
+        return int(format(v, "016b")[::-1], 2)
+
+    for i in range(96):
+        w = oracle_mod.philox4x32_10([i >> 4, 0, 1, 5], [seed & 0xFFFFFFFF, seed >> 32])
+        word = int(w[(i >> 2) & 3])
+        a = (((word >> 16) & 0xFF) << 8) | (word & 0xFF)
+        b = (((word >> 24) & 0xFF) << 8) | ((word >> 8) & 0xFF)
+        assert got[i] == [a, rev16(a), b, rev16(b)][i & 3], i
+
+
+def test_sr_decisions_of_paired_elements_are_unbiased(oracle_mod):
+    """Elements 4k and 4k+1 draw on the same 16 bits (one reversed): each is still
+    exactly uniform, so each element's SR stays unbiased; and the pair is not
+    degenerate (both round-up events occur together about p^2 of the time)."""
+    n = 1 << 16
+    bits = oracle_mod.sr_bits(seed=5, stream=0, offset=0, idx=np.arange(4 * n, dtype=np.uint64)).reshape(n, 4)
+    for c in range(4):
+        hist = np.bincount(bits[:, c] >> 12, minlength=16)
+        assert float(((hist - n / 16) ** 2 / (n / 16)).sum()) < 45.0        # 15 dof
+    y = np.full(n, 1.3, np.float32)                                      # p = 0.6 on [1, 1.5)
+    up0 = oracle_mod.e2m1_encode_sr(y, bits[:, 0]) == 3
+    up1 = oracle_mod.e2m1_encode_sr(y, bits[:, 1]) == 3
+    for u in (up0, up1):
+        assert abs(u.mean() - 0.6) < 4 * math.sqrt(0.24 / n)
+    assert abs((up0 & up1).mean() - 0.36) < 0.02
 
 
 # ---------------------------------------------------------------- RHT --------------
