@@ -37,7 +37,11 @@ __global__ void debug_e4m3_kernel(const float* v, int64_t n, uint8_t* out) {
 __global__ void debug_e2m1_kernel(const float* y, const uint32_t* r16, int64_t n, int round, int hw, uint8_t* out) {
     for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
         uint32_t c;
-        if (round == NVFP4_ROUND_SR) c = e2m1x2_hw(0.0f, e2m1_sr_value(y[i], r16[i] & 0xFFFFu)) & 0xFu;
+        if (round == NVFP4_ROUND_SR) {
+            // value 0 of the four-wide conversion draws R from bits 16-23 : bits 0-7
+            const uint32_t r = r16[i] & 0xFFFFu;
+            c = e2m1x4_sr(y[i], 0.0f, 0.0f, 0.0f, ((r >> 8) << 16) | (r & 0xFFu)) & 0xFu;
+        }
         else if (hw) c = e2m1x2_hw(0.0f, y[i]) & 0xFu;
         else c = e2m1_rne_sw(y[i]);
         out[i] = (uint8_t)c;

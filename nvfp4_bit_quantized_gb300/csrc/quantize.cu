@@ -342,7 +342,6 @@ __global__ void __launch_bounds__(kThreads) encode_row_kernel(const T* __restric
                                                               int nparts, QOut out, uint64_t sr_seed,
                                                               uint32_t sr_offset, int v8, uint32_t* dev_status) {
     using B = Block16<T>;
-    constexpr int U = 2;
     const Scales sc = tensor_scales(partials, nparts, out.s_dec, dev_status);
     const PhiloxKey key = philox_key(sr_seed);
     const int lane = threadIdx.x & 31;
@@ -352,50 +351,51 @@ __global__ void __launch_bounds__(kThreads) encode_row_kernel(const T* __restric
     const int64_t nkb = (C + 255) / 256;
     const int64_t warp0 = (int64_t)blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5);
     const int64_t nwarps = (int64_t)gridDim.x * (kThreads / 32);
-    if (nseg == 0) return;
+    if (warp0 >= nseg) return;
+    // One warp segment per iteration; the next segment's load is issued before this
+    // one is encoded, so a load is always in flight behind the arithmetic.
     Walk2D w(warp0, nwarps, spr);
-    for (int64_t base = warp0; base < nseg; base += nwarps * U) {
-        uint32_t raw[U][B::WORDS];
-        int64_t rr[U], blk[U];
-        bool valid[U];
+    uint32_t raw[B::WORDS];
+    int64_t rr = w.row, blk = w.col * 32 + lane;
+    bool valid = blk < bpr;
+    if (valid) B::load(x + rr * ldx + blk * 16, v8 != 0, raw);
+    for (int64_t seg = warp0; seg < nseg; seg += nwarps) {
+        uint32_t cur[B::WORDS];
 #pragma unroll
-        for (int u = 0; u < U; ++u) {
-            const int64_t seg = base + (int64_t)u * nwarps;
-            rr[u] = w.row;
-            blk[u] = w.col * 32 + lane;
-            valid[u] = seg < nseg && blk[u] < bpr;
-            if (valid[u]) B::load(x + rr[u] * ldx + blk[u] * 16, v8 != 0, raw[u]);
-            w.advance();
+        for (int i = 0; i < B::WORDS; ++i) cur[i] = raw[i];
+        const int64_t r = rr, bk = blk;
+        const bool ok = valid;
+        w.advance();
+        rr = w.row;
+        blk = w.col * 32 + lane;
+        valid = seg + nwarps < nseg && blk < bpr;
+        if (valid) B::load(x + rr * ldx + blk * 16, v8 != 0, raw);
+        if (!ok) continue;
+        float f[16];
+        B::unpack(cur, f);
+        float amax = 0.0f;
+#pragma unroll
+        for (int j = 0; j < 16; ++j) amax = fmaxf(amax, fabsf(f[j]));
+        const uint32_t sb = block_scale_code(amax, sc.s_enc);
+        const float2 eb = make_float2(g_eb_table[sb], g_eb_table[sb]);
+        float y[16];
+#pragma unroll
+        for (int j = 0; j < 16; j += 2) {
+            const float2 v = __fmul2_rn(make_float2(f[j], f[j + 1]), eb);
+            y[j] = v.x;
+            y[j + 1] = v.y;
         }
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-            if (!valid[u]) continue;
-            float f[16];
-            B::unpack(raw[u], f);
-            float amax = 0.0f;
-#pragma unroll
-            for (int j = 0; j < 16; ++j) amax = fmaxf(amax, fabsf(f[j]));
-            const uint32_t sb = block_scale_code(amax, sc.s_enc);
-            const float e_b = g_eb_table[sb];
-            const int64_t r = rr[u], col = blk[u] * 16;
-            float ylo[8], yhi[8];
-            if constexpr (SR) {
-                const uint64_t g0 = (uint64_t)(r * C + col) >> 3;     // C % 16 == 0: 8-aligned
-                const Philox4 p0 = sr_philox(key, 0u, sr_offset, g0);
-                const Philox4 p1 = sr_philox(key, 0u, sr_offset, g0 + 1);
-#pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    ylo[j] = e2m1_sr_value(__fmul_rn(f[j], e_b), sr_r16(p0, j));
-                    yhi[j] = e2m1_sr_value(__fmul_rn(f[8 + j], e_b), sr_r16(p1, j));
-                }
-            } else {
-#pragma unroll
-                for (int j = 0; j < 8; ++j) { ylo[j] = __fmul_rn(f[j], e_b); yhi[j] = __fmul_rn(f[8 + j], e_b); }
-            }
-            *reinterpret_cast<uint2*>(out.codes + r * (C / 2) + col / 2) = make_uint2(e2m1x8_rn(ylo), e2m1x8_rn(yhi));
-            if (out.scales) out.scales[r * bpr + blk[u]] = (uint8_t)sb;
-            if (out.scales_mma) out.scales_mma[mma_sf_offset(r, blk[u], nkb)] = (uint8_t)sb;
+        const int64_t col = bk * 16;
+        uint2 codes;
+        if constexpr (SR) {
+            const Philox4 p = sr_philox(key, 0u, sr_offset, (uint64_t)(r * C + col) >> 4);   // C % 16 == 0
+            codes = e2m1x16_sr(y, p.w);
+        } else {
+            codes = e2m1x16_rn(y);
         }
+        *reinterpret_cast<uint2*>(out.codes + r * (C / 2) + col / 2) = codes;
+        if (out.scales) out.scales[r * bpr + bk] = (uint8_t)sb;
+        if (out.scales_mma) out.scales_mma[mma_sf_offset(r, bk, nkb)] = (uint8_t)sb;
     }
 }
 
@@ -434,24 +434,22 @@ __global__ void __launch_bounds__(kThreads) encode_col_kernel(const T* __restric
             const uint32_t sb = block_scale_code(amax, sc.s_enc);
             const float e_b = g_eb_table[sb];
             const int64_t c = c0 + j;                // operand row
-            float ylo[8], yhi[8];
-            if constexpr (SR) {
-                const uint64_t idx0 = (uint64_t)(c * R + r0);
-                const Philox4 p0 = sr_philox(key, 1u, sr_offset, idx0 >> 3);
-                const Philox4 p1 = sr_philox(key, 1u, sr_offset, (idx0 >> 3) + 1);
+            const float2 eb = make_float2(e_b, e_b);
+            float y[16];
 #pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    ylo[i] = e2m1_sr_value(__fmul_rn(t[j][i], e_b), sr_r16(p0, i));
-                    yhi[i] = e2m1_sr_value(__fmul_rn(t[j][8 + i], e_b), sr_r16(p1, i));
-                }
-            } else {
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    ylo[i] = __fmul_rn(t[j][i], e_b);
-                    yhi[i] = __fmul_rn(t[j][8 + i], e_b);
-                }
+            for (int i = 0; i < 16; i += 2) {
+                const float2 v = __fmul2_rn(make_float2(t[j][i], t[j][i + 1]), eb);
+                y[i] = v.x;
+                y[i + 1] = v.y;
             }
-            *reinterpret_cast<uint2*>(out.codes + c * (R / 2) + r0 / 2) = make_uint2(e2m1x8_rn(ylo), e2m1x8_rn(yhi));
+            uint2 codes;
+            if constexpr (SR) {
+                const Philox4 p = sr_philox(key, 1u, sr_offset, (uint64_t)(c * R + r0) >> 4);   // r0 % 16 == 0
+                codes = e2m1x16_sr(y, p.w);
+            } else {
+                codes = e2m1x16_rn(y);
+            }
+            *reinterpret_cast<uint2*>(out.codes + c * (R / 2) + r0 / 2) = codes;
             const int64_t s = r0 / 16;
             if (out.scales) out.scales[c * (R / 16) + s] = (uint8_t)sb;
             if (out.scales_mma) out.scales_mma[mma_sf_offset(c, s, nkb)] = (uint8_t)sb;
@@ -504,20 +502,26 @@ __global__ void __launch_bounds__(kThreads) encode_2d_kernel(const T* __restrict
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
             float y[VEC];
-            if constexpr (SR) {
-                const uint64_t idx0 = (uint64_t)((r0 + i) * C + c0);
-                const Philox4 p = sr_philox(key, 0u, sr_offset, idx0 >> 3);
-                const bool upper = (VEC == 4) && (idx0 & 4);
 #pragma unroll
-                for (int j = 0; j < VEC; ++j)
-                    y[j] = e2m1_sr_value(__fmul_rn(t[j][i], e_b), upper ? sr_r16(p, 4 + j) : sr_r16(p, j));
-            } else {
-#pragma unroll
-                for (int j = 0; j < VEC; ++j) y[j] = __fmul_rn(t[j][i], e_b);
-            }
+            for (int j = 0; j < VEC; ++j) y[j] = __fmul_rn(t[j][i], e_b);
             uint32_t packed;
-            if constexpr (VEC == 8) packed = e2m1x8_rn(y);
-            else packed = e2m1x4_rn(y);
+            if constexpr (SR) {
+                // elements idx0 .. idx0+VEC-1 use words ((idx0 >> 2) & 3) .. of their 16-element call
+                const uint64_t idx0 = (uint64_t)((r0 + i) * C + c0);
+                const Philox4 p = sr_philox(key, 0u, sr_offset, idx0 >> 4);
+                if constexpr (VEC == 8) {
+                    const bool hi = (idx0 & 8) != 0;
+                    packed = e2m1x4_sr(y[0], y[1], y[2], y[3], hi ? p.w[2] : p.w[0]) |
+                             (e2m1x4_sr(y[4], y[5], y[6], y[7], hi ? p.w[3] : p.w[1]) << 16);
+                } else {
+                    const uint32_t k = (uint32_t)(idx0 >> 2) & 3u;
+                    const uint32_t word = k == 0 ? p.w[0] : k == 1 ? p.w[1] : k == 2 ? p.w[2] : p.w[3];
+                    packed = e2m1x4_sr(y[0], y[1], y[2], y[3], word);
+                }
+            } else {
+                if constexpr (VEC == 8) packed = e2m1x8_rn(y);
+                else packed = e2m1x4_rn(y);
+            }
             uint8_t* dst = out.codes + (r0 + i) * (C / 2) + c0 / 2;
             if constexpr (VEC == 8) *reinterpret_cast<uint32_t*>(dst) = packed;
             else *reinterpret_cast<uint16_t*>(dst) = (uint16_t)packed;
