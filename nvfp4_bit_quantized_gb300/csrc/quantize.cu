@@ -23,6 +23,8 @@
 #include <cstdint>
 #include <cstdio>
 #include <mutex>
+#include <set>
+#include <utility>
 
 #include "device_common.cuh"
 #include "host_common.h"
@@ -136,14 +138,84 @@ __global__ void __launch_bounds__(kThreads) amax_flat_kernel(const T* __restrict
     block_max_store(m, partials);
 }
 
-// Loads the 16-row x VEC-column patch at (r0, c0) into t[col][row] as fp32.
+// ---- Patch pipeline.  The column and 16x16 kernels (and the RHT maxima) give each
+// lane a 16-row x 16-byte patch of a warp's 64-row x (8 * 16 B) tile.  Their per-patch
+// arithmetic is long and their register footprint leaves one CTA per SM, so each
+// lane copies its next patch global -> shared memory with cp.async (no registers held)
+// while it transforms the current one: two slots per lane, laid out [slot][row][lane]
+// x 16 B so that reading a row back is one conflict-free 512-byte access per warp.
+extern __shared__ __align__(16) uint8_t patch_smem[];
+constexpr int kPatchSlotBytes = 16 * 32 * 16;
+constexpr int kPatchSmemBytes = (kThreads / 32) * 2 * kPatchSlotBytes;    // 128 KB per CTA
+
 template <typename T>
-__device__ __forceinline__ void load_patch(const T* __restrict__ x, int64_t ldx, int64_t r0, int64_t c0,
-                                           float (&t)[Vec<T>::N][16]) {
-    constexpr int VEC = Vec<T>::N;
-    uint4 v[16];
+struct PatchPipe {
+    static constexpr int VEC = Vec<T>::N;
+    const T* x;
+    int64_t ldx, R, C, tiles, nwarps, tile;
+    Walk2D w;
+    int rg, cc;
+    uint32_t sbase;                 // shared address of this lane's slot 0, row 0
+    uint32_t slot = 0, rslot = 0;
+    int64_t r0 = 0, c0 = 0, nr0 = 0, nc0 = 0;   // current patch / the one in flight
+    bool ok = false, nok = false;
+
+    __device__ __forceinline__ PatchPipe(const T* x_, int64_t ldx_, int64_t R_, int64_t C_, int64_t warp0,
+                                         int64_t nwarps_, int64_t tiles_, int64_t tiles_c, uint8_t* smem)
+        : x(x_), ldx(ldx_), R(R_), C(C_), tiles(tiles_), nwarps(nwarps_), tile(warp0),
+          w(warp0, nwarps_, tiles_c > 0 ? tiles_c : 1) {
+        const int lane = threadIdx.x & 31;
+        rg = lane >> 3;
+        cc = lane & 7;
+        sbase = smem_addr(smem) + (uint32_t)((threadIdx.x >> 5) * 2 * kPatchSlotBytes + lane * 16);
+        if (tile < tiles) issue(0);
+        else commit();
+    }
+    __device__ __forceinline__ static void commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+    // copies the patch at the walker's position into slot s (one commit group)
+    __device__ __forceinline__ void issue(uint32_t s) {
+        nr0 = w.row * 64 + rg * 16;
+        nc0 = w.col * (8 * VEC) + cc * VEC;
+        nok = nr0 < R && nc0 < C;
+        if (nok) {
+            const char* src = reinterpret_cast<const char*>(x + nr0 * ldx + nc0);
+            const int64_t pitch = ldx * (int64_t)sizeof(T);
 #pragma unroll
-    for (int i = 0; i < 16; ++i) v[i] = ld_stream(x + (r0 + i) * ldx + c0);
+            for (int i = 0; i < 16; ++i)
+                asm volatile("cp.async.cg.shared.global [%0], [%1], 16;"
+                             :: "r"(sbase + s * kPatchSlotBytes + i * 512), "l"(src + i * pitch) : "memory");
+        }
+        commit();
+    }
+    // Makes the next patch of this warp current (r0, c0, ok) and starts the copy of the
+    // one after it; false when the warp has no patch left.
+    __device__ __forceinline__ bool next() {
+        if (tile >= tiles) return false;
+        r0 = nr0;
+        c0 = nc0;
+        ok = nok;
+        rslot = slot;
+        slot ^= 1u;
+        w.advance();
+        if (tile + nwarps < tiles) issue(slot);
+        else commit();
+        tile += nwarps;
+        asm volatile("cp.async.wait_group 1;" ::: "memory");     // the current patch has landed
+        return true;
+    }
+    __device__ __forceinline__ void read(uint4 (&v)[16]) const {
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+            asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                         : "=r"(v[i].x), "=r"(v[i].y), "=r"(v[i].z), "=r"(v[i].w)
+                         : "r"(sbase + rslot * kPatchSlotBytes + i * 512) : "memory");
+    }
+};
+
+// Unpacks a patch into t[col][row] as fp32.
+template <typename T>
+__device__ __forceinline__ void unpack_patch(const uint4 (&v)[16], float (&t)[Vec<T>::N][16]) {
+    constexpr int VEC = Vec<T>::N;
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
         float f[VEC];
@@ -153,27 +225,109 @@ __device__ __forceinline__ void load_patch(const T* __restrict__ x, int64_t ldx,
     }
 }
 
+// ---- bf16 patches: 16 rows x 8 columns per thread, kept as column pairs so the
+// transform and the scaling use packed two-wide fp32 instructions.
+
+// max(|m|, |v|), NaN propagating (the sign bit of the result is unspecified).
+__device__ __forceinline__ float max_abs_nan(float m, float v) {
+    float r;
+    asm("max.NaN.xorsign.abs.f32 %0, %1, %2;" : "=f"(r) : "f"(m), "f"(v));
+    return r;
+}
+__device__ __forceinline__ uint32_t max_abs_nan_bf16x2(uint32_t m, uint32_t v) {
+    uint32_t r;
+    asm("max.NaN.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(m), "r"(v));
+    return r;
+}
+// The larger |.| of a packed bf16 pair as fp32 bits (NaN sorts above Inf).
+__device__ __forceinline__ uint32_t bf16x2_abs_max_bits(uint32_t m) {
+    m &= 0x7FFF7FFFu;
+    return max(m << 16, m & 0xFFFF0000u);
+}
+
+// Unpacks a bf16 patch as t[k][i] = (x[r0+i][c0+2k], x[r0+i][c0+2k+1]), negating row i
+// where bit i of `neg` is set (the RHT signs).  With PLAIN, returns the packed bf16 |x|
+// maximum of the patch (NaN propagating), else 0.
+template <bool PLAIN>
+__device__ __forceinline__ uint32_t unpack_patch_bf16(const uint4 (&v)[16], uint32_t neg, float2 (&t)[4][16]) {
+    uint32_t m = 0u;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        const uint32_t s = ((neg >> i) & 1u) ? 0x80008000u : 0u;
+        const uint32_t w[4] = {v[i].x ^ s, v[i].y ^ s, v[i].z ^ s, v[i].w ^ s};
+        if (PLAIN) m = max_abs_nan_bf16x2(m, max_abs_nan_bf16x2(max_abs_nan_bf16x2(w[0], w[1]),
+                                                                max_abs_nan_bf16x2(w[2], w[3])));
+#pragma unroll
+        for (int k = 0; k < 4; ++k) t[k][i] = make_float2(bf16_lo(w[k]), bf16_hi(w[k]));
+    }
+    return m;
+}
+
+// The 16-point Hadamard butterflies of two columns at once, unnormalised (the 1/4 of
+// the transform is applied by the caller): h = 1, 2, 4, 8, lower index first,
+// (t_i, t_{i+h}) <- (t_i + t_{i+h}, t_i - t_{i+h}), each one fp32 RN operation.
+__device__ __forceinline__ void hadamard16_x2(float2 (&t)[16]) {
+    const float2 neg1 = make_float2(-1.0f, -1.0f);
+#pragma unroll
+    for (int h = 1; h < 16; h <<= 1) {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            if ((i & h) == 0) {
+                const float2 a = t[i], b = t[i + h];
+                t[i] = __fadd2_rn(a, b);
+                t[i + h] = __ffma2_rn(b, neg1, a);           // a - b, one rounding
+            }
+        }
+    }
+}
+
+// For bf16 inputs every RHT intermediate is a multiple of 2^-133 (the bf16 quantum), so
+// multiplying by 1/4 is exact; the quarter is folded into the block and tensor maxima
+// (max|t/4| = max|t| / 4) and into the element multiplier (t * (e_b / 4) == (t / 4) * e_b
+// whenever e_b / 4 is exact, i.e. e_b >= 2^-124; the smallest e_b of a tensor belongs to the
+// largest scale code 126, so one check per CTA decides).
+
 // amax of RHT(x) along rows: the Wgrad operands' tensor amax after the transform.
 template <typename T>
 __global__ void __launch_bounds__(kThreads) amax_rht_kernel(const T* __restrict__ x, int64_t R, int64_t C,
                                                             int64_t ldx, uint64_t rht_seed,
                                                             uint32_t* __restrict__ partials) {
     constexpr int VEC = Vec<T>::N;
-    const int lane = threadIdx.x & 31, rg = lane >> 3, cc = lane & 7;
     const int64_t tiles_c = (C + 8 * VEC - 1) / (8 * VEC);
     const int64_t tiles = ((R + 63) / 64) * tiles_c;
     const int64_t warp0 = (int64_t)blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5);
     const int64_t nwarps = (int64_t)gridDim.x * (kThreads / 32);
     const uint32_t sign_mask = rht_sign_mask(rht_seed);
+    if constexpr (sizeof(T) == 2) {
+        float m = 0.0f;
+        PatchPipe<T> pp(x, ldx, R, C, warp0, nwarps, tiles, tiles_c, patch_smem);
+        while (pp.next()) {
+            if (!pp.ok) continue;
+            const int64_t r0 = pp.r0, c0 = pp.c0;
+            uint4 v[16];
+            pp.read(v);
+            float2 t[4][16];
+            unpack_patch_bf16<false>(v, sign_mask, t);
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                hadamard16_x2(t[k]);
+#pragma unroll
+                for (int i = 0; i < 16; ++i) m = max_abs_nan(max_abs_nan(m, t[k][i].x), t[k][i].y);
+            }
+        }
+        block_max_store(__float_as_uint(__fmul_rn(fabsf(m), 0.25f)) & 0x7FFFFFFFu, partials);
+        return;
+    }
     float m = 0.0f;
     bool bad = false;                                // NaN: fmaxf would drop it
-    Walk2D w(warp0, nwarps, tiles_c > 0 ? tiles_c : 1);
-    for (int64_t tile = warp0; tile < tiles; tile += nwarps, w.advance()) {
-        const int64_t r0 = w.row * 64 + rg * 16;
-        const int64_t c0 = w.col * (8 * VEC) + cc * VEC;
-        if (r0 >= R || c0 >= C) continue;
+    PatchPipe<T> pp(x, ldx, R, C, warp0, nwarps, tiles, tiles_c, patch_smem);
+    while (pp.next()) {
+        if (!pp.ok) continue;
+        const int64_t r0 = pp.r0, c0 = pp.c0;
+        uint4 v[16];
+        pp.read(v);
         float t[VEC][16];
-        load_patch<T>(x, ldx, r0, c0, t);
+        unpack_patch<T>(v, t);
 #pragma unroll
         for (int j = 0; j < VEC; ++j) {
             rht16(t[j], sign_mask);
@@ -196,7 +350,6 @@ __global__ void __launch_bounds__(kThreads) amax_dual_kernel(const T* __restrict
                                                              uint32_t* __restrict__ partials_plain,
                                                              uint32_t* __restrict__ partials_rht) {
     constexpr int VEC = Vec<T>::N;
-    const int lane = threadIdx.x & 31, rg = lane >> 3, cc = lane & 7;
     const int64_t tiles_c = (C + 8 * VEC - 1) / (8 * VEC);
     const int64_t tiles = ((R + 63) / 64) * tiles_c;
     const int64_t warp0 = (int64_t)blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5);
@@ -204,13 +357,34 @@ __global__ void __launch_bounds__(kThreads) amax_dual_kernel(const T* __restrict
     const uint32_t sign_mask = rht_sign_mask(rht_seed);
     float mp = 0.0f, mr = 0.0f;
     bool bad = false;
-    Walk2D w(warp0, nwarps, tiles_c > 0 ? tiles_c : 1);
-    for (int64_t tile = warp0; tile < tiles; tile += nwarps, w.advance()) {
-        const int64_t r0 = w.row * 64 + rg * 16;
-        const int64_t c0 = w.col * (8 * VEC) + cc * VEC;
-        if (r0 >= R || c0 >= C) continue;
+    if constexpr (sizeof(T) == 2) {
+        uint32_t mpk = 0u;                           // packed bf16 |x| maxima
+        PatchPipe<T> pp(x, ldx, R, C, warp0, nwarps, tiles, tiles_c, patch_smem);
+        while (pp.next()) {
+            if (!pp.ok) continue;
+            const int64_t r0 = pp.r0, c0 = pp.c0;
+            uint4 v[16];
+            pp.read(v);
+            float2 t[4][16];
+            mpk = max_abs_nan_bf16x2(mpk, unpack_patch_bf16<true>(v, sign_mask, t));
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                hadamard16_x2(t[k]);
+#pragma unroll
+                for (int i = 0; i < 16; ++i) mr = max_abs_nan(max_abs_nan(mr, t[k][i].x), t[k][i].y);
+            }
+        }
+        mp = __uint_as_float(bf16x2_abs_max_bits(mpk));
+        mr = __uint_as_float(__float_as_uint(__fmul_rn(fabsf(mr), 0.25f)) & 0x7FFFFFFFu);
+    } else {
+    PatchPipe<T> pp(x, ldx, R, C, warp0, nwarps, tiles, tiles_c, patch_smem);
+    while (pp.next()) {
+        if (!pp.ok) continue;
+        const int64_t r0 = pp.r0, c0 = pp.c0;
+        uint4 v[16];
+        pp.read(v);
         float t[VEC][16];
-        load_patch<T>(x, ldx, r0, c0, t);
+        unpack_patch<T>(v, t);
 #pragma unroll
         for (int j = 0; j < VEC; ++j) {
 #pragma unroll
@@ -227,6 +401,7 @@ __global__ void __launch_bounds__(kThreads) amax_dual_kernel(const T* __restrict
                 bad |= !(a <= FLT_MAX);
             }
         }
+    }
     }
     __shared__ uint32_t red[2][kThreads / 32];
     uint32_t vp = bad ? 0x7FC00000u : __float_as_uint(mp);
@@ -412,19 +587,76 @@ __global__ void __launch_bounds__(kThreads) encode_col_kernel(const T* __restric
     const uint32_t sign_mask = RHT ? rht_sign_mask(rht_seed) : 0u;
     const Scales sc = tensor_scales(partials, nparts, out.s_dec, dev_status);
     const PhiloxKey key = philox_key(sr_seed);
-    const int lane = threadIdx.x & 31, rg = lane >> 3, cc = lane & 7;
     const int64_t tiles_c = (C + 8 * VEC - 1) / (8 * VEC);
     const int64_t tiles = ((R + 63) / 64) * tiles_c;
     const int64_t nkb = (R + 255) / 256;             // operand cols = R
     const int64_t warp0 = (int64_t)blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5);
     const int64_t nwarps = (int64_t)gridDim.x * (kThreads / 32);
-    Walk2D w(warp0, nwarps, tiles_c > 0 ? tiles_c : 1);
-    for (int64_t tile = warp0; tile < tiles; tile += nwarps, w.advance()) {
-        const int64_t r0 = w.row * 64 + rg * 16;
-        const int64_t c0 = w.col * (8 * VEC) + cc * VEC;
-        if (r0 >= R || c0 >= C) continue;
+    if constexpr (sizeof(T) == 2) {
+        // the quarter of the transform folds into e_b when the smallest e_b (code 126) stays exact
+        const bool fold = !RHT || __fmul_rn(g_eb_table[126], 0.25f) >= FLT_MIN;
+        const float quarter = RHT ? 0.25f : 1.0f;
+        PatchPipe<T> pp(x, ldx, R, C, warp0, nwarps, tiles, tiles_c, patch_smem);
+        while (pp.next()) {
+            if (!pp.ok) continue;
+            const int64_t r0 = pp.r0, c0 = pp.c0;
+            uint4 v[16];
+            pp.read(v);
+            float2 t[4][16];
+            unpack_patch_bf16<false>(v, sign_mask, t);
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {                // columns c0 + 2k, c0 + 2k + 1
+                if constexpr (RHT) hadamard16_x2(t[k]);
+                float m0 = 0.0f, m1 = 0.0f;
+#pragma unroll
+                for (int i = 0; i < 16; ++i) { m0 = max_abs_nan(m0, t[k][i].x); m1 = max_abs_nan(m1, t[k][i].y); }
+                const uint32_t sb0 = block_scale_code(__fmul_rn(fabsf(m0), quarter), sc.s_enc);
+                const uint32_t sb1 = block_scale_code(__fmul_rn(fabsf(m1), quarter), sc.s_enc);
+                float2 eb = make_float2(g_eb_table[sb0], g_eb_table[sb1]);
+                if (fold) eb = __fmul2_rn(eb, make_float2(quarter, quarter));
+                float y0[16], y1[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    float2 v = t[k][i];
+                    if (!fold) v = __fmul2_rn(v, make_float2(0.25f, 0.25f));
+                    v = __fmul2_rn(v, eb);
+                    y0[i] = v.x;
+                    y1[i] = v.y;
+                }
+                const int64_t c = c0 + 2 * k;            // operand rows c, c + 1
+                uint2 codes0, codes1;
+                if constexpr (SR) {
+                    const Philox4 p0 = sr_philox(key, 1u, sr_offset, (uint64_t)(c * R + r0) >> 4);   // r0 % 16 == 0
+                    const Philox4 p1 = sr_philox(key, 1u, sr_offset, (uint64_t)((c + 1) * R + r0) >> 4);
+                    codes0 = e2m1x16_sr(y0, p0.w);
+                    codes1 = e2m1x16_sr(y1, p1.w);
+                } else {
+                    codes0 = e2m1x16_rn(y0);
+                    codes1 = e2m1x16_rn(y1);
+                }
+                *reinterpret_cast<uint2*>(out.codes + c * (R / 2) + r0 / 2) = codes0;
+                *reinterpret_cast<uint2*>(out.codes + (c + 1) * (R / 2) + r0 / 2) = codes1;
+                const int64_t s = r0 / 16;
+                if (out.scales) {
+                    out.scales[c * (R / 16) + s] = (uint8_t)sb0;
+                    out.scales[(c + 1) * (R / 16) + s] = (uint8_t)sb1;
+                }
+                if (out.scales_mma) {
+                    out.scales_mma[mma_sf_offset(c, s, nkb)] = (uint8_t)sb0;
+                    out.scales_mma[mma_sf_offset(c + 1, s, nkb)] = (uint8_t)sb1;
+                }
+            }
+        }
+        return;
+    }
+    PatchPipe<T> pp(x, ldx, R, C, warp0, nwarps, tiles, tiles_c, patch_smem);
+    while (pp.next()) {
+        if (!pp.ok) continue;
+        const int64_t r0 = pp.r0, c0 = pp.c0;
+        uint4 v[16];
+        pp.read(v);
         float t[VEC][16];
-        load_patch<T>(x, ldx, r0, c0, t);
+        unpack_patch<T>(v, t);
 #pragma unroll
         for (int j = 0; j < VEC; ++j) {
             if constexpr (RHT) rht16(t[j], sign_mask);
@@ -469,22 +701,23 @@ __global__ void __launch_bounds__(kThreads) encode_2d_kernel(const T* __restrict
     constexpr int LPT = 16 / VEC;                    // lanes per 16-column tile
     const Scales sc = tensor_scales(partials, nparts, out.s_dec, dev_status);
     const PhiloxKey key = philox_key(sr_seed);
-    const int lane = threadIdx.x & 31, rg = lane >> 3, cc = lane & 7;
+    const int lane = threadIdx.x & 31, cc = lane & 7;
     const int64_t tiles_c = (C + 8 * VEC - 1) / (8 * VEC);
     const int64_t tiles = ((R + 63) / 64) * tiles_c;
     const int64_t nkb = (C + 255) / 256, nkb_t = (R + 255) / 256;
     const int64_t warp0 = (int64_t)blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5);
     const int64_t nwarps = (int64_t)gridDim.x * (kThreads / 32);
-    Walk2D w(warp0, nwarps, tiles_c > 0 ? tiles_c : 1);
-    for (int64_t tile = warp0; tile < tiles; tile += nwarps, w.advance()) {
-        const int64_t r0 = w.row * 64 + rg * 16;
-        const int64_t c0 = w.col * (8 * VEC) + cc * VEC;
+    PatchPipe<T> pp(x, ldx, R, C, warp0, nwarps, tiles, tiles_c, patch_smem);
+    while (pp.next()) {
+        const int64_t r0 = pp.r0, c0 = pp.c0;
         // every lane takes part in the shuffles; invalid ones contribute 0
-        const bool valid = (r0 < R) && (c0 < C);
+        const bool valid = pp.ok;
         float t[VEC][16];
         float amax = 0.0f;
         if (valid) {
-            load_patch<T>(x, ldx, r0, c0, t);
+            uint4 v[16];
+            pp.read(v);
+            unpack_patch<T>(v, t);
 #pragma unroll
             for (int j = 0; j < VEC; ++j)
 #pragma unroll
@@ -602,19 +835,56 @@ int amax_grid(int sms, int64_t R, int64_t C, bool is16) {
     return std::min(g, kMaxPartials);
 }
 
-// Pass 1 for one quantization: per-CTA partial maxima of |x| or |RHT(x)|.
+// Grid of the patch kernels: one CTA (eight warps) per SM at most, one warp per
+// 64 x (8 * 16 B) tile at least.
+int patch_grid(int sms, int64_t R, int64_t C, bool is16) {
+    const int vec = is16 ? 8 : 4;
+    const int64_t tiles = (R == 0 || C == 0) ? 0 : ((R + 63) / 64) * ((C + 8 * vec - 1) / (8 * vec));
+    const int64_t g = std::max<int64_t>(1, std::min<int64_t>(sms, (tiles + kThreads / 32 - 1) / (kThreads / 32)));
+    return (int)std::min<int64_t>(g, kMaxPartials);
+}
+
+// The patch kernels' dynamic shared memory (the cp.async double buffer), allowed once
+// per kernel and device.
+template <typename K>
+cudaError_t allow_patch_smem(K* kern) {
+    static std::mutex mu;
+    static std::set<std::pair<int, const void*>> done;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    std::lock_guard<std::mutex> lk(mu);
+    const auto key = std::make_pair(dev, reinterpret_cast<const void*>(kern));
+    if (done.count(key)) return cudaSuccess;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kPatchSmemBytes);
+    if (e == cudaSuccess) done.insert(key);
+    return e;
+}
+
+template <typename K, typename... Args>
+cudaError_t launch_patch(K* kern, int grid, cudaStream_t stream, Args... args) {
+    const cudaError_t e = allow_patch_smem(kern);
+    if (e != cudaSuccess) return e;
+    kern<<<grid, kThreads, kPatchSmemBytes, stream>>>(args...);
+    return cudaGetLastError();
+}
+
+// Pass 1 for one quantization: per-CTA partial maxima of |x| or |RHT(x)|; *g1 = their count.
 cudaError_t amax_pass(const void* x, bool is16, int64_t R, int64_t C, int64_t ldx, bool rht, uint64_t rht_seed,
-                      uint32_t* partials, int g1, cudaStream_t stream) {
+                      uint32_t* partials, int sms, int* g1, cudaStream_t stream) {
     const int64_t chunks = (R == 0 || C == 0) ? 0 : R * (C / (is16 ? 8 : 4));
     if (rht) {
-        if (is16) amax_rht_kernel<uint16_t><<<g1, kThreads, 0, stream>>>((const uint16_t*)x, R, C, ldx, rht_seed, partials);
-        else amax_rht_kernel<float><<<g1, kThreads, 0, stream>>>((const float*)x, R, C, ldx, rht_seed, partials);
-    } else if (ldx == C) {
-        if (is16) amax_flat_kernel<uint16_t><<<g1, kThreads, 0, stream>>>((const uint16_t*)x, chunks, partials);
-        else amax_flat_kernel<float><<<g1, kThreads, 0, stream>>>((const float*)x, chunks, partials);
+        *g1 = patch_grid(sms, R, C, is16);
+        return is16 ? launch_patch(amax_rht_kernel<uint16_t>, *g1, stream, (const uint16_t*)x, R, C, ldx, rht_seed, partials)
+                    : launch_patch(amax_rht_kernel<float>, *g1, stream, (const float*)x, R, C, ldx, rht_seed, partials);
+    }
+    *g1 = amax_grid(sms, R, C, is16);
+    if (ldx == C) {
+        if (is16) amax_flat_kernel<uint16_t><<<*g1, kThreads, 0, stream>>>((const uint16_t*)x, chunks, partials);
+        else amax_flat_kernel<float><<<*g1, kThreads, 0, stream>>>((const float*)x, chunks, partials);
     } else {
-        if (is16) amax_kernel<uint16_t><<<g1, kThreads, 0, stream>>>((const uint16_t*)x, R, C, ldx, partials);
-        else amax_kernel<float><<<g1, kThreads, 0, stream>>>((const float*)x, R, C, ldx, partials);
+        if (is16) amax_kernel<uint16_t><<<*g1, kThreads, 0, stream>>>((const uint16_t*)x, R, C, ldx, partials);
+        else amax_kernel<float><<<*g1, kThreads, 0, stream>>>((const float*)x, R, C, ldx, partials);
     }
     return cudaGetLastError();
 }
@@ -644,35 +914,35 @@ nvfp4_status encode_pass(const void* x, int32_t x_dtype, int64_t R, int64_t C, i
     }
 
     const bool sr = p->round == NVFP4_ROUND_SR;
-    const int per_sm = (p->block == NVFP4_BLOCK_1X16_ROW) ? 8 : 4;
-    const int64_t work_warps = (p->block == NVFP4_BLOCK_1X16_ROW)
-        ? (empty ? 0 : R * ((C / 16 + 31) / 32))
-        : (empty ? 0 : ((R + 63) / 64) * ((C + 8 * (is16 ? 8 : 4) - 1) / (8 * (is16 ? 8 : 4))));
-    const int g2 = (int)std::max<int64_t>(1, std::min<int64_t>((int64_t)sms * per_sm, (work_warps + 7) / 8));
+    const int64_t row_warps = empty ? 0 : R * ((C / 16 + 31) / 32);
+    const int g_row = (int)std::max<int64_t>(1, std::min<int64_t>((int64_t)sms * 8, (row_warps + 7) / 8));
+    const int g_patch = patch_grid(sms, R, C, is16);
     // 32-byte loads when every 16-element block starts on a 32-byte boundary
     const int v8 = ((reinterpret_cast<uintptr_t>(x) & 31u) == 0 && ((size_t)ldx * esz) % 32 == 0) ? 1 : 0;
     const uint64_t ss = p->sr_seed;
     const uint32_t so = p->sr_offset;
+    cudaError_t e = cudaSuccess;
 #define NVFP4_LAUNCH_T(T)                                                                                  \
     do {                                                                                                   \
         const T* xt = (const T*)x;                                                                         \
         if (p->block == NVFP4_BLOCK_1X16_ROW) {                                                            \
-            if (sr) encode_row_kernel<T, true><<<g2, kThreads, 0, stream>>>(xt, R, C, ldx, partials, g1, q, ss, so, v8, dev_status); \
-            else encode_row_kernel<T, false><<<g2, kThreads, 0, stream>>>(xt, R, C, ldx, partials, g1, q, ss, so, v8, dev_status); \
+            if (sr) encode_row_kernel<T, true><<<g_row, kThreads, 0, stream>>>(xt, R, C, ldx, partials, g1, q, ss, so, v8, dev_status); \
+            else encode_row_kernel<T, false><<<g_row, kThreads, 0, stream>>>(xt, R, C, ldx, partials, g1, q, ss, so, v8, dev_status); \
+            e = cudaGetLastError();                                                                        \
         } else if (p->block == NVFP4_BLOCK_1X16_COL) {                                                     \
-            if (sr && p->rht) encode_col_kernel<T, true, true><<<g2, kThreads, 0, stream>>>(xt, R, C, ldx, partials, g1, q, ss, so, rs, dev_status); \
-            else if (sr) encode_col_kernel<T, true, false><<<g2, kThreads, 0, stream>>>(xt, R, C, ldx, partials, g1, q, ss, so, rs, dev_status); \
-            else if (p->rht) encode_col_kernel<T, false, true><<<g2, kThreads, 0, stream>>>(xt, R, C, ldx, partials, g1, q, ss, so, rs, dev_status); \
-            else encode_col_kernel<T, false, false><<<g2, kThreads, 0, stream>>>(xt, R, C, ldx, partials, g1, q, ss, so, rs, dev_status); \
+            if (sr && p->rht) e = launch_patch(encode_col_kernel<T, true, true>, g_patch, stream, xt, R, C, ldx, partials, g1, q, ss, so, rs, dev_status); \
+            else if (sr) e = launch_patch(encode_col_kernel<T, true, false>, g_patch, stream, xt, R, C, ldx, partials, g1, q, ss, so, rs, dev_status); \
+            else if (p->rht) e = launch_patch(encode_col_kernel<T, false, true>, g_patch, stream, xt, R, C, ldx, partials, g1, q, ss, so, rs, dev_status); \
+            else e = launch_patch(encode_col_kernel<T, false, false>, g_patch, stream, xt, R, C, ldx, partials, g1, q, ss, so, rs, dev_status); \
         } else {                                                                                           \
-            if (sr) encode_2d_kernel<T, true><<<g2, kThreads, 0, stream>>>(xt, R, C, ldx, partials, g1, q, ss, so, dev_status); \
-            else encode_2d_kernel<T, false><<<g2, kThreads, 0, stream>>>(xt, R, C, ldx, partials, g1, q, ss, so, dev_status); \
+            if (sr) e = launch_patch(encode_2d_kernel<T, true>, g_patch, stream, xt, R, C, ldx, partials, g1, q, ss, so, dev_status); \
+            else e = launch_patch(encode_2d_kernel<T, false>, g_patch, stream, xt, R, C, ldx, partials, g1, q, ss, so, dev_status); \
         }                                                                                                  \
     } while (0)
     if (is16) NVFP4_LAUNCH_T(uint16_t);
     else NVFP4_LAUNCH_T(float);
 #undef NVFP4_LAUNCH_T
-    if (cudaGetLastError() != cudaSuccess) return NVFP4_ERR_CUDA;
+    if (e != cudaSuccess) return NVFP4_ERR_CUDA;
     return NVFP4_OK;
 }
 
@@ -690,8 +960,8 @@ nvfp4_status quantize_impl(const void* x, int32_t x_dtype, int64_t R, int64_t C,
     if (sms <= 0) return NVFP4_ERR_CUDA;
     const bool is16 = x_dtype == NVFP4_BF16;
     uint32_t* partials = static_cast<uint32_t*>(ws);
-    const int g1 = amax_grid(sms, R, C, is16);
-    if (amax_pass(x, is16, R, C, ldx, p->rht != 0, p->rht_seed, partials, g1, stream) != cudaSuccess)
+    int g1 = 0;
+    if (amax_pass(x, is16, R, C, ldx, p->rht != 0, p->rht_seed, partials, sms, &g1, stream) != cudaSuccess)
         return NVFP4_ERR_CUDA;
     return encode_pass(x, x_dtype, R, C, ldx, p, out, partials, g1, sms, dev_status, stream);
 }
@@ -714,15 +984,17 @@ nvfp4_status quantize_dual_impl(const void* x, int32_t x_dtype, int64_t R, int64
     const bool is16 = x_dtype == NVFP4_BF16;
     uint32_t* part_plain = static_cast<uint32_t*>(ws);
     uint32_t* part_col = part_plain + kMaxPartials;
-    const int g1 = amax_grid(sms, R, C, is16);
+    int g1 = 0;
     if (p_col->rht) {
         // one read of x for both tensor amaxes
-        if (is16) amax_dual_kernel<uint16_t><<<g1, kThreads, 0, stream>>>((const uint16_t*)x, R, C, ldx, p_col->rht_seed, part_plain, part_col);
-        else amax_dual_kernel<float><<<g1, kThreads, 0, stream>>>((const float*)x, R, C, ldx, p_col->rht_seed, part_plain, part_col);
-        if (cudaGetLastError() != cudaSuccess) return NVFP4_ERR_CUDA;
+        g1 = patch_grid(sms, R, C, is16);
+        const cudaError_t e = is16
+            ? launch_patch(amax_dual_kernel<uint16_t>, g1, stream, (const uint16_t*)x, R, C, ldx, p_col->rht_seed, part_plain, part_col)
+            : launch_patch(amax_dual_kernel<float>, g1, stream, (const float*)x, R, C, ldx, p_col->rht_seed, part_plain, part_col);
+        if (e != cudaSuccess) return NVFP4_ERR_CUDA;
     } else {
         // without the RHT both operands share the plain amax
-        if (amax_pass(x, is16, R, C, ldx, false, 0, part_plain, g1, stream) != cudaSuccess) return NVFP4_ERR_CUDA;
+        if (amax_pass(x, is16, R, C, ldx, false, 0, part_plain, sms, &g1, stream) != cudaSuccess) return NVFP4_ERR_CUDA;
         part_col = part_plain;
     }
     st = encode_pass(x, x_dtype, R, C, ldx, p_row, out_row, part_plain, g1, sms, dev_status, stream);
