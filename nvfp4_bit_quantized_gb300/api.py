@@ -147,16 +147,18 @@ def quantize(x: torch.Tensor, block: int = L.ROW, round: int = L.RNE, rht: bool 
 
 def quantize_dual(x: torch.Tensor, row_round: int = L.RNE, col_round: int = L.RNE, rht: bool = True,
                   sr_seed: int = 0, sr_offset: int = 0, rht_seed: int = 0, scales: bool = True,
-                  scales_mma: bool = True):
+                  scales_mma: bool = True, col_sr_seed: Optional[int] = None, col_sr_offset: Optional[int] = None):
     """Both training quantizations of x [R, C] from one amax read: the 1x16 row
     operand [R, C] and the 1x16 column operand [C, R] (RHT along R when ``rht``).
-    Identical to two ``quantize`` calls with the same parameters."""
+    Identical to two ``quantize`` calls with the same parameters; the column
+    operand's SR seed / offset default to the row's."""
     _check_2d(x, "x")
     R, C = x.shape
     qr = _alloc_q(R, C, L.ROW, x.device, scales, scales_mma, False)
     qc = _alloc_q(R, C, L.COL, x.device, scales, scales_mma, False)
     pr = _params(L.ROW, row_round, False, sr_seed, sr_offset, rht_seed)
-    pc = _params(L.COL, col_round, rht, sr_seed, sr_offset, rht_seed)
+    pc = _params(L.COL, col_round, rht, sr_seed if col_sr_seed is None else col_sr_seed,
+                 sr_offset if col_sr_offset is None else col_sr_offset, rht_seed)
     a, b = qr.c_struct(), qc.c_struct()
     lib = L.lib()
     ws = _workspace(int(lib.nvfp4_quantize_dual_workspace_bytes(R, C)))

@@ -138,6 +138,30 @@ __global__ void __launch_bounds__(kThreads) amax_flat_kernel(const T* __restrict
     block_max_store(m, partials);
 }
 
+// max |v_i| of 16 values as a tree (short dependency chains).
+__device__ __forceinline__ float abs_max16(const float (&v)[16]) {
+    float a[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) a[i] = fmaxf(fabsf(v[2 * i]), fabsf(v[2 * i + 1]));
+#pragma unroll
+    for (int s = 4; s >= 1; s >>= 1)
+#pragma unroll
+        for (int i = 0; i < s; ++i) a[i] = fmaxf(a[i], a[i + s]);
+    return a[0];
+}
+
+// max(|a|, |b|) of packed bf16 pairs (sign bits of the result unspecified).
+__device__ __forceinline__ uint32_t max_abs_bf16x2(uint32_t a, uint32_t b) {
+    uint32_t r;
+    asm("max.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
+}
+// The larger |.| of a packed bf16 pair as fp32 bits.
+__device__ __forceinline__ uint32_t bf16x2_abs_max_bits(uint32_t m) {
+    m &= 0x7FFF7FFFu;
+    return max(m << 16, m & 0xFFFF0000u);
+}
+
 // ---- Patch pipeline.  The column and 16x16 kernels (and the RHT maxima) give each
 // lane a 16-row x 16-byte patch of a warp's 64-row x (8 * 16 B) tile.  Their per-patch
 // arithmetic is long and their register footprint leaves one CTA per SM, so each
@@ -239,11 +263,6 @@ __device__ __forceinline__ uint32_t max_abs_nan_bf16x2(uint32_t m, uint32_t v) {
     asm("max.NaN.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(m), "r"(v));
     return r;
 }
-// The larger |.| of a packed bf16 pair as fp32 bits (NaN sorts above Inf).
-__device__ __forceinline__ uint32_t bf16x2_abs_max_bits(uint32_t m) {
-    m &= 0x7FFF7FFFu;
-    return max(m << 16, m & 0xFFFF0000u);
-}
 
 // Unpacks a bf16 patch as t[k][i] = (x[r0+i][c0+2k], x[r0+i][c0+2k+1]), negating row i
 // where bit i of `neg` is set (the RHT signs).  With PLAIN, returns the packed bf16 |x|
@@ -261,6 +280,19 @@ __device__ __forceinline__ uint32_t unpack_patch_bf16(const uint4 (&v)[16], uint
         for (int k = 0; k < 4; ++k) t[k][i] = make_float2(bf16_lo(w[k]), bf16_hi(w[k]));
     }
     return m;
+}
+
+// |.| maxima of the two columns of a pair (NaN propagating), as a tree for ILP.
+__device__ __forceinline__ void col_pair_abs_max(const float2 (&t)[16], float& m0, float& m1) {
+    float a[8], b[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) { a[i] = max_abs_nan(t[2 * i].x, t[2 * i + 1].x); b[i] = max_abs_nan(t[2 * i].y, t[2 * i + 1].y); }
+#pragma unroll
+    for (int s = 4; s >= 1; s >>= 1)
+#pragma unroll
+        for (int i = 0; i < s; ++i) { a[i] = max_abs_nan(a[i], a[i + s]); b[i] = max_abs_nan(b[i], b[i + s]); }
+    m0 = a[0];
+    m1 = b[0];
 }
 
 // The 16-point Hadamard butterflies of two columns at once, unnormalised (the 1/4 of
@@ -308,12 +340,15 @@ __global__ void __launch_bounds__(kThreads) amax_rht_kernel(const T* __restrict_
             pp.read(v);
             float2 t[4][16];
             unpack_patch_bf16<false>(v, sign_mask, t);
+            float pm[4];
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
                 hadamard16_x2(t[k]);
-#pragma unroll
-                for (int i = 0; i < 16; ++i) m = max_abs_nan(max_abs_nan(m, t[k][i].x), t[k][i].y);
+                float m0, m1;
+                col_pair_abs_max(t[k], m0, m1);
+                pm[k] = max_abs_nan(m0, m1);
             }
+            m = max_abs_nan(m, max_abs_nan(max_abs_nan(pm[0], pm[1]), max_abs_nan(pm[2], pm[3])));
         }
         block_max_store(__float_as_uint(__fmul_rn(fabsf(m), 0.25f)) & 0x7FFFFFFFu, partials);
         return;
@@ -367,12 +402,15 @@ __global__ void __launch_bounds__(kThreads) amax_dual_kernel(const T* __restrict
             pp.read(v);
             float2 t[4][16];
             mpk = max_abs_nan_bf16x2(mpk, unpack_patch_bf16<true>(v, sign_mask, t));
+            float pm[4];
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
                 hadamard16_x2(t[k]);
-#pragma unroll
-                for (int i = 0; i < 16; ++i) mr = max_abs_nan(max_abs_nan(mr, t[k][i].x), t[k][i].y);
+                float m0, m1;
+                col_pair_abs_max(t[k], m0, m1);
+                pm[k] = max_abs_nan(m0, m1);
             }
+            mr = max_abs_nan(mr, max_abs_nan(max_abs_nan(pm[0], pm[1]), max_abs_nan(pm[2], pm[3])));
         }
         mp = __uint_as_float(bf16x2_abs_max_bits(mpk));
         mr = __uint_as_float(__float_as_uint(__fmul_rn(fabsf(mr), 0.25f)) & 0x7FFFFFFFu);
@@ -429,7 +467,7 @@ struct Scales { float s_enc; bool finite; };
 __shared__ float g_eb_table[128];
 
 __device__ __forceinline__ Scales tensor_scales(const uint32_t* __restrict__ partials, int nparts,
-                                                float* s_dec_out, uint32_t* dev_status) {
+                                                float* s_dec_out, uint32_t* dev_status, float* table = g_eb_table) {
     __shared__ uint32_t red[kThreads / 32];
     __shared__ uint32_t total;
     uint32_t m = 0;
@@ -452,7 +490,7 @@ __device__ __forceinline__ Scales tensor_scales(const uint32_t* __restrict__ par
         *s_dec_out = __fdiv_rn(1.0f, s.s_enc);
         if (!s.finite) set_status(dev_status, NVFP4_ERR_NONFINITE);
     }
-    if (threadIdx.x < 128) g_eb_table[threadIdx.x] = block_multiplier(threadIdx.x, s.s_enc);
+    if (threadIdx.x < 128) table[threadIdx.x] = block_multiplier(threadIdx.x, s.s_enc);
     __syncthreads();
     return s;
 }
@@ -527,31 +565,28 @@ __global__ void __launch_bounds__(kThreads) encode_row_kernel(const T* __restric
     const int64_t warp0 = (int64_t)blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5);
     const int64_t nwarps = (int64_t)gridDim.x * (kThreads / 32);
     if (warp0 >= nseg) return;
-    // One warp segment per iteration; the next segment's load is issued before this
-    // one is encoded, so a load is always in flight behind the arithmetic.
+    // One warp segment at a time, two buffers: the next segment's load is in flight
+    // while the current one is encoded.
     Walk2D w(warp0, nwarps, spr);
-    uint32_t raw[B::WORDS];
-    int64_t rr = w.row, blk = w.col * 32 + lane;
-    bool valid = blk < bpr;
-    if (valid) B::load(x + rr * ldx + blk * 16, v8 != 0, raw);
-    for (int64_t seg = warp0; seg < nseg; seg += nwarps) {
-        uint32_t cur[B::WORDS];
-#pragma unroll
-        for (int i = 0; i < B::WORDS; ++i) cur[i] = raw[i];
-        const int64_t r = rr, bk = blk;
-        const bool ok = valid;
+    auto fetch = [&](int64_t seg, uint32_t (&buf)[B::WORDS], int64_t& r, int64_t& bk) -> bool {
+        r = w.row;
+        bk = w.col * 32 + lane;
         w.advance();
-        rr = w.row;
-        blk = w.col * 32 + lane;
-        valid = seg + nwarps < nseg && blk < bpr;
-        if (valid) B::load(x + rr * ldx + blk * 16, v8 != 0, raw);
-        if (!ok) continue;
+        const bool ok = seg < nseg && bk < bpr;
+        if (ok) B::load(x + r * ldx + bk * 16, v8 != 0, buf);
+        return ok;
+    };
+    auto encode = [&](const uint32_t (&raw)[B::WORDS], int64_t r, int64_t bk) {
         float f[16];
-        B::unpack(cur, f);
-        float amax = 0.0f;
-#pragma unroll
-        for (int j = 0; j < 16; ++j) amax = fmaxf(amax, fabsf(f[j]));
-        const uint32_t sb = block_scale_code(amax, sc.s_enc);
+        B::unpack(raw, f);
+        uint32_t sb;
+        if constexpr (sizeof(T) == 2) {
+            const uint32_t m = max_abs_bf16x2(max_abs_bf16x2(max_abs_bf16x2(raw[0], raw[1]), max_abs_bf16x2(raw[2], raw[3])),
+                                              max_abs_bf16x2(max_abs_bf16x2(raw[4], raw[5]), max_abs_bf16x2(raw[6], raw[7])));
+            sb = block_scale_code_bf16(__uint_as_float(bf16x2_abs_max_bits(m)), sc.s_enc);
+        } else {
+            sb = block_scale_code(abs_max16(f), sc.s_enc);
+        }
         const float2 eb = make_float2(g_eb_table[sb], g_eb_table[sb]);
         float y[16];
 #pragma unroll
@@ -571,6 +606,69 @@ __global__ void __launch_bounds__(kThreads) encode_row_kernel(const T* __restric
         *reinterpret_cast<uint2*>(out.codes + r * (C / 2) + col / 2) = codes;
         if (out.scales) out.scales[r * bpr + bk] = (uint8_t)sb;
         if (out.scales_mma) out.scales_mma[mma_sf_offset(r, bk, nkb)] = (uint8_t)sb;
+    };
+    uint32_t bufa[B::WORDS], bufb[B::WORDS];
+    int64_t ra, ka, rb, kb;
+    bool oka = fetch(warp0, bufa, ra, ka), okb;
+    for (int64_t seg = warp0; seg < nseg; seg += 2 * nwarps) {
+        okb = fetch(seg + nwarps, bufb, rb, kb);
+        if (oka) encode(bufa, ra, ka);
+        if (seg + nwarps >= nseg) break;
+        oka = fetch(seg + 2 * nwarps, bufa, ra, ka);
+        if (okb) encode(bufb, rb, kb);
+    }
+}
+
+// Column operand (x^T: 1x16 blocks along the rows of x, the RHT along the same rows)
+// of one bf16 patch at (r0, c0): two columns at a time with packed arithmetic.
+template <bool SR, bool RHT>
+__device__ __forceinline__ void encode_col_patch_bf16(const uint4 (&v)[16], int64_t r0, int64_t c0, int64_t R,
+                                                      uint32_t sign_mask, bool fold, const float* eb_table,
+                                                      float s_enc, const PhiloxKey& key, uint32_t sr_offset,
+                                                      const QOut& out, int64_t nkb) {
+    const float quarter = RHT ? 0.25f : 1.0f;
+    float2 t[4][16];
+    unpack_patch_bf16<false>(v, sign_mask, t);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {                    // columns c0 + 2k, c0 + 2k + 1
+        if constexpr (RHT) hadamard16_x2(t[k]);
+        float m0, m1;
+        col_pair_abs_max(t[k], m0, m1);
+        const uint32_t sb0 = block_scale_code(__fmul_rn(fabsf(m0), quarter), s_enc);
+        const uint32_t sb1 = block_scale_code(__fmul_rn(fabsf(m1), quarter), s_enc);
+        float2 eb = make_float2(eb_table[sb0], eb_table[sb1]);
+        if (fold) eb = __fmul2_rn(eb, make_float2(quarter, quarter));
+        float y0[16], y1[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            float2 u = t[k][i];
+            if (!fold) u = __fmul2_rn(u, make_float2(0.25f, 0.25f));
+            u = __fmul2_rn(u, eb);
+            y0[i] = u.x;
+            y1[i] = u.y;
+        }
+        const int64_t c = c0 + 2 * k;                // operand rows c, c + 1
+        uint2 codes0, codes1;
+        if constexpr (SR) {
+            const Philox4 p0 = sr_philox(key, 1u, sr_offset, (uint64_t)(c * R + r0) >> 4);   // r0 % 16 == 0
+            const Philox4 p1 = sr_philox(key, 1u, sr_offset, (uint64_t)((c + 1) * R + r0) >> 4);
+            codes0 = e2m1x16_sr(y0, p0.w);
+            codes1 = e2m1x16_sr(y1, p1.w);
+        } else {
+            codes0 = e2m1x16_rn(y0);
+            codes1 = e2m1x16_rn(y1);
+        }
+        *reinterpret_cast<uint2*>(out.codes + c * (R / 2) + r0 / 2) = codes0;
+        *reinterpret_cast<uint2*>(out.codes + (c + 1) * (R / 2) + r0 / 2) = codes1;
+        const int64_t s = r0 / 16;
+        if (out.scales) {
+            out.scales[c * (R / 16) + s] = (uint8_t)sb0;
+            out.scales[(c + 1) * (R / 16) + s] = (uint8_t)sb1;
+        }
+        if (out.scales_mma) {
+            out.scales_mma[mma_sf_offset(c, s, nkb)] = (uint8_t)sb0;
+            out.scales_mma[mma_sf_offset(c + 1, s, nkb)] = (uint8_t)sb1;
+        }
     }
 }
 
@@ -595,57 +693,13 @@ __global__ void __launch_bounds__(kThreads) encode_col_kernel(const T* __restric
     if constexpr (sizeof(T) == 2) {
         // the quarter of the transform folds into e_b when the smallest e_b (code 126) stays exact
         const bool fold = !RHT || __fmul_rn(g_eb_table[126], 0.25f) >= FLT_MIN;
-        const float quarter = RHT ? 0.25f : 1.0f;
         PatchPipe<T> pp(x, ldx, R, C, warp0, nwarps, tiles, tiles_c, patch_smem);
         while (pp.next()) {
             if (!pp.ok) continue;
-            const int64_t r0 = pp.r0, c0 = pp.c0;
             uint4 v[16];
             pp.read(v);
-            float2 t[4][16];
-            unpack_patch_bf16<false>(v, sign_mask, t);
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {                // columns c0 + 2k, c0 + 2k + 1
-                if constexpr (RHT) hadamard16_x2(t[k]);
-                float m0 = 0.0f, m1 = 0.0f;
-#pragma unroll
-                for (int i = 0; i < 16; ++i) { m0 = max_abs_nan(m0, t[k][i].x); m1 = max_abs_nan(m1, t[k][i].y); }
-                const uint32_t sb0 = block_scale_code(__fmul_rn(fabsf(m0), quarter), sc.s_enc);
-                const uint32_t sb1 = block_scale_code(__fmul_rn(fabsf(m1), quarter), sc.s_enc);
-                float2 eb = make_float2(g_eb_table[sb0], g_eb_table[sb1]);
-                if (fold) eb = __fmul2_rn(eb, make_float2(quarter, quarter));
-                float y0[16], y1[16];
-#pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    float2 v = t[k][i];
-                    if (!fold) v = __fmul2_rn(v, make_float2(0.25f, 0.25f));
-                    v = __fmul2_rn(v, eb);
-                    y0[i] = v.x;
-                    y1[i] = v.y;
-                }
-                const int64_t c = c0 + 2 * k;            // operand rows c, c + 1
-                uint2 codes0, codes1;
-                if constexpr (SR) {
-                    const Philox4 p0 = sr_philox(key, 1u, sr_offset, (uint64_t)(c * R + r0) >> 4);   // r0 % 16 == 0
-                    const Philox4 p1 = sr_philox(key, 1u, sr_offset, (uint64_t)((c + 1) * R + r0) >> 4);
-                    codes0 = e2m1x16_sr(y0, p0.w);
-                    codes1 = e2m1x16_sr(y1, p1.w);
-                } else {
-                    codes0 = e2m1x16_rn(y0);
-                    codes1 = e2m1x16_rn(y1);
-                }
-                *reinterpret_cast<uint2*>(out.codes + c * (R / 2) + r0 / 2) = codes0;
-                *reinterpret_cast<uint2*>(out.codes + (c + 1) * (R / 2) + r0 / 2) = codes1;
-                const int64_t s = r0 / 16;
-                if (out.scales) {
-                    out.scales[c * (R / 16) + s] = (uint8_t)sb0;
-                    out.scales[(c + 1) * (R / 16) + s] = (uint8_t)sb1;
-                }
-                if (out.scales_mma) {
-                    out.scales_mma[mma_sf_offset(c, s, nkb)] = (uint8_t)sb0;
-                    out.scales_mma[mma_sf_offset(c + 1, s, nkb)] = (uint8_t)sb1;
-                }
-            }
+            encode_col_patch_bf16<SR, RHT>(v, pp.r0, pp.c0, R, sign_mask, fold, g_eb_table, sc.s_enc, key, sr_offset,
+                                           out, nkb);
         }
         return;
     }
@@ -718,15 +772,19 @@ __global__ void __launch_bounds__(kThreads) encode_2d_kernel(const T* __restrict
             uint4 v[16];
             pp.read(v);
             unpack_patch<T>(v, t);
+            float cm[VEC];
 #pragma unroll
-            for (int j = 0; j < VEC; ++j)
+            for (int j = 0; j < VEC; ++j) cm[j] = abs_max16(t[j]);
 #pragma unroll
-                for (int i = 0; i < 16; ++i) amax = fmaxf(amax, fabsf(t[j][i]));
+            for (int s = VEC / 2; s >= 1; s >>= 1)
+#pragma unroll
+                for (int j = 0; j < s; ++j) cm[j] = fmaxf(cm[j], cm[j + s]);
+            amax = cm[0];
         }
 #pragma unroll
         for (int o = 1; o < LPT; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
         if (!valid) continue;
-        const uint32_t sb = block_scale_code(amax, sc.s_enc);
+        const uint32_t sb = sizeof(T) == 2 ? block_scale_code_bf16(amax, sc.s_enc) : block_scale_code(amax, sc.s_enc);
         const float e_b = g_eb_table[sb];
         // Encode row by row (W); the W^T codes are the same nibbles, transposed in registers.
         uint32_t lo_t[VEC], hi_t[VEC];
@@ -889,29 +947,36 @@ cudaError_t amax_pass(const void* x, bool is16, int64_t R, int64_t C, int64_t ld
     return cudaGetLastError();
 }
 
+// The kernels' view of an output, with the padding of its tensor-core scale layout
+// (rows to 128, scale columns to 16) zeroed.
+nvfp4_status prepare_output(const nvfp4_qparams* p, const nvfp4_qtensor* out, int64_t R, int64_t C, QOut* q,
+                            cudaStream_t stream) {
+    const bool col = p->block == NVFP4_BLOCK_1X16_COL;
+    const int64_t rows = col ? C : R, cols = col ? R : C;
+    *q = QOut{out->codes, out->scales, out->scales_mma,
+              p->block == NVFP4_BLOCK_16X16 ? out->codes_t : nullptr,
+              p->block == NVFP4_BLOCK_16X16 ? out->scales_mma_t : nullptr, out->s_dec};
+    if (R == 0 || C == 0) return NVFP4_OK;
+    if (q->scales_mma && (rows % 128 != 0 || cols % 256 != 0))
+        if (cudaMemsetAsync(q->scales_mma, 0, nvfp4_scales_mma_bytes(rows, cols), stream) != cudaSuccess)
+            return NVFP4_ERR_CUDA;
+    if (q->scales_mma_t && (cols % 128 != 0 || rows % 256 != 0))
+        if (cudaMemsetAsync(q->scales_mma_t, 0, nvfp4_scales_mma_bytes(cols, rows), stream) != cudaSuccess)
+            return NVFP4_ERR_CUDA;
+    return NVFP4_OK;
+}
+
 // Pass 2 for one quantization, given the pass-1 partials (g1 of them).
 nvfp4_status encode_pass(const void* x, int32_t x_dtype, int64_t R, int64_t C, int64_t ldx, const nvfp4_qparams* p,
                          const nvfp4_qtensor* out, const uint32_t* partials, int g1, int sms, uint32_t* dev_status,
                          cudaStream_t stream) {
-    const bool col = p->block == NVFP4_BLOCK_1X16_COL;
-    const int64_t rows = col ? C : R, cols = col ? R : C;
     const bool empty = (R == 0 || C == 0);
     const bool is16 = x_dtype == NVFP4_BF16;
     const size_t esz = is16 ? 2 : 4;
     const uint64_t rs = p->rht_seed;
-    QOut q{out->codes, out->scales, out->scales_mma,
-           p->block == NVFP4_BLOCK_16X16 ? out->codes_t : nullptr,
-           p->block == NVFP4_BLOCK_16X16 ? out->scales_mma_t : nullptr, out->s_dec};
-
-    // Zero the padding of the tensor-core scale layout (rows to 128, scale columns to 16).
-    if (!empty) {
-        if (q.scales_mma && (rows % 128 != 0 || cols % 256 != 0))
-            if (cudaMemsetAsync(q.scales_mma, 0, nvfp4_scales_mma_bytes(rows, cols), stream) != cudaSuccess)
-                return NVFP4_ERR_CUDA;
-        if (q.scales_mma_t && (cols % 128 != 0 || rows % 256 != 0))
-            if (cudaMemsetAsync(q.scales_mma_t, 0, nvfp4_scales_mma_bytes(cols, rows), stream) != cudaSuccess)
-                return NVFP4_ERR_CUDA;
-    }
+    QOut q;
+    const nvfp4_status st = prepare_output(p, out, R, C, &q, stream);
+    if (st != NVFP4_OK) return st;
 
     const bool sr = p->round == NVFP4_ROUND_SR;
     const int64_t row_warps = empty ? 0 : R * ((C / 16 + 31) / 32);

@@ -86,6 +86,13 @@ def _layer(nv, oracle_mod, X, W, dY, seed):
     dyq = nv.quantize(dY, nv.ROW, nv.SR, sr_seed=7, sr_offset=3)
     dyt = nv.quantize(dY, nv.COL, nv.SR, rht=True, sr_seed=7, sr_offset=3, rht_seed=11)
     xt = nv.quantize(X, nv.COL, nv.RNE, rht=True, rht_seed=11)
+    # the bench's dual quantizations (one read of X / dY for both operands) equal the single calls
+    dxr, dxc = nv.quantize_dual(X, nv.RNE, nv.RNE, rht=True, rht_seed=11)
+    dyr, dyc = nv.quantize_dual(dY, nv.SR, nv.SR, rht=True, sr_seed=7, sr_offset=3, rht_seed=11)
+    for d, s in ((dxr, xq), (dxc, xt), (dyr, dyq), (dyc, dyt)):
+        assert torch.equal(d.codes, s.codes) and torch.equal(d.scales, s.scales)
+        assert torch.equal(d.scales_mma, s.scales_mma) and torch.equal(d.s_dec[:1], s.s_dec[:1])
+    del dxr, dxc, dyr, dyc
     nv.reset_status()
     Y = nv.gemm(xq, wq, torch.bfloat16)
     dX = nv.gemm(dyq, wq.transposed(), torch.bfloat16)

@@ -160,3 +160,17 @@ def test_dual_quantization_matches_two_single_calls(nv, oracle_mod, dtype, shape
     r = oracle_mod.quantize(xh, oracle_mod.ROW, rnd, sr_seed=31, sr_offset=2)
     c = oracle_mod.quantize(xh, oracle_mod.COL, rnd, rht=rht, sr_seed=31, sr_offset=2, rht_seed=8)
     assert np.array_equal(qr.codes.cpu().numpy(), r["codes"]) and np.array_equal(qc.codes.cpu().numpy(), c["codes"])
+
+
+@pytest.mark.parametrize("rnd_row,rnd_col", [(1, 0), (0, 1)])
+def test_dual_quantization_mixed_rounding_and_seeds(nv, oracle_mod, rnd_row, rnd_col):
+    """Row and column operands with different rounding modes, SR seeds and offsets."""
+    x = _input((192, 320), torch.bfloat16, seed=77).cuda()
+    qr, qc = nv.quantize_dual(x, rnd_row, rnd_col, rht=True, sr_seed=11, sr_offset=5, rht_seed=6,
+                              col_sr_seed=23, col_sr_offset=9)
+    torch.cuda.synchronize()
+    xh = host_input(x)
+    r = oracle_mod.quantize(xh, oracle_mod.ROW, rnd_row, sr_seed=11, sr_offset=5)
+    c = oracle_mod.quantize(xh, oracle_mod.COL, rnd_col, rht=True, sr_seed=23, sr_offset=9, rht_seed=6)
+    assert np.array_equal(qr.codes.cpu().numpy(), r["codes"]) and np.array_equal(qr.scales.cpu().numpy(), r["scales"])
+    assert np.array_equal(qc.codes.cpu().numpy(), c["codes"]) and np.array_equal(qc.scales.cpu().numpy(), c["scales"])
