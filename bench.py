@@ -473,7 +473,7 @@ def run_ours(args):
         "quantize_ms_per_step": round(quant_ms, 4),
         "roofline": {"bound": "tensor", "achieved": round(achieved, 1), "peak": round(fp4_peak, 1),
                      "unit": "TFLOP/s", "frac": round(achieved / fp4_peak, 4), "traffic": gemm_traffic_bytes(),
-                     "kernel": "gemm_nvfp4_kernel",
+                     "kernel": "gemm_nvfp4_pair_kernel",
                      "peak_source": f"{peak_src} bf16 sustained x {FP4_PER_BF16:g} (nominal dense FP4:BF16)"},
         "quantize_roofline": {"bound": "hbm", "achieved": round(sum(qbytes.values()) / (quant_ms * 1e-3) / 1e9, 1),
                               "peak": peaks["hbm_gbs"], "unit": "GB/s",
