@@ -73,7 +73,7 @@ __device__ __forceinline__ void block_max_store(uint32_t m, uint32_t* partials) 
     if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
     __syncthreads();
     if (threadIdx.x < 32) {
-        uint32_t v = threadIdx.x < (kThreads / 32) ? red[threadIdx.x] : 0u;
+        uint32_t v = threadIdx.x < (blockDim.x >> 5) ? red[threadIdx.x] : 0u;
         v = __reduce_max_sync(0xFFFFFFFFu, v);
         if (threadIdx.x == 0) partials[blockIdx.x] = v;
     }
@@ -162,6 +162,22 @@ __device__ __forceinline__ uint32_t bf16x2_abs_max_bits(uint32_t m) {
     return max(m << 16, m & 0xFFFF0000u);
 }
 
+// In-place transpose of an 8 x 8 matrix of nibbles held as 8 words (element (i, j) in
+// nibble j of word i -> nibble i of word j): three rounds of block swaps (4 x 4, 2 x 2,
+// 1 x 1), each a shift, a masked xor and two xors per word pair.
+__device__ __forceinline__ void transpose_nibbles8(uint32_t (&w)[8]) {
+    auto swap = [&](int a, int b, int k, uint32_t m) {
+        const uint32_t t = ((w[a] >> k) ^ w[b]) & m;
+        w[a] ^= t << k;
+        w[b] ^= t;
+    };
+#pragma unroll
+    for (int i = 0; i < 4; ++i) swap(i, i + 4, 16, 0x0000FFFFu);
+    swap(0, 2, 8, 0x00FF00FFu); swap(1, 3, 8, 0x00FF00FFu); swap(4, 6, 8, 0x00FF00FFu); swap(5, 7, 8, 0x00FF00FFu);
+#pragma unroll
+    for (int i = 0; i < 8; i += 2) swap(i, i + 1, 4, 0x0F0F0F0Fu);
+}
+
 // ---- Patch pipeline.  The column and 16x16 kernels (and the RHT maxima) give each
 // lane a 16-row x 16-byte patch of a warp's 64-row x (8 * 16 B) tile.  Their per-patch
 // arithmetic is long and their register footprint leaves one CTA per SM, so each
@@ -170,7 +186,9 @@ __device__ __forceinline__ uint32_t bf16x2_abs_max_bits(uint32_t m) {
 // x 16 B so that reading a row back is one conflict-free 512-byte access per warp.
 extern __shared__ __align__(16) uint8_t patch_smem[];
 constexpr int kPatchSlotBytes = 16 * 32 * 16;
-constexpr int kPatchSmemBytes = (kThreads / 32) * 2 * kPatchSlotBytes;    // 128 KB per CTA
+constexpr int kPatchThreads = 128;                                          // 4 warps per CTA
+constexpr int kPatchCtasPerSm = 3;                                          // by registers (~140 / thread) and shared memory
+constexpr int kPatchSmemBytes = (kPatchThreads / 32) * 2 * kPatchSlotBytes;   // 64 KB per CTA
 
 template <typename T>
 struct PatchPipe {
@@ -226,6 +244,13 @@ struct PatchPipe {
         tile += nwarps;
         asm volatile("cp.async.wait_group 1;" ::: "memory");     // the current patch has landed
         return true;
+    }
+    __device__ __forceinline__ uint4 read_row(int i) const {
+        uint4 r;
+        asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                     : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+                     : "r"(sbase + rslot * kPatchSlotBytes + i * 512) : "memory");
+        return r;
     }
     __device__ __forceinline__ void read(uint4 (&v)[16]) const {
 #pragma unroll
@@ -321,14 +346,14 @@ __device__ __forceinline__ void hadamard16_x2(float2 (&t)[16]) {
 
 // amax of RHT(x) along rows: the Wgrad operands' tensor amax after the transform.
 template <typename T>
-__global__ void __launch_bounds__(kThreads) amax_rht_kernel(const T* __restrict__ x, int64_t R, int64_t C,
+__global__ void __launch_bounds__(kPatchThreads, kPatchCtasPerSm) amax_rht_kernel(const T* __restrict__ x, int64_t R, int64_t C,
                                                             int64_t ldx, uint64_t rht_seed,
                                                             uint32_t* __restrict__ partials) {
     constexpr int VEC = Vec<T>::N;
     const int64_t tiles_c = (C + 8 * VEC - 1) / (8 * VEC);
     const int64_t tiles = ((R + 63) / 64) * tiles_c;
-    const int64_t warp0 = (int64_t)blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5);
-    const int64_t nwarps = (int64_t)gridDim.x * (kThreads / 32);
+    const int64_t warp0 = (int64_t)blockIdx.x * (kPatchThreads / 32) + (threadIdx.x >> 5);
+    const int64_t nwarps = (int64_t)gridDim.x * (kPatchThreads / 32);
     const uint32_t sign_mask = rht_sign_mask(rht_seed);
     if constexpr (sizeof(T) == 2) {
         float m = 0.0f;
@@ -380,15 +405,15 @@ __global__ void __launch_bounds__(kThreads) amax_rht_kernel(const T* __restrict_
 // Both tensor amaxes of a dual quantization in one read: |x| (row operand) and
 // |RHT(x)| along rows (column operand).
 template <typename T>
-__global__ void __launch_bounds__(kThreads) amax_dual_kernel(const T* __restrict__ x, int64_t R, int64_t C,
+__global__ void __launch_bounds__(kPatchThreads, kPatchCtasPerSm) amax_dual_kernel(const T* __restrict__ x, int64_t R, int64_t C,
                                                              int64_t ldx, uint64_t rht_seed,
                                                              uint32_t* __restrict__ partials_plain,
                                                              uint32_t* __restrict__ partials_rht) {
     constexpr int VEC = Vec<T>::N;
     const int64_t tiles_c = (C + 8 * VEC - 1) / (8 * VEC);
     const int64_t tiles = ((R + 63) / 64) * tiles_c;
-    const int64_t warp0 = (int64_t)blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5);
-    const int64_t nwarps = (int64_t)gridDim.x * (kThreads / 32);
+    const int64_t warp0 = (int64_t)blockIdx.x * (kPatchThreads / 32) + (threadIdx.x >> 5);
+    const int64_t nwarps = (int64_t)gridDim.x * (kPatchThreads / 32);
     const uint32_t sign_mask = rht_sign_mask(rht_seed);
     float mp = 0.0f, mr = 0.0f;
     bool bad = false;
@@ -449,8 +474,8 @@ __global__ void __launch_bounds__(kThreads) amax_dual_kernel(const T* __restrict
     if ((threadIdx.x & 31) == 0) { red[0][threadIdx.x >> 5] = vp; red[1][threadIdx.x >> 5] = vr; }
     __syncthreads();
     if (threadIdx.x < 32) {
-        uint32_t a = threadIdx.x < (kThreads / 32) ? red[0][threadIdx.x] : 0u;
-        uint32_t b = threadIdx.x < (kThreads / 32) ? red[1][threadIdx.x] : 0u;
+        uint32_t a = threadIdx.x < (blockDim.x >> 5) ? red[0][threadIdx.x] : 0u;
+        uint32_t b = threadIdx.x < (blockDim.x >> 5) ? red[1][threadIdx.x] : 0u;
         a = __reduce_max_sync(0xFFFFFFFFu, a);
         b = __reduce_max_sync(0xFFFFFFFFu, b);
         if (threadIdx.x == 0) { partials_plain[blockIdx.x] = a; partials_rht[blockIdx.x] = b; }
@@ -676,7 +701,7 @@ __device__ __forceinline__ void encode_col_patch_bf16(const uint4 (&v)[16], int6
 // Pass 2, 1x16 blocks along columns (operand x^T), optional RHT along rows.
 // ---------------------------------------------------------------------------
 template <typename T, bool SR, bool RHT>
-__global__ void __launch_bounds__(kThreads) encode_col_kernel(const T* __restrict__ x, int64_t R, int64_t C,
+__global__ void __launch_bounds__(kPatchThreads, kPatchCtasPerSm) encode_col_kernel(const T* __restrict__ x, int64_t R, int64_t C,
                                                               int64_t ldx, const uint32_t* __restrict__ partials,
                                                               int nparts, QOut out, uint64_t sr_seed,
                                                               uint32_t sr_offset, uint64_t rht_seed,
@@ -688,8 +713,8 @@ __global__ void __launch_bounds__(kThreads) encode_col_kernel(const T* __restric
     const int64_t tiles_c = (C + 8 * VEC - 1) / (8 * VEC);
     const int64_t tiles = ((R + 63) / 64) * tiles_c;
     const int64_t nkb = (R + 255) / 256;             // operand cols = R
-    const int64_t warp0 = (int64_t)blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5);
-    const int64_t nwarps = (int64_t)gridDim.x * (kThreads / 32);
+    const int64_t warp0 = (int64_t)blockIdx.x * (kPatchThreads / 32) + (threadIdx.x >> 5);
+    const int64_t nwarps = (int64_t)gridDim.x * (kPatchThreads / 32);
     if constexpr (sizeof(T) == 2) {
         // the quarter of the transform folds into e_b when the smallest e_b (code 126) stays exact
         const bool fold = !RHT || __fmul_rn(g_eb_table[126], 0.25f) >= FLT_MIN;
@@ -747,7 +772,7 @@ __global__ void __launch_bounds__(kThreads) encode_col_kernel(const T* __restric
 // Pass 2, 16x16 tiles (weights): writes W and W^T codes from one tile scale.
 // ---------------------------------------------------------------------------
 template <typename T, bool SR>
-__global__ void __launch_bounds__(kThreads) encode_2d_kernel(const T* __restrict__ x, int64_t R, int64_t C,
+__global__ void __launch_bounds__(kPatchThreads, kPatchCtasPerSm) encode_2d_kernel(const T* __restrict__ x, int64_t R, int64_t C,
                                                              int64_t ldx, const uint32_t* __restrict__ partials,
                                                              int nparts, QOut out, uint64_t sr_seed,
                                                              uint32_t sr_offset, uint32_t* dev_status) {
@@ -759,82 +784,144 @@ __global__ void __launch_bounds__(kThreads) encode_2d_kernel(const T* __restrict
     const int64_t tiles_c = (C + 8 * VEC - 1) / (8 * VEC);
     const int64_t tiles = ((R + 63) / 64) * tiles_c;
     const int64_t nkb = (C + 255) / 256, nkb_t = (R + 255) / 256;
-    const int64_t warp0 = (int64_t)blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5);
-    const int64_t nwarps = (int64_t)gridDim.x * (kThreads / 32);
+    const int64_t warp0 = (int64_t)blockIdx.x * (kPatchThreads / 32) + (threadIdx.x >> 5);
+    const int64_t nwarps = (int64_t)gridDim.x * (kPatchThreads / 32);
     PatchPipe<T> pp(x, ldx, R, C, warp0, nwarps, tiles, tiles_c, patch_smem);
-    while (pp.next()) {
-        const int64_t r0 = pp.r0, c0 = pp.c0;
-        // every lane takes part in the shuffles; invalid ones contribute 0
-        const bool valid = pp.ok;
-        float t[VEC][16];
-        float amax = 0.0f;
-        if (valid) {
-            uint4 v[16];
-            pp.read(v);
-            unpack_patch<T>(v, t);
-            float cm[VEC];
+    if constexpr (sizeof(T) == 2) {
+        // bf16: tile maxima on the packed words, then row by row from shared memory; the
+        // W^T codes come from two 8 x 8 nibble transposes of the 16 row words.
+        while (pp.next()) {
+            const int64_t r0 = pp.r0, c0 = pp.c0;
+            uint32_t am = 0u;                        // every lane takes part in the shuffle
+            if (pp.ok) {
 #pragma unroll
-            for (int j = 0; j < VEC; ++j) cm[j] = abs_max16(t[j]);
-#pragma unroll
-            for (int s = VEC / 2; s >= 1; s >>= 1)
-#pragma unroll
-                for (int j = 0; j < s; ++j) cm[j] = fmaxf(cm[j], cm[j + s]);
-            amax = cm[0];
-        }
-#pragma unroll
-        for (int o = 1; o < LPT; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
-        if (!valid) continue;
-        const uint32_t sb = sizeof(T) == 2 ? block_scale_code_bf16(amax, sc.s_enc) : block_scale_code(amax, sc.s_enc);
-        const float e_b = g_eb_table[sb];
-        // Encode row by row (W); the W^T codes are the same nibbles, transposed in registers.
-        uint32_t lo_t[VEC], hi_t[VEC];
-#pragma unroll
-        for (int j = 0; j < VEC; ++j) { lo_t[j] = 0u; hi_t[j] = 0u; }
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-            float y[VEC];
-#pragma unroll
-            for (int j = 0; j < VEC; ++j) y[j] = __fmul_rn(t[j][i], e_b);
-            uint32_t packed;
-            if constexpr (SR) {
-                // elements idx0 .. idx0+VEC-1 use words ((idx0 >> 2) & 3) .. of their 16-element call
-                const uint64_t idx0 = (uint64_t)((r0 + i) * C + c0);
-                const Philox4 p = sr_philox(key, 0u, sr_offset, idx0 >> 4);
-                if constexpr (VEC == 8) {
-                    const bool hi = (idx0 & 8) != 0;
-                    packed = e2m1x4_sr(y[0], y[1], y[2], y[3], hi ? p.w[2] : p.w[0]) |
-                             (e2m1x4_sr(y[4], y[5], y[6], y[7], hi ? p.w[3] : p.w[1]) << 16);
-                } else {
-                    const uint32_t k = (uint32_t)(idx0 >> 2) & 3u;
-                    const uint32_t word = k == 0 ? p.w[0] : k == 1 ? p.w[1] : k == 2 ? p.w[2] : p.w[3];
-                    packed = e2m1x4_sr(y[0], y[1], y[2], y[3], word);
+                for (int i = 0; i < 16; ++i) {
+                    const uint4 q = pp.read_row(i);
+                    am = max_abs_bf16x2(am, max_abs_bf16x2(max_abs_bf16x2(q.x, q.y), max_abs_bf16x2(q.z, q.w)));
                 }
-            } else {
-                if constexpr (VEC == 8) packed = e2m1x8_rn(y);
-                else packed = e2m1x4_rn(y);
             }
-            uint8_t* dst = out.codes + (r0 + i) * (C / 2) + c0 / 2;
-            if constexpr (VEC == 8) *reinterpret_cast<uint32_t*>(dst) = packed;
-            else *reinterpret_cast<uint16_t*>(dst) = (uint16_t)packed;
+            float amax = __uint_as_float(bf16x2_abs_max_bits(am));
+            amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));      // the tile's other 8 columns
+            if (!pp.ok) continue;
+            const uint32_t sb = block_scale_code_bf16(amax, sc.s_enc);
+            const float2 eb = make_float2(g_eb_table[sb], g_eb_table[sb]);
+            uint32_t lo[8], hi[8];                   // row words: rows 0-7, 8-15
 #pragma unroll
-            for (int j = 0; j < VEC; ++j) {
-                const uint32_t nib = (packed >> (4 * j)) & 0xFu;
-                if (i < 8) lo_t[j] |= nib << (4 * i);
-                else hi_t[j] |= nib << (4 * (i - 8));
+            for (int i = 0; i < 16; ++i) {
+                const uint4 q = pp.read_row(i);
+                const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+                float y[8];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const float2 u = __fmul2_rn(make_float2(bf16_lo(w[j]), bf16_hi(w[j])), eb);
+                    y[2 * j] = u.x;
+                    y[2 * j + 1] = u.y;
+                }
+                uint32_t packed;
+                if constexpr (SR) {
+                    const uint64_t idx0 = (uint64_t)((r0 + i) * C + c0);      // c0 % 8 == 0
+                    const Philox4 p = sr_philox(key, 0u, sr_offset, idx0 >> 4);
+                    const bool upper = (idx0 & 8) != 0;
+                    packed = e2m1x4_sr(y[0], y[1], y[2], y[3], upper ? p.w[2] : p.w[0]) |
+                             (e2m1x4_sr(y[4], y[5], y[6], y[7], upper ? p.w[3] : p.w[1]) << 16);
+                } else {
+                    packed = e2m1x8_rn(y);
+                }
+                *reinterpret_cast<uint32_t*>(out.codes + (r0 + i) * (C / 2) + c0 / 2) = packed;
+                if (i < 8) lo[i] = packed;
+                else hi[i - 8] = packed;
+            }
+            if (out.codes_t) {
+                transpose_nibbles8(lo);
+                transpose_nibbles8(hi);
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    *reinterpret_cast<uint2*>(out.codes_t + (c0 + j) * (R / 2) + r0 / 2) = make_uint2(lo[j], hi[j]);
+            }
+            if ((cc & 1) == 0) {
+                const int64_t s = c0 / 16, st = r0 / 16;
+                if (out.scales) out.scales[st * (C / 16) + s] = (uint8_t)sb;
+                if (out.scales_mma)
+                    for (int i = 0; i < 16; ++i) out.scales_mma[mma_sf_offset(r0 + i, s, nkb)] = (uint8_t)sb;
+                if (out.scales_mma_t)
+                    for (int j = 0; j < 16; ++j) out.scales_mma_t[mma_sf_offset(c0 + j, st, nkb_t)] = (uint8_t)sb;
             }
         }
-        if (out.codes_t) {
-#pragma unroll
-            for (int j = 0; j < VEC; ++j)
-                *reinterpret_cast<uint2*>(out.codes_t + (c0 + j) * (R / 2) + r0 / 2) = make_uint2(lo_t[j], hi_t[j]);
-        }
-        if ((cc % LPT) == 0) {
-            const int64_t s = c0 / 16, st = r0 / 16;
-            if (out.scales) out.scales[st * (C / 16) + s] = (uint8_t)sb;
-            if (out.scales_mma)
-                for (int i = 0; i < 16; ++i) out.scales_mma[mma_sf_offset(r0 + i, s, nkb)] = (uint8_t)sb;
-            if (out.scales_mma_t)
-                for (int j = 0; j < 16; ++j) out.scales_mma_t[mma_sf_offset(c0 + j, st, nkb_t)] = (uint8_t)sb;
+    } else {
+        while (pp.next()) {
+            const int64_t r0 = pp.r0, c0 = pp.c0;
+            // every lane takes part in the shuffles; invalid ones contribute 0
+            const bool valid = pp.ok;
+            float t[VEC][16];
+            float amax = 0.0f;
+            if (valid) {
+                uint4 v[16];
+                pp.read(v);
+                unpack_patch<T>(v, t);
+                float cm[VEC];
+    #pragma unroll
+                for (int j = 0; j < VEC; ++j) cm[j] = abs_max16(t[j]);
+    #pragma unroll
+                for (int s = VEC / 2; s >= 1; s >>= 1)
+    #pragma unroll
+                    for (int j = 0; j < s; ++j) cm[j] = fmaxf(cm[j], cm[j + s]);
+                amax = cm[0];
+            }
+    #pragma unroll
+            for (int o = 1; o < LPT; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
+            if (!valid) continue;
+            const uint32_t sb = sizeof(T) == 2 ? block_scale_code_bf16(amax, sc.s_enc) : block_scale_code(amax, sc.s_enc);
+            const float e_b = g_eb_table[sb];
+            // Encode row by row (W); the W^T codes are the same nibbles, transposed in registers.
+            uint32_t lo_t[VEC], hi_t[VEC];
+    #pragma unroll
+            for (int j = 0; j < VEC; ++j) { lo_t[j] = 0u; hi_t[j] = 0u; }
+    #pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                float y[VEC];
+    #pragma unroll
+                for (int j = 0; j < VEC; ++j) y[j] = __fmul_rn(t[j][i], e_b);
+                uint32_t packed;
+                if constexpr (SR) {
+                    // elements idx0 .. idx0+VEC-1 use words ((idx0 >> 2) & 3) .. of their 16-element call
+                    const uint64_t idx0 = (uint64_t)((r0 + i) * C + c0);
+                    const Philox4 p = sr_philox(key, 0u, sr_offset, idx0 >> 4);
+                    if constexpr (VEC == 8) {
+                        const bool hi = (idx0 & 8) != 0;
+                        packed = e2m1x4_sr(y[0], y[1], y[2], y[3], hi ? p.w[2] : p.w[0]) |
+                                 (e2m1x4_sr(y[4], y[5], y[6], y[7], hi ? p.w[3] : p.w[1]) << 16);
+                    } else {
+                        const uint32_t k = (uint32_t)(idx0 >> 2) & 3u;
+                        const uint32_t word = k == 0 ? p.w[0] : k == 1 ? p.w[1] : k == 2 ? p.w[2] : p.w[3];
+                        packed = e2m1x4_sr(y[0], y[1], y[2], y[3], word);
+                    }
+                } else {
+                    if constexpr (VEC == 8) packed = e2m1x8_rn(y);
+                    else packed = e2m1x4_rn(y);
+                }
+                uint8_t* dst = out.codes + (r0 + i) * (C / 2) + c0 / 2;
+                if constexpr (VEC == 8) *reinterpret_cast<uint32_t*>(dst) = packed;
+                else *reinterpret_cast<uint16_t*>(dst) = (uint16_t)packed;
+    #pragma unroll
+                for (int j = 0; j < VEC; ++j) {
+                    const uint32_t nib = (packed >> (4 * j)) & 0xFu;
+                    if (i < 8) lo_t[j] |= nib << (4 * i);
+                    else hi_t[j] |= nib << (4 * (i - 8));
+                }
+            }
+            if (out.codes_t) {
+    #pragma unroll
+                for (int j = 0; j < VEC; ++j)
+                    *reinterpret_cast<uint2*>(out.codes_t + (c0 + j) * (R / 2) + r0 / 2) = make_uint2(lo_t[j], hi_t[j]);
+            }
+            if ((cc % LPT) == 0) {
+                const int64_t s = c0 / 16, st = r0 / 16;
+                if (out.scales) out.scales[st * (C / 16) + s] = (uint8_t)sb;
+                if (out.scales_mma)
+                    for (int i = 0; i < 16; ++i) out.scales_mma[mma_sf_offset(r0 + i, s, nkb)] = (uint8_t)sb;
+                if (out.scales_mma_t)
+                    for (int j = 0; j < 16; ++j) out.scales_mma_t[mma_sf_offset(c0 + j, st, nkb_t)] = (uint8_t)sb;
+            }
         }
     }
 }
@@ -898,7 +985,8 @@ int amax_grid(int sms, int64_t R, int64_t C, bool is16) {
 int patch_grid(int sms, int64_t R, int64_t C, bool is16) {
     const int vec = is16 ? 8 : 4;
     const int64_t tiles = (R == 0 || C == 0) ? 0 : ((R + 63) / 64) * ((C + 8 * vec - 1) / (8 * vec));
-    const int64_t g = std::max<int64_t>(1, std::min<int64_t>(sms, (tiles + kThreads / 32 - 1) / (kThreads / 32)));
+    const int64_t g = std::max<int64_t>(1, std::min<int64_t>((int64_t)sms * kPatchCtasPerSm,
+                                                             (tiles + kPatchThreads / 32 - 1) / (kPatchThreads / 32)));
     return (int)std::min<int64_t>(g, kMaxPartials);
 }
 
@@ -923,7 +1011,7 @@ template <typename K, typename... Args>
 cudaError_t launch_patch(K* kern, int grid, cudaStream_t stream, Args... args) {
     const cudaError_t e = allow_patch_smem(kern);
     if (e != cudaSuccess) return e;
-    kern<<<grid, kThreads, kPatchSmemBytes, stream>>>(args...);
+    kern<<<grid, kPatchThreads, kPatchSmemBytes, stream>>>(args...);
     return cudaGetLastError();
 }
 
