@@ -34,10 +34,12 @@ namespace nvfp4 {
 constexpr int kThreads = 256;
 constexpr int kMaxPartials = 4096;
 
-// Byte offset of (row r, scale-column s) in the tensor-core scale layout.
-__device__ __forceinline__ size_t mma_sf_offset(int64_t r, int64_t s, int64_t nkb) {
-    return ((size_t)((r >> 7) * nkb + (s >> 4)) << 11) + (size_t)(((s >> 2) & 3) << 9) +
-           (size_t)((r & 31) << 4) + (size_t)(((r >> 5) & 3) << 2) + (size_t)(s & 3);
+// Byte offset of (row r, scale-column s) in the tensor-core scale layout.  32-bit
+// arithmetic: the host rejects operands whose scale layout reaches 4 GB.
+__device__ __forceinline__ uint32_t mma_sf_offset(int64_t r, int64_t s, int64_t nkb) {
+    const uint32_t r32 = (uint32_t)r, s32 = (uint32_t)s;
+    return ((((r32 >> 7) * (uint32_t)nkb + (s32 >> 4)) << 11) | (((s32 >> 2) & 3u) << 9) | ((r32 & 31u) << 4) |
+            (((r32 >> 5) & 3u) << 2) | (s32 & 3u));
 }
 
 // Walks the sequence k = start, start + step, ... as (k / width, k % width) without a
@@ -690,9 +692,10 @@ __device__ __forceinline__ void encode_col_patch_bf16(const uint4 (&v)[16], int6
             out.scales[c * (R / 16) + s] = (uint8_t)sb0;
             out.scales[(c + 1) * (R / 16) + s] = (uint8_t)sb1;
         }
-        if (out.scales_mma) {
-            out.scales_mma[mma_sf_offset(c, s, nkb)] = (uint8_t)sb0;
-            out.scales_mma[mma_sf_offset(c + 1, s, nkb)] = (uint8_t)sb1;
+        if (out.scales_mma) {                        // rows c, c + 1 (c even): 16 bytes apart
+            uint8_t* d = out.scales_mma + mma_sf_offset(c, s, nkb);
+            d[0] = (uint8_t)sb0;
+            d[16] = (uint8_t)sb1;
         }
     }
 }
@@ -839,12 +842,19 @@ __global__ void __launch_bounds__(kPatchThreads, kPatchCtasPerSm) encode_2d_kern
                     *reinterpret_cast<uint2*>(out.codes_t + (c0 + j) * (R / 2) + r0 / 2) = make_uint2(lo[j], hi[j]);
             }
             if ((cc & 1) == 0) {
+                // rows r0 .. r0 + 15 (r0 % 16 == 0) differ only in the (r & 31) << 4 term
                 const int64_t s = c0 / 16, st = r0 / 16;
                 if (out.scales) out.scales[st * (C / 16) + s] = (uint8_t)sb;
-                if (out.scales_mma)
-                    for (int i = 0; i < 16; ++i) out.scales_mma[mma_sf_offset(r0 + i, s, nkb)] = (uint8_t)sb;
-                if (out.scales_mma_t)
-                    for (int j = 0; j < 16; ++j) out.scales_mma_t[mma_sf_offset(c0 + j, st, nkb_t)] = (uint8_t)sb;
+                if (out.scales_mma) {
+                    uint8_t* d = out.scales_mma + mma_sf_offset(r0, s, nkb);
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) d[16 * i] = (uint8_t)sb;
+                }
+                if (out.scales_mma_t) {
+                    uint8_t* d = out.scales_mma_t + mma_sf_offset(c0, st, nkb_t);
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) d[16 * j] = (uint8_t)sb;
+                }
             }
         }
     } else {
@@ -960,6 +970,9 @@ nvfp4_status check_quantize_args(const void* x, int32_t x_dtype, int64_t R, int6
     if (out->rows != rows || out->cols != cols) return NVFP4_ERR_SHAPE;
     if (C % 16 != 0) return NVFP4_ERR_SHAPE;
     if ((col || p->block == NVFP4_BLOCK_16X16) && R % 16 != 0) return NVFP4_ERR_SHAPE;
+    // the kernels address the tensor-core scale layout with 32-bit offsets
+    if (nvfp4_scales_mma_bytes(rows, cols) >= (1ull << 32) || nvfp4_scales_mma_bytes(cols, rows) >= (1ull << 32))
+        return NVFP4_ERR_SHAPE;
     const size_t esz = x_dtype == NVFP4_BF16 ? 2 : 4;
     const bool empty = (R == 0 || C == 0);
     if (!empty) {
