@@ -315,6 +315,63 @@ def run_heavy(args):
                       "rel_error_vs_bf16": err, "device_status": nv.status_query()}))
 
 
+def run_yardstick(args):
+    """Library yardsticks at the three GEMM shapes of the bench workload (context, not the
+    target): the same NVFP4 operands through torch._scaled_mm's block-scaled FP4 path
+    (cuBLASLt) where this torch offers it -- also a cross-check of the result -- and an FP8
+    (e4m3, per-tensor scale) GEMM through torch._scaled_mm, against this library's GEMM."""
+    import torch
+    import nvfp4_bit_quantized_gb300 as nv
+    from nvfp4_bit_quantized_gb300 import inputs
+    shapes = {"fprop": (M, K, N), "dgrad": (M, N, K), "wgrad": (N, M, K)}     # (rows of A, K, rows of B)
+    out = {"config": "gemm_yardsticks", "shapes_MKN": {}, "ours_tflops": {}, "cublaslt_nvfp4_tflops": {},
+           "cublaslt_fp8_tflops": {}, "nvfp4_vs_cublaslt_rel_diff": {}, "notes": []}
+    fp4 = getattr(torch, "float4_e2m1fn_x2", None)
+    for name, (m, k, n) in shapes.items():
+        out["shapes_MKN"][name] = [m, k, n]
+        flop = 2.0 * m * n * k
+        a = inputs.normal((m, k), 1.0, 1, device="cuda").to(torch.bfloat16)
+        b = inputs.normal((n, k), 0.02, 2, device="cuda").to(torch.bfloat16)
+        qa = nv.quantize(a, nv.ROW, nv.RNE, scales=False)
+        qb = nv.quantize(b, nv.ROW, nv.RNE, scales=False)
+        d = torch.empty((m, n), dtype=torch.bfloat16, device="cuda")
+        t = _timed(lambda: nv.gemm(qa, qb, out=d), args.steps, args.warmup)
+        out["ours_tflops"][name] = round(flop / (t * 1e-3) / 1e12, 1)
+        try:
+            if fp4 is None:
+                raise RuntimeError("torch has no float4_e2m1fn_x2")
+            af = qa.codes.view(fp4)
+            bf = qb.codes.view(fp4).t()
+            sa = qa.scales_mma.view(torch.float8_e4m3fn)
+            sb = qb.scales_mma.view(torch.float8_e4m3fn)
+            fn = lambda: torch._scaled_mm(af, bf, sa, sb, out_dtype=torch.bfloat16)
+            r = fn()
+            torch.cuda.synchronize()
+            alpha = (qa.s_dec[0] * qb.s_dec[0]).float()
+            ref = r.float() * alpha
+            out["nvfp4_vs_cublaslt_rel_diff"][name] = round(((d.float() - ref).norm() / ref.norm()).item(), 6)
+            t = _timed(fn, args.steps, args.warmup)
+            out["cublaslt_nvfp4_tflops"][name] = round(flop / (t * 1e-3) / 1e12, 1)
+        except Exception as e:                                    # not offered by this torch / cuBLASLt
+            out["cublaslt_nvfp4_tflops"][name] = None
+            out["notes"].append(f"nvfp4 {name}: {type(e).__name__}: {str(e)[:160]}")
+        try:
+            a8 = a.to(torch.float8_e4m3fn)
+            b8 = b.to(torch.float8_e4m3fn).t()
+            one = torch.ones((), dtype=torch.float32, device="cuda")
+            fn = lambda: torch._scaled_mm(a8, b8, one, one, out_dtype=torch.bfloat16)
+            fn()
+            t = _timed(fn, args.steps, args.warmup)
+            out["cublaslt_fp8_tflops"][name] = round(flop / (t * 1e-3) / 1e12, 1)
+        except Exception as e:
+            out["cublaslt_fp8_tflops"][name] = None
+            out["notes"].append(f"fp8 {name}: {type(e).__name__}: {str(e)[:160]}")
+        del a, b, qa, qb, d
+        torch.cuda.empty_cache()
+    out["device_status"] = nv.status_query()
+    print(json.dumps(out))
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
@@ -325,7 +382,7 @@ def run_ours(args):
         return run_kernel_only(args)
     if args.config != "ffn_up":
         torch.cuda.set_device(0)
-        return {"sweep": run_sweep, "mlp": run_mlp, "heavy": run_heavy}[args.config](args)
+        return {"sweep": run_sweep, "mlp": run_mlp, "heavy": run_heavy, "yardstick": run_yardstick}[args.config](args)
 
     rank, world, local = env_rank()
     torch.cuda.set_device(local)
@@ -564,8 +621,8 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--kernel", choices=["step", "gemm", "quantize"], default="step",
                     help="step: the whole hot path (the bench line); gemm / quantize: one kernel family alone")
-    ap.add_argument("--config", choices=["ffn_up", "mlp", "sweep", "heavy"], default="ffn_up",
-                    help="ffn_up: the headline workload (default); mlp / sweep / heavy: the other workloads, "
+    ap.add_argument("--config", choices=["ffn_up", "mlp", "sweep", "heavy", "yardstick"], default="ffn_up",
+                    help="ffn_up: the headline workload (default); mlp / sweep / heavy / yardstick: the other workloads, "
                          "one JSON line each (not the headline metric)")
     ap.add_argument("--sweep-min", type=int, default=20)
     ap.add_argument("--sweep-max", type=int, default=28)

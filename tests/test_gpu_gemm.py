@@ -112,3 +112,27 @@ def test_single_cta_and_cta_pair_kernels_agree_with_oracle(nv, oracle_mod, force
         err = rel_fro(outs[path], ref)
         assert err <= TOL, (path, err)
     assert np.array_equal(outs[1], outs[2]) or rel_fro(outs[2], outs[1]) <= 1e-6
+
+
+def test_operands_read_identically_by_cublaslt(nv):
+    """The same codes and tensor-core scale buffers through torch._scaled_mm's block-scaled
+    FP4 path (cuBLASLt), where this torch offers it: the two bf16 results differ by no more
+    than two bf16 roundings, so both read the operand format the same way."""
+    fp4 = getattr(torch, "float4_e2m1fn_x2", None)
+    if fp4 is None:
+        pytest.skip("torch has no float4_e2m1fn_x2")
+    from nvfp4_bit_quantized_gb300 import inputs
+    m, k, n = 1024, 2048, 768
+    a = inputs.normal((m, k), 1.0, 3, device="cuda").to(torch.bfloat16)
+    b = inputs.normal((n, k), 0.02, 4, device="cuda").to(torch.bfloat16)
+    qa = nv.quantize(a, nv.ROW, nv.RNE)
+    qb = nv.quantize(b, nv.ROW, nv.RNE)
+    ours = nv.gemm(qa, qb, torch.bfloat16).float()
+    try:
+        lib = torch._scaled_mm(qa.codes.view(fp4), qb.codes.view(fp4).t(), qa.scales_mma.view(torch.float8_e4m3fn),
+                               qb.scales_mma.view(torch.float8_e4m3fn), out_dtype=torch.bfloat16)
+    except (RuntimeError, TypeError, NotImplementedError) as e:
+        pytest.skip(f"block-scaled FP4 _scaled_mm not available: {e}")
+    ref = lib.float() * (qa.s_dec[0] * qb.s_dec[0]).float()
+    rel = ((ours - ref).norm() / ref.norm()).item()
+    assert rel < 4e-3, rel
