@@ -155,6 +155,21 @@ NVFP4_API nvfp4_status nvfp4_quantize_dual(const void* x, int32_t x_dtype, int64
                                            void* stream);
 
 /*
+ * nvfp4_quantize_dual_sqrelu -- nvfp4_quantize_dual of A = relu(H)^2 (the squared
+ * ReLU of an MLP block, applied element by element to bf16 H: max(h, 0)^2 in fp32,
+ * rounded to bf16) without A ever being stored: every pass applies the activation to
+ * H as it is loaded.  Results are identical to nvfp4_sqrelu_forward followed by
+ * nvfp4_quantize_dual.  BF16 input only (else NVFP4_ERR_UNSUPPORTED); arguments as
+ * for nvfp4_quantize_dual, with H, its row pitch ldh and its shape [R, C].  Not on
+ * the page, whose MLP activation is unspecified: a fusion of the block's two steps.
+ */
+NVFP4_API nvfp4_status nvfp4_quantize_dual_sqrelu(const void* h, int32_t h_dtype, int64_t R, int64_t C, int64_t ldh,
+                                                  const nvfp4_qparams* params_row, const nvfp4_qtensor* out_row,
+                                                  const nvfp4_qparams* params_col, const nvfp4_qtensor* out_col,
+                                                  void* workspace, size_t workspace_bytes, uint32_t* dev_status,
+                                                  void* stream);
+
+/*
  * nvfp4_quantize_noalloc -- nvfp4_quantize without a workspace argument; it
  * allocates nothing.  The page describes no such call: it exists for callers
  * that can hand over their input and output buffers but cannot obtain one more

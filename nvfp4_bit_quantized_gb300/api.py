@@ -147,11 +147,13 @@ def quantize(x: torch.Tensor, block: int = L.ROW, round: int = L.RNE, rht: bool 
 
 def quantize_dual(x: torch.Tensor, row_round: int = L.RNE, col_round: int = L.RNE, rht: bool = True,
                   sr_seed: int = 0, sr_offset: int = 0, rht_seed: int = 0, scales: bool = True,
-                  scales_mma: bool = True, col_sr_seed: Optional[int] = None, col_sr_offset: Optional[int] = None):
+                  scales_mma: bool = True, col_sr_seed: Optional[int] = None, col_sr_offset: Optional[int] = None,
+                  pre: Optional[str] = None):
     """Both training quantizations of x [R, C] from one amax read: the 1x16 row
     operand [R, C] and the 1x16 column operand [C, R] (RHT along R when ``rht``).
     Identical to two ``quantize`` calls with the same parameters; the column
-    operand's SR seed / offset default to the row's."""
+    operand's SR seed / offset default to the row's.  ``pre="sqrelu"`` quantizes
+    relu(x)^2 (bf16 x) without storing it, identical to ``sqrelu_forward`` first."""
     _check_2d(x, "x")
     R, C = x.shape
     qr = _alloc_q(R, C, L.ROW, x.device, scales, scales_mma, False)
@@ -163,10 +165,12 @@ def quantize_dual(x: torch.Tensor, row_round: int = L.RNE, col_round: int = L.RN
     lib = L.lib()
     ws = _workspace(int(lib.nvfp4_quantize_dual_workspace_bytes(R, C)))
     ld = x.stride(0) if R > 1 else max(C, 1)
-    st = lib.nvfp4_quantize_dual(_ptr(x), _DT[x.dtype], R, C, ld, ctypes.byref(pr), ctypes.byref(a),
-                                 ctypes.byref(pc), ctypes.byref(b), ws.data_ptr(), ws.numel(),
-                                 dev_status(x.device).data_ptr(), _stream())
-    L.check(st, "nvfp4_quantize_dual")
+    if pre not in (None, "sqrelu"):
+        raise ValueError(f"unknown pre transform {pre!r}")
+    fn = lib.nvfp4_quantize_dual_sqrelu if pre == "sqrelu" else lib.nvfp4_quantize_dual
+    st = fn(_ptr(x), _DT[x.dtype], R, C, ld, ctypes.byref(pr), ctypes.byref(a), ctypes.byref(pc), ctypes.byref(b),
+            ws.data_ptr(), ws.numel(), dev_status(x.device).data_ptr(), _stream())
+    L.check(st, "nvfp4_quantize_dual_sqrelu" if pre else "nvfp4_quantize_dual")
     return qr, qc
 
 

@@ -20,6 +20,7 @@
 //                 4 full 128-byte lines, every transposed store writes full
 //                 32-byte sectors (4 lanes x 8 bytes per output row).
 #include <cuda_runtime.h>
+#include <cuda_bf16.h>
 #include <cstdint>
 #include <cstdio>
 #include <mutex>
@@ -69,6 +70,25 @@ __device__ __forceinline__ uint32_t abs_bits_max(uint4 v, const float*) {
     return max(max(v.x & 0x7FFFFFFFu, v.y & 0x7FFFFFFFu), max(v.z & 0x7FFFFFFFu, v.w & 0x7FFFFFFFu));
 }
 
+// Squared ReLU of two packed bf16 values, rounded back to bf16: relu(h)^2 in fp32, one
+// rounding to bf16 (max(h, 0) squares to +0 for h <= 0, -0 and NaN alike).  The MLP's
+// activation, applied to H as it is loaded, so A = relu(H)^2 is quantized without being
+// stored (SQR kernels).
+__device__ __forceinline__ uint32_t sqrelu_bf16x2(uint32_t w) {
+    const float2 r = make_float2(fmaxf(__uint_as_float(w << 16), 0.0f), fmaxf(__uint_as_float(w & 0xFFFF0000u), 0.0f));
+    const __nv_bfloat162 b = __float22bfloat162_rn(__fmul2_rn(r, r));
+    return *reinterpret_cast<const uint32_t*>(&b);
+}
+__device__ __forceinline__ uint4 sqrelu_bf16x8(uint4 v) {
+    return make_uint4(sqrelu_bf16x2(v.x), sqrelu_bf16x2(v.y), sqrelu_bf16x2(v.z), sqrelu_bf16x2(v.w));
+}
+// Applies the load transform of a kernel (identity, or the squared ReLU for bf16).
+template <typename T, bool SQR>
+__device__ __forceinline__ uint4 pre16(uint4 v) {
+    if constexpr (SQR && sizeof(T) == 2) return sqrelu_bf16x8(v);
+    else return v;
+}
+
 __device__ __forceinline__ void block_max_store(uint32_t m, uint32_t* partials) {
     __shared__ uint32_t red[kThreads / 32];
     m = __reduce_max_sync(0xFFFFFFFFu, m);
@@ -82,7 +102,7 @@ __device__ __forceinline__ void block_max_store(uint32_t m, uint32_t* partials) 
 }
 
 // |x| max, unsigned compare of the magnitude bits (NaN sorts above Inf).
-template <typename T>
+template <typename T, bool SQR = false>
 __global__ void __launch_bounds__(kThreads) amax_kernel(const T* __restrict__ x, int64_t R, int64_t C,
                                                         int64_t ldx, uint32_t* __restrict__ partials) {
     constexpr int VEC = Vec<T>::N;
@@ -106,7 +126,7 @@ __global__ void __launch_bounds__(kThreads) amax_kernel(const T* __restrict__ x,
             if (seg < nseg) {
                 const int64_t ch = w.col * 32 + lane;
                 if (ch < cpr) {
-                    v[u] = ld_stream(x + w.row * ldx + ch * VEC);
+                    v[u] = pre16<T, SQR>(ld_stream(x + w.row * ldx + ch * VEC));
                     ok[u] = true;
                 }
             }
@@ -121,7 +141,7 @@ __global__ void __launch_bounds__(kThreads) amax_kernel(const T* __restrict__ x,
 
 // |x| max over a contiguous tensor (row pitch == C) as one flat array of 16-byte
 // chunks: no 2D index arithmetic per chunk.
-template <typename T>
+template <typename T, bool SQR = false>
 __global__ void __launch_bounds__(kThreads) amax_flat_kernel(const T* __restrict__ x, int64_t nchunks,
                                                              uint32_t* __restrict__ partials) {
     constexpr int VEC = Vec<T>::N;
@@ -132,7 +152,7 @@ __global__ void __launch_bounds__(kThreads) amax_flat_kernel(const T* __restrict
         uint4 v[U];
 #pragma unroll
         for (int u = 0; u < U; ++u)
-            if (base + u * stride < nchunks) v[u] = ld_stream(x + (base + u * stride) * VEC);
+            if (base + u * stride < nchunks) v[u] = pre16<T, SQR>(ld_stream(x + (base + u * stride) * VEC));
 #pragma unroll
         for (int u = 0; u < U; ++u)
             if (base + u * stride < nchunks) m = max(m, abs_bits_max(v[u], (const T*)nullptr));
@@ -406,7 +426,7 @@ __global__ void __launch_bounds__(kPatchThreads, kPatchCtasPerSm) amax_rht_kerne
 
 // Both tensor amaxes of a dual quantization in one read: |x| (row operand) and
 // |RHT(x)| along rows (column operand).
-template <typename T>
+template <typename T, bool SQR = false>
 __global__ void __launch_bounds__(kPatchThreads, kPatchCtasPerSm) amax_dual_kernel(const T* __restrict__ x, int64_t R, int64_t C,
                                                              int64_t ldx, uint64_t rht_seed,
                                                              uint32_t* __restrict__ partials_plain,
@@ -427,6 +447,8 @@ __global__ void __launch_bounds__(kPatchThreads, kPatchCtasPerSm) amax_dual_kern
             const int64_t r0 = pp.r0, c0 = pp.c0;
             uint4 v[16];
             pp.read(v);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) v[i] = pre16<T, SQR>(v[i]);
             float2 t[4][16];
             mpk = max_abs_nan_bf16x2(mpk, unpack_patch_bf16<true>(v, sign_mask, t));
             float pm[4];
@@ -576,7 +598,7 @@ template <> struct Block16<float> {               // 64 bytes
     }
 };
 
-template <typename T, bool SR>
+template <typename T, bool SR, bool SQR = false>
 __global__ void __launch_bounds__(kThreads) encode_row_kernel(const T* __restrict__ x, int64_t R, int64_t C,
                                                               int64_t ldx, const uint32_t* __restrict__ partials,
                                                               int nparts, QOut out, uint64_t sr_seed,
@@ -603,7 +625,11 @@ __global__ void __launch_bounds__(kThreads) encode_row_kernel(const T* __restric
         if (ok) B::load(x + r * ldx + bk * 16, v8 != 0, buf);
         return ok;
     };
-    auto encode = [&](const uint32_t (&raw)[B::WORDS], int64_t r, int64_t bk) {
+    auto encode = [&](uint32_t (&raw)[B::WORDS], int64_t r, int64_t bk) {
+        if constexpr (SQR && sizeof(T) == 2) {
+#pragma unroll
+            for (int i = 0; i < B::WORDS; ++i) raw[i] = sqrelu_bf16x2(raw[i]);
+        }
         float f[16];
         B::unpack(raw, f);
         uint32_t sb;
@@ -703,7 +729,7 @@ __device__ __forceinline__ void encode_col_patch_bf16(const uint4 (&v)[16], int6
 // ---------------------------------------------------------------------------
 // Pass 2, 1x16 blocks along columns (operand x^T), optional RHT along rows.
 // ---------------------------------------------------------------------------
-template <typename T, bool SR, bool RHT>
+template <typename T, bool SR, bool RHT, bool SQR = false>
 __global__ void __launch_bounds__(kPatchThreads, kPatchCtasPerSm) encode_col_kernel(const T* __restrict__ x, int64_t R, int64_t C,
                                                               int64_t ldx, const uint32_t* __restrict__ partials,
                                                               int nparts, QOut out, uint64_t sr_seed,
@@ -726,6 +752,8 @@ __global__ void __launch_bounds__(kPatchThreads, kPatchCtasPerSm) encode_col_ker
             if (!pp.ok) continue;
             uint4 v[16];
             pp.read(v);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) v[i] = pre16<T, SQR>(v[i]);
             encode_col_patch_bf16<SR, RHT>(v, pp.r0, pp.c0, R, sign_mask, fold, g_eb_table, sc.s_enc, key, sr_offset,
                                            out, nkb);
         }
@@ -1030,7 +1058,7 @@ cudaError_t launch_patch(K* kern, int grid, cudaStream_t stream, Args... args) {
 
 // Pass 1 for one quantization: per-CTA partial maxima of |x| or |RHT(x)|; *g1 = their count.
 cudaError_t amax_pass(const void* x, bool is16, int64_t R, int64_t C, int64_t ldx, bool rht, uint64_t rht_seed,
-                      uint32_t* partials, int sms, int* g1, cudaStream_t stream) {
+                      uint32_t* partials, int sms, int* g1, cudaStream_t stream, bool sqr = false) {
     const int64_t chunks = (R == 0 || C == 0) ? 0 : R * (C / (is16 ? 8 : 4));
     if (rht) {
         *g1 = patch_grid(sms, R, C, is16);
@@ -1038,11 +1066,14 @@ cudaError_t amax_pass(const void* x, bool is16, int64_t R, int64_t C, int64_t ld
                     : launch_patch(amax_rht_kernel<float>, *g1, stream, (const float*)x, R, C, ldx, rht_seed, partials);
     }
     *g1 = amax_grid(sms, R, C, is16);
+    const uint16_t* xb = (const uint16_t*)x;
     if (ldx == C) {
-        if (is16) amax_flat_kernel<uint16_t><<<*g1, kThreads, 0, stream>>>((const uint16_t*)x, chunks, partials);
+        if (is16 && sqr) amax_flat_kernel<uint16_t, true><<<*g1, kThreads, 0, stream>>>(xb, chunks, partials);
+        else if (is16) amax_flat_kernel<uint16_t><<<*g1, kThreads, 0, stream>>>(xb, chunks, partials);
         else amax_flat_kernel<float><<<*g1, kThreads, 0, stream>>>((const float*)x, chunks, partials);
     } else {
-        if (is16) amax_kernel<uint16_t><<<*g1, kThreads, 0, stream>>>((const uint16_t*)x, R, C, ldx, partials);
+        if (is16 && sqr) amax_kernel<uint16_t, true><<<*g1, kThreads, 0, stream>>>(xb, R, C, ldx, partials);
+        else if (is16) amax_kernel<uint16_t><<<*g1, kThreads, 0, stream>>>(xb, R, C, ldx, partials);
         else amax_kernel<float><<<*g1, kThreads, 0, stream>>>((const float*)x, R, C, ldx, partials);
     }
     return cudaGetLastError();
@@ -1070,7 +1101,7 @@ nvfp4_status prepare_output(const nvfp4_qparams* p, const nvfp4_qtensor* out, in
 // Pass 2 for one quantization, given the pass-1 partials (g1 of them).
 nvfp4_status encode_pass(const void* x, int32_t x_dtype, int64_t R, int64_t C, int64_t ldx, const nvfp4_qparams* p,
                          const nvfp4_qtensor* out, const uint32_t* partials, int g1, int sms, uint32_t* dev_status,
-                         cudaStream_t stream) {
+                         cudaStream_t stream, bool sqr = false) {
     const bool empty = (R == 0 || C == 0);
     const bool is16 = x_dtype == NVFP4_BF16;
     const size_t esz = is16 ? 2 : 4;
@@ -1105,8 +1136,26 @@ nvfp4_status encode_pass(const void* x, int32_t x_dtype, int64_t R, int64_t C, i
             else e = launch_patch(encode_2d_kernel<T, false>, g_patch, stream, xt, R, C, ldx, partials, g1, q, ss, so, dev_status); \
         }                                                                                                  \
     } while (0)
-    if (is16) NVFP4_LAUNCH_T(uint16_t);
-    else NVFP4_LAUNCH_T(float);
+    if (is16 && sqr) {
+        // bf16 with the squared-ReLU load transform (row and column operands only)
+        const uint16_t* xt = (const uint16_t*)x;
+        if (p->block == NVFP4_BLOCK_1X16_ROW) {
+            if (sr) encode_row_kernel<uint16_t, true, true><<<g_row, kThreads, 0, stream>>>(xt, R, C, ldx, partials, g1, q, ss, so, v8, dev_status);
+            else encode_row_kernel<uint16_t, false, true><<<g_row, kThreads, 0, stream>>>(xt, R, C, ldx, partials, g1, q, ss, so, v8, dev_status);
+            e = cudaGetLastError();
+        } else if (p->block == NVFP4_BLOCK_1X16_COL) {
+            if (sr && p->rht) e = launch_patch(encode_col_kernel<uint16_t, true, true, true>, g_patch, stream, xt, R, C, ldx, partials, g1, q, ss, so, rs, dev_status);
+            else if (sr) e = launch_patch(encode_col_kernel<uint16_t, true, false, true>, g_patch, stream, xt, R, C, ldx, partials, g1, q, ss, so, rs, dev_status);
+            else if (p->rht) e = launch_patch(encode_col_kernel<uint16_t, false, true, true>, g_patch, stream, xt, R, C, ldx, partials, g1, q, ss, so, rs, dev_status);
+            else e = launch_patch(encode_col_kernel<uint16_t, false, false, true>, g_patch, stream, xt, R, C, ldx, partials, g1, q, ss, so, rs, dev_status);
+        } else {
+            return NVFP4_ERR_UNSUPPORTED;
+        }
+    } else if (is16) {
+        NVFP4_LAUNCH_T(uint16_t);
+    } else {
+        NVFP4_LAUNCH_T(float);
+    }
 #undef NVFP4_LAUNCH_T
     if (e != cudaSuccess) return NVFP4_ERR_CUDA;
     return NVFP4_OK;
@@ -1135,8 +1184,9 @@ nvfp4_status quantize_impl(const void* x, int32_t x_dtype, int64_t R, int64_t C,
 nvfp4_status quantize_dual_impl(const void* x, int32_t x_dtype, int64_t R, int64_t C, int64_t ldx,
                                 const nvfp4_qparams* p_row, const nvfp4_qtensor* out_row,
                                 const nvfp4_qparams* p_col, const nvfp4_qtensor* out_col, void* ws,
-                                size_t ws_bytes, uint32_t* dev_status, cudaStream_t stream) {
+                                size_t ws_bytes, uint32_t* dev_status, cudaStream_t stream, bool sqr = false) {
     if (!p_row || !p_col) return NVFP4_ERR_INVALID_ARG;
+    if (sqr && x_dtype != NVFP4_BF16) return NVFP4_ERR_UNSUPPORTED;
     if (p_row->block != NVFP4_BLOCK_1X16_ROW || p_col->block != NVFP4_BLOCK_1X16_COL) return NVFP4_ERR_INVALID_ARG;
     nvfp4_status st = check_quantize_args(x, x_dtype, R, C, ldx, p_row, out_row);
     if (st != NVFP4_OK) return st;
@@ -1154,18 +1204,19 @@ nvfp4_status quantize_dual_impl(const void* x, int32_t x_dtype, int64_t R, int64
     if (p_col->rht) {
         // one read of x for both tensor amaxes
         g1 = patch_grid(sms, R, C, is16);
-        const cudaError_t e = is16
-            ? launch_patch(amax_dual_kernel<uint16_t>, g1, stream, (const uint16_t*)x, R, C, ldx, p_col->rht_seed, part_plain, part_col)
-            : launch_patch(amax_dual_kernel<float>, g1, stream, (const float*)x, R, C, ldx, p_col->rht_seed, part_plain, part_col);
+        const cudaError_t e = !is16
+            ? launch_patch(amax_dual_kernel<float>, g1, stream, (const float*)x, R, C, ldx, p_col->rht_seed, part_plain, part_col)
+            : sqr ? launch_patch(amax_dual_kernel<uint16_t, true>, g1, stream, (const uint16_t*)x, R, C, ldx, p_col->rht_seed, part_plain, part_col)
+                  : launch_patch(amax_dual_kernel<uint16_t>, g1, stream, (const uint16_t*)x, R, C, ldx, p_col->rht_seed, part_plain, part_col);
         if (e != cudaSuccess) return NVFP4_ERR_CUDA;
     } else {
         // without the RHT both operands share the plain amax
-        if (amax_pass(x, is16, R, C, ldx, false, 0, part_plain, sms, &g1, stream) != cudaSuccess) return NVFP4_ERR_CUDA;
+        if (amax_pass(x, is16, R, C, ldx, false, 0, part_plain, sms, &g1, stream, sqr) != cudaSuccess) return NVFP4_ERR_CUDA;
         part_col = part_plain;
     }
-    st = encode_pass(x, x_dtype, R, C, ldx, p_row, out_row, part_plain, g1, sms, dev_status, stream);
+    st = encode_pass(x, x_dtype, R, C, ldx, p_row, out_row, part_plain, g1, sms, dev_status, stream, sqr);
     if (st != NVFP4_OK) return st;
-    return encode_pass(x, x_dtype, R, C, ldx, p_col, out_col, part_col, g1, sms, dev_status, stream);
+    return encode_pass(x, x_dtype, R, C, ldx, p_col, out_col, part_col, g1, sms, dev_status, stream, sqr);
 }
 
 }  // namespace nvfp4
@@ -1176,6 +1227,15 @@ extern "C" nvfp4_status nvfp4_quantize(const void* x, int32_t x_dtype, int64_t R
                                        void* stream) {
     return nvfp4::quantize_impl(x, x_dtype, R, C, ldx, params, out, workspace, workspace_bytes, dev_status,
                                 static_cast<cudaStream_t>(stream));
+}
+
+extern "C" nvfp4_status nvfp4_quantize_dual_sqrelu(const void* h, int32_t h_dtype, int64_t R, int64_t C, int64_t ldh,
+                                                   const nvfp4_qparams* params_row, const nvfp4_qtensor* out_row,
+                                                   const nvfp4_qparams* params_col, const nvfp4_qtensor* out_col,
+                                                   void* workspace, size_t workspace_bytes, uint32_t* dev_status,
+                                                   void* stream) {
+    return nvfp4::quantize_dual_impl(h, h_dtype, R, C, ldh, params_row, out_row, params_col, out_col, workspace,
+                                     workspace_bytes, dev_status, static_cast<cudaStream_t>(stream), true);
 }
 
 extern "C" size_t nvfp4_quantize_dual_workspace_bytes(int64_t, int64_t) {

@@ -27,8 +27,9 @@ def mlp_step(nv, X, W1, W2, dY, sr_seed=5, rht_seed=9):
     out["w2q"] = nv.quantize_weight(W2)
     out["xq"], out["xt"] = nv.quantize_dual(X, nv.RNE, nv.RNE, rht=True, rht_seed=rht_seed)
     out["H"] = nv.gemm(out["xq"], out["w1q"], torch.bfloat16)
-    out["A"] = nv.sqrelu_forward(out["H"])
-    out["aq"], out["at"] = nv.quantize_dual(out["A"], nv.RNE, nv.RNE, rht=True, rht_seed=rht_seed)
+    out["A"] = nv.sqrelu_forward(out["H"])                  # kept for the checks; the step itself
+    out["aq"], out["at"] = nv.quantize_dual(out["H"], nv.RNE, nv.RNE, rht=True, rht_seed=rht_seed,
+                                            pre="sqrelu")    # quantizes relu(H)^2 straight from H
     out["Y"] = nv.gemm(out["aq"], out["w2q"], torch.bfloat16)
     out["dyq"], out["dyt"] = nv.quantize_dual(dY, nv.SR, nv.SR, rht=True, sr_seed=sr_seed, sr_offset=0,
                                               rht_seed=rht_seed)
@@ -140,3 +141,25 @@ def test_mlp_block_full_size_sampled(nv, oracle_mod):
     check(o["dyt"], o["at"], o["dW2"])
     check(o["dhq"], None, o["dX"], b_dict=_wt(o["w1q"], d, f))
     check(o["dht"], o["xt"], o["dW1"])
+
+
+@pytest.mark.parametrize("rnd,rht", [(0, True), (1, True), (0, False)])
+@pytest.mark.parametrize("shape", [(208, 336), (1024, 2048)])
+def test_quantize_dual_sqrelu_equals_activation_then_quantize(nv, oracle_mod, rnd, rht, shape):
+    """relu(H)^2 quantized straight from H (the activation applied as H is loaded) is bit
+    for bit the quantization of the stored activation, and both equal the oracle."""
+    g = torch.Generator().manual_seed(sum(shape) + rnd)
+    h = (torch.randn(shape, generator=g) * 2).to(torch.bfloat16).cuda()
+    h[0, :4] = torch.tensor([0.0, -0.0, -1e-30, 1e-30])
+    fr, fc = nv.quantize_dual(h, rnd, rnd, rht=rht, sr_seed=3, sr_offset=1, rht_seed=5, pre="sqrelu")
+    a = nv.sqrelu_forward(h)
+    sr_, sc_ = nv.quantize_dual(a, rnd, rnd, rht=rht, sr_seed=3, sr_offset=1, rht_seed=5)
+    torch.cuda.synchronize()
+    for f, s in ((fr, sr_), (fc, sc_)):
+        assert torch.equal(f.codes, s.codes) and torch.equal(f.scales, s.scales)
+        assert torch.equal(f.scales_mma, s.scales_mma) and torch.equal(f.s_dec[:1], s.s_dec[:1])
+    ah = oracle_mod.sqrelu_forward(host_input(h.cpu()))
+    r = oracle_mod.quantize(ah, oracle_mod.ROW, rnd, sr_seed=3, sr_offset=1)
+    c = oracle_mod.quantize(ah, oracle_mod.COL, rnd, rht=rht, sr_seed=3, sr_offset=1, rht_seed=5)
+    assert np.array_equal(fr.codes.cpu().numpy(), r["codes"]) and np.array_equal(fc.codes.cpu().numpy(), c["codes"])
+    assert np.array_equal(fr.scales.cpu().numpy(), r["scales"]) and np.array_equal(fc.scales.cpu().numpy(), c["scales"])

@@ -72,6 +72,13 @@ def test_quantize_rejects_bad_arguments_without_launching(lib):
         assert st == expect, (kw, st)
     st = L.nvfp4_quantize(fake, lib.BF16, 32, 64, 64, None, ctypes.byref(q), 0x3000, ws, None, None)
     assert st == lib.ERR_INVALID_ARG
+    # the squared-ReLU dual quantization takes bf16 only
+    pr, pc = _qp(lib, 0, 0, 0), _qp(lib, 1, 0, 1)
+    qr = lib.QTensorC(0x1000, 0x1000, None, sdec.value, None, None, 32, 64)
+    qc = lib.QTensorC(0x1000, 0x1000, None, sdec.value, None, None, 64, 32)
+    st = L.nvfp4_quantize_dual_sqrelu(fake, lib.F32, 32, 64, 64, ctypes.byref(pr), ctypes.byref(qr), ctypes.byref(pc),
+                                      ctypes.byref(qc), 0x3000, 2 * ws, None, None)
+    assert st == lib.ERR_UNSUPPORTED
 
 
 def test_gemm_and_linear_reject_bad_arguments(lib):
