@@ -71,6 +71,10 @@ def _load():
         "orc_e2m1_encode_rne_array": (None, [P, c.c_int64, P]),
         "orc_e2m1_encode_sr_array": (None, [P, P, c.c_int64, P]),
         "orc_sr_bits_array": (None, [c.c_uint64, c.c_uint32, c.c_uint32, P, c.c_int64, P]),
+        "orc_mx_scale_code": (c.c_uint8, [c.c_float]),
+        "orc_mx_scale_value": (c.c_double, [c.c_int]),
+        "orc_mx_quantize": (c.c_int, [P, c.c_int, c.c_int64, c.c_int64, c.c_int64, c.c_int, P, P]),
+        "orc_mx_dequant": (None, [P, P, c.c_int64, c.c_int64, c.c_int64, P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -240,3 +244,44 @@ def sqrelu_backward(h_bits: np.ndarray, da_bits: np.ndarray) -> np.ndarray:
     da = _bf16_to_f32(da_bits)
     t = np.where(h > 0, (np.float32(2) * h).astype(np.float32), np.float32(0)).astype(np.float32)
     return _f32_to_bf16((da * t).astype(np.float32))
+
+
+# --- MXFP4 (the comparison format: 1x32 blocks, power-of-two scales, no tensor scale) ---
+
+def mx_scale_code(amax: float) -> int:
+    return int(_load().orc_mx_scale_code(float(amax)))
+
+
+def mx_scale_value(code: int) -> float:
+    return float(_load().orc_mx_scale_value(int(code)))
+
+
+def mx_quantize(x: np.ndarray, col: bool = False) -> dict:
+    """MXFP4 of ``x`` ([R, C] float32 or uint16 bf16 bits): operand x (or x^T with
+    ``col``), 1x32 blocks along the operand's rows.  dict(codes, scales, rows, cols)."""
+    if x.dtype == np.float32:
+        dtype = F32
+    elif x.dtype == np.uint16:
+        dtype = BF16
+    else:
+        raise TypeError("oracle.mx_quantize takes float32 or uint16 (bf16 bits)")
+    x = np.ascontiguousarray(x)
+    R, C = x.shape
+    rows, cols = (C, R) if col else (R, C)
+    codes = np.zeros((rows, cols // 2), dtype=np.uint8)
+    scales = np.zeros((rows, cols // 32), dtype=np.uint8)
+    st = _load().orc_mx_quantize(_ptr(x), dtype, R, C, C, int(bool(col)), _ptr(codes), _ptr(scales))
+    if st == ERR_NONFINITE:
+        raise FloatingPointError("non-finite input")
+    if st != 0:
+        raise ValueError(f"oracle mx_quantize rejected the arguments (status {st})")
+    return dict(codes=codes, scales=scales, rows=rows, cols=cols)
+
+
+def mx_dequant(q: dict, row_begin: int = 0, row_end: int | None = None) -> np.ndarray:
+    rows, cols = q["rows"], q["cols"]
+    row_end = rows if row_end is None else row_end
+    out = np.empty((row_end - row_begin, cols), dtype=np.float64)
+    _load().orc_mx_dequant(_ptr(np.ascontiguousarray(q["codes"])), _ptr(np.ascontiguousarray(q["scales"])),
+                           cols, row_begin, row_end, _ptr(out))
+    return out

@@ -28,7 +28,8 @@
  *
  * Parity status per function (what pins it, see tests/test_oracle_pins.py):
  *   e2m1 decode / RNE / SR encode, e4m3 decode / encode, Philox, RHT,
- *   tensor and block scales, 2D consistency, dequant + fp64 GEMM: pinned.
+ *   tensor and block scales, 2D consistency, dequant + fp64 GEMM, the MXFP4
+ *   comparison format (scale code, elements, dequant): pinned.
  *   Model-level quality (loss, downstream accuracy): parity unpinned, out of
  *   scope (needs training runs).
  */
@@ -445,6 +446,74 @@ void orc_gemm_f64(const double* A, const double* B, int64_t M, int64_t N, int64_
             double s = 0.0;
             for (int64_t k = 0; k < K; ++k) s += A[m * K + k] * B[n * K + k];
             C[m * N + n] = s;
+        }
+}
+
+/* ------------------------------------------------------------------------- */
+/* MXFP4, the comparison format the page names next to NVFP4 [page ¶3]: E2M1    */
+/* elements in blocks of 32 with one power-of-two scale per block (UE8M0) and   */
+/* no tensor scale.  [reading] the conversion of the OCP Microscaling spec:     */
+/* the block's shared exponent e = floor(log2(amax_b)) - 2 (2 = the largest     */
+/* E2M1 exponent, so amax_b / 2^e lies in [4, 8)); the scale 2^e is stored as  */
+/* the byte e + 127 clamped to [0, 254] (an all-zero block stores 0); each      */
+/* element y = x / 2^e (one fp32 rounding, exact unless below the normal range) */
+/* goes to the nearest E2M1 value, ties to even, |y| > 6 saturating to 6.       */
+/* ------------------------------------------------------------------------- */
+uint8_t orc_mx_scale_code(float amax_b) {
+    if (!(amax_b > 0.0f)) return 0;
+    int e2 = 0;
+    (void)frexpf(amax_b, &e2);                 /* amax_b = m 2^e2, m in [0.5, 1) */
+    int biased = (e2 - 1) - 2 + 127;
+    if (biased < 0) biased = 0;
+    if (biased > 254) biased = 254;
+    return (uint8_t)biased;
+}
+
+double orc_mx_scale_value(int code) { return ldexp(1.0, code - 127); }
+
+/*
+ * orc_mx_quantize: MXFP4 of x [R, C] (row pitch ldx): the operand T = x (col = 0,
+ * [R, C]) or x^T (col = 1, [C, R]), 1x32 blocks along T's rows, cols % 32 == 0.
+ * codes [rows, cols/2] (element 2j in the low nibble of byte j), scales
+ * [rows, cols/32] (UE8M0 bytes).
+ */
+int orc_mx_quantize(const void* x, int dtype, int64_t R, int64_t C, int64_t ldx, int col,
+                    uint8_t* codes, uint8_t* scales) {
+    if (R < 0 || C < 0 || ldx < C) return ORC_ERR_ARG;
+    int64_t rows = col ? C : R, cols = col ? R : C;
+    if (cols % 32 != 0) return ORC_ERR_ARG;
+    for (int64_t i = 0; i < rows; ++i)
+        for (int64_t j0 = 0; j0 < cols; j0 += 32) {
+            float v[32];
+            float amax_b = 0.0f;
+            for (int d = 0; d < 32; ++d) {
+                v[d] = col ? load_elem(x, dtype, ldx, j0 + d, i) : load_elem(x, dtype, ldx, i, j0 + d);
+                if (!isfinite(v[d])) return ORC_ERR_NONFINITE;
+                if (fabsf(v[d]) > amax_b) amax_b = fabsf(v[d]);
+            }
+            uint8_t sc = orc_mx_scale_code(amax_b);
+            scales[i * (cols / 32) + j0 / 32] = sc;
+            double X = orc_mx_scale_value(sc);
+            for (int d = 0; d < 32; ++d) {
+                float y = (float)((double)v[d] / X);   /* exact quotient, one rounding to fp32 */
+                int code = orc_e2m1_encode_rne(y);
+                int64_t j = j0 + d;
+                uint8_t* byte = &codes[i * (cols / 2) + j / 2];
+                if ((j & 1) == 0) *byte = (uint8_t)((*byte & 0xF0) | code);
+                else *byte = (uint8_t)((*byte & 0x0F) | (code << 4));
+            }
+        }
+    return ORC_OK;
+}
+
+/* MXFP4 dequantization in fp64 (exact), rows [row_begin, row_end). */
+void orc_mx_dequant(const uint8_t* codes, const uint8_t* scales, int64_t cols, int64_t row_begin,
+                    int64_t row_end, double* out) {
+    for (int64_t i = row_begin; i < row_end; ++i)
+        for (int64_t j = 0; j < cols; ++j) {
+            uint8_t byte = codes[i * (cols / 2) + j / 2];
+            int code = (j & 1) ? (byte >> 4) : (byte & 15);
+            out[(i - row_begin) * cols + j] = orc_e2m1_value(code) * orc_mx_scale_value(scales[i * (cols / 32) + j / 32]);
         }
 }
 

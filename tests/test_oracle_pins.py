@@ -505,3 +505,70 @@ def test_bf16_rounding_helper_matches_torch(oracle_mod):
                         np.array([0.0, -0.0, 1.0, 3.0e38])]).astype(np.float32)
     ref = torch.from_numpy(x).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
     assert np.array_equal(oracle_mod._f32_to_bf16(x), ref)
+
+
+# ---------------------------------------------------------------- MXFP4 (comparison format) --
+
+def _brute_e2m1_times(y: Fraction) -> Fraction:
+    """Nearest E2M1 magnitude to |y| (ties to the even code, > 6 saturates), with y's sign."""
+    grid = [Fraction(v) for v in (0, 0.5, 1, 1.5, 2, 3, 4, 6)]
+    a = abs(y)
+    if a > 6:
+        best = 7
+    else:
+        best = min(range(8), key=lambda k: (abs(a - grid[k]), k % 2))
+    return grid[best] if y >= 0 else -grid[best]
+
+
+def test_mx_scale_puts_the_block_maximum_in_4_to_8(oracle_mod):
+    """The shared exponent maps the block's largest magnitude into [4, 8) (the top E2M1
+    binade), the defining property of the MX scale; an all-zero block stores code 0."""
+    rng = np.random.default_rng(11)
+    vals = list((2.0 ** rng.uniform(-120, 120, 4000)).astype(np.float32))
+    vals += [np.float32(2.0 ** k) for k in range(-120, 121)]
+    vals += [np.nextafter(np.float32(2.0 ** k), np.float32(0)) for k in range(-120, 121)]
+    for a in vals:
+        c = oracle_mod.mx_scale_code(float(a))
+        X = Fraction(2) ** (c - 127)
+        assert 4 * X <= Fraction(float(a)) < 8 * X, (float(a), c)
+    assert oracle_mod.mx_scale_code(0.0) == 0
+
+
+def test_mx_elements_are_the_nearest_grid_points(oracle_mod):
+    """Every dequantized element is the nearest E2M1 value (ties to even) of x / X,
+    checked in exact rational arithmetic."""
+    rng = np.random.default_rng(12)
+    x = (rng.standard_normal((6, 64)) * np.exp(rng.uniform(-8, 8, (6, 1)))).astype(np.float32)
+    x[0, :8] = [0.0, -0.0, 1e-30, -1e-30, 2.5, -3.5, 5.0, 0.75]       # ties and tiny values
+    q = oracle_mod.mx_quantize(x)
+    d = oracle_mod.mx_dequant(q)
+    for i in range(x.shape[0]):
+        for b in range(2):
+            X = Fraction(2) ** (int(q["scales"][i, b]) - 127)
+            for j in range(32 * b, 32 * b + 32):
+                y = Fraction(float(np.float32(Fraction(float(x[i, j])) / X)))   # one fp32 rounding
+                assert Fraction(d[i, j]) == _brute_e2m1_times(y) * X, (i, j, float(x[i, j]))
+
+
+def test_mx_round_trip_and_saturation(oracle_mod):
+    """Blocks of E2M1 values times 2^k that contain +-6 * 2^k come back exactly; a block
+    maximum of 7 * 2^k saturates to 6 * 2^k."""
+    grid = np.array([0, .5, 1, 1.5, 2, 3, 4, 6], np.float32)
+    rng = np.random.default_rng(13)
+    for k in (-20, -3, 0, 5, 30):
+        v = rng.choice(grid, 32) * rng.choice([-1, 1], 32)
+        v[7] = 6.0
+        x = (v * np.float32(2.0 ** k)).astype(np.float32)[None, :]
+        q = oracle_mod.mx_quantize(x)
+        assert np.array_equal(oracle_mod.mx_dequant(q)[0], x[0].astype(np.float64)), k
+        x2 = x.copy()
+        x2[0, 7] = np.float32(7.0 * 2.0 ** k)
+        d2 = oracle_mod.mx_dequant(oracle_mod.mx_quantize(x2))[0]
+        assert d2[7] == 6.0 * 2.0 ** k
+
+
+def test_mx_col_operand_is_the_transpose(oracle_mod):
+    x = np.random.default_rng(14).standard_normal((64, 96)).astype(np.float32)
+    a = oracle_mod.mx_quantize(x, col=True)
+    b = oracle_mod.mx_quantize(np.ascontiguousarray(x.T))
+    assert np.array_equal(a["codes"], b["codes"]) and np.array_equal(a["scales"], b["scales"])
