@@ -373,6 +373,79 @@ def run_yardstick(args):
     print(json.dumps(out))
 
 
+def run_mx(args):
+    """MXFP4, the comparison format (32-element blocks, UE8M0 scales, no tensor scale):
+    its three GEMMs and its quantizer at the FFN up-projection shapes next to NVFP4's,
+    and the error of each format's Fprop / Dgrad / Wgrad against BF16 (cuBLAS) on the
+    heavy-tailed layer -- NVFP4 both as plain 1x16 RNE (format against format) and as the
+    full recipe (16x16 weights, RHT and SR on the Wgrad inputs)."""
+    import torch
+    import nvfp4_bit_quantized_gb300 as nv
+    from nvfp4_bit_quantized_gb300 import inputs
+    peaks, src = measured_peaks()
+    out = {"config": "mxfp4_comparison", "gemm_shapes_MKN": {}, "mx_gemm_tflops": {}, "nvfp4_gemm_tflops": {},
+           "mx_quantize": {}, "rel_error_vs_bf16_heavy_tailed": {}, "peak_source": src}
+    X, W, dY = inputs.linear_layer(M, K, N, seed=0, device="cuda")
+    # operands of the three products, each as [rows, K] of its GEMM
+    mx_ops = {"fprop": (lambda: nv.mx_quantize(X), lambda: nv.mx_quantize(W)),
+              "dgrad": (lambda: nv.mx_quantize(dY), lambda: nv.mx_quantize(W, col=True)),
+              "wgrad": (lambda: nv.mx_quantize(dY, col=True), lambda: nv.mx_quantize(X, col=True))}
+    nv_ops = {"fprop": (lambda: nv.quantize(X, nv.ROW, nv.RNE, scales=False),
+                        lambda: nv.quantize(W, nv.ROW, nv.RNE, scales=False)),
+              "dgrad": (lambda: nv.quantize(dY, nv.ROW, nv.RNE, scales=False),
+                        lambda: nv.quantize(W, nv.COL, nv.RNE, scales=False)),
+              "wgrad": (lambda: nv.quantize(dY, nv.COL, nv.RNE, scales=False),
+                        lambda: nv.quantize(X, nv.COL, nv.RNE, scales=False))}
+    for name in ("fprop", "dgrad", "wgrad"):
+        qa, qb = mx_ops[name][0](), mx_ops[name][1]()
+        m, n, k = qa.rows, qb.rows, qa.cols
+        out["gemm_shapes_MKN"][name] = [m, k, n]
+        flop = 2.0 * m * n * k
+        d = torch.empty((m, n), dtype=torch.bfloat16, device="cuda")
+        t = _timed(lambda: nv.mx_gemm(qa, qb, out=d), args.steps, args.warmup)
+        out["mx_gemm_tflops"][name] = round(flop / (t * 1e-3) / 1e12, 1)
+        del qa, qb
+        qa, qb = nv_ops[name][0](), nv_ops[name][1]()
+        t = _timed(lambda: nv.gemm(qa, qb, out=d), args.steps, args.warmup)
+        out["nvfp4_gemm_tflops"][name] = round(flop / (t * 1e-3) / 1e12, 1)
+        del qa, qb, d
+        torch.cuda.empty_cache()
+    # quantizer: bf16 in (2 B), codes (0.5 B) and UE8M0 scales (1/32 B) out per element
+    bpe = 2 + 0.5 + 1 / 32
+    for mode, col in (("row", False), ("col", True)):
+        t = _timed(lambda: nv.mx_quantize(dY, col=col, scales=False), args.steps, args.warmup)
+        gbs = dY.numel() * bpe / (t * 1e-3) / 1e9
+        out["mx_quantize"][f"{mode}_{M}x{N}"] = {"ms": round(t, 4), "GB/s": round(gbs, 1),
+                                                "hbm_frac": round(gbs / peaks["hbm_gbs"], 3)}
+    del X, W, dY
+    torch.cuda.empty_cache()
+    Mh, Kh, Nh = 16384, 4096, 14336
+    X, W, dY = inputs.heavy_tailed_layer(Mh, Kh, Nh, seed=0, device="cuda")
+    ref = {"fprop": X @ W.t(), "dgrad": dY @ W, "wgrad": dY.t() @ X}
+
+    def rel(name, d):
+        r = ref[name].float()
+        return round(((d.float() - r).norm() / r.norm()).item(), 5)
+    mx = {"fprop": nv.mx_gemm(nv.mx_quantize(X), nv.mx_quantize(W)),
+          "dgrad": nv.mx_gemm(nv.mx_quantize(dY), nv.mx_quantize(W, col=True)),
+          "wgrad": nv.mx_gemm(nv.mx_quantize(dY, col=True), nv.mx_quantize(X, col=True))}
+    out["rel_error_vs_bf16_heavy_tailed"]["mxfp4"] = {k: rel(k, v) for k, v in mx.items()}
+    del mx
+    q = lambda x, b, r=nv.RNE, rht=False: nv.quantize(x, b, r, rht=rht, sr_seed=7, rht_seed=11, scales=False)
+    plain = {"fprop": nv.gemm(q(X, nv.ROW), q(W, nv.ROW)),
+             "dgrad": nv.gemm(q(dY, nv.ROW), q(W, nv.COL)),
+             "wgrad": nv.gemm(q(dY, nv.COL), q(X, nv.COL))}
+    out["rel_error_vs_bf16_heavy_tailed"]["nvfp4_1x16_rne"] = {k: rel(k, v) for k, v in plain.items()}
+    del plain
+    wq = nv.quantize_weight(W)
+    recipe = {"fprop": nv.gemm(q(X, nv.ROW), wq),
+              "dgrad": nv.gemm(q(dY, nv.ROW, nv.SR), wq.transposed()),
+              "wgrad": nv.gemm(q(dY, nv.COL, nv.SR, True), q(X, nv.COL, nv.RNE, True))}
+    out["rel_error_vs_bf16_heavy_tailed"]["nvfp4_recipe"] = {k: rel(k, v) for k, v in recipe.items()}
+    out["device_status"] = nv.status_query()
+    print(json.dumps(out))
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
@@ -383,7 +456,8 @@ def run_ours(args):
         return run_kernel_only(args)
     if args.config != "ffn_up":
         torch.cuda.set_device(0)
-        return {"sweep": run_sweep, "mlp": run_mlp, "heavy": run_heavy, "yardstick": run_yardstick}[args.config](args)
+        return {"sweep": run_sweep, "mlp": run_mlp, "heavy": run_heavy, "yardstick": run_yardstick,
+                "mxfp4": run_mx}[args.config](args)
 
     rank, world, local = env_rank()
     torch.cuda.set_device(local)
@@ -645,9 +719,9 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--kernel", choices=["step", "gemm", "quantize"], default="step",
                     help="step: the whole hot path (the bench line); gemm / quantize: one kernel family alone")
-    ap.add_argument("--config", choices=["ffn_up", "mlp", "sweep", "heavy", "yardstick"], default="ffn_up",
-                    help="ffn_up: the headline workload (default); mlp / sweep / heavy / yardstick: the other workloads, "
-                         "one JSON line each (not the headline metric)")
+    ap.add_argument("--config", choices=["ffn_up", "mlp", "sweep", "heavy", "yardstick", "mxfp4"], default="ffn_up",
+                    help="ffn_up: the headline workload (default); mlp / sweep / heavy / yardstick / mxfp4: the other "
+                         "workloads, one JSON line each (not the headline metric)")
     ap.add_argument("--sweep-min", type=int, default=20)
     ap.add_argument("--sweep-max", type=int, default=28)
     args = ap.parse_args()

@@ -205,6 +205,49 @@ NVFP4_API nvfp4_status nvfp4_quantize_noalloc(const void* x, int32_t x_dtype, in
 NVFP4_API nvfp4_status nvfp4_gemm(const nvfp4_qtensor* A, const nvfp4_qtensor* B, void* D, int32_t d_dtype,
                         int64_t ldd, uint32_t* dev_status, void* stream);
 
+/*
+ * MXFP4 -- the earlier 4-bit microscaling format the page compares NVFP4 with
+ * [page ¶3: at 8B parameters MXFP4 trails NVFP4 in loss and needs ~36% more
+ * tokens].  The page gives no rules for it; these follow the OCP Microscaling
+ * format: blocks of 32 elements along the quantized axis, one UE8M0 scale per
+ * block X = 2^(code - 127) with code = floor(log2(amax_b)) - 2 + 127 clamped
+ * to [0, 254] (0 for an all-zero block), element code = e2m1_rne_sat(x / X),
+ * no tensor scale, no stochastic rounding.  Dequantized value: e2m1(code) * X.
+ *
+ * The operand uses nvfp4_qtensor with these meanings (s_dec, codes_t and
+ * scales_mma_t are ignored):
+ *   codes       [rows, cols/2] bytes, as for NVFP4;
+ *   scales      UE8M0 codes, row-major [rows, cols/32].  May be NULL;
+ *   scales_mma  the tile layout the MXFP4 GEMM reads: ceil(rows/128) x
+ *               ceil(cols/256) tiles of 1024 bytes, tile (rb, kb) at byte
+ *               ((rb * ceil(cols/256)) + kb) * 1024; inside a tile, row r,
+ *               scale-column s (s = k/32) at ((s/4)%2)*512 + (r%32)*16 +
+ *               ((r%128)/32)*4 + s%4.  Padding holds 0.  May be NULL.
+ */
+NVFP4_API size_t nvfp4_mx_scales_mma_bytes(int64_t rows, int64_t cols);
+
+/*
+ * nvfp4_mx_quantize -- MXFP4 quantization of x [R, C] (row pitch ldx elements,
+ * F32 or BF16).  col = 0: blocks along C, the operand is [R, C]; col = 1:
+ * blocks along R, the operand is x^T [C, R] (out->rows = C, out->cols = R).
+ * Rules: the operand's cols % 32 == 0; x and its row pitch 32-byte aligned
+ * (col = 0) or 16-byte aligned (col = 1); codes 16-byte aligned; with col = 1,
+ * R <= 65535 * 64.  Non-finite input gives unspecified codes.  Asynchronous on
+ * `stream`; nothing is allocated.
+ */
+NVFP4_API nvfp4_status nvfp4_mx_quantize(const void* x, int32_t x_dtype, int64_t R, int64_t C, int64_t ldx,
+                                         int32_t col, const nvfp4_qtensor* out, void* stream);
+
+/*
+ * nvfp4_mx_gemm -- D[M, N] = sum_k qA[m,k]*XA[m,k/32] * qB[n,k]*XB[n,k/32] with
+ * MXFP4 operands (scales_mma required) on the tcgen05 block-scaled FP4 tensor
+ * cores (scale_vec::2X, UE8M0 scales, fp32 accumulation), CTA-pair kernel.
+ * D: BF16 only (F32 gives NVFP4_ERR_UNSUPPORTED), base and pitch ldd 16-byte
+ * aligned.  Other rules as for nvfp4_gemm.
+ */
+NVFP4_API nvfp4_status nvfp4_mx_gemm(const nvfp4_qtensor* A, const nvfp4_qtensor* B, void* D, int32_t d_dtype,
+                                     int64_t ldd, uint32_t* dev_status, void* stream);
+
 /* Workspace bytes for the three linear-layer calls below with these sizes. */
 NVFP4_API size_t nvfp4_linear_workspace_bytes(int64_t M, int64_t N, int64_t K);
 

@@ -192,6 +192,57 @@ def gemm(A: QTensor, B: QTensor, out_dtype=torch.bfloat16, out: Optional[torch.T
     return out
 
 
+# ----------------------------------------------------------------------------- MXFP4 comparison format
+
+@dataclass
+class MXTensor:
+    """An MXFP4 operand of logical shape [rows, cols]: 32-element blocks along cols,
+    UE8M0 power-of-two scales, no tensor scale."""
+    codes: torch.Tensor                       # uint8 [rows, cols/2]
+    scales: Optional[torch.Tensor]            # uint8 [rows, cols/32]
+    scales_mma: Optional[torch.Tensor]        # uint8, 1 KB-tile layout
+    rows: int
+    cols: int
+
+    def c_struct(self) -> L.QTensorC:
+        return L.QTensorC(_ptr(self.codes), _ptr(self.scales), _ptr(self.scales_mma), None, None, None,
+                          self.rows, self.cols)
+
+
+def mx_scales_mma_bytes(rows: int, cols: int) -> int:
+    return int(L.lib().nvfp4_mx_scales_mma_bytes(rows, cols))
+
+
+def mx_quantize(x: torch.Tensor, col: bool = False, scales: bool = True, scales_mma: bool = True) -> MXTensor:
+    """MXFP4 quantization of x [R, C] (blocks along C), or of x^T [C, R] with ``col``."""
+    _check_2d(x, "x")
+    R, C = x.shape
+    rows, cols = (C, R) if col else (R, C)
+    dev = x.device
+    q = MXTensor(torch.empty((rows, cols // 2), dtype=torch.uint8, device=dev),
+                 torch.empty((rows, cols // 32), dtype=torch.uint8, device=dev) if scales else None,
+                 torch.empty(max(mx_scales_mma_bytes(rows, cols), 16), dtype=torch.uint8, device=dev)
+                 if scales_mma else None, rows, cols)
+    qc = q.c_struct()
+    ld = x.stride(0) if R > 1 else max(C, 1)
+    st = L.lib().nvfp4_mx_quantize(_ptr(x), _DT[x.dtype], R, C, ld, int(bool(col)), ctypes.byref(qc), _stream())
+    L.check(st, "nvfp4_mx_quantize")
+    return q
+
+
+def mx_gemm(A: MXTensor, B: MXTensor, out: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """D[M, N] = dequant(A) . dequant(B)^T for MXFP4 operands (bf16 out) on the FP4 tensor cores."""
+    M, N = A.rows, B.rows
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.bfloat16, device=A.codes.device)
+    _check_2d(out, "out")
+    a, b = A.c_struct(), B.c_struct()
+    st = L.lib().nvfp4_mx_gemm(ctypes.byref(a), ctypes.byref(b), _ptr(out), _DT[out.dtype], out.stride(0),
+                               dev_status(out.device).data_ptr(), _stream())
+    L.check(st, "nvfp4_mx_gemm")
+    return out
+
+
 def _linear_ws(M: int, N: int, K: int) -> torch.Tensor:
     return _workspace(int(L.lib().nvfp4_linear_workspace_bytes(M, N, K)))
 

@@ -17,7 +17,7 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libnvfp4_gb300.so")
-SOURCES = ["quantize.cu", "gemm.cu", "linear.cu", "capi.cu", "activation.cu"]
+SOURCES = ["quantize.cu", "gemm.cu", "linear.cu", "capi.cu", "activation.cu", "mx.cu"]
 HEADERS = ["device_common.cuh", "host_common.h"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

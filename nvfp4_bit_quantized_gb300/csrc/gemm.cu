@@ -565,6 +565,11 @@ static_assert(P_SMEM_BYTES <= SMEM_LIMIT, "pair shared memory budget");
 static_assert(SF_COL0 + P_STAGES * SF_STAGE_COLS <= TMEM_COLS, "pair TMEM budget");
 // M = 256 (both CTAs), N = 256
 constexpr uint32_t IDESC_PAIR = (1u << 7) | (1u << 10) | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(256 >> 4) << 24);
+// MXFP4 operands: the same E2M1 codes with UE8M0 scales (bit 23), one per 32 elements
+// (scale_vec::2X: two scale bytes per row per K = 64 MMA, scale-factor IDs 0).
+constexpr uint32_t IDESC_PAIR_MX = IDESC_PAIR | (1u << 23);
+// Scale bytes of one 128-row block per 256-wide K tile: 16 E4M3 (NVFP4) or 8 UE8M0 (MXFP4) a row.
+template <bool MX> struct PairSf { static constexpr uint32_t TILE = MX ? 1024u : 2048u; };
 
 __device__ __forceinline__ uint32_t cluster_rank() {
     uint32_t r;
@@ -585,13 +590,21 @@ __device__ __forceinline__ uint32_t map_to_rank(uint32_t saddr, uint32_t rank) {
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
     asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" :: "r"(cluster_addr) : "memory");
 }
-__device__ __forceinline__ void tc_mma_pair(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc, uint32_t sfa,
-                                            uint32_t sfb, uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::2.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%5], [%6], p;\n\t}"
-        :: "r"(d), "l"(a), "l"(b), "r"(idesc), "r"(accumulate), "r"(sfa), "r"(sfb) : "memory");
+template <bool MX>
+__device__ __forceinline__ void tc_mma_pair(uint32_t d, uint64_t a, uint64_t b, uint32_t sfa, uint32_t sfb,
+                                            uint32_t accumulate) {
+    if constexpr (MX)
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "setp.ne.b32 p, %4, 0;\n\t"
+            "tcgen05.mma.cta_group::2.kind::mxf4nvf4.block_scale.scale_vec::2X [%0], %1, %2, %3, [%5], [%6], p;\n\t}"
+            :: "r"(d), "l"(a), "l"(b), "r"(IDESC_PAIR_MX), "r"(accumulate), "r"(sfa), "r"(sfb) : "memory");
+    else
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "setp.ne.b32 p, %4, 0;\n\t"
+            "tcgen05.mma.cta_group::2.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%5], [%6], p;\n\t}"
+            :: "r"(d), "l"(a), "l"(b), "r"(IDESC_PAIR), "r"(accumulate), "r"(sfa), "r"(sfb) : "memory");
 }
 // Arrive on the barrier at this offset in both CTAs of the pair when the MMAs issued so far complete.
 __device__ __forceinline__ void tc_commit_pair(uint32_t bar) {
@@ -631,6 +644,7 @@ __device__ __forceinline__ void reg_fence64(uint32_t (&v)[64]) {
     reg_fence32(*reinterpret_cast<uint32_t (*)[32]>(&v[32]));
 }
 
+template <bool MX>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
 gemm_nvfp4_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                        const __grid_constant__ CUtensorMap tmD, const Params p) {
@@ -703,7 +717,8 @@ gemm_nvfp4_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_con
                 // rows past M (the follower's half of the last pair tile) have no scale block:
                 // their codes load as zeros and their output rows are never stored
                 const bool has_sfa = mrow < p.M;
-                const uint32_t sf_bytes = (has_sfa ? SFA_BYTES : 0) + SFB_BYTES - (second_sfb ? 0 : 2048);
+                constexpr uint32_t SFT = PairSf<MX>::TILE;
+                const uint32_t sf_bytes = (has_sfa ? SFT : 0) + (second_sfb ? 2 * SFT : SFT);
                 for (int kt = 0; kt < p.nkt; ++kt) {
                     if (!mbar_wait_bounded(&empty[stage], phase ^ 1u, p.timeout_ns, abort_flag, p.dev_status)) {
                         ok = false;
@@ -720,11 +735,11 @@ gemm_nvfp4_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_con
                         uint8_t* sSFB = sSFA + SFA_BYTES;
                         mbar_arrive_expect_tx(&sf_loaded[stage], sf_bytes);
                         if (has_sfa)
-                            bulk_load(smem_addr(sSFA), p.sfa + ((size_t)(mrow / 128) * p.nkt + kt) * 2048u, 2048u, bar);
-                        bulk_load(smem_addr(sSFB), p.sfb + ((size_t)(2 * nt) * p.nkt + kt) * 2048u, 2048u, bar);
+                            bulk_load(smem_addr(sSFA), p.sfa + ((size_t)(mrow / 128) * p.nkt + kt) * SFT, SFT, bar);
+                        bulk_load(smem_addr(sSFB), p.sfb + ((size_t)(2 * nt) * p.nkt + kt) * SFT, SFT, bar);
                         if (second_sfb)
-                            bulk_load(smem_addr(sSFB + 2048), p.sfb + ((size_t)(2 * nt + 1) * p.nkt + kt) * 2048u,
-                                      2048u, bar);
+                            bulk_load(smem_addr(sSFB + SFT), p.sfb + ((size_t)(2 * nt + 1) * p.nkt + kt) * SFT,
+                                      SFT, bar);
                     }
                     issued_mask |= 1u << stage;
                     issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
@@ -759,8 +774,8 @@ gemm_nvfp4_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_con
                     const uint32_t tsf = tmem + SF_COL0 + stage * SF_STAGE_COLS;
 #pragma unroll
                     for (int j = 0; j < 4; ++j)
-                        tc_mma_pair(tmem + ACC_COL, da + 2 * j, db + 2 * j, IDESC_PAIR, tsf + 4 * j, tsf + 16 + 8 * j,
-                                    (kt | j) != 0 ? 1u : 0u);
+                        tc_mma_pair<MX>(tmem + ACC_COL, da + 2 * j, db + 2 * j, tsf + 4 * j, tsf + 16 + 8 * j,
+                                        (kt | j) != 0 ? 1u : 0u);
                     issued = true;
                     tc_commit_pair(smem_addr(&empty[stage]));
                     if (++stage == STAGES) { stage = 0; phase ^= 1u; }
@@ -789,19 +804,51 @@ gemm_nvfp4_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_con
                 const uint8_t* sSFA = smem + stage * P_STAGE_BYTES + A_BYTES + P_B_BYTES;
                 const uint8_t* sSFB = sSFA + SFA_BYTES;
                 uint32_t va[16], vb0[16], vb1[16];
+                if constexpr (!MX) {
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const uint4 a4 = *reinterpret_cast<const uint4*>(sSFA + 512 * j + 16 * lane);
-                    va[4 * j] = a4.x; va[4 * j + 1] = a4.y; va[4 * j + 2] = a4.z; va[4 * j + 3] = a4.w;
-                }
+                    for (int j = 0; j < 4; ++j) {
+                        const uint4 a4 = *reinterpret_cast<const uint4*>(sSFA + 512 * j + 16 * lane);
+                        va[4 * j] = a4.x; va[4 * j + 1] = a4.y; va[4 * j + 2] = a4.z; va[4 * j + 3] = a4.w;
+                    }
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
+                    for (int j = 0; j < 4; ++j) {
 #pragma unroll
-                    for (int nb = 0; nb < 2; ++nb) {
-                        const uint4 b4 = *reinterpret_cast<const uint4*>(sSFB + 2048 * nb + 512 * j + 16 * lane);
-                        const int o = 8 * j + 4 * nb;
-                        uint32_t* dst = o < 16 ? vb0 : vb1;
-                        dst[(o & 15)] = b4.x; dst[(o & 15) + 1] = b4.y; dst[(o & 15) + 2] = b4.z; dst[(o & 15) + 3] = b4.w;
+                        for (int nb = 0; nb < 2; ++nb) {
+                            const uint4 b4 = *reinterpret_cast<const uint4*>(sSFB + 2048 * nb + 512 * j + 16 * lane);
+                            const int o = 8 * j + 4 * nb;
+                            uint32_t* dst = o < 16 ? vb0 : vb1;
+                            dst[(o & 15)] = b4.x; dst[(o & 15) + 1] = b4.y; dst[(o & 15) + 2] = b4.z;
+                            dst[(o & 15) + 3] = b4.w;
+                        }
+                    }
+                } else {
+                    // a 512-byte piece holds 4 scales (= two K = 64 steps) per row: the low
+                    // halfword of a row's word feeds step 2h, the high one step 2h + 1, each
+                    // written to the low halfword of that step's column (scale-factor ID 0)
+                    auto split = [](uint32_t w, int step_odd) { return step_odd ? (w >> 16) : (w & 0xFFFFu); };
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const uint4 a4 = *reinterpret_cast<const uint4*>(sSFA + 512 * h + 16 * lane);
+                        const uint32_t aw[4] = {a4.x, a4.y, a4.z, a4.w};
+#pragma unroll
+                        for (int odd = 0; odd < 2; ++odd)
+#pragma unroll
+                            for (int c = 0; c < 4; ++c) va[4 * (2 * h + odd) + c] = split(aw[c], odd);
+                    }
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+#pragma unroll
+                        for (int nb = 0; nb < 2; ++nb) {
+                            const uint4 b4 = *reinterpret_cast<const uint4*>(sSFB + 1024 * nb + 512 * h + 16 * lane);
+                            const uint32_t bw[4] = {b4.x, b4.y, b4.z, b4.w};
+#pragma unroll
+                            for (int odd = 0; odd < 2; ++odd) {
+                                const int o = 8 * (2 * h + odd) + 4 * nb;
+                                uint32_t* dst = o < 16 ? vb0 : vb1;
+#pragma unroll
+                                for (int c = 0; c < 4; ++c) dst[(o & 15) + c] = split(bw[c], odd);
+                            }
+                        }
                     }
                 }
                 const uint32_t tsf = tq + SF_COL0 + stage * SF_STAGE_COLS;
@@ -823,7 +870,7 @@ gemm_nvfp4_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_con
     } else {
         // ------------------------------------------------ epilogue (warps 2-5, each CTA, its 128 rows)
         const int q = warp & 3;
-        const float alpha = __fmul_rn(*p.sdec_a, *p.sdec_b);
+        const float alpha = MX ? 1.0f : __fmul_rn(*p.sdec_a, *p.sdec_b);   // MXFP4 has no tensor scale
         const uint32_t tmem_row = tmem + ((uint32_t)(q * 32) << 16);
         uint8_t* stg = staging + q * (2 * BOX_BYTES);
         uint32_t acc_phase = 0;
@@ -939,13 +986,14 @@ cudaError_t launch(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorM
     return cudaGetLastError();
 }
 
+template <bool MX>
 cudaError_t launch_pair(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& td, const Params& p,
                         int pair_tiles, int sms, cudaStream_t stream) {
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
     static int max_clusters = 0;
     std::call_once(once, [sms] {
-        attr_err = cudaFuncSetAttribute(gemm_nvfp4_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        attr_err = cudaFuncSetAttribute(gemm_nvfp4_pair_kernel<MX>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                         P_SMEM_BYTES);
         if (attr_err != cudaSuccess) return;
         cudaLaunchConfig_t cfg = {};
@@ -953,12 +1001,12 @@ cudaError_t launch_pair(const CUtensorMap& ta, const CUtensorMap& tb, const CUte
         cfg.blockDim = dim3(P_THREADS, 1, 1);
         cfg.dynamicSmemBytes = P_SMEM_BYTES;
         int n = 0;
-        if (cudaOccupancyMaxActiveClusters(&n, gemm_nvfp4_pair_kernel, &cfg) != cudaSuccess || n <= 0) n = sms / 2;
+        if (cudaOccupancyMaxActiveClusters(&n, gemm_nvfp4_pair_kernel<MX>, &cfg) != cudaSuccess || n <= 0) n = sms / 2;
         max_clusters = n;
     });
     if (attr_err != cudaSuccess) return attr_err;
     const int clusters = std::max(1, std::min(pair_tiles, max_clusters));
-    gemm_nvfp4_pair_kernel<<<2 * clusters, P_THREADS, P_SMEM_BYTES, stream>>>(ta, tb, td, p);
+    gemm_nvfp4_pair_kernel<MX><<<2 * clusters, P_THREADS, P_SMEM_BYTES, stream>>>(ta, tb, td, p);
     return cudaGetLastError();
 }
 
@@ -1020,14 +1068,62 @@ nvfp4_status gemm_impl(const nvfp4_qtensor* A, const nvfp4_qtensor* B, void* D, 
     if (pair) {
         CUtensorMap tb2;      // B boxes of 128 rows (each CTA loads its half of the N tile)
         if (!make_codes_map(&tb2, B->codes, N, K, 128)) return NVFP4_ERR_CUDA;
-        e = launch_pair(ta, tb2, td, p, pair_tiles, sm_count(dev), stream);
+        e = launch_pair<false>(ta, tb2, td, p, pair_tiles, sm_count(dev), stream);
     } else {
         e = staged ? launch<true>(ta, tb, td, p, grid, stream) : launch<false>(ta, tb, td, p, grid, stream);
     }
     return e == cudaSuccess ? NVFP4_OK : NVFP4_ERR_CUDA;
 }
 
+// MXFP4 operands through the CTA-pair kernel (bf16 output, 16-byte aligned base and pitch).
+nvfp4_status mx_gemm_impl(const nvfp4_qtensor* A, const nvfp4_qtensor* B, void* D, int32_t d_dtype, int64_t ldd,
+                          uint32_t* dev_status, cudaStream_t stream) {
+    using namespace gemm;
+    if (!A || !B || !D) return NVFP4_ERR_INVALID_ARG;
+    if (d_dtype != NVFP4_F32 && d_dtype != NVFP4_BF16) return NVFP4_ERR_INVALID_ARG;
+    if (d_dtype != NVFP4_BF16) return NVFP4_ERR_UNSUPPORTED;
+    if (!A->codes || !B->codes || !A->scales_mma || !B->scales_mma) return NVFP4_ERR_INVALID_ARG;
+    const int64_t M = A->rows, N = B->rows, K = A->cols;
+    if (B->cols != K) return NVFP4_ERR_SHAPE;
+    if (M < 1 || N < 1 || K < 32 || K % 32 != 0 || ldd < N) return NVFP4_ERR_SHAPE;
+    if (M > (1ll << 30) || N > (1ll << 30) || K > (1ll << 30)) return NVFP4_ERR_SHAPE;
+    if (!aligned16(A->codes) || !aligned16(B->codes) || !aligned16(A->scales_mma) || !aligned16(B->scales_mma) ||
+        !aligned16(D) || (ldd * 2) % 16 != 0)
+        return NVFP4_ERR_ALIGNMENT;
+    CUtensorMap ta, tb, td;
+    if (!make_codes_map(&ta, A->codes, M, K, BM) || !make_codes_map(&tb, B->codes, N, K, 128) ||
+        !make_out_map(&td, D, M, N, ldd))
+        return NVFP4_ERR_CUDA;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return NVFP4_ERR_CUDA;
+    Params p;
+    std::memset(&p, 0, sizeof(p));
+    p.sfa = A->scales_mma;
+    p.sfb = B->scales_mma;
+    p.D = D;
+    p.ldd = ldd;
+    p.M = (int)M;
+    p.N = (int)N;
+    p.K = (int)K;
+    p.d_bf16 = 1;
+    p.vec_store = 1;
+    p.nkt = (int)((K + BK - 1) / BK);
+    p.m_tiles = (int)((M + BM - 1) / BM);
+    p.n_tiles = (int)((N + BN - 1) / BN);
+    p.n_fastest = (M > N) ? 1 : 0;
+    p.dev_status = dev_status;
+    p.timeout_ns = wait_timeout_ns();
+    const int pair_tiles = (int)((M + 255) / 256) * p.n_tiles;
+    const cudaError_t e = launch_pair<true>(ta, tb, td, p, pair_tiles, sm_count(dev), stream);
+    return e == cudaSuccess ? NVFP4_OK : NVFP4_ERR_CUDA;
+}
+
 }  // namespace nvfp4
+
+extern "C" nvfp4_status nvfp4_mx_gemm(const nvfp4_qtensor* A, const nvfp4_qtensor* B, void* D, int32_t d_dtype,
+                                      int64_t ldd, uint32_t* dev_status, void* stream) {
+    return nvfp4::mx_gemm_impl(A, B, D, d_dtype, ldd, dev_status, static_cast<cudaStream_t>(stream));
+}
 
 // Test hook: 0 chooses the kernel automatically, 1 forces the single-CTA kernel,
 // 2 forces the CTA-pair kernel where its epilogue applies (bf16, aligned output).

@@ -54,3 +54,15 @@ def bf16_round(a: np.ndarray) -> np.ndarray:
     fp64 -> fp32 first can double-round; the bf16 comparisons use a Frobenius
     bound far above that effect."""
     return torch.from_numpy(a.astype(np.float32)).to(torch.bfloat16).to(torch.float64).numpy()
+
+
+def mx_mma_layout_from_canonical(scales: np.ndarray, rows: int, cols: int) -> np.ndarray:
+    """Expected MXFP4 tensor-core scale buffer (1 KB tiles, include/nvfp4.h) from [rows, cols/32] scales."""
+    nrb = (rows + 127) // 128
+    nkb = (cols + 255) // 256
+    out = np.zeros(nrb * nkb * 1024, dtype=np.uint8)
+    r = np.arange(rows)[:, None]
+    s = np.arange(cols // 32)[None, :]
+    off = (((r >> 7) * nkb + (s >> 3)) << 10) + (((s >> 2) & 1) << 9) + ((r & 31) << 4) + (((r >> 5) & 3) << 2) + (s & 3)
+    out[off.reshape(-1)] = scales.reshape(-1)
+    return out

@@ -129,3 +129,32 @@ def test_linear_workspace_covers_every_operand_orientation(lib, M, N, K):
 
     need = 4096 * 4 + max(slot(M, K), slot(M, N), slot(N, M)) + slot(K, M)
     assert L.nvfp4_linear_workspace_bytes(M, N, K) >= need
+
+
+def test_mx_entry_points_reject_bad_arguments(lib):
+    L = lib.lib()
+    assert L.nvfp4_mx_scales_mma_bytes(128, 256) == 1024
+    assert L.nvfp4_mx_scales_mma_bytes(129, 288) == 4096
+    assert L.nvfp4_mx_scales_mma_bytes(8192, 5120) == 64 * 20 * 1024
+    q = lib.QTensorC(0x1000, 0x1000, None, None, None, None, 32, 64)
+    mxq = L.nvfp4_mx_quantize
+    assert mxq(0x1000, 5, 32, 64, 64, 0, ctypes.byref(q), None) == lib.ERR_INVALID_ARG      # dtype
+    assert mxq(0x1000, lib.BF16, 32, 64, 64, 2, ctypes.byref(q), None) == lib.ERR_INVALID_ARG  # col flag
+    assert mxq(0x1000, lib.BF16, 32, 64, 48, 0, ctypes.byref(q), None) == lib.ERR_SHAPE     # ldx < C
+    assert mxq(0x1000, lib.BF16, 32, 64, 64, 1, ctypes.byref(q), None) == lib.ERR_SHAPE     # x^T is [64, 32]
+    q48 = lib.QTensorC(0x1000, 0x1000, None, None, None, None, 32, 48)
+    assert mxq(0x1000, lib.BF16, 32, 48, 48, 0, ctypes.byref(q48), None) == lib.ERR_SHAPE   # 32-element blocks
+    assert mxq(0x1010, lib.BF16, 32, 64, 64, 0, ctypes.byref(q), None) == lib.ERR_ALIGNMENT  # 32-byte loads
+    assert mxq(0x1000, lib.BF16, 32, 64, 64, 0, None, None) == lib.ERR_INVALID_ARG
+    A = lib.QTensorC(0x1000, None, 0x1000, None, None, None, 128, 256)
+    B = lib.QTensorC(0x1000, None, 0x1000, None, None, None, 256, 256)
+    g = L.nvfp4_mx_gemm
+    assert g(ctypes.byref(A), ctypes.byref(B), 0x4000, lib.F32, 256, None, None) == lib.ERR_UNSUPPORTED
+    assert g(ctypes.byref(A), ctypes.byref(B), 0x4000, 9, 256, None, None) == lib.ERR_INVALID_ARG
+    assert g(ctypes.byref(A), ctypes.byref(B), 0x4008, lib.BF16, 256, None, None) == lib.ERR_ALIGNMENT
+    assert g(ctypes.byref(A), ctypes.byref(B), 0x4000, lib.BF16, 260, None, None) == lib.ERR_ALIGNMENT
+    B.cols = 128
+    assert g(ctypes.byref(A), ctypes.byref(B), 0x4000, lib.BF16, 256, None, None) == lib.ERR_SHAPE
+    B.cols = 256
+    B.scales_mma = None
+    assert g(ctypes.byref(A), ctypes.byref(B), 0x4000, lib.BF16, 256, None, None) == lib.ERR_INVALID_ARG
