@@ -206,6 +206,18 @@ NVFP4_API nvfp4_status nvfp4_gemm(const nvfp4_qtensor* A, const nvfp4_qtensor* B
                         int64_t ldd, uint32_t* dev_status, void* stream);
 
 /*
+ * nvfp4_gemm_sqrelu_bwd -- the Dgrad GEMM of a squared-ReLU MLP with the activation's
+ * backward in its epilogue: with dA = bf16(s_dec(A) s_dec(B) sum_k qA qB) (what nvfp4_gemm
+ * stores in BF16), D[m, n] = bf16(dA[m, n] * (H[m, n] > 0 ? 2 H[m, n] : +0)) in fp32 --
+ * bit for bit nvfp4_gemm (CTA-pair kernel, BF16) followed by nvfp4_sqrelu_backward, without
+ * writing and re-reading dA.  H and D: BF16 [M, N], row pitches ldh, ldd >= N elements,
+ * bases and pitches 16-byte aligned (else NVFP4_ERR_ALIGNMENT).  A, B as for nvfp4_gemm.
+ */
+NVFP4_API nvfp4_status nvfp4_gemm_sqrelu_bwd(const nvfp4_qtensor* A, const nvfp4_qtensor* B, const void* H,
+                                             int64_t ldh, void* D, int64_t ldd, uint32_t* dev_status,
+                                             void* stream);
+
+/*
  * MXFP4 -- the earlier 4-bit microscaling format the page compares NVFP4 with
  * [page ¶3: at 8B parameters MXFP4 trails NVFP4 in loss and needs ~36% more
  * tokens].  The page gives no rules for it; these follow the OCP Microscaling

@@ -22,7 +22,7 @@ EXPORTS = [
     "nvfp4_status_query", "nvfp4_status_string", "nvfp4_set_wait_timeout_ns", "nvfp4_debug_e4m3",
     "nvfp4_debug_e2m1", "nvfp4_debug_philox", "nvfp4_selftest_wait_timeout", "nvfp4_gemm_force_path",
     "nvfp4_sqrelu_forward", "nvfp4_sqrelu_backward",
-    "nvfp4_mx_scales_mma_bytes", "nvfp4_mx_quantize", "nvfp4_mx_gemm",
+    "nvfp4_mx_scales_mma_bytes", "nvfp4_mx_quantize", "nvfp4_mx_gemm", "nvfp4_gemm_sqrelu_bwd",
 ]
 
 
@@ -89,6 +89,7 @@ def lib():
             "nvfp4_mx_scales_mma_bytes": (SZ, [I64, I64]),
             "nvfp4_mx_quantize": (I32, [P, I32, I64, I64, I64, I32, QT, P]),
             "nvfp4_mx_gemm": (I32, [QT, QT, P, I32, I64, P, P]),
+            "nvfp4_gemm_sqrelu_bwd": (I32, [QT, QT, P, I64, P, I64, P, P]),
         }
         for name, (res, args) in sigs.items():
             fn = getattr(L, name)

@@ -243,6 +243,25 @@ def mx_gemm(A: MXTensor, B: MXTensor, out: Optional[torch.Tensor] = None) -> tor
     return out
 
 
+def gemm_sqrelu_backward(A: QTensor, B: QTensor, H: torch.Tensor, out: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """dH = dA * 2 relu(H) with dA = dequant(A) . dequant(B)^T in bf16 -- the Dgrad GEMM of a
+    squared-ReLU MLP with the activation's backward in its epilogue (dA is never stored);
+    bit for bit ``sqrelu_backward(H, gemm(A, B, torch.bfloat16))``.  H: bf16 [M, N]."""
+    M, N = A.rows, B.rows
+    _check_2d(H, "H")
+    if H.dtype != torch.bfloat16 or tuple(H.shape) != (M, N):
+        raise NVFP4Error(L.ERR_INVALID_ARG, f"H must be bfloat16 [{M}, {N}]")
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.bfloat16, device=A.codes.device)
+    _check_2d(out, "out")
+    a, b = A.c_struct(), B.c_struct()
+    st = L.lib().nvfp4_gemm_sqrelu_bwd(ctypes.byref(a), ctypes.byref(b), _ptr(H), H.stride(0) if M > 1 else N,
+                                       _ptr(out), out.stride(0) if M > 1 else N, dev_status(out.device).data_ptr(),
+                                       _stream())
+    L.check(st, "nvfp4_gemm_sqrelu_bwd")
+    return out
+
+
 def _linear_ws(M: int, N: int, K: int) -> torch.Tensor:
     return _workspace(int(L.lib().nvfp4_linear_workspace_bytes(M, N, K)))
 

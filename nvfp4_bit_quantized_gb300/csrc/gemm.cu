@@ -126,6 +126,24 @@ __device__ __forceinline__ void tma_store_2d(const CUtensorMap* tm, uint32_t src
     asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];"
                  :: "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y), "r"(src) : "memory");
 }
+// Streaming data (the output tiles, the epilogue's H tiles) is marked evict-first in L2, so it
+// does not push out the operand that consecutive tiles re-read.
+__device__ __forceinline__ uint64_t l2_evict_first_policy() {
+    uint64_t pol;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+__device__ __forceinline__ void tma_store_2d_hint(const CUtensorMap* tm, uint32_t src, int x, int y, uint64_t pol) {
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group.L2::cache_hint [%0, {%1, %2}], [%3], %4;"
+                 :: "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y), "r"(src), "l"(pol) : "memory");
+}
+__device__ __forceinline__ void tma_load_2d_hint(uint32_t dst, const CUtensorMap* tm, int x, int y, uint32_t bar,
+                                                 uint64_t pol) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%2, %3}], [%4], %5;"
+        :: "r"(dst), "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y), "r"(bar), "l"(pol) : "memory");
+}
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void bulk_wait_read0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
 __device__ __forceinline__ void bulk_wait0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
@@ -635,6 +653,40 @@ __device__ __forceinline__ void box_to_smem(const uint32_t (&v)[64], uint8_t* bo
     }
 }
 
+// The same box for D = dH = dA * 2 relu(H): the slot already holds the matching 32 x 64 box of
+// H (TMA-loaded, same swizzle); each value is first rounded to bf16 exactly as the plain
+// epilogue stores dA, then multiplied by (h > 0 ? 2h : +0) in fp32 and rounded to bf16 --
+// the arithmetic of the separate squared-ReLU backward kernel, so the fused result equals
+// GEMM-then-backward bit for bit.
+__device__ __forceinline__ void box_to_smem_dsqr(const uint32_t (&v)[64], uint8_t* box, int lane, float alpha) {
+    uint8_t* row = box + lane * 128;
+    const float2 al = make_float2(alpha, alpha);
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+        uint4* slot = reinterpret_cast<uint4*>(row + ((c ^ (lane & 7)) << 4));
+        const uint4 hq = *slot;
+        const uint32_t hw[4] = {hq.x, hq.y, hq.z, hq.w};
+        uint32_t w[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float2 s = __fmul2_rn(make_float2(__uint_as_float(v[8 * c + 2 * i]),
+                                                    __uint_as_float(v[8 * c + 2 * i + 1])), al);
+            const __nv_bfloat162 da = __float22bfloat162_rn(s);
+            const float hl = bf16_lo(hw[i]), hh = bf16_hi(hw[i]);
+            const float2 t = make_float2(hl > 0.0f ? __fmul_rn(2.0f, hl) : 0.0f, hh > 0.0f ? __fmul_rn(2.0f, hh) : 0.0f);
+            const __nv_bfloat162 dh = __float22bfloat162_rn(__fmul2_rn(__bfloat1622float2(da), t));
+            w[i] = *reinterpret_cast<const uint32_t*>(&dh);
+        }
+        *slot = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+}
+
+template <bool DSQR>
+__device__ __forceinline__ void box_out(const uint32_t (&v)[64], uint8_t* box, int lane, float alpha) {
+    if constexpr (DSQR) box_to_smem_dsqr(v, box, lane, alpha);
+    else box_to_smem(v, box, lane, alpha);
+}
+
 __device__ __forceinline__ void tmem_ld_64cols(uint32_t taddr, uint32_t (&v)[64]) {
     tmem_ld_32cols_nowait(taddr, *reinterpret_cast<uint32_t (*)[32]>(&v[0]));
     tmem_ld_32cols_nowait(taddr + 32, *reinterpret_cast<uint32_t (*)[32]>(&v[32]));
@@ -644,10 +696,12 @@ __device__ __forceinline__ void reg_fence64(uint32_t (&v)[64]) {
     reg_fence32(*reinterpret_cast<uint32_t (*)[32]>(&v[32]));
 }
 
-template <bool MX>
+// MX: MXFP4 operands.  DSQR: the output is dH = dA * 2 relu(H) (tmH: H, bf16, same shape and box as D).
+template <bool MX, bool DSQR>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
 gemm_nvfp4_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                       const __grid_constant__ CUtensorMap tmD, const Params p) {
+                       const __grid_constant__ CUtensorMap tmD, const __grid_constant__ CUtensorMap tmH,
+                       const Params p) {
     constexpr int STAGES = P_STAGES;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -659,7 +713,8 @@ gemm_nvfp4_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_con
     uint64_t* acc_full = sf_ready + STAGES;              // accumulator complete (leader's commit)
     uint64_t* acc_empty = acc_full + 1;                  // leader: 8 epilogue warps drained
     uint64_t* drain = acc_empty + 1;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+    uint64_t* h_full = drain + 1;                        // DSQR: per epilogue warp, its H boxes landed
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(h_full + 4);
     volatile uint32_t* abort_flag = tmem_slot + 1;
     // identical in both CTAs (same kernel, same dynamic smem base), so layout_ok is uniform
     const bool layout_ok = (reinterpret_cast<uintptr_t>(tmem_slot + 2) - reinterpret_cast<uintptr_t>(smem_raw)) <=
@@ -681,6 +736,7 @@ gemm_nvfp4_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_con
         mbar_init(acc_full, 1);
         mbar_init(acc_empty, 8);
         mbar_init(drain, 1);
+        for (int q = 0; q < 4; ++q) mbar_init(&h_full[q], 1);
         *abort_flag = 0u;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -873,13 +929,34 @@ gemm_nvfp4_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_con
         const float alpha = MX ? 1.0f : __fmul_rn(*p.sdec_a, *p.sdec_b);   // MXFP4 has no tensor scale
         const uint32_t tmem_row = tmem + ((uint32_t)(q * 32) << 16);
         uint8_t* stg = staging + q * (2 * BOX_BYTES);
-        uint32_t acc_phase = 0;
-        for (int tile = cluster; tile < tiles; tile += nclusters) {
+        const uint64_t stream_pol = l2_evict_first_policy();
+        uint32_t acc_phase = 0, h_phase = 0;
+        bool h_pending = false;                          // DSQR: H boxes in flight into the slots
+        bool ok = true;
+        for (int tile = cluster; tile < tiles && ok; tile += nclusters) {
             int mp, nt;
             tile_coords(p, tile, m_pairs, mp, nt);
             const int m0 = mp * 256 + (int)rank * 128 + q * 32, n0 = nt * BN;
+            // DSQR: H boxes b0, b0+1 of this warp's 32 rows into the two slots (boxes past M or N
+            // read the fill value; their results are never stored), and the wait for them
+            auto load_h2 = [&](int b0) {
+                if (lane == 0) {
+                    mbar_arrive_expect_tx(&h_full[q], 2 * BOX_BYTES);
+                    for (int b = 0; b < 2; ++b)
+                        tma_load_2d_hint(smem_addr(stg + b * BOX_BYTES), &tmH, n0 + (b0 + b) * BOX_COLS, m0,
+                                         smem_addr(&h_full[q]), stream_pol);
+                }
+                h_pending = true;
+            };
+            auto wait_h2 = [&]() -> bool {
+                if (!mbar_wait_bounded(&h_full[q], h_phase, p.timeout_ns, abort_flag, p.dev_status)) return false;
+                h_phase ^= 1u;
+                h_pending = false;
+                return true;
+            };
             if (lane == 0) bulk_wait_read0();            // the previous tile's stores have left the slots
             __syncwarp();
+            if constexpr (DSQR) load_h2(0);
             if (!mbar_wait_bounded(acc_full, acc_phase, p.timeout_ns, abort_flag, p.dev_status)) break;
             tc_fence_after();
             auto store2 = [&](int b0) {                  // TMA-store boxes b0, b0+1 from the two slots
@@ -888,7 +965,8 @@ gemm_nvfp4_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_con
                 if (lane == 0 && m0 < p.M) {
                     for (int b = 0; b < 2; ++b)
                         if (n0 + (b0 + b) * BOX_COLS < p.N)
-                            tma_store_2d(&tmD, smem_addr(stg + b * BOX_BYTES), n0 + (b0 + b) * BOX_COLS, m0);
+                            tma_store_2d_hint(&tmD, smem_addr(stg + b * BOX_BYTES), n0 + (b0 + b) * BOX_COLS, m0,
+                                              stream_pol);
                     bulk_commit();
                 }
             };
@@ -898,9 +976,12 @@ gemm_nvfp4_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_con
             tmem_ld_wait();
             reg_fence64(va);
             reg_fence64(vb);
-            box_to_smem(va, stg, lane, alpha);
+            if constexpr (DSQR) {
+                if (!wait_h2()) { ok = false; break; }
+            }
+            box_out<DSQR>(va, stg, lane, alpha);
             tmem_ld_64cols(tmem_row + ACC_COL + 128, va);
-            box_to_smem(vb, stg + BOX_BYTES, lane, alpha);
+            box_out<DSQR>(vb, stg + BOX_BYTES, lane, alpha);
             tmem_ld_wait();
             reg_fence64(va);
             tmem_ld_64cols(tmem_row + ACC_COL + 192, vb);
@@ -913,11 +994,17 @@ gemm_nvfp4_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_con
             store2(0);
             if (lane == 0) bulk_wait_read0();
             __syncwarp();
-            box_to_smem(va, stg, lane, alpha);
-            box_to_smem(vb, stg + BOX_BYTES, lane, alpha);
+            if constexpr (DSQR) {
+                load_h2(2);
+                if (!wait_h2()) { ok = false; break; }
+            }
+            box_out<DSQR>(va, stg, lane, alpha);
+            box_out<DSQR>(vb, stg + BOX_BYTES, lane, alpha);
             store2(2);
             acc_phase ^= 1u;
         }
+        if (h_pending)                                   // after an abort: let the H copies land first
+            mbar_wait_bounded(&h_full[q], h_phase, p.timeout_ns, nullptr, p.dev_status);
         if (lane == 0) bulk_wait0();
         __syncwarp();
     }
@@ -986,14 +1073,14 @@ cudaError_t launch(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorM
     return cudaGetLastError();
 }
 
-template <bool MX>
-cudaError_t launch_pair(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& td, const Params& p,
-                        int pair_tiles, int sms, cudaStream_t stream) {
+template <bool MX, bool DSQR = false>
+cudaError_t launch_pair(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& td, const CUtensorMap& th,
+                        const Params& p, int pair_tiles, int sms, cudaStream_t stream) {
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
     static int max_clusters = 0;
     std::call_once(once, [sms] {
-        attr_err = cudaFuncSetAttribute(gemm_nvfp4_pair_kernel<MX>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        attr_err = cudaFuncSetAttribute(gemm_nvfp4_pair_kernel<MX, DSQR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                         P_SMEM_BYTES);
         if (attr_err != cudaSuccess) return;
         cudaLaunchConfig_t cfg = {};
@@ -1001,12 +1088,13 @@ cudaError_t launch_pair(const CUtensorMap& ta, const CUtensorMap& tb, const CUte
         cfg.blockDim = dim3(P_THREADS, 1, 1);
         cfg.dynamicSmemBytes = P_SMEM_BYTES;
         int n = 0;
-        if (cudaOccupancyMaxActiveClusters(&n, gemm_nvfp4_pair_kernel<MX>, &cfg) != cudaSuccess || n <= 0) n = sms / 2;
+        if (cudaOccupancyMaxActiveClusters(&n, gemm_nvfp4_pair_kernel<MX, DSQR>, &cfg) != cudaSuccess || n <= 0)
+            n = sms / 2;
         max_clusters = n;
     });
     if (attr_err != cudaSuccess) return attr_err;
     const int clusters = std::max(1, std::min(pair_tiles, max_clusters));
-    gemm_nvfp4_pair_kernel<MX><<<2 * clusters, P_THREADS, P_SMEM_BYTES, stream>>>(ta, tb, td, p);
+    gemm_nvfp4_pair_kernel<MX, DSQR><<<2 * clusters, P_THREADS, P_SMEM_BYTES, stream>>>(ta, tb, td, th, p);
     return cudaGetLastError();
 }
 
@@ -1068,7 +1156,7 @@ nvfp4_status gemm_impl(const nvfp4_qtensor* A, const nvfp4_qtensor* B, void* D, 
     if (pair) {
         CUtensorMap tb2;      // B boxes of 128 rows (each CTA loads its half of the N tile)
         if (!make_codes_map(&tb2, B->codes, N, K, 128)) return NVFP4_ERR_CUDA;
-        e = launch_pair<false>(ta, tb2, td, p, pair_tiles, sm_count(dev), stream);
+        e = launch_pair<false>(ta, tb2, td, td, p, pair_tiles, sm_count(dev), stream);
     } else {
         e = staged ? launch<true>(ta, tb, td, p, grid, stream) : launch<false>(ta, tb, td, p, grid, stream);
     }
@@ -1114,11 +1202,62 @@ nvfp4_status mx_gemm_impl(const nvfp4_qtensor* A, const nvfp4_qtensor* B, void* 
     p.dev_status = dev_status;
     p.timeout_ns = wait_timeout_ns();
     const int pair_tiles = (int)((M + 255) / 256) * p.n_tiles;
-    const cudaError_t e = launch_pair<true>(ta, tb, td, p, pair_tiles, sm_count(dev), stream);
+    const cudaError_t e = launch_pair<true>(ta, tb, td, td, p, pair_tiles, sm_count(dev), stream);
+    return e == cudaSuccess ? NVFP4_OK : NVFP4_ERR_CUDA;
+}
+
+// dH = bf16(dA) * 2 relu(H) with dA = s_dec(A) s_dec(B) A B^T: the NVFP4 GEMM with the squared-ReLU
+// backward in its epilogue (CTA-pair kernel; bf16 H and D, 16-byte aligned bases and pitches).
+nvfp4_status gemm_sqrelu_bwd_impl(const nvfp4_qtensor* A, const nvfp4_qtensor* B, const void* H, int64_t ldh,
+                                  void* D, int64_t ldd, uint32_t* dev_status, cudaStream_t stream) {
+    using namespace gemm;
+    if (!A || !B || !H || !D) return NVFP4_ERR_INVALID_ARG;
+    if (!A->codes || !B->codes || !A->scales_mma || !B->scales_mma || !A->s_dec || !B->s_dec)
+        return NVFP4_ERR_INVALID_ARG;
+    const int64_t M = A->rows, N = B->rows, K = A->cols;
+    if (B->cols != K) return NVFP4_ERR_SHAPE;
+    if (M < 1 || N < 1 || K < 32 || K % 32 != 0 || ldd < N || ldh < N) return NVFP4_ERR_SHAPE;
+    if (M > (1ll << 30) || N > (1ll << 30) || K > (1ll << 30)) return NVFP4_ERR_SHAPE;
+    if (!aligned16(A->codes) || !aligned16(B->codes) || !aligned16(A->scales_mma) || !aligned16(B->scales_mma) ||
+        !aligned16(D) || !aligned16(H) || (ldd * 2) % 16 != 0 || (ldh * 2) % 16 != 0)
+        return NVFP4_ERR_ALIGNMENT;
+    CUtensorMap ta, tb, td, th;
+    if (!make_codes_map(&ta, A->codes, M, K, BM) || !make_codes_map(&tb, B->codes, N, K, 128) ||
+        !make_out_map(&td, D, M, N, ldd) || !make_out_map(&th, const_cast<void*>(H), M, N, ldh))
+        return NVFP4_ERR_CUDA;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return NVFP4_ERR_CUDA;
+    Params p;
+    std::memset(&p, 0, sizeof(p));
+    p.sfa = A->scales_mma;
+    p.sfb = B->scales_mma;
+    p.sdec_a = A->s_dec;
+    p.sdec_b = B->s_dec;
+    p.D = D;
+    p.ldd = ldd;
+    p.M = (int)M;
+    p.N = (int)N;
+    p.K = (int)K;
+    p.d_bf16 = 1;
+    p.vec_store = 1;
+    p.nkt = (int)((K + BK - 1) / BK);
+    p.m_tiles = (int)((M + BM - 1) / BM);
+    p.n_tiles = (int)((N + BN - 1) / BN);
+    p.n_fastest = (M > N) ? 1 : 0;
+    p.dev_status = dev_status;
+    p.timeout_ns = wait_timeout_ns();
+    const int pair_tiles = (int)((M + 255) / 256) * p.n_tiles;
+    const cudaError_t e = launch_pair<false, true>(ta, tb, td, th, p, pair_tiles, sm_count(dev), stream);
     return e == cudaSuccess ? NVFP4_OK : NVFP4_ERR_CUDA;
 }
 
 }  // namespace nvfp4
+
+extern "C" nvfp4_status nvfp4_gemm_sqrelu_bwd(const nvfp4_qtensor* A, const nvfp4_qtensor* B, const void* H,
+                                              int64_t ldh, void* D, int64_t ldd, uint32_t* dev_status,
+                                              void* stream) {
+    return nvfp4::gemm_sqrelu_bwd_impl(A, B, H, ldh, D, ldd, dev_status, static_cast<cudaStream_t>(stream));
+}
 
 extern "C" nvfp4_status nvfp4_mx_gemm(const nvfp4_qtensor* A, const nvfp4_qtensor* B, void* D, int32_t d_dtype,
                                       int64_t ldd, uint32_t* dev_status, void* stream) {

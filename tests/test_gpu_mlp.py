@@ -20,8 +20,10 @@ def nv():
     return nv
 
 
-def mlp_step(nv, X, W1, W2, dY, sr_seed=5, rht_seed=9):
-    """Forward and backward of one MLP block, every GEMM in NVFP4 (bf16 out)."""
+def mlp_step(nv, X, W1, W2, dY, sr_seed=5, rht_seed=9, fused_dgrad=False):
+    """Forward and backward of one MLP block, every GEMM in NVFP4 (bf16 out).  With
+    ``fused_dgrad`` (as the bench runs it) dH comes straight out of the Dgrad GEMM's
+    epilogue and dA is not formed."""
     out = {}
     out["w1q"] = nv.quantize_weight(W1)
     out["w2q"] = nv.quantize_weight(W2)
@@ -33,9 +35,12 @@ def mlp_step(nv, X, W1, W2, dY, sr_seed=5, rht_seed=9):
     out["Y"] = nv.gemm(out["aq"], out["w2q"], torch.bfloat16)
     out["dyq"], out["dyt"] = nv.quantize_dual(dY, nv.SR, nv.SR, rht=True, sr_seed=sr_seed, sr_offset=0,
                                               rht_seed=rht_seed)
-    out["dA"] = nv.gemm(out["dyq"], out["w2q"].transposed(), torch.bfloat16)
+    if fused_dgrad:
+        out["dH"] = nv.gemm_sqrelu_backward(out["dyq"], out["w2q"].transposed(), out["H"])
+    else:
+        out["dA"] = nv.gemm(out["dyq"], out["w2q"].transposed(), torch.bfloat16)
+        out["dH"] = nv.sqrelu_backward(out["H"], out["dA"])
     out["dW2"] = nv.gemm(out["dyt"], out["at"], torch.bfloat16)
-    out["dH"] = nv.sqrelu_backward(out["H"], out["dA"])
     out["dhq"], out["dht"] = nv.quantize_dual(out["dH"], nv.SR, nv.SR, rht=True, sr_seed=sr_seed, sr_offset=1,
                                               rht_seed=rht_seed)
     out["dX"] = nv.gemm(out["dhq"], out["w1q"].transposed(), torch.bfloat16)
@@ -115,7 +120,10 @@ def test_mlp_block_full_size_sampled(nv, oracle_mod):
     W2 = inputs.normal((d, f), 0.02, 12, device="cuda")
     dY = inputs.normal((T, d), 1e-3, 13, device="cuda")
     nv.reset_status()
-    o = mlp_step(nv, X, W1, W2, dY)
+    o = mlp_step(nv, X, W1, W2, dY, fused_dgrad=True)
+    # dA as the separate GEMM would store it; the fused dH must equal its backward exactly
+    o["dA"] = nv.gemm(o["dyq"], o["w2q"].transposed(), torch.bfloat16)
+    assert torch.equal(o["dH"], nv.sqrelu_backward(o["H"], o["dA"]))
     assert nv.status_query() == 0
     rng = np.random.default_rng(4)
     om = oracle_mod
@@ -163,3 +171,48 @@ def test_quantize_dual_sqrelu_equals_activation_then_quantize(nv, oracle_mod, rn
     c = oracle_mod.quantize(ah, oracle_mod.COL, rnd, rht=rht, sr_seed=3, sr_offset=1, rht_seed=5)
     assert np.array_equal(fr.codes.cpu().numpy(), r["codes"]) and np.array_equal(fc.codes.cpu().numpy(), c["codes"])
     assert np.array_equal(fr.scales.cpu().numpy(), r["scales"]) and np.array_equal(fc.scales.cpu().numpy(), c["scales"])
+
+
+@pytest.fixture
+def pair_path():
+    from nvfp4_bit_quantized_gb300 import _lib as L
+    L.lib().nvfp4_gemm_force_path(2)
+    yield
+    L.lib().nvfp4_gemm_force_path(0)
+
+
+@pytest.mark.parametrize("M,N,K", [(256, 256, 256), (200, 296, 224), (512, 1024, 768), (384, 648, 1056),
+                                   (1, 8, 32)])
+def test_gemm_sqrelu_backward_equals_gemm_then_backward(nv, oracle_mod, pair_path, M, N, K):
+    """The Dgrad GEMM with the squared-ReLU backward in its epilogue is bit for bit the
+    CTA-pair GEMM's bf16 dA followed by the backward kernel, and that chain equals the
+    oracle's backward of the GEMM output; ragged M and N, signed zeros in H."""
+    g = torch.Generator().manual_seed(M + 3 * N + K)
+    dy = (torch.randn((M, K), generator=g) * 1e-3).to(torch.bfloat16).cuda()
+    w = (torch.randn((N, K), generator=g) * 0.02).to(torch.bfloat16).cuda()
+    H = (torch.randn((M, N), generator=g) * 2).to(torch.bfloat16)
+    H.view(-1)[:4] = torch.tensor([0.0, -0.0, 1e-30, -1e-30], dtype=torch.bfloat16)
+    H = H.cuda()
+    qa = nv.quantize(dy, nv.ROW, nv.SR, sr_seed=3)
+    qb = nv.quantize(w, nv.ROW, nv.RNE)
+    nv.reset_status()
+    dH = nv.gemm_sqrelu_backward(qa, qb, H)
+    dA = nv.gemm(qa, qb, torch.bfloat16)
+    ref = nv.sqrelu_backward(H, dA)
+    torch.cuda.synchronize()
+    assert nv.status_query() == 0
+    assert torch.equal(dH.view(torch.int16), ref.view(torch.int16))
+    assert np.array_equal(host_input(dH.cpu()), oracle_mod.sqrelu_backward(host_input(H.cpu()), host_input(dA.cpu())))
+
+
+def test_gemm_sqrelu_backward_strided(nv, pair_path):
+    M, N, K = 256, 512, 512
+    g = torch.Generator().manual_seed(9)
+    qa = nv.quantize(torch.randn((M, K), generator=g).to(torch.bfloat16).cuda(), nv.ROW, nv.RNE)
+    qb = nv.quantize((torch.randn((N, K), generator=g) * 0.02).to(torch.bfloat16).cuda(), nv.ROW, nv.RNE)
+    Hbig = torch.randn((M, N + 64), generator=g).to(torch.bfloat16).cuda()
+    out = torch.full((M, N + 32), 7.0, dtype=torch.bfloat16, device="cuda")
+    nv.gemm_sqrelu_backward(qa, qb, Hbig[:, :N], out=out[:, :N])
+    ref = nv.sqrelu_backward(Hbig[:, :N].contiguous(), nv.gemm(qa, qb, torch.bfloat16))
+    torch.cuda.synchronize()
+    assert torch.equal(out[:, :N], ref) and torch.all(out[:, N:] == 7.0)

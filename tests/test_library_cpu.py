@@ -158,3 +158,16 @@ def test_mx_entry_points_reject_bad_arguments(lib):
     B.cols = 256
     B.scales_mma = None
     assert g(ctypes.byref(A), ctypes.byref(B), 0x4000, lib.BF16, 256, None, None) == lib.ERR_INVALID_ARG
+
+
+def test_gemm_sqrelu_backward_rejects_bad_arguments(lib):
+    L = lib.lib()
+    A = lib.QTensorC(0x1000, None, 0x1000, 0x2000, None, None, 128, 256)
+    B = lib.QTensorC(0x1000, None, 0x1000, 0x2000, None, None, 256, 256)
+    f = L.nvfp4_gemm_sqrelu_bwd
+    assert f(ctypes.byref(A), ctypes.byref(B), None, 256, 0x4000, 256, None, None) == lib.ERR_INVALID_ARG   # no H
+    assert f(ctypes.byref(A), ctypes.byref(B), 0x8000, 200, 0x4000, 256, None, None) == lib.ERR_SHAPE       # ldh < N
+    assert f(ctypes.byref(A), ctypes.byref(B), 0x8008, 256, 0x4000, 256, None, None) == lib.ERR_ALIGNMENT
+    assert f(ctypes.byref(A), ctypes.byref(B), 0x8000, 260, 0x4000, 256, None, None) == lib.ERR_ALIGNMENT
+    A.s_dec = None
+    assert f(ctypes.byref(A), ctypes.byref(B), 0x8000, 256, 0x4000, 256, None, None) == lib.ERR_INVALID_ARG
