@@ -220,8 +220,9 @@ def run_sweep(args):
 def run_mlp(args):
     """One dense MLP block step (5120 -> 20480 -> 5120, squared-ReLU, 16384 tokens), all six
     GEMMs in NVFP4 with re-quantization between them: step time and per-GEMM TFLOP/s.  The
-    activation A = relu(H)^2 is quantized straight from H and never stored; dH = dA * 2 relu(H)
-    comes out of the dgrad2 GEMM's epilogue (dA is never stored)."""
+    activation A = relu(H)^2 is quantized straight from H and never stored, from tensor maxima
+    the fwd1 GEMM's epilogue leaves (no amax read of H); dH = dA * 2 relu(H) comes out of the
+    dgrad2 GEMM's epilogue (dA is never stored)."""
     import torch
     import nvfp4_bit_quantized_gb300 as nv
     from nvfp4_bit_quantized_gb300 import inputs
@@ -238,16 +239,20 @@ def run_mlp(args):
         w1q, w2q = nv.quantize_weight(W1), nv.quantize_weight(W2)
         xq, xt = nv.quantize_dual(X, nv.RNE, nv.RNE, rht=True, rht_seed=9, scales=False)
 
-        def gemm(a, b, k, h=None):
+        def gemm(a, b, k, h=None, maxima=False):
             if ev is not None:
                 ev[k][0].record(stream)
-            out = nv.gemm(a, b, torch.bfloat16) if h is None else nv.gemm_sqrelu_backward(a, b, h)
+            if maxima:
+                out = nv.gemm_sqrelu_maxima(a, b, rht_seed=9)
+            else:
+                out = nv.gemm(a, b, torch.bfloat16) if h is None else nv.gemm_sqrelu_backward(a, b, h)
             if ev is not None:
                 ev[k][1].record(stream)
             return out
-        H = gemm(xq, w1q, 0)
+        H, maxima = gemm(xq, w1q, 0, maxima=True)          # + relu(H)^2's tensor maxima in the epilogue
         # A = relu(H)^2 is quantized straight from H (the activation is applied as H is loaded)
-        aq, at = nv.quantize_dual(H, nv.RNE, nv.RNE, rht=True, rht_seed=9, scales=False, pre="sqrelu")
+        aq, at = nv.quantize_dual(H, nv.RNE, nv.RNE, rht=True, rht_seed=9, scales=False, pre="sqrelu",
+                                  maxima=maxima)
         gemm(aq, w2q, 1)
         dyq, dyt = nv.quantize_dual(dY, nv.SR, nv.SR, rht=True, sr_seed=5, sr_offset=2 * i, rht_seed=9, scales=False)
         dH = gemm(dyq, w2q.transposed(), 2, h=H)          # dH = dA * 2 relu(H) in the epilogue
@@ -274,7 +279,7 @@ def run_mlp(args):
     print(json.dumps({"config": "mlp_block_16384x5120x20480_sqrelu", "ms_per_step": round(ms, 4),
                       "tflops_step": round(6 * flop / (ms * 1e-3) / 1e12, 1),
                       "gemm_tflops": {k: round(v, 1) for k, v in per.items()},
-                      "launches_per_step": 2 * 2 + 4 * 3 + 6, "device_status": nv.status_query()}))
+                      "launches_per_step": 2 * 2 + 3 * 3 + 2 + 6, "device_status": nv.status_query()}))
 
 
 def run_heavy(args):

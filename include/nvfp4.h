@@ -217,6 +217,38 @@ NVFP4_API nvfp4_status nvfp4_gemm_sqrelu_bwd(const nvfp4_qtensor* A, const nvfp4
                                              int64_t ldh, void* D, int64_t ldd, uint32_t* dev_status,
                                              void* stream);
 
+/* Bytes of the partial-maxima buffer nvfp4_gemm_sqrelu_maxima writes (device memory). */
+NVFP4_API size_t nvfp4_sqrelu_maxima_bytes(void);
+
+/*
+ * nvfp4_gemm_sqrelu_maxima -- the first GEMM of a squared-ReLU MLP with the next
+ * quantization's tensor maxima in its epilogue: H = bf16(s_dec(A) s_dec(B) sum_k qA qB),
+ * stored exactly as nvfp4_gemm (CTA-pair kernel, BF16) stores it, and, for A = relu(H)^2
+ * as nvfp4_quantize_dual_sqrelu forms it, max|A| and max|RHT(A)| along rows (the RHT sign
+ * vector of rht_seed) as partial maxima in `maxima` (nvfp4_sqrelu_maxima_bytes() of device
+ * memory, 4-byte aligned; contents on entry ignored).  nvfp4_quantize_dual_sqrelu_premax
+ * then needs no amax pass over H.  H: BF16 [M, N], pitch ldh >= N, base and pitch 16-byte
+ * aligned; M % 16 == 0 and N % 16 == 0.  A, B as for nvfp4_gemm.  NVFP4_ERR_UNSUPPORTED on
+ * a GPU with more than 152 multiprocessors (one partial per epilogue warp).
+ */
+NVFP4_API nvfp4_status nvfp4_gemm_sqrelu_maxima(const nvfp4_qtensor* A, const nvfp4_qtensor* B, void* H,
+                                                int64_t ldh, uint64_t rht_seed, uint32_t* maxima,
+                                                uint32_t* dev_status, void* stream);
+
+/*
+ * nvfp4_quantize_dual_sqrelu_premax -- nvfp4_quantize_dual_sqrelu of H using the maxima that
+ * nvfp4_gemm_sqrelu_maxima left for this same H (with rht_seed == params_col->rht_seed when
+ * params_col->rht is set): only the two encode passes run, and the results are identical to
+ * nvfp4_quantize_dual_sqrelu's.  BF16 H only (else NVFP4_ERR_UNSUPPORTED); no workspace;
+ * other arguments as for nvfp4_quantize_dual_sqrelu.
+ */
+NVFP4_API nvfp4_status nvfp4_quantize_dual_sqrelu_premax(const void* h, int32_t h_dtype, int64_t R, int64_t C,
+                                                         int64_t ldh, const nvfp4_qparams* params_row,
+                                                         const nvfp4_qtensor* out_row,
+                                                         const nvfp4_qparams* params_col,
+                                                         const nvfp4_qtensor* out_col, const uint32_t* maxima,
+                                                         uint32_t* dev_status, void* stream);
+
 /*
  * MXFP4 -- the earlier 4-bit microscaling format the page compares NVFP4 with
  * [page ¶3: at 8B parameters MXFP4 trails NVFP4 in loss and needs ~36% more

@@ -148,12 +148,14 @@ def quantize(x: torch.Tensor, block: int = L.ROW, round: int = L.RNE, rht: bool 
 def quantize_dual(x: torch.Tensor, row_round: int = L.RNE, col_round: int = L.RNE, rht: bool = True,
                   sr_seed: int = 0, sr_offset: int = 0, rht_seed: int = 0, scales: bool = True,
                   scales_mma: bool = True, col_sr_seed: Optional[int] = None, col_sr_offset: Optional[int] = None,
-                  pre: Optional[str] = None):
+                  pre: Optional[str] = None, maxima: Optional[torch.Tensor] = None):
     """Both training quantizations of x [R, C] from one amax read: the 1x16 row
     operand [R, C] and the 1x16 column operand [C, R] (RHT along R when ``rht``).
     Identical to two ``quantize`` calls with the same parameters; the column
     operand's SR seed / offset default to the row's.  ``pre="sqrelu"`` quantizes
-    relu(x)^2 (bf16 x) without storing it, identical to ``sqrelu_forward`` first."""
+    relu(x)^2 (bf16 x) without storing it, identical to ``sqrelu_forward`` first.
+    ``maxima`` (with ``pre="sqrelu"``): the partial maxima ``gemm_sqrelu_maxima`` left
+    for this x with the same ``rht_seed``; the amax read is then skipped."""
     _check_2d(x, "x")
     R, C = x.shape
     qr = _alloc_q(R, C, L.ROW, x.device, scales, scales_mma, False)
@@ -167,6 +169,14 @@ def quantize_dual(x: torch.Tensor, row_round: int = L.RNE, col_round: int = L.RN
     ld = x.stride(0) if R > 1 else max(C, 1)
     if pre not in (None, "sqrelu"):
         raise ValueError(f"unknown pre transform {pre!r}")
+    if maxima is not None:
+        if pre != "sqrelu":
+            raise ValueError("maxima are the squared-ReLU GEMM epilogue's: pass pre='sqrelu'")
+        st = lib.nvfp4_quantize_dual_sqrelu_premax(_ptr(x), _DT[x.dtype], R, C, ld, ctypes.byref(pr), ctypes.byref(a),
+                                                   ctypes.byref(pc), ctypes.byref(b), _ptr(maxima),
+                                                   dev_status(x.device).data_ptr(), _stream())
+        L.check(st, "nvfp4_quantize_dual_sqrelu_premax")
+        return qr, qc
     fn = lib.nvfp4_quantize_dual_sqrelu if pre == "sqrelu" else lib.nvfp4_quantize_dual
     st = fn(_ptr(x), _DT[x.dtype], R, C, ld, ctypes.byref(pr), ctypes.byref(a), ctypes.byref(pc), ctypes.byref(b),
             ws.data_ptr(), ws.numel(), dev_status(x.device).data_ptr(), _stream())
@@ -241,6 +251,23 @@ def mx_gemm(A: MXTensor, B: MXTensor, out: Optional[torch.Tensor] = None) -> tor
                                dev_status(out.device).data_ptr(), _stream())
     L.check(st, "nvfp4_mx_gemm")
     return out
+
+
+def gemm_sqrelu_maxima(A: QTensor, B: QTensor, rht_seed: int = 0, out: Optional[torch.Tensor] = None):
+    """H = dequant(A) . dequant(B)^T in bf16 (as ``gemm`` stores it), plus the partial tensor
+    maxima of relu(H)^2 that ``quantize_dual(H, ..., pre="sqrelu", maxima=m)`` needs, computed
+    in the GEMM's epilogue (RHT signs from ``rht_seed``).  Returns (H, m)."""
+    M, N = A.rows, B.rows
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.bfloat16, device=A.codes.device)
+    _check_2d(out, "out")
+    lib = L.lib()
+    m = torch.empty(int(lib.nvfp4_sqrelu_maxima_bytes()) // 4, dtype=torch.int32, device=out.device)
+    a, b = A.c_struct(), B.c_struct()
+    st = lib.nvfp4_gemm_sqrelu_maxima(ctypes.byref(a), ctypes.byref(b), _ptr(out), out.stride(0) if M > 1 else N,
+                                      rht_seed & (2**64 - 1), _ptr(m), dev_status(out.device).data_ptr(), _stream())
+    L.check(st, "nvfp4_gemm_sqrelu_maxima")
+    return out, m
 
 
 def gemm_sqrelu_backward(A: QTensor, B: QTensor, H: torch.Tensor, out: Optional[torch.Tensor] = None) -> torch.Tensor:

@@ -1,7 +1,7 @@
 // device_common.cuh -- device-side building blocks of the NVFP4 quantizers and GEMM
 // (sm_103a): bf16 unpacking, the E4M3 block-scale cast, E2M1 element encoding
-// (round-to-nearest-even and stochastic), Philox4x32-10, the 16-point Hadamard
-// butterfly, and bounded mbarrier waits.
+// (round-to-nearest-even and stochastic), the squared ReLU on packed bf16, Philox4x32-10,
+// the 16-point Hadamard butterflies, and bounded mbarrier waits.
 //
 // Method: news page "NVIDIA NVFP4 paper: 4-bit pretrain hits FP8 parity (12B,
 // 10T tokens)" (zubnet.ai), ¶2.  The readings this file implements where the
@@ -12,6 +12,7 @@
 #include <cfloat>
 #include <cuda_runtime.h>
 #include <cuda_fp16.h>
+#include <cuda_bf16.h>
 
 #include "../../include/nvfp4.h"
 
@@ -187,6 +188,38 @@ __device__ __forceinline__ uint2 e2m1x16_sr(const float (&y)[16], const uint32_t
     return make_uint2(e2m1x4_sr(y[0], y[1], y[2], y[3], w[0]) | (e2m1x4_sr(y[4], y[5], y[6], y[7], w[1]) << 16),
                       e2m1x4_sr(y[8], y[9], y[10], y[11], w[2]) | (e2m1x4_sr(y[12], y[13], y[14], y[15], w[3]) << 16));
 }
+
+// ----------------------------------------------------------------------------
+// Packed bf16 / fp32x2 helpers shared by the quantizers and the GEMM epilogue.
+// ----------------------------------------------------------------------------
+// Squared ReLU of two packed bf16 values, rounded back to bf16: relu(h)^2 in fp32, one
+// rounding to bf16 (max(h, 0) squares to +0 for h <= 0, -0 and NaN alike).  The MLP's
+// activation, applied to H as it is loaded, so A = relu(H)^2 is quantized without being
+// stored (SQR kernels).
+__device__ __forceinline__ uint32_t sqrelu_bf16x2(uint32_t w) {
+    const float2 r = make_float2(fmaxf(__uint_as_float(w << 16), 0.0f), fmaxf(__uint_as_float(w & 0xFFFF0000u), 0.0f));
+    const __nv_bfloat162 b = __float22bfloat162_rn(__fmul2_rn(r, r));
+    return *reinterpret_cast<const uint32_t*>(&b);
+}
+
+// The 16-point Hadamard butterflies of two columns at once, unnormalised (the 1/4 of
+// the transform is applied by the caller): h = 1, 2, 4, 8, lower index first,
+// (t_i, t_{i+h}) <- (t_i + t_{i+h}, t_i - t_{i+h}), each one fp32 RN operation.
+__device__ __forceinline__ void hadamard16_x2(float2 (&t)[16]) {
+    const float2 neg1 = make_float2(-1.0f, -1.0f);
+#pragma unroll
+    for (int h = 1; h < 16; h <<= 1) {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            if ((i & h) == 0) {
+                const float2 a = t[i], b = t[i + h];
+                t[i] = __fadd2_rn(a, b);
+                t[i + h] = __ffma2_rn(b, neg1, a);           // a - b, one rounding
+            }
+        }
+    }
+}
+
 
 // ----------------------------------------------------------------------------
 // Philox4x32-10 (Salmon, Moraes, Dror, Shaw, SC'11): ten rounds of two 32x32->64

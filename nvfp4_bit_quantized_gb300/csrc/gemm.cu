@@ -99,7 +99,16 @@ struct Params {
     int n_fastest;               // tile order: 1 = consecutive tiles walk N (A tile reused), 0 = walk M
     uint32_t* dev_status;
     uint64_t timeout_ns;
+    uint32_t* maxima;            // EPI_SQAMAX: 2 x kMaximaParts partial maxima (|A|, then |RHT(A)| / 4)
+    uint64_t rht_seed;           // EPI_SQAMAX: the RHT sign vector of the column quantization
 };
+
+// Epilogue variants of the CTA-pair kernel.
+//   EPI_PLAIN   D = alpha * acc;
+//   EPI_DSQR    D = dH = bf16(alpha * acc) * 2 relu(H)  (the squared-ReLU backward);
+//   EPI_SQAMAX  D = H = alpha * acc, plus the tensor maxima that quantizing A = relu(H)^2 in
+//               both orientations needs (|A| and |RHT(A)| along rows), as per-warp partials.
+constexpr int EPI_PLAIN = 0, EPI_DSQR = 1, EPI_SQAMAX = 2;
 
 // Tile order.  Consecutive persistent CTAs (clusters) take consecutive tiles, so the
 // operand indexed by the slow coordinate is shared by the CTAs running together
@@ -681,10 +690,59 @@ __device__ __forceinline__ void box_to_smem_dsqr(const uint32_t (&v)[64], uint8_
     }
 }
 
-template <bool DSQR>
+// 64 accumulator columns -> x alpha -> 32 packed bf16 words (the same rounding as box_to_smem),
+// and those words into a box: word 4c + i of row `lane` in 16-byte chunk c (swizzled).
+__device__ __forceinline__ void pack_bf16_64(const uint32_t (&v)[64], uint32_t (&pk)[32], float alpha) {
+    const float2 al = make_float2(alpha, alpha);
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+        const __nv_bfloat162 h = __float22bfloat162_rn(
+            __fmul2_rn(make_float2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1])), al));
+        pk[i] = *reinterpret_cast<const uint32_t*>(&h);
+    }
+}
+__device__ __forceinline__ void packed_to_box(const uint32_t (&pk)[32], uint8_t* box, int lane) {
+    uint8_t* row = box + lane * 128;
+#pragma unroll
+    for (int c = 0; c < 8; ++c)
+        *reinterpret_cast<uint4*>(row + ((c ^ (lane & 7)) << 4)) =
+            make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+}
+
+template <int EPI>
 __device__ __forceinline__ void box_out(const uint32_t (&v)[64], uint8_t* box, int lane, float alpha) {
-    if constexpr (DSQR) box_to_smem_dsqr(v, box, lane, alpha);
+    if constexpr (EPI == EPI_DSQR) box_to_smem_dsqr(v, box, lane, alpha);
     else box_to_smem(v, box, lane, alpha);
+}
+
+// EPI_SQAMAX: folds one stored 32 x 64 box of H (rows m0.., columns n0..) into the warp's
+// running maxima of A = relu(H)^2, computed exactly as the quantizer's load transform and
+// its dual amax pass compute them: mabs = max |a| and mrht = max |t| with t the unnormalised
+// 16-point butterflies of (s_i * a_i) down each 16-row group (bit patterns of non-negative
+// floats; a NaN lands above every finite value).  Lane l takes column pair 2l, 2l+1; rows
+// past M and columns past N (both multiples of 16) are left out.
+__device__ __forceinline__ void box_sqrelu_maxima(const uint8_t* box, int lane, int m0, int M, int n0, int N,
+                                                  uint32_t sign_mask, uint32_t& mabs, uint32_t& mrht) {
+    if (n0 + 2 * lane >= N) return;
+#pragma unroll 1
+    for (int g = 0; g < 2; ++g) {                        // one group at a time: bounded registers
+        if (m0 + 16 * g >= M) break;
+        float2 t[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            const int r = 16 * g + i;
+            uint32_t w = *reinterpret_cast<const uint32_t*>(box + r * 128 + ((((lane >> 2) ^ (r & 7)) << 4) |
+                                                                              ((lane & 3) << 2)));
+            w = sqrelu_bf16x2(w);
+            mabs = max(mabs, max((w << 16) & 0x7FFFFFFFu, w & 0x7FFF0000u));
+            if ((sign_mask >> i) & 1u) w ^= 0x80008000u;
+            t[i] = make_float2(bf16_lo(w), bf16_hi(w));
+        }
+        hadamard16_x2(t);
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+            mrht = max(mrht, max(__float_as_uint(t[i].x) & 0x7FFFFFFFu, __float_as_uint(t[i].y) & 0x7FFFFFFFu));
+    }
 }
 
 __device__ __forceinline__ void tmem_ld_64cols(uint32_t taddr, uint32_t (&v)[64]) {
@@ -696,13 +754,16 @@ __device__ __forceinline__ void reg_fence64(uint32_t (&v)[64]) {
     reg_fence32(*reinterpret_cast<uint32_t (*)[32]>(&v[32]));
 }
 
-// MX: MXFP4 operands.  DSQR: the output is dH = dA * 2 relu(H) (tmH: H, bf16, same shape and box as D).
-template <bool MX, bool DSQR>
+// MX: MXFP4 operands.  EPI: the epilogue variant (EPI_DSQR reads H through tmH: bf16, same
+// shape and box as D).
+template <bool MX, int EPI>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
 gemm_nvfp4_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                        const __grid_constant__ CUtensorMap tmD, const __grid_constant__ CUtensorMap tmH,
                        const Params p) {
     constexpr int STAGES = P_STAGES;
+    constexpr bool DSQR = EPI == EPI_DSQR;
+    constexpr bool SQAMAX = EPI == EPI_SQAMAX;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* staging = smem + P_RING_BYTES;
@@ -932,6 +993,8 @@ gemm_nvfp4_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_con
         const uint64_t stream_pol = l2_evict_first_policy();
         uint32_t acc_phase = 0, h_phase = 0;
         bool h_pending = false;                          // DSQR: H boxes in flight into the slots
+        uint32_t mabs = 0u, mrht = 0u;                   // SQAMAX: running maxima (float bits)
+        const uint32_t sign_mask = SQAMAX ? rht_sign_mask(p.rht_seed) : 0u;
         bool ok = true;
         for (int tile = cluster; tile < tiles && ok; tile += nclusters) {
             int mp, nt;
@@ -979,29 +1042,64 @@ gemm_nvfp4_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_con
             if constexpr (DSQR) {
                 if (!wait_h2()) { ok = false; break; }
             }
-            box_out<DSQR>(va, stg, lane, alpha);
+            box_out<EPI>(va, stg, lane, alpha);
             tmem_ld_64cols(tmem_row + ACC_COL + 128, va);
-            box_out<DSQR>(vb, stg + BOX_BYTES, lane, alpha);
+            box_out<EPI>(vb, stg + BOX_BYTES, lane, alpha);
             tmem_ld_wait();
             reg_fence64(va);
             tmem_ld_64cols(tmem_row + ACC_COL + 192, vb);
             tmem_ld_wait();
             reg_fence64(vb);
+            // SQAMAX: the last two boxes as packed bf16 (half the registers), so the maxima of the
+            // first two fit beside them
+            uint32_t pa[32], pb[32];
+            if constexpr (SQAMAX) {
+                pack_bf16_64(va, pa, alpha);
+                pack_bf16_64(vb, pb, alpha);
+            }
             // the whole accumulator is in registers or shared memory: hand it back
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive_cluster(acc_empty_leader);
             store2(0);
+            if constexpr (SQAMAX) {                      // read alongside the stores: both only read the slots
+                box_sqrelu_maxima(stg, lane, m0, p.M, n0, p.N, sign_mask, mabs, mrht);
+                box_sqrelu_maxima(stg + BOX_BYTES, lane, m0, p.M, n0 + BOX_COLS, p.N, sign_mask, mabs, mrht);
+            }
             if (lane == 0) bulk_wait_read0();
             __syncwarp();
             if constexpr (DSQR) {
                 load_h2(2);
                 if (!wait_h2()) { ok = false; break; }
             }
-            box_out<DSQR>(va, stg, lane, alpha);
-            box_out<DSQR>(vb, stg + BOX_BYTES, lane, alpha);
+            if constexpr (SQAMAX) {
+                packed_to_box(pa, stg, lane);
+                packed_to_box(pb, stg + BOX_BYTES, lane);
+            } else {
+                box_out<EPI>(va, stg, lane, alpha);
+                box_out<EPI>(vb, stg + BOX_BYTES, lane, alpha);
+            }
             store2(2);
+            if constexpr (SQAMAX) {
+                box_sqrelu_maxima(stg, lane, m0, p.M, n0 + 2 * BOX_COLS, p.N, sign_mask, mabs, mrht);
+                box_sqrelu_maxima(stg + BOX_BYTES, lane, m0, p.M, n0 + 3 * BOX_COLS, p.N, sign_mask, mabs, mrht);
+            }
             acc_phase ^= 1u;
+        }
+        if constexpr (SQAMAX) {
+            // this warp's partials; the first CTA zeroes the slots no CTA of this grid owns
+            mabs = __reduce_max_sync(0xFFFFFFFFu, mabs);
+            mrht = __reduce_max_sync(0xFFFFFFFFu, mrht);
+            const int gid = (int)blockIdx.x * 4 + q;
+            if (lane == 0) {
+                p.maxima[gid] = mabs;
+                p.maxima[kMaximaParts + gid] = __float_as_uint(__fmul_rn(__uint_as_float(mrht), 0.25f)) & 0x7FFFFFFFu;
+            }
+            if (blockIdx.x == 0)
+                for (int i = (int)gridDim.x * 4 + q * 32 + lane; i < kMaximaParts; i += 128) {
+                    p.maxima[i] = 0u;
+                    p.maxima[kMaximaParts + i] = 0u;
+                }
         }
         if (h_pending)                                   // after an abort: let the H copies land first
             mbar_wait_bounded(&h_full[q], h_phase, p.timeout_ns, nullptr, p.dev_status);
@@ -1073,14 +1171,14 @@ cudaError_t launch(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorM
     return cudaGetLastError();
 }
 
-template <bool MX, bool DSQR = false>
+template <bool MX, int EPI = EPI_PLAIN>
 cudaError_t launch_pair(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& td, const CUtensorMap& th,
                         const Params& p, int pair_tiles, int sms, cudaStream_t stream) {
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
     static int max_clusters = 0;
     std::call_once(once, [sms] {
-        attr_err = cudaFuncSetAttribute(gemm_nvfp4_pair_kernel<MX, DSQR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        attr_err = cudaFuncSetAttribute(gemm_nvfp4_pair_kernel<MX, EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                         P_SMEM_BYTES);
         if (attr_err != cudaSuccess) return;
         cudaLaunchConfig_t cfg = {};
@@ -1088,13 +1186,13 @@ cudaError_t launch_pair(const CUtensorMap& ta, const CUtensorMap& tb, const CUte
         cfg.blockDim = dim3(P_THREADS, 1, 1);
         cfg.dynamicSmemBytes = P_SMEM_BYTES;
         int n = 0;
-        if (cudaOccupancyMaxActiveClusters(&n, gemm_nvfp4_pair_kernel<MX, DSQR>, &cfg) != cudaSuccess || n <= 0)
+        if (cudaOccupancyMaxActiveClusters(&n, gemm_nvfp4_pair_kernel<MX, EPI>, &cfg) != cudaSuccess || n <= 0)
             n = sms / 2;
         max_clusters = n;
     });
     if (attr_err != cudaSuccess) return attr_err;
     const int clusters = std::max(1, std::min(pair_tiles, max_clusters));
-    gemm_nvfp4_pair_kernel<MX, DSQR><<<2 * clusters, P_THREADS, P_SMEM_BYTES, stream>>>(ta, tb, td, th, p);
+    gemm_nvfp4_pair_kernel<MX, EPI><<<2 * clusters, P_THREADS, P_SMEM_BYTES, stream>>>(ta, tb, td, th, p);
     return cudaGetLastError();
 }
 
@@ -1247,11 +1345,68 @@ nvfp4_status gemm_sqrelu_bwd_impl(const nvfp4_qtensor* A, const nvfp4_qtensor* B
     p.dev_status = dev_status;
     p.timeout_ns = wait_timeout_ns();
     const int pair_tiles = (int)((M + 255) / 256) * p.n_tiles;
-    const cudaError_t e = launch_pair<false, true>(ta, tb, td, th, p, pair_tiles, sm_count(dev), stream);
+    const cudaError_t e = launch_pair<false, EPI_DSQR>(ta, tb, td, th, p, pair_tiles, sm_count(dev), stream);
+    return e == cudaSuccess ? NVFP4_OK : NVFP4_ERR_CUDA;
+}
+
+// H = s_dec(A) s_dec(B) A B^T in bf16, plus the partial maxima that quantizing A = relu(H)^2
+// in both orientations needs (CTA-pair kernel, EPI_SQAMAX).
+nvfp4_status gemm_sqrelu_maxima_impl(const nvfp4_qtensor* A, const nvfp4_qtensor* B, void* D, int64_t ldd,
+                                     uint64_t rht_seed, uint32_t* maxima, uint32_t* dev_status, cudaStream_t stream) {
+    using namespace gemm;
+    if (!A || !B || !D || !maxima) return NVFP4_ERR_INVALID_ARG;
+    if (!A->codes || !B->codes || !A->scales_mma || !B->scales_mma || !A->s_dec || !B->s_dec)
+        return NVFP4_ERR_INVALID_ARG;
+    const int64_t M = A->rows, N = B->rows, K = A->cols;
+    if (B->cols != K) return NVFP4_ERR_SHAPE;
+    if (M < 1 || N < 1 || K < 32 || K % 32 != 0 || ldd < N || M % 16 != 0 || N % 16 != 0) return NVFP4_ERR_SHAPE;
+    if (M > (1ll << 30) || N > (1ll << 30) || K > (1ll << 30)) return NVFP4_ERR_SHAPE;
+    if (!aligned16(A->codes) || !aligned16(B->codes) || !aligned16(A->scales_mma) || !aligned16(B->scales_mma) ||
+        !aligned16(D) || (ldd * 2) % 16 != 0 || (reinterpret_cast<uintptr_t>(maxima) & 3u) != 0)
+        return NVFP4_ERR_ALIGNMENT;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return NVFP4_ERR_CUDA;
+    if (4 * sm_count(dev) > kMaximaParts) return NVFP4_ERR_UNSUPPORTED;   // one partial per epilogue warp
+    CUtensorMap ta, tb, td;
+    if (!make_codes_map(&ta, A->codes, M, K, BM) || !make_codes_map(&tb, B->codes, N, K, 128) ||
+        !make_out_map(&td, D, M, N, ldd))
+        return NVFP4_ERR_CUDA;
+    Params p;
+    std::memset(&p, 0, sizeof(p));
+    p.sfa = A->scales_mma;
+    p.sfb = B->scales_mma;
+    p.sdec_a = A->s_dec;
+    p.sdec_b = B->s_dec;
+    p.D = D;
+    p.ldd = ldd;
+    p.M = (int)M;
+    p.N = (int)N;
+    p.K = (int)K;
+    p.d_bf16 = 1;
+    p.vec_store = 1;
+    p.nkt = (int)((K + BK - 1) / BK);
+    p.m_tiles = (int)((M + BM - 1) / BM);
+    p.n_tiles = (int)((N + BN - 1) / BN);
+    p.n_fastest = (M > N) ? 1 : 0;
+    p.dev_status = dev_status;
+    p.timeout_ns = wait_timeout_ns();
+    p.maxima = maxima;
+    p.rht_seed = rht_seed;
+    const int pair_tiles = (int)((M + 255) / 256) * p.n_tiles;
+    const cudaError_t e = launch_pair<false, EPI_SQAMAX>(ta, tb, td, td, p, pair_tiles, sm_count(dev), stream);
     return e == cudaSuccess ? NVFP4_OK : NVFP4_ERR_CUDA;
 }
 
 }  // namespace nvfp4
+
+extern "C" size_t nvfp4_sqrelu_maxima_bytes(void) { return 2u * nvfp4::kMaximaParts * sizeof(uint32_t); }
+
+extern "C" nvfp4_status nvfp4_gemm_sqrelu_maxima(const nvfp4_qtensor* A, const nvfp4_qtensor* B, void* H, int64_t ldh,
+                                                 uint64_t rht_seed, uint32_t* maxima, uint32_t* dev_status,
+                                                 void* stream) {
+    return nvfp4::gemm_sqrelu_maxima_impl(A, B, H, ldh, rht_seed, maxima, dev_status,
+                                          static_cast<cudaStream_t>(stream));
+}
 
 extern "C" nvfp4_status nvfp4_gemm_sqrelu_bwd(const nvfp4_qtensor* A, const nvfp4_qtensor* B, const void* H,
                                               int64_t ldh, void* D, int64_t ldd, uint32_t* dev_status,

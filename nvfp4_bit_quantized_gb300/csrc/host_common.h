@@ -9,6 +9,10 @@
 
 namespace nvfp4 {
 
+// Partial maxima a producing GEMM epilogue leaves for the quantizer (nvfp4_gemm_sqrelu_maxima):
+// one per epilogue warp of up to 152 CTAs, for |A| then for |RHT(A)| / 4.
+constexpr int kMaximaParts = 608;
+
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 // Multiprocessor count of `dev`, cached (152 on GB300).

@@ -70,15 +70,6 @@ __device__ __forceinline__ uint32_t abs_bits_max(uint4 v, const float*) {
     return max(max(v.x & 0x7FFFFFFFu, v.y & 0x7FFFFFFFu), max(v.z & 0x7FFFFFFFu, v.w & 0x7FFFFFFFu));
 }
 
-// Squared ReLU of two packed bf16 values, rounded back to bf16: relu(h)^2 in fp32, one
-// rounding to bf16 (max(h, 0) squares to +0 for h <= 0, -0 and NaN alike).  The MLP's
-// activation, applied to H as it is loaded, so A = relu(H)^2 is quantized without being
-// stored (SQR kernels).
-__device__ __forceinline__ uint32_t sqrelu_bf16x2(uint32_t w) {
-    const float2 r = make_float2(fmaxf(__uint_as_float(w << 16), 0.0f), fmaxf(__uint_as_float(w & 0xFFFF0000u), 0.0f));
-    const __nv_bfloat162 b = __float22bfloat162_rn(__fmul2_rn(r, r));
-    return *reinterpret_cast<const uint32_t*>(&b);
-}
 __device__ __forceinline__ uint4 sqrelu_bf16x8(uint4 v) {
     return make_uint4(sqrelu_bf16x2(v.x), sqrelu_bf16x2(v.y), sqrelu_bf16x2(v.z), sqrelu_bf16x2(v.w));
 }
@@ -340,24 +331,6 @@ __device__ __forceinline__ void col_pair_abs_max(const float2 (&t)[16], float& m
         for (int i = 0; i < s; ++i) { a[i] = max_abs_nan(a[i], a[i + s]); b[i] = max_abs_nan(b[i], b[i + s]); }
     m0 = a[0];
     m1 = b[0];
-}
-
-// The 16-point Hadamard butterflies of two columns at once, unnormalised (the 1/4 of
-// the transform is applied by the caller): h = 1, 2, 4, 8, lower index first,
-// (t_i, t_{i+h}) <- (t_i + t_{i+h}, t_i - t_{i+h}), each one fp32 RN operation.
-__device__ __forceinline__ void hadamard16_x2(float2 (&t)[16]) {
-    const float2 neg1 = make_float2(-1.0f, -1.0f);
-#pragma unroll
-    for (int h = 1; h < 16; h <<= 1) {
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-            if ((i & h) == 0) {
-                const float2 a = t[i], b = t[i + h];
-                t[i] = __fadd2_rn(a, b);
-                t[i + h] = __ffma2_rn(b, neg1, a);           // a - b, one rounding
-            }
-        }
-    }
 }
 
 // For bf16 inputs every RHT intermediate is a multiple of 2^-133 (the bf16 quantum), so
@@ -1236,6 +1209,34 @@ extern "C" nvfp4_status nvfp4_quantize_dual_sqrelu(const void* h, int32_t h_dtyp
                                                    void* stream) {
     return nvfp4::quantize_dual_impl(h, h_dtype, R, C, ldh, params_row, out_row, params_col, out_col, workspace,
                                      workspace_bytes, dev_status, static_cast<cudaStream_t>(stream), true);
+}
+
+// nvfp4_quantize_dual_sqrelu with the tensor maxima already known (left by the GEMM that
+// produced H): only the two encode passes run.
+extern "C" nvfp4_status nvfp4_quantize_dual_sqrelu_premax(const void* h, int32_t h_dtype, int64_t R, int64_t C,
+                                                          int64_t ldh, const nvfp4_qparams* params_row,
+                                                          const nvfp4_qtensor* out_row, const nvfp4_qparams* params_col,
+                                                          const nvfp4_qtensor* out_col, const uint32_t* maxima,
+                                                          uint32_t* dev_status, void* stream_) {
+    using namespace nvfp4;
+    cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+    if (!params_row || !params_col || !maxima) return NVFP4_ERR_INVALID_ARG;
+    if (h_dtype != NVFP4_BF16) return NVFP4_ERR_UNSUPPORTED;
+    if (params_row->block != NVFP4_BLOCK_1X16_ROW || params_col->block != NVFP4_BLOCK_1X16_COL)
+        return NVFP4_ERR_INVALID_ARG;
+    nvfp4_status st = check_quantize_args(h, h_dtype, R, C, ldh, params_row, out_row);
+    if (st != NVFP4_OK) return st;
+    st = check_quantize_args(h, h_dtype, R, C, ldh, params_col, out_col);
+    if (st != NVFP4_OK) return st;
+    if ((reinterpret_cast<uintptr_t>(maxima) & 3u) != 0) return NVFP4_ERR_ALIGNMENT;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return NVFP4_ERR_CUDA;
+    const int sms = sm_count(dev);
+    if (sms <= 0) return NVFP4_ERR_CUDA;
+    const uint32_t* part_col = params_col->rht ? maxima + kMaximaParts : maxima;
+    st = encode_pass(h, h_dtype, R, C, ldh, params_row, out_row, maxima, kMaximaParts, sms, dev_status, stream, true);
+    if (st != NVFP4_OK) return st;
+    return encode_pass(h, h_dtype, R, C, ldh, params_col, out_col, part_col, kMaximaParts, sms, dev_status, stream, true);
 }
 
 extern "C" size_t nvfp4_quantize_dual_workspace_bytes(int64_t, int64_t) {

@@ -20,18 +20,23 @@ def nv():
     return nv
 
 
-def mlp_step(nv, X, W1, W2, dY, sr_seed=5, rht_seed=9, fused_dgrad=False):
+def mlp_step(nv, X, W1, W2, dY, sr_seed=5, rht_seed=9, fused_dgrad=False, fused_fwd=False):
     """Forward and backward of one MLP block, every GEMM in NVFP4 (bf16 out).  With
     ``fused_dgrad`` (as the bench runs it) dH comes straight out of the Dgrad GEMM's
-    epilogue and dA is not formed."""
+    epilogue and dA is not formed; with ``fused_fwd`` (as the bench runs it) the first
+    GEMM's epilogue leaves the maxima of relu(H)^2 and its quantization skips the amax read."""
     out = {}
     out["w1q"] = nv.quantize_weight(W1)
     out["w2q"] = nv.quantize_weight(W2)
     out["xq"], out["xt"] = nv.quantize_dual(X, nv.RNE, nv.RNE, rht=True, rht_seed=rht_seed)
-    out["H"] = nv.gemm(out["xq"], out["w1q"], torch.bfloat16)
+    maxima = None
+    if fused_fwd:
+        out["H"], maxima = nv.gemm_sqrelu_maxima(out["xq"], out["w1q"], rht_seed=rht_seed)
+    else:
+        out["H"] = nv.gemm(out["xq"], out["w1q"], torch.bfloat16)
     out["A"] = nv.sqrelu_forward(out["H"])                  # kept for the checks; the step itself
     out["aq"], out["at"] = nv.quantize_dual(out["H"], nv.RNE, nv.RNE, rht=True, rht_seed=rht_seed,
-                                            pre="sqrelu")    # quantizes relu(H)^2 straight from H
+                                            pre="sqrelu", maxima=maxima)   # relu(H)^2 straight from H
     out["Y"] = nv.gemm(out["aq"], out["w2q"], torch.bfloat16)
     out["dyq"], out["dyt"] = nv.quantize_dual(dY, nv.SR, nv.SR, rht=True, sr_seed=sr_seed, sr_offset=0,
                                               rht_seed=rht_seed)
@@ -120,10 +125,16 @@ def test_mlp_block_full_size_sampled(nv, oracle_mod):
     W2 = inputs.normal((d, f), 0.02, 12, device="cuda")
     dY = inputs.normal((T, d), 1e-3, 13, device="cuda")
     nv.reset_status()
-    o = mlp_step(nv, X, W1, W2, dY, fused_dgrad=True)
+    o = mlp_step(nv, X, W1, W2, dY, fused_dgrad=True, fused_fwd=True)
     # dA as the separate GEMM would store it; the fused dH must equal its backward exactly
     o["dA"] = nv.gemm(o["dyq"], o["w2q"].transposed(), torch.bfloat16)
     assert torch.equal(o["dH"], nv.sqrelu_backward(o["H"], o["dA"]))
+    # H and the quantization of relu(H)^2 from the epilogue's maxima equal the unfused path
+    assert torch.equal(o["H"], nv.gemm(o["xq"], o["w1q"], torch.bfloat16))
+    aq, at = nv.quantize_dual(o["H"], nv.RNE, nv.RNE, rht=True, rht_seed=9, pre="sqrelu")
+    for fq, uq in ((o["aq"], aq), (o["at"], at)):
+        assert torch.equal(fq.codes, uq.codes) and torch.equal(fq.scales, uq.scales)
+        assert torch.equal(fq.s_dec[:1], uq.s_dec[:1])
     assert nv.status_query() == 0
     rng = np.random.default_rng(4)
     om = oracle_mod
@@ -216,3 +227,28 @@ def test_gemm_sqrelu_backward_strided(nv, pair_path):
     ref = nv.sqrelu_backward(Hbig[:, :N].contiguous(), nv.gemm(qa, qb, torch.bfloat16))
     torch.cuda.synchronize()
     assert torch.equal(out[:, :N], ref) and torch.all(out[:, N:] == 7.0)
+
+
+@pytest.mark.parametrize("rnd,rht", [(0, True), (1, True), (0, False)])
+@pytest.mark.parametrize("M,N,K", [(256, 256, 256), (208, 336, 224), (512, 1024, 768), (16, 16, 32),
+                                   (1040, 656, 544)])
+def test_gemm_sqrelu_maxima_then_quantize_equals_unfused(nv, pair_path, M, N, K, rnd, rht):
+    """The first MLP GEMM with relu(H)^2's tensor maxima in its epilogue: H is bit for bit the
+    CTA-pair GEMM's, and quantizing relu(H)^2 from those maxima (no amax read) gives the same
+    codes, scales and tensor scales as the dual quantization with its own amax pass."""
+    g = torch.Generator().manual_seed(M + 5 * N + K + rnd)
+    x = torch.randn((M, K), generator=g).to(torch.bfloat16).cuda()
+    w = (torch.randn((N, K), generator=g) * 0.05).to(torch.bfloat16).cuda()
+    qa, qb = nv.quantize(x, nv.ROW, nv.RNE), nv.quantize(w, nv.ROW, nv.RNE)
+    nv.reset_status()
+    H, m = nv.gemm_sqrelu_maxima(qa, qb, rht_seed=7)
+    H2 = nv.gemm(qa, qb, torch.bfloat16)
+    kw = dict(rht=rht, sr_seed=3, sr_offset=2, rht_seed=7, pre="sqrelu")
+    fr, fc = nv.quantize_dual(H, rnd, rnd, maxima=m, **kw)
+    ur, uc = nv.quantize_dual(H, rnd, rnd, **kw)
+    torch.cuda.synchronize()
+    assert nv.status_query() == 0
+    assert torch.equal(H, H2)
+    for f, u in ((fr, ur), (fc, uc)):
+        assert torch.equal(f.codes, u.codes) and torch.equal(f.scales, u.scales)
+        assert torch.equal(f.scales_mma, u.scales_mma) and torch.equal(f.s_dec[:1], u.s_dec[:1])
