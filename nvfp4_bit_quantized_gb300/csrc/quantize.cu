@@ -806,55 +806,73 @@ __global__ void __launch_bounds__(kPatchThreads, kPatchCtasPerSm) encode_2d_kern
             }
             float amax = __uint_as_float(bf16x2_abs_max_bits(am));
             amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));      // the tile's other 8 columns
-            if (!pp.ok) continue;
-            const uint32_t sb = block_scale_code_bf16(amax, sc.s_enc);
-            const float2 eb = make_float2(g_eb_table[sb], g_eb_table[sb]);
-            uint32_t lo[8], hi[8];                   // row words: rows 0-7, 8-15
+            const bool ok = pp.ok;
+            uint32_t sb = 0u;                        // lanes without a patch: 0, the padding value
+            if (ok) {
+                sb = block_scale_code_bf16(amax, sc.s_enc);
+                const float2 eb = make_float2(g_eb_table[sb], g_eb_table[sb]);
+                uint32_t lo[8], hi[8];                   // row words: rows 0-7, 8-15
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                const uint4 q = pp.read_row(i);
-                const uint32_t w[4] = {q.x, q.y, q.z, q.w};
-                float y[8];
+                for (int i = 0; i < 16; ++i) {
+                    const uint4 q = pp.read_row(i);
+                    const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+                    float y[8];
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const float2 u = __fmul2_rn(make_float2(bf16_lo(w[j]), bf16_hi(w[j])), eb);
-                    y[2 * j] = u.x;
-                    y[2 * j + 1] = u.y;
+                    for (int j = 0; j < 4; ++j) {
+                        const float2 u = __fmul2_rn(make_float2(bf16_lo(w[j]), bf16_hi(w[j])), eb);
+                        y[2 * j] = u.x;
+                        y[2 * j + 1] = u.y;
+                    }
+                    uint32_t packed;
+                    if constexpr (SR) {
+                        const uint64_t idx0 = (uint64_t)((r0 + i) * C + c0);      // c0 % 8 == 0
+                        const Philox4 p = sr_philox(key, 0u, sr_offset, idx0 >> 4);
+                        const bool upper = (idx0 & 8) != 0;
+                        packed = e2m1x4_sr(y[0], y[1], y[2], y[3], upper ? p.w[2] : p.w[0]) |
+                                 (e2m1x4_sr(y[4], y[5], y[6], y[7], upper ? p.w[3] : p.w[1]) << 16);
+                    } else {
+                        packed = e2m1x8_rn(y);
+                    }
+                    *reinterpret_cast<uint32_t*>(out.codes + (r0 + i) * (C / 2) + c0 / 2) = packed;
+                    if (i < 8) lo[i] = packed;
+                    else hi[i - 8] = packed;
                 }
-                uint32_t packed;
-                if constexpr (SR) {
-                    const uint64_t idx0 = (uint64_t)((r0 + i) * C + c0);      // c0 % 8 == 0
-                    const Philox4 p = sr_philox(key, 0u, sr_offset, idx0 >> 4);
-                    const bool upper = (idx0 & 8) != 0;
-                    packed = e2m1x4_sr(y[0], y[1], y[2], y[3], upper ? p.w[2] : p.w[0]) |
-                             (e2m1x4_sr(y[4], y[5], y[6], y[7], upper ? p.w[3] : p.w[1]) << 16);
-                } else {
-                    packed = e2m1x8_rn(y);
+                if (out.codes_t) {
+                    transpose_nibbles8(lo);
+                    transpose_nibbles8(hi);
+#pragma unroll
+                    for (int j = 0; j < 8; ++j)
+                        *reinterpret_cast<uint2*>(out.codes_t + (c0 + j) * (R / 2) + r0 / 2) = make_uint2(lo[j], hi[j]);
                 }
-                *reinterpret_cast<uint32_t*>(out.codes + (r0 + i) * (C / 2) + c0 / 2) = packed;
-                if (i < 8) lo[i] = packed;
-                else hi[i - 8] = packed;
+                if ((cc & 1) == 0 && out.scales) out.scales[(r0 / 16) * (C / 16) + c0 / 16] = (uint8_t)sb;
             }
-            if (out.codes_t) {
-                transpose_nibbles8(lo);
-                transpose_nibbles8(hi);
+            // Tile-layout scales as 32-bit words (four adjacent scale columns of one row), so a
+            // lane stores two words instead of sixteen bytes; every lane takes part in the shuffles.
+            const int rg = lane >> 3;
+            if (out.scales_mma) {
+                // scale columns c0/16 of the lanes cc = 0, 2, 4, 6 of this row group; rows r0 + cc, r0 + cc + 8
+                uint32_t w = 0u;
 #pragma unroll
-                for (int j = 0; j < 8; ++j)
-                    *reinterpret_cast<uint2*>(out.codes_t + (c0 + j) * (R / 2) + r0 / 2) = make_uint2(lo[j], hi[j]);
-            }
-            if ((cc & 1) == 0) {
-                // rows r0 .. r0 + 15 (r0 % 16 == 0) differ only in the (r & 31) << 4 term
-                const int64_t s = c0 / 16, st = r0 / 16;
-                if (out.scales) out.scales[st * (C / 16) + s] = (uint8_t)sb;
-                if (out.scales_mma) {
-                    uint8_t* d = out.scales_mma + mma_sf_offset(r0, s, nkb);
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) d[16 * i] = (uint8_t)sb;
+                for (int k = 0; k < 4; ++k) w |= __shfl_sync(0xFFFFFFFFu, sb, (lane & 24) | (2 * k)) << (8 * k);
+                const bool base_ok = __shfl_sync(0xFFFFFFFFu, ok ? 1u : 0u, lane & 24) != 0u;
+                if (base_ok) {
+                    const int64_t s0 = (c0 - cc * 8) / 16;              // a multiple of 4
+                    *reinterpret_cast<uint32_t*>(out.scales_mma + mma_sf_offset(r0 + cc, s0, nkb)) = w;
+                    *reinterpret_cast<uint32_t*>(out.scales_mma + mma_sf_offset(r0 + cc + 8, s0, nkb)) = w;
                 }
-                if (out.scales_mma_t) {
-                    uint8_t* d = out.scales_mma_t + mma_sf_offset(c0, st, nkb_t);
+            }
+            if (out.scales_mma_t) {
+                // W^T rows = this 16-column block's columns; scale columns r0/16 of the row groups 0..3
+                uint32_t w = 0u;
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) d[16 * j] = (uint8_t)sb;
+                for (int k = 0; k < 4; ++k) w |= __shfl_sync(0xFFFFFFFFu, sb, (k << 3) | (cc & 6)) << (8 * k);
+                const bool base_ok = __shfl_sync(0xFFFFFFFFu, ok ? 1u : 0u, cc & 6) != 0u;
+                if (base_ok) {
+                    const int64_t st0 = (r0 - rg * 16) / 16;            // a multiple of 4
+                    const int64_t cb = c0 - (cc & 1) * 8;                // the block's first column
+                    const int64_t j = (cc & 1) * 8 + rg * 2;
+                    *reinterpret_cast<uint32_t*>(out.scales_mma_t + mma_sf_offset(cb + j, st0, nkb_t)) = w;
+                    *reinterpret_cast<uint32_t*>(out.scales_mma_t + mma_sf_offset(cb + j + 1, st0, nkb_t)) = w;
                 }
             }
         }
