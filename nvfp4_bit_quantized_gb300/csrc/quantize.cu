@@ -202,6 +202,7 @@ constexpr int kPatchSlotBytes = 16 * 32 * 16;
 constexpr int kPatchThreads = 128;                                          // 4 warps per CTA
 constexpr int kPatchCtasPerSm = 3;                                          // by registers (~140 / thread) and shared memory
 constexpr int kPatchSmemBytes = (kPatchThreads / 32) * 2 * kPatchSlotBytes;   // 64 KB per CTA
+constexpr int kBandGroup = 8;                                               // bands per tile group (power of 2)
 
 template <typename T>
 struct PatchPipe {
@@ -215,10 +216,16 @@ struct PatchPipe {
     int64_t r0 = 0, c0 = 0, nr0 = 0, nc0 = 0;   // current patch / the one in flight
     bool ok = false, nok = false;
 
+    // Tile order: groups of kBandGroup 64-row bands, column-major inside a group, so
+    // neighbouring warps (the warps of a CTA and of the next CTA) take vertically adjacent
+    // tiles and their transposed outputs (32 bytes per output row each) land as whole
+    // 128-byte lines and longer runs.  Tiles past the last band are skipped like any other
+    // out-of-range patch.
     __device__ __forceinline__ PatchPipe(const T* x_, int64_t ldx_, int64_t R_, int64_t C_, int64_t warp0,
-                                         int64_t nwarps_, int64_t tiles_, int64_t tiles_c, uint8_t* smem)
-        : x(x_), ldx(ldx_), R(R_), C(C_), tiles(tiles_), nwarps(nwarps_), tile(warp0),
-          w(warp0, nwarps_, tiles_c > 0 ? tiles_c : 1) {
+                                         int64_t nwarps_, int64_t /*tiles*/, int64_t tiles_c, uint8_t* smem)
+        : x(x_), ldx(ldx_), R(R_), C(C_),
+          tiles((((R_ + 63) / 64 + kBandGroup - 1) / kBandGroup) * kBandGroup * tiles_c), nwarps(nwarps_),
+          tile(warp0), w(warp0, nwarps_, kBandGroup * (tiles_c > 0 ? tiles_c : 1)) {
         const int lane = threadIdx.x & 31;
         rg = lane >> 3;
         cc = lane & 7;
@@ -229,8 +236,8 @@ struct PatchPipe {
     __device__ __forceinline__ static void commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
     // copies the patch at the walker's position into slot s (one commit group)
     __device__ __forceinline__ void issue(uint32_t s) {
-        nr0 = w.row * 64 + rg * 16;
-        nc0 = w.col * (8 * VEC) + cc * VEC;
+        nr0 = (w.row * kBandGroup + (w.col & (kBandGroup - 1))) * 64 + rg * 16;
+        nc0 = (w.col / kBandGroup) * (8 * VEC) + cc * VEC;
         nok = nr0 < R && nc0 < C;
         if (nok) {
             const char* src = reinterpret_cast<const char*>(x + nr0 * ldx + nc0);
