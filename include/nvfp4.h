@@ -217,6 +217,18 @@ NVFP4_API nvfp4_status nvfp4_gemm_sqrelu_bwd(const nvfp4_qtensor* A, const nvfp4
                                              int64_t ldh, void* D, int64_t ldd, uint32_t* dev_status,
                                              void* stream);
 
+/*
+ * nvfp4_gemm_sqrelu_bwd_maxima -- nvfp4_gemm_sqrelu_bwd whose epilogue also leaves the two
+ * tensor maxima the dual quantization of its output dH needs (max|dH| and max|RHT(dH)| along
+ * rows with the RHT sign vector of rht_seed), as nvfp4_gemm_sqrelu_maxima does for relu(H)^2;
+ * nvfp4_quantize_dual_premax then quantizes dH without an amax read.  dH is identical to
+ * nvfp4_gemm_sqrelu_bwd's.  Additional rules: maxima non-NULL (nvfp4_sqrelu_maxima_bytes(),
+ * 4-byte aligned), M % 16 == 0 and N % 16 == 0.
+ */
+NVFP4_API nvfp4_status nvfp4_gemm_sqrelu_bwd_maxima(const nvfp4_qtensor* A, const nvfp4_qtensor* B, const void* H,
+                                                    int64_t ldh, void* D, int64_t ldd, uint64_t rht_seed,
+                                                    uint32_t* maxima, uint32_t* dev_status, void* stream);
+
 /* Bytes of the partial-maxima buffer nvfp4_gemm_sqrelu_maxima writes (device memory). */
 NVFP4_API size_t nvfp4_sqrelu_maxima_bytes(void);
 
@@ -248,6 +260,17 @@ NVFP4_API nvfp4_status nvfp4_quantize_dual_sqrelu_premax(const void* h, int32_t 
                                                          const nvfp4_qparams* params_col,
                                                          const nvfp4_qtensor* out_col, const uint32_t* maxima,
                                                          uint32_t* dev_status, void* stream);
+
+/*
+ * nvfp4_quantize_dual_premax -- nvfp4_quantize_dual of x using the maxima that
+ * nvfp4_gemm_sqrelu_bwd_maxima left for this same x (rht_seed == params_col->rht_seed when
+ * params_col->rht is set): only the two encode passes run; results identical to
+ * nvfp4_quantize_dual's.  BF16 x only (else NVFP4_ERR_UNSUPPORTED); no workspace.
+ */
+NVFP4_API nvfp4_status nvfp4_quantize_dual_premax(const void* x, int32_t x_dtype, int64_t R, int64_t C, int64_t ldx,
+                                                  const nvfp4_qparams* params_row, const nvfp4_qtensor* out_row,
+                                                  const nvfp4_qparams* params_col, const nvfp4_qtensor* out_col,
+                                                  const uint32_t* maxima, uint32_t* dev_status, void* stream);
 
 /*
  * MXFP4 -- the earlier 4-bit microscaling format the page compares NVFP4 with

@@ -24,6 +24,7 @@ EXPORTS = [
     "nvfp4_sqrelu_forward", "nvfp4_sqrelu_backward",
     "nvfp4_mx_scales_mma_bytes", "nvfp4_mx_quantize", "nvfp4_mx_gemm", "nvfp4_gemm_sqrelu_bwd",
     "nvfp4_sqrelu_maxima_bytes", "nvfp4_gemm_sqrelu_maxima", "nvfp4_quantize_dual_sqrelu_premax",
+    "nvfp4_gemm_sqrelu_bwd_maxima", "nvfp4_quantize_dual_premax",
 ]
 
 
@@ -94,6 +95,8 @@ def lib():
             "nvfp4_sqrelu_maxima_bytes": (SZ, []),
             "nvfp4_gemm_sqrelu_maxima": (I32, [QT, QT, P, I64, U64, P, P, P]),
             "nvfp4_quantize_dual_sqrelu_premax": (I32, [P, I32, I64, I64, I64, QP, QT, QP, QT, P, P, P]),
+            "nvfp4_gemm_sqrelu_bwd_maxima": (I32, [QT, QT, P, I64, P, I64, U64, P, P, P]),
+            "nvfp4_quantize_dual_premax": (I32, [P, I32, I64, I64, I64, QP, QT, QP, QT, P, P, P]),
         }
         for name, (res, args) in sigs.items():
             fn = getattr(L, name)

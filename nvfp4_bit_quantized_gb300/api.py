@@ -154,8 +154,9 @@ def quantize_dual(x: torch.Tensor, row_round: int = L.RNE, col_round: int = L.RN
     Identical to two ``quantize`` calls with the same parameters; the column
     operand's SR seed / offset default to the row's.  ``pre="sqrelu"`` quantizes
     relu(x)^2 (bf16 x) without storing it, identical to ``sqrelu_forward`` first.
-    ``maxima`` (with ``pre="sqrelu"``): the partial maxima ``gemm_sqrelu_maxima`` left
-    for this x with the same ``rht_seed``; the amax read is then skipped."""
+    ``maxima``: the partial maxima a producing GEMM left for this x with the same
+    ``rht_seed`` (``gemm_sqrelu_maxima`` with ``pre="sqrelu"``, ``gemm_sqrelu_backward(...,
+    maxima=True)`` without); the amax read is then skipped."""
     _check_2d(x, "x")
     R, C = x.shape
     qr = _alloc_q(R, C, L.ROW, x.device, scales, scales_mma, False)
@@ -170,12 +171,10 @@ def quantize_dual(x: torch.Tensor, row_round: int = L.RNE, col_round: int = L.RN
     if pre not in (None, "sqrelu"):
         raise ValueError(f"unknown pre transform {pre!r}")
     if maxima is not None:
-        if pre != "sqrelu":
-            raise ValueError("maxima are the squared-ReLU GEMM epilogue's: pass pre='sqrelu'")
-        st = lib.nvfp4_quantize_dual_sqrelu_premax(_ptr(x), _DT[x.dtype], R, C, ld, ctypes.byref(pr), ctypes.byref(a),
-                                                   ctypes.byref(pc), ctypes.byref(b), _ptr(maxima),
-                                                   dev_status(x.device).data_ptr(), _stream())
-        L.check(st, "nvfp4_quantize_dual_sqrelu_premax")
+        fn = lib.nvfp4_quantize_dual_sqrelu_premax if pre == "sqrelu" else lib.nvfp4_quantize_dual_premax
+        st = fn(_ptr(x), _DT[x.dtype], R, C, ld, ctypes.byref(pr), ctypes.byref(a), ctypes.byref(pc), ctypes.byref(b),
+                _ptr(maxima), dev_status(x.device).data_ptr(), _stream())
+        L.check(st, "nvfp4_quantize_dual_sqrelu_premax" if pre else "nvfp4_quantize_dual_premax")
         return qr, qc
     fn = lib.nvfp4_quantize_dual_sqrelu if pre == "sqrelu" else lib.nvfp4_quantize_dual
     st = fn(_ptr(x), _DT[x.dtype], R, C, ld, ctypes.byref(pr), ctypes.byref(a), ctypes.byref(pc), ctypes.byref(b),
@@ -270,10 +269,13 @@ def gemm_sqrelu_maxima(A: QTensor, B: QTensor, rht_seed: int = 0, out: Optional[
     return out, m
 
 
-def gemm_sqrelu_backward(A: QTensor, B: QTensor, H: torch.Tensor, out: Optional[torch.Tensor] = None) -> torch.Tensor:
+def gemm_sqrelu_backward(A: QTensor, B: QTensor, H: torch.Tensor, out: Optional[torch.Tensor] = None,
+                         maxima: bool = False, rht_seed: int = 0):
     """dH = dA * 2 relu(H) with dA = dequant(A) . dequant(B)^T in bf16 -- the Dgrad GEMM of a
     squared-ReLU MLP with the activation's backward in its epilogue (dA is never stored);
-    bit for bit ``sqrelu_backward(H, gemm(A, B, torch.bfloat16))``.  H: bf16 [M, N]."""
+    bit for bit ``sqrelu_backward(H, gemm(A, B, torch.bfloat16))``.  H: bf16 [M, N].  With
+    ``maxima`` the epilogue also leaves dH's tensor maxima for ``quantize_dual(dH, ...,
+    maxima=m)`` (RHT signs from ``rht_seed``) and (dH, m) is returned."""
     M, N = A.rows, B.rows
     _check_2d(H, "H")
     if H.dtype != torch.bfloat16 or tuple(H.shape) != (M, N):
@@ -282,9 +284,17 @@ def gemm_sqrelu_backward(A: QTensor, B: QTensor, H: torch.Tensor, out: Optional[
         out = torch.empty((M, N), dtype=torch.bfloat16, device=A.codes.device)
     _check_2d(out, "out")
     a, b = A.c_struct(), B.c_struct()
-    st = L.lib().nvfp4_gemm_sqrelu_bwd(ctypes.byref(a), ctypes.byref(b), _ptr(H), H.stride(0) if M > 1 else N,
-                                       _ptr(out), out.stride(0) if M > 1 else N, dev_status(out.device).data_ptr(),
-                                       _stream())
+    lib = L.lib()
+    ldh, ldd = H.stride(0) if M > 1 else N, out.stride(0) if M > 1 else N
+    if maxima:
+        m = torch.empty(int(lib.nvfp4_sqrelu_maxima_bytes()) // 4, dtype=torch.int32, device=out.device)
+        st = lib.nvfp4_gemm_sqrelu_bwd_maxima(ctypes.byref(a), ctypes.byref(b), _ptr(H), ldh, _ptr(out), ldd,
+                                              rht_seed & (2**64 - 1), _ptr(m), dev_status(out.device).data_ptr(),
+                                              _stream())
+        L.check(st, "nvfp4_gemm_sqrelu_bwd_maxima")
+        return out, m
+    st = lib.nvfp4_gemm_sqrelu_bwd(ctypes.byref(a), ctypes.byref(b), _ptr(H), ldh, _ptr(out), ldd,
+                                   dev_status(out.device).data_ptr(), _stream())
     L.check(st, "nvfp4_gemm_sqrelu_bwd")
     return out
 

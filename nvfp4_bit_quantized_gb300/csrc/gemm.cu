@@ -99,16 +99,17 @@ struct Params {
     int n_fastest;               // tile order: 1 = consecutive tiles walk N (A tile reused), 0 = walk M
     uint32_t* dev_status;
     uint64_t timeout_ns;
-    uint32_t* maxima;            // EPI_SQAMAX: 2 x kMaximaParts partial maxima (|A|, then |RHT(A)| / 4)
-    uint64_t rht_seed;           // EPI_SQAMAX: the RHT sign vector of the column quantization
+    uint32_t* maxima;            // EPI_SQAMAX / EPI_DSQR_AMAX: 2 x kMaximaParts partial maxima (|X|, then |RHT(X)| / 4)
+    uint64_t rht_seed;           // the RHT sign vector of the column quantization those maxima serve
 };
 
 // Epilogue variants of the CTA-pair kernel.
 //   EPI_PLAIN   D = alpha * acc;
 //   EPI_DSQR    D = dH = bf16(alpha * acc) * 2 relu(H)  (the squared-ReLU backward);
 //   EPI_SQAMAX  D = H = alpha * acc, plus the tensor maxima that quantizing A = relu(H)^2 in
-//               both orientations needs (|A| and |RHT(A)| along rows), as per-warp partials.
-constexpr int EPI_PLAIN = 0, EPI_DSQR = 1, EPI_SQAMAX = 2;
+//               both orientations needs (|A| and |RHT(A)| along rows), as per-warp partials;
+//   EPI_DSQR_AMAX  EPI_DSQR plus the same two maxima of dH itself.
+constexpr int EPI_PLAIN = 0, EPI_DSQR = 1, EPI_SQAMAX = 2, EPI_DSQR_AMAX = 3;
 
 // Tile order.  Consecutive persistent CTAs (clusters) take consecutive tiles, so the
 // operand indexed by the slow coordinate is shared by the CTAs running together
@@ -709,20 +710,44 @@ __device__ __forceinline__ void packed_to_box(const uint32_t (&pk)[32], uint8_t*
             make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
 }
 
+// The squared-ReLU backward of box_to_smem_dsqr from dA already packed to bf16 (pack_bf16_64):
+// the H box in the slot is replaced by dH, with the same arithmetic.
+__device__ __forceinline__ void packed_dsqr_to_box(const uint32_t (&pk)[32], uint8_t* box, int lane) {
+    uint8_t* row = box + lane * 128;
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+        uint4* slot = reinterpret_cast<uint4*>(row + ((c ^ (lane & 7)) << 4));
+        const uint4 hq = *slot;
+        const uint32_t hw[4] = {hq.x, hq.y, hq.z, hq.w};
+        uint32_t w[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const uint32_t da = pk[4 * c + i];
+            const float hl = bf16_lo(hw[i]), hh = bf16_hi(hw[i]);
+            const float2 t = make_float2(hl > 0.0f ? __fmul_rn(2.0f, hl) : 0.0f, hh > 0.0f ? __fmul_rn(2.0f, hh) : 0.0f);
+            const __nv_bfloat162 dh = __float22bfloat162_rn(__fmul2_rn(make_float2(bf16_lo(da), bf16_hi(da)), t));
+            w[i] = *reinterpret_cast<const uint32_t*>(&dh);
+        }
+        *slot = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+}
+
 template <int EPI>
 __device__ __forceinline__ void box_out(const uint32_t (&v)[64], uint8_t* box, int lane, float alpha) {
-    if constexpr (EPI == EPI_DSQR) box_to_smem_dsqr(v, box, lane, alpha);
+    if constexpr (EPI == EPI_DSQR || EPI == EPI_DSQR_AMAX) box_to_smem_dsqr(v, box, lane, alpha);
     else box_to_smem(v, box, lane, alpha);
 }
 
-// EPI_SQAMAX: folds one stored 32 x 64 box of H (rows m0.., columns n0..) into the warp's
-// running maxima of A = relu(H)^2, computed exactly as the quantizer's load transform and
-// its dual amax pass compute them: mabs = max |a| and mrht = max |t| with t the unnormalised
-// 16-point butterflies of (s_i * a_i) down each 16-row group (bit patterns of non-negative
-// floats; a NaN lands above every finite value).  Lane l takes column pair 2l, 2l+1; rows
-// past M and columns past N (both multiples of 16) are left out.
-__device__ __forceinline__ void box_sqrelu_maxima(const uint8_t* box, int lane, int m0, int M, int n0, int N,
-                                                  uint32_t sign_mask, uint32_t& mabs, uint32_t& mrht) {
+// Folds one stored 32 x 64 box (rows m0.., columns n0..) into the warp's running maxima of
+// the tensor the next quantization reads -- the box's values x, or with SQR a = relu(x)^2
+// formed as the quantizer's load transform forms it -- exactly as its dual amax pass computes
+// them: mabs = max |a| and mrht = max |t| with t the unnormalised 16-point butterflies of
+// (s_i * a_i) down each 16-row group (bit patterns of non-negative floats; a NaN lands above
+// every finite value).  Lane l takes column pair 2l, 2l+1; rows past M and columns past N
+// (both multiples of 16) are left out.
+template <bool SQR>
+__device__ __forceinline__ void box_maxima(const uint8_t* box, int lane, int m0, int M, int n0, int N,
+                                           uint32_t sign_mask, uint32_t& mabs, uint32_t& mrht) {
     if (n0 + 2 * lane >= N) return;
 #pragma unroll 1
     for (int g = 0; g < 2; ++g) {                        // one group at a time: bounded registers
@@ -733,7 +758,7 @@ __device__ __forceinline__ void box_sqrelu_maxima(const uint8_t* box, int lane, 
             const int r = 16 * g + i;
             uint32_t w = *reinterpret_cast<const uint32_t*>(box + r * 128 + ((((lane >> 2) ^ (r & 7)) << 4) |
                                                                               ((lane & 3) << 2)));
-            w = sqrelu_bf16x2(w);
+            if constexpr (SQR) w = sqrelu_bf16x2(w);
             mabs = max(mabs, max((w << 16) & 0x7FFFFFFFu, w & 0x7FFF0000u));
             if ((sign_mask >> i) & 1u) w ^= 0x80008000u;
             t[i] = make_float2(bf16_lo(w), bf16_hi(w));
@@ -762,8 +787,9 @@ gemm_nvfp4_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_con
                        const __grid_constant__ CUtensorMap tmD, const __grid_constant__ CUtensorMap tmH,
                        const Params p) {
     constexpr int STAGES = P_STAGES;
-    constexpr bool DSQR = EPI == EPI_DSQR;
-    constexpr bool SQAMAX = EPI == EPI_SQAMAX;
+    constexpr bool DSQR = EPI == EPI_DSQR || EPI == EPI_DSQR_AMAX;   // output dH from dA and H
+    constexpr bool AMAX = EPI == EPI_SQAMAX || EPI == EPI_DSQR_AMAX; // leave the output's tensor maxima
+    constexpr bool SQR_MAX = EPI == EPI_SQAMAX;                      // ... of relu(output)^2
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* staging = smem + P_RING_BYTES;
@@ -993,8 +1019,8 @@ gemm_nvfp4_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_con
         const uint64_t stream_pol = l2_evict_first_policy();
         uint32_t acc_phase = 0, h_phase = 0;
         bool h_pending = false;                          // DSQR: H boxes in flight into the slots
-        uint32_t mabs = 0u, mrht = 0u;                   // SQAMAX: running maxima (float bits)
-        const uint32_t sign_mask = SQAMAX ? rht_sign_mask(p.rht_seed) : 0u;
+        uint32_t mabs = 0u, mrht = 0u;                   // AMAX: running maxima (float bits)
+        const uint32_t sign_mask = AMAX ? rht_sign_mask(p.rht_seed) : 0u;
         bool ok = true;
         for (int tile = cluster; tile < tiles && ok; tile += nclusters) {
             int mp, nt;
@@ -1050,10 +1076,10 @@ gemm_nvfp4_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_con
             tmem_ld_64cols(tmem_row + ACC_COL + 192, vb);
             tmem_ld_wait();
             reg_fence64(vb);
-            // SQAMAX: the last two boxes as packed bf16 (half the registers), so the maxima of the
+            // AMAX: the last two boxes as packed bf16 (half the registers), so the maxima of the
             // first two fit beside them
             uint32_t pa[32], pb[32];
-            if constexpr (SQAMAX) {
+            if constexpr (AMAX) {
                 pack_bf16_64(va, pa, alpha);
                 pack_bf16_64(vb, pb, alpha);
             }
@@ -1062,9 +1088,9 @@ gemm_nvfp4_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_con
             __syncwarp();
             if (lane == 0) mbar_arrive_cluster(acc_empty_leader);
             store2(0);
-            if constexpr (SQAMAX) {                      // read alongside the stores: both only read the slots
-                box_sqrelu_maxima(stg, lane, m0, p.M, n0, p.N, sign_mask, mabs, mrht);
-                box_sqrelu_maxima(stg + BOX_BYTES, lane, m0, p.M, n0 + BOX_COLS, p.N, sign_mask, mabs, mrht);
+            if constexpr (AMAX) {                        // read alongside the stores: both only read the slots
+                box_maxima<SQR_MAX>(stg, lane, m0, p.M, n0, p.N, sign_mask, mabs, mrht);
+                box_maxima<SQR_MAX>(stg + BOX_BYTES, lane, m0, p.M, n0 + BOX_COLS, p.N, sign_mask, mabs, mrht);
             }
             if (lane == 0) bulk_wait_read0();
             __syncwarp();
@@ -1072,21 +1098,24 @@ gemm_nvfp4_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_con
                 load_h2(2);
                 if (!wait_h2()) { ok = false; break; }
             }
-            if constexpr (SQAMAX) {
+            if constexpr (EPI == EPI_SQAMAX) {
                 packed_to_box(pa, stg, lane);
                 packed_to_box(pb, stg + BOX_BYTES, lane);
+            } else if constexpr (EPI == EPI_DSQR_AMAX) {
+                packed_dsqr_to_box(pa, stg, lane);
+                packed_dsqr_to_box(pb, stg + BOX_BYTES, lane);
             } else {
                 box_out<EPI>(va, stg, lane, alpha);
                 box_out<EPI>(vb, stg + BOX_BYTES, lane, alpha);
             }
             store2(2);
-            if constexpr (SQAMAX) {
-                box_sqrelu_maxima(stg, lane, m0, p.M, n0 + 2 * BOX_COLS, p.N, sign_mask, mabs, mrht);
-                box_sqrelu_maxima(stg + BOX_BYTES, lane, m0, p.M, n0 + 3 * BOX_COLS, p.N, sign_mask, mabs, mrht);
+            if constexpr (AMAX) {
+                box_maxima<SQR_MAX>(stg, lane, m0, p.M, n0 + 2 * BOX_COLS, p.N, sign_mask, mabs, mrht);
+                box_maxima<SQR_MAX>(stg + BOX_BYTES, lane, m0, p.M, n0 + 3 * BOX_COLS, p.N, sign_mask, mabs, mrht);
             }
             acc_phase ^= 1u;
         }
-        if constexpr (SQAMAX) {
+        if constexpr (AMAX) {
             // this warp's partials; the first CTA zeroes the slots no CTA of this grid owns
             mabs = __reduce_max_sync(0xFFFFFFFFu, mabs);
             mrht = __reduce_max_sync(0xFFFFFFFFu, mrht);
@@ -1306,8 +1335,10 @@ nvfp4_status mx_gemm_impl(const nvfp4_qtensor* A, const nvfp4_qtensor* B, void* 
 
 // dH = bf16(dA) * 2 relu(H) with dA = s_dec(A) s_dec(B) A B^T: the NVFP4 GEMM with the squared-ReLU
 // backward in its epilogue (CTA-pair kernel; bf16 H and D, 16-byte aligned bases and pitches).
+// With `maxima`, the epilogue also leaves dH's two tensor maxima for its dual quantization.
 nvfp4_status gemm_sqrelu_bwd_impl(const nvfp4_qtensor* A, const nvfp4_qtensor* B, const void* H, int64_t ldh,
-                                  void* D, int64_t ldd, uint32_t* dev_status, cudaStream_t stream) {
+                                  void* D, int64_t ldd, uint64_t rht_seed, uint32_t* maxima, uint32_t* dev_status,
+                                  cudaStream_t stream) {
     using namespace gemm;
     if (!A || !B || !H || !D) return NVFP4_ERR_INVALID_ARG;
     if (!A->codes || !B->codes || !A->scales_mma || !B->scales_mma || !A->s_dec || !B->s_dec)
@@ -1315,9 +1346,11 @@ nvfp4_status gemm_sqrelu_bwd_impl(const nvfp4_qtensor* A, const nvfp4_qtensor* B
     const int64_t M = A->rows, N = B->rows, K = A->cols;
     if (B->cols != K) return NVFP4_ERR_SHAPE;
     if (M < 1 || N < 1 || K < 32 || K % 32 != 0 || ldd < N || ldh < N) return NVFP4_ERR_SHAPE;
+    if (maxima && (M % 16 != 0 || N % 16 != 0)) return NVFP4_ERR_SHAPE;
     if (M > (1ll << 30) || N > (1ll << 30) || K > (1ll << 30)) return NVFP4_ERR_SHAPE;
     if (!aligned16(A->codes) || !aligned16(B->codes) || !aligned16(A->scales_mma) || !aligned16(B->scales_mma) ||
-        !aligned16(D) || !aligned16(H) || (ldd * 2) % 16 != 0 || (ldh * 2) % 16 != 0)
+        !aligned16(D) || !aligned16(H) || (ldd * 2) % 16 != 0 || (ldh * 2) % 16 != 0 ||
+        (reinterpret_cast<uintptr_t>(maxima) & 3u) != 0)
         return NVFP4_ERR_ALIGNMENT;
     CUtensorMap ta, tb, td, th;
     if (!make_codes_map(&ta, A->codes, M, K, BM) || !make_codes_map(&tb, B->codes, N, K, 128) ||
@@ -1325,6 +1358,7 @@ nvfp4_status gemm_sqrelu_bwd_impl(const nvfp4_qtensor* A, const nvfp4_qtensor* B
         return NVFP4_ERR_CUDA;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return NVFP4_ERR_CUDA;
+    if (maxima && 4 * sm_count(dev) > kMaximaParts) return NVFP4_ERR_UNSUPPORTED;
     Params p;
     std::memset(&p, 0, sizeof(p));
     p.sfa = A->scales_mma;
@@ -1344,8 +1378,12 @@ nvfp4_status gemm_sqrelu_bwd_impl(const nvfp4_qtensor* A, const nvfp4_qtensor* B
     p.n_fastest = (M > N) ? 1 : 0;
     p.dev_status = dev_status;
     p.timeout_ns = wait_timeout_ns();
+    p.maxima = maxima;
+    p.rht_seed = rht_seed;
     const int pair_tiles = (int)((M + 255) / 256) * p.n_tiles;
-    const cudaError_t e = launch_pair<false, EPI_DSQR>(ta, tb, td, th, p, pair_tiles, sm_count(dev), stream);
+    const cudaError_t e = maxima
+        ? launch_pair<false, EPI_DSQR_AMAX>(ta, tb, td, th, p, pair_tiles, sm_count(dev), stream)
+        : launch_pair<false, EPI_DSQR>(ta, tb, td, th, p, pair_tiles, sm_count(dev), stream);
     return e == cudaSuccess ? NVFP4_OK : NVFP4_ERR_CUDA;
 }
 
@@ -1411,7 +1449,15 @@ extern "C" nvfp4_status nvfp4_gemm_sqrelu_maxima(const nvfp4_qtensor* A, const n
 extern "C" nvfp4_status nvfp4_gemm_sqrelu_bwd(const nvfp4_qtensor* A, const nvfp4_qtensor* B, const void* H,
                                               int64_t ldh, void* D, int64_t ldd, uint32_t* dev_status,
                                               void* stream) {
-    return nvfp4::gemm_sqrelu_bwd_impl(A, B, H, ldh, D, ldd, dev_status, static_cast<cudaStream_t>(stream));
+    return nvfp4::gemm_sqrelu_bwd_impl(A, B, H, ldh, D, ldd, 0, nullptr, dev_status, static_cast<cudaStream_t>(stream));
+}
+
+extern "C" nvfp4_status nvfp4_gemm_sqrelu_bwd_maxima(const nvfp4_qtensor* A, const nvfp4_qtensor* B, const void* H,
+                                                     int64_t ldh, void* D, int64_t ldd, uint64_t rht_seed,
+                                                     uint32_t* maxima, uint32_t* dev_status, void* stream) {
+    if (!maxima) return NVFP4_ERR_INVALID_ARG;
+    return nvfp4::gemm_sqrelu_bwd_impl(A, B, H, ldh, D, ldd, rht_seed, maxima, dev_status,
+                                       static_cast<cudaStream_t>(stream));
 }
 
 extern "C" nvfp4_status nvfp4_mx_gemm(const nvfp4_qtensor* A, const nvfp4_qtensor* B, void* D, int32_t d_dtype,

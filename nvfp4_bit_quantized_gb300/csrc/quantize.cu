@@ -1236,32 +1236,48 @@ extern "C" nvfp4_status nvfp4_quantize_dual_sqrelu(const void* h, int32_t h_dtyp
                                      workspace_bytes, dev_status, static_cast<cudaStream_t>(stream), true);
 }
 
-// nvfp4_quantize_dual_sqrelu with the tensor maxima already known (left by the GEMM that
-// produced H): only the two encode passes run.
-extern "C" nvfp4_status nvfp4_quantize_dual_sqrelu_premax(const void* h, int32_t h_dtype, int64_t R, int64_t C,
-                                                          int64_t ldh, const nvfp4_qparams* params_row,
-                                                          const nvfp4_qtensor* out_row, const nvfp4_qparams* params_col,
-                                                          const nvfp4_qtensor* out_col, const uint32_t* maxima,
-                                                          uint32_t* dev_status, void* stream_) {
-    using namespace nvfp4;
-    cudaStream_t stream = static_cast<cudaStream_t>(stream_);
-    if (!params_row || !params_col || !maxima) return NVFP4_ERR_INVALID_ARG;
-    if (h_dtype != NVFP4_BF16) return NVFP4_ERR_UNSUPPORTED;
-    if (params_row->block != NVFP4_BLOCK_1X16_ROW || params_col->block != NVFP4_BLOCK_1X16_COL)
-        return NVFP4_ERR_INVALID_ARG;
-    nvfp4_status st = check_quantize_args(h, h_dtype, R, C, ldh, params_row, out_row);
+namespace nvfp4 {
+// The dual quantization with the tensor maxima already known (left by the GEMM epilogue that
+// produced x): only the two encode passes run.  BF16 x; with sqr, of relu(x)^2.
+static nvfp4_status quantize_dual_premax_impl(const void* x, int32_t x_dtype, int64_t R, int64_t C, int64_t ldx,
+                                              const nvfp4_qparams* p_row, const nvfp4_qtensor* out_row,
+                                              const nvfp4_qparams* p_col, const nvfp4_qtensor* out_col,
+                                              const uint32_t* maxima, uint32_t* dev_status, cudaStream_t stream,
+                                              bool sqr) {
+    if (!p_row || !p_col || !maxima) return NVFP4_ERR_INVALID_ARG;
+    if (x_dtype != NVFP4_BF16) return NVFP4_ERR_UNSUPPORTED;
+    if (p_row->block != NVFP4_BLOCK_1X16_ROW || p_col->block != NVFP4_BLOCK_1X16_COL) return NVFP4_ERR_INVALID_ARG;
+    nvfp4_status st = check_quantize_args(x, x_dtype, R, C, ldx, p_row, out_row);
     if (st != NVFP4_OK) return st;
-    st = check_quantize_args(h, h_dtype, R, C, ldh, params_col, out_col);
+    st = check_quantize_args(x, x_dtype, R, C, ldx, p_col, out_col);
     if (st != NVFP4_OK) return st;
     if ((reinterpret_cast<uintptr_t>(maxima) & 3u) != 0) return NVFP4_ERR_ALIGNMENT;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return NVFP4_ERR_CUDA;
     const int sms = sm_count(dev);
     if (sms <= 0) return NVFP4_ERR_CUDA;
-    const uint32_t* part_col = params_col->rht ? maxima + kMaximaParts : maxima;
-    st = encode_pass(h, h_dtype, R, C, ldh, params_row, out_row, maxima, kMaximaParts, sms, dev_status, stream, true);
+    const uint32_t* part_col = p_col->rht ? maxima + kMaximaParts : maxima;
+    st = encode_pass(x, x_dtype, R, C, ldx, p_row, out_row, maxima, kMaximaParts, sms, dev_status, stream, sqr);
     if (st != NVFP4_OK) return st;
-    return encode_pass(h, h_dtype, R, C, ldh, params_col, out_col, part_col, kMaximaParts, sms, dev_status, stream, true);
+    return encode_pass(x, x_dtype, R, C, ldx, p_col, out_col, part_col, kMaximaParts, sms, dev_status, stream, sqr);
+}
+}  // namespace nvfp4
+
+extern "C" nvfp4_status nvfp4_quantize_dual_sqrelu_premax(const void* h, int32_t h_dtype, int64_t R, int64_t C,
+                                                          int64_t ldh, const nvfp4_qparams* params_row,
+                                                          const nvfp4_qtensor* out_row, const nvfp4_qparams* params_col,
+                                                          const nvfp4_qtensor* out_col, const uint32_t* maxima,
+                                                          uint32_t* dev_status, void* stream) {
+    return nvfp4::quantize_dual_premax_impl(h, h_dtype, R, C, ldh, params_row, out_row, params_col, out_col, maxima,
+                                            dev_status, static_cast<cudaStream_t>(stream), true);
+}
+
+extern "C" nvfp4_status nvfp4_quantize_dual_premax(const void* x, int32_t x_dtype, int64_t R, int64_t C, int64_t ldx,
+                                                   const nvfp4_qparams* params_row, const nvfp4_qtensor* out_row,
+                                                   const nvfp4_qparams* params_col, const nvfp4_qtensor* out_col,
+                                                   const uint32_t* maxima, uint32_t* dev_status, void* stream) {
+    return nvfp4::quantize_dual_premax_impl(x, x_dtype, R, C, ldx, params_row, out_row, params_col, out_col, maxima,
+                                            dev_status, static_cast<cudaStream_t>(stream), false);
 }
 
 extern "C" size_t nvfp4_quantize_dual_workspace_bytes(int64_t, int64_t) {

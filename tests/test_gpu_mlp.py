@@ -40,14 +40,16 @@ def mlp_step(nv, X, W1, W2, dY, sr_seed=5, rht_seed=9, fused_dgrad=False, fused_
     out["Y"] = nv.gemm(out["aq"], out["w2q"], torch.bfloat16)
     out["dyq"], out["dyt"] = nv.quantize_dual(dY, nv.SR, nv.SR, rht=True, sr_seed=sr_seed, sr_offset=0,
                                               rht_seed=rht_seed)
-    if fused_dgrad:
-        out["dH"] = nv.gemm_sqrelu_backward(out["dyq"], out["w2q"].transposed(), out["H"])
+    dh_maxima = None
+    if fused_dgrad:                                       # dH and its tensor maxima from the epilogue
+        out["dH"], dh_maxima = nv.gemm_sqrelu_backward(out["dyq"], out["w2q"].transposed(), out["H"],
+                                                       maxima=True, rht_seed=rht_seed)
     else:
         out["dA"] = nv.gemm(out["dyq"], out["w2q"].transposed(), torch.bfloat16)
         out["dH"] = nv.sqrelu_backward(out["H"], out["dA"])
     out["dW2"] = nv.gemm(out["dyt"], out["at"], torch.bfloat16)
     out["dhq"], out["dht"] = nv.quantize_dual(out["dH"], nv.SR, nv.SR, rht=True, sr_seed=sr_seed, sr_offset=1,
-                                              rht_seed=rht_seed)
+                                              rht_seed=rht_seed, maxima=dh_maxima)
     out["dX"] = nv.gemm(out["dhq"], out["w1q"].transposed(), torch.bfloat16)
     out["dW1"] = nv.gemm(out["dht"], out["xt"], torch.bfloat16)
     return out
@@ -132,7 +134,8 @@ def test_mlp_block_full_size_sampled(nv, oracle_mod):
     # H and the quantization of relu(H)^2 from the epilogue's maxima equal the unfused path
     assert torch.equal(o["H"], nv.gemm(o["xq"], o["w1q"], torch.bfloat16))
     aq, at = nv.quantize_dual(o["H"], nv.RNE, nv.RNE, rht=True, rht_seed=9, pre="sqrelu")
-    for fq, uq in ((o["aq"], aq), (o["at"], at)):
+    dhq, dht = nv.quantize_dual(o["dH"], nv.SR, nv.SR, rht=True, sr_seed=5, sr_offset=1, rht_seed=9)
+    for fq, uq in ((o["aq"], aq), (o["at"], at), (o["dhq"], dhq), (o["dht"], dht)):
         assert torch.equal(fq.codes, uq.codes) and torch.equal(fq.scales, uq.scales)
         assert torch.equal(fq.s_dec[:1], uq.s_dec[:1])
     assert nv.status_query() == 0
@@ -249,6 +252,31 @@ def test_gemm_sqrelu_maxima_then_quantize_equals_unfused(nv, pair_path, M, N, K,
     torch.cuda.synchronize()
     assert nv.status_query() == 0
     assert torch.equal(H, H2)
+    for f, u in ((fr, ur), (fc, uc)):
+        assert torch.equal(f.codes, u.codes) and torch.equal(f.scales, u.scales)
+        assert torch.equal(f.scales_mma, u.scales_mma) and torch.equal(f.s_dec[:1], u.s_dec[:1])
+
+
+@pytest.mark.parametrize("rht", [True, False])
+@pytest.mark.parametrize("M,N,K", [(256, 256, 256), (208, 336, 224), (512, 1024, 768), (16, 16, 32)])
+def test_gemm_sqrelu_backward_maxima_then_quantize_equals_unfused(nv, pair_path, M, N, K, rht):
+    """The fused Dgrad GEMM leaving dH's tensor maxima: dH is bit for bit the plain fused
+    GEMM's, and the SR dual quantization of dH from those maxima (no amax read) equals the
+    one with its own amax pass."""
+    g = torch.Generator().manual_seed(2 * M + N + K)
+    dy = (torch.randn((M, K), generator=g) * 1e-3).to(torch.bfloat16).cuda()
+    w = (torch.randn((N, K), generator=g) * 0.02).to(torch.bfloat16).cuda()
+    H = (torch.randn((M, N), generator=g) * 2).to(torch.bfloat16).cuda()
+    qa, qb = nv.quantize(dy, nv.ROW, nv.SR, sr_seed=3), nv.quantize(w, nv.ROW, nv.RNE)
+    nv.reset_status()
+    dH, m = nv.gemm_sqrelu_backward(qa, qb, H, maxima=True, rht_seed=13)
+    dH2 = nv.gemm_sqrelu_backward(qa, qb, H)
+    kw = dict(rht=rht, sr_seed=4, sr_offset=6, rht_seed=13)
+    fr, fc = nv.quantize_dual(dH, nv.SR, nv.SR, maxima=m, **kw)
+    ur, uc = nv.quantize_dual(dH, nv.SR, nv.SR, **kw)
+    torch.cuda.synchronize()
+    assert nv.status_query() == 0
+    assert torch.equal(dH.view(torch.int16), dH2.view(torch.int16))
     for f, u in ((fr, ur), (fc, uc)):
         assert torch.equal(f.codes, u.codes) and torch.equal(f.scales, u.scales)
         assert torch.equal(f.scales_mma, u.scales_mma) and torch.equal(f.s_dec[:1], u.s_dec[:1])

@@ -194,3 +194,22 @@ def test_sqrelu_maxima_entries_reject_bad_arguments(lib):
              None, None, None) == lib.ERR_INVALID_ARG
     assert q(0x1000, lib.BF16, 32, 64, 64, ctypes.byref(pc), ctypes.byref(qr), ctypes.byref(pc), ctypes.byref(qc),
              0x8000, None, None) == lib.ERR_INVALID_ARG                                             # row params
+
+
+def test_dh_maxima_entries_reject_bad_arguments(lib):
+    L = lib.lib()
+    A = lib.QTensorC(0x1000, None, 0x1000, 0x2000, None, None, 128, 256)
+    B = lib.QTensorC(0x1000, None, 0x1000, 0x2000, None, None, 256, 256)
+    f = L.nvfp4_gemm_sqrelu_bwd_maxima
+    assert f(ctypes.byref(A), ctypes.byref(B), 0x8000, 256, 0x4000, 256, 0, None, None, None) == lib.ERR_INVALID_ARG
+    assert f(ctypes.byref(A), ctypes.byref(B), 0x8000, 256, 0x4000, 256, 0, 0x9002, None, None) == lib.ERR_ALIGNMENT
+    B.rows = 200                                                                                     # N % 16
+    assert f(ctypes.byref(A), ctypes.byref(B), 0x8000, 256, 0x4000, 256, 0, 0x9000, None, None) == lib.ERR_SHAPE
+    pr, pc = _qp(lib, 0, 1, 0), _qp(lib, 1, 1, 1)
+    qr = lib.QTensorC(0x1000, 0x1000, None, 0x2000, None, None, 32, 64)
+    qc = lib.QTensorC(0x1000, 0x1000, None, 0x2000, None, None, 64, 32)
+    q = L.nvfp4_quantize_dual_premax
+    assert q(0x1000, lib.F32, 32, 64, 64, ctypes.byref(pr), ctypes.byref(qr), ctypes.byref(pc), ctypes.byref(qc),
+             0x8000, None, None) == lib.ERR_UNSUPPORTED
+    assert q(0x1000, lib.BF16, 32, 64, 64, ctypes.byref(pr), ctypes.byref(qr), ctypes.byref(pc), ctypes.byref(qc),
+             None, None, None) == lib.ERR_INVALID_ARG
