@@ -40,7 +40,8 @@ def digest(a: np.ndarray) -> str:
 
 def make():
     out = {"_how": "inputs: numpy default_rng(seed=case index).standard_normal(shape)*std -> bf16 (RNE); "
-                   "outputs: oracle.quantize; digests are sha256 of the raw code / scale bytes"}
+                   "outputs: oracle.quantize (oracle.mx_quantize for the mx_ cases); digests are sha256 of "
+                   "the raw code / scale bytes"}
     for i, (name, shape, std, block, rnd, rht, sr_seed, rht_seed) in enumerate(CASES):
         x = bf16_bits_from_f32(np.random.default_rng(i).standard_normal(shape) * std)
         q = oracle.quantize(x, block, rnd, rht=rht, sr_seed=sr_seed, rht_seed=rht_seed)
@@ -49,6 +50,14 @@ def make():
                          s_dec=float(np.float32(q["s_dec"])).hex(),
                          codes_sha256=digest(q["codes"]), scales_sha256=digest(q["scales"]),
                          first_codes=q["codes"][0, :8].tolist(), first_scales=q["scales"][0, :4].tolist())
+    # MXFP4 (the comparison format): 1x32 blocks, UE8M0 scales, rows and the transposed operand
+    for j, (name, shape, std, col) in enumerate((("mx_row", (32, 96), 1.0, False), ("mx_col", (64, 48), 0.02, True))):
+        seed = len(CASES) + j
+        x = bf16_bits_from_f32(np.random.default_rng(seed).standard_normal(shape) * std)
+        q = oracle.mx_quantize(x, col=col)
+        out[name] = dict(shape=list(shape), std=std, col=col, seed=seed,
+                         codes_sha256=digest(q["codes"]), scales_sha256=digest(q["scales"]),
+                         first_codes=q["codes"][0, :8].tolist(), first_scales=q["scales"][0, :2].tolist())
     return out
 
 
