@@ -189,6 +189,7 @@ extern "C" nvfp4_status nvfp4_mx_quantize(const void* x, int32_t x_dtype, int64_
     const uintptr_t need = col ? 16 : 32;
     if ((reinterpret_cast<uintptr_t>(x) % need) != 0 || ((size_t)ldx * esz) % need != 0 || !aligned16(out->codes))
         return NVFP4_ERR_ALIGNMENT;
+    if (col && (R + mx::kColRows - 1) / mx::kColRows > 65535) return NVFP4_ERR_SHAPE;   // grid.y of the col kernel
     if (R == 0 || C == 0) return NVFP4_OK;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return NVFP4_ERR_CUDA;
@@ -211,7 +212,6 @@ extern "C" nvfp4_status nvfp4_mx_quantize(const void* x, int32_t x_dtype, int64_
     } else {
         // x walks the column tiles (neighbouring CTAs read neighbouring pieces of the same rows)
         const int64_t row_tiles = (R + mx::kColRows - 1) / mx::kColRows;
-        if (row_tiles > 65535) return NVFP4_ERR_SHAPE;
         const dim3 grid((unsigned)((C + mx::kColCols - 1) / mx::kColCols), (unsigned)row_tiles);
         if (x_dtype == NVFP4_BF16)
             mx::mx_col_kernel<uint16_t><<<grid, mx::kColCols, 0, stream>>>(

@@ -146,6 +146,9 @@ def test_mx_entry_points_reject_bad_arguments(lib):
     assert mxq(0x1000, lib.BF16, 32, 48, 48, 0, ctypes.byref(q48), None) == lib.ERR_SHAPE   # 32-element blocks
     assert mxq(0x1010, lib.BF16, 32, 64, 64, 0, ctypes.byref(q), None) == lib.ERR_ALIGNMENT  # 32-byte loads
     assert mxq(0x1000, lib.BF16, 32, 64, 64, 0, None, None) == lib.ERR_INVALID_ARG
+    big = 65536 * 64 + 32                                                    # x^T rows past the col grid
+    qt = lib.QTensorC(0x1000, 0x1000, None, None, None, None, 64, big)
+    assert mxq(0x1000, lib.BF16, big, 64, 64, 1, ctypes.byref(qt), None) == lib.ERR_SHAPE
     A = lib.QTensorC(0x1000, None, 0x1000, None, None, None, 128, 256)
     B = lib.QTensorC(0x1000, None, 0x1000, None, None, None, 256, 256)
     g = L.nvfp4_mx_gemm
