@@ -572,3 +572,29 @@ def test_mx_col_operand_is_the_transpose(oracle_mod):
     a = oracle_mod.mx_quantize(x, col=True)
     b = oracle_mod.mx_quantize(np.ascontiguousarray(x.T))
     assert np.array_equal(a["codes"], b["codes"]) and np.array_equal(a["scales"], b["scales"])
+
+
+def test_nvfp4_error_below_mxfp4_on_heavy_tailed_activations(oracle_mod):
+    """The direction of the page's format comparison at the quantizer level (no training):
+    on the heavy-tailed activations (Student-t(3), 1% of channels x50) the oracle's NVFP4
+    (1x16, E4M3 scales, FP32 tensor scale) dequantizes closer to the input than its MXFP4
+    (1x32, power-of-two scales); likewise on N(0, 1) data."""
+    import torch
+    from nvfp4_bit_quantized_gb300 import inputs
+    X = inputs.student_t((128, 512), 3, seed=3)
+    inputs.outlier_columns(X, 0.01, 50.0, seed=103)
+    bits = X.contiguous().view(torch.int16).numpy().view(np.uint16)
+    x = X.float().numpy().astype(np.float64)
+
+    def rel(d):
+        return float(np.linalg.norm(d - x) / np.linalg.norm(x))
+    e_nv = rel(oracle_mod.dequant(oracle_mod.quantize(bits, oracle_mod.ROW)))
+    e_mx = rel(oracle_mod.mx_dequant(oracle_mod.mx_quantize(bits)))
+    assert 0 < e_nv < e_mx, (e_nv, e_mx)
+    # the same inputs on a N(0, 1) tensor: the ordering does not hinge on the outliers
+    Y = inputs.normal((128, 512), 1.0, seed=4)
+    ybits = Y.contiguous().view(torch.int16).numpy().view(np.uint16)
+    y = Y.float().numpy().astype(np.float64)
+    e_nv_y = float(np.linalg.norm(oracle_mod.dequant(oracle_mod.quantize(ybits, oracle_mod.ROW)) - y) / np.linalg.norm(y))
+    e_mx_y = float(np.linalg.norm(oracle_mod.mx_dequant(oracle_mod.mx_quantize(ybits)) - y) / np.linalg.norm(y))
+    assert e_nv_y < e_mx_y, (e_nv_y, e_mx_y)
