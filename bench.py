@@ -314,13 +314,21 @@ def run_heavy(args):
     fp4, ref = full(), bf16()
     err = {n: round(((a.float() - b.float()).norm() / b.float().norm()).item(), 4)
            for n, a, b in zip(("fprop", "dgrad", "wgrad"), fp4, ref)}
+    # the RHT's effect on the Wgrad product alone: both operands RNE, with and without the transform
+    wq = {}
+    for rht in (True, False):
+        gt = nv.quantize(dY, nv.COL, nv.RNE, rht=rht, rht_seed=11, scales=False)
+        at = nv.quantize(X, nv.COL, nv.RNE, rht=rht, rht_seed=11, scales=False)
+        d = nv.gemm(gt, at, torch.bfloat16).float()
+        wq["rht" if rht else "no_rht"] = round(((d - ref[2].float()).norm() / ref[2].float().norm()).item(), 4)
     flop = 3 * 2.0 * Mh * Kh * Nh
     print(json.dumps({"config": "heavy_tailed_16384x4096x14336", "nvfp4_gemm_ms": round(t_g, 4),
                       "nvfp4_step_ms": round(t_f, 4), "bf16_cublas_ms": round(t_b, 4),
                       "speedup_gemm_only": round(t_b / t_g, 2), "speedup_with_quantization": round(t_b / t_f, 2),
                       "nvfp4_tflops_gemm": round(flop / (t_g * 1e-3) / 1e12, 1),
                       "bf16_tflops": round(flop / (t_b * 1e-3) / 1e12, 1),
-                      "rel_error_vs_bf16": err, "device_status": nv.status_query()}))
+                      "rel_error_vs_bf16": err, "wgrad_rne_rel_error_vs_bf16": wq,
+                      "device_status": nv.status_query()}))
 
 
 def run_yardstick(args):
