@@ -84,7 +84,7 @@ def measured_peaks():
 
 
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons sampled every 200 ms during the timed region."""
+    """nvidia-smi clocks and throttle reasons sampled every 100 ms during the timed region."""
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
@@ -96,7 +96,7 @@ class ClockSampler:
     def __enter__(self):
         try:
             self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
-                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
                                          stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except Exception:
             self.proc = None
@@ -105,8 +105,7 @@ class ClockSampler:
     def __exit__(self, *a):
         self.lines = []
         if self.proc is not None:
-            time.sleep(0.25)
-            self.proc.terminate()
+            self.proc.terminate()                 # no readings after the timed region (an idle GPU)
             try:
                 out, _ = self.proc.communicate(timeout=5)
             except Exception:
@@ -669,13 +668,14 @@ def run_ours(args):
 
 # --------------------------------------------------------------------------- oracle (CPU) arm
 
-def oracle_sample(budget_s: float = 15.0, reps: int | None = None):
+def oracle_sample(budget_s: float = 15.0, reps: int | None = None, rotate: bool = False):
     """Times the CPU oracle on a bounded sample of the step: one output block of
     each GEMM with the full contraction length of the workload, the oracle
     quantizing the operand rows that block needs:
       Fprop  64x128 block of Y,  K = 5120   (X rows 1x16 RNE, W rows 16x16)
       Dgrad  64x128 block of dX, N = 20480  (dY rows 1x16 SR, W^T rows 16x16)
       Wgrad 128x64  block of dW, M = 8192   (dY^T, X^T columns with the RHT; SR / RNE)
+    With ``rotate`` a rep is one of the three blocks in turn (a third of the work).
     value = sampled GEMM flops / oracle time (single-threaded C)."""
     import numpy as np
     import oracle
@@ -692,22 +692,28 @@ def oracle_sample(budget_s: float = 15.0, reps: int | None = None):
     wts = bits(inputs.normal((nb, N), 0.02, 3))          # W^T rows (= W columns)
     dyc = bits(inputs.normal((M, nb), 1e-3, 4))          # dY columns
     xc = bits(inputs.normal((M, mb), 1.0, 5))            # X columns
-    flops_rep = 2.0 * mb * nb * (K + N + M)
-    n, t0 = 0, time.perf_counter()
+    deq, gemm = oracle.dequant, oracle.gemm_f64
+    blocks = [
+        (lambda: gemm(deq(oracle.quantize(xs, oracle.ROW)), deq(oracle.quantize(ws, oracle.TILE16))), K),
+        (lambda: gemm(deq(oracle.quantize(dys, oracle.ROW, oracle.SR, sr_seed=7)),
+                      deq(oracle.quantize(wts, oracle.TILE16))), N),
+        (lambda: gemm(deq(oracle.quantize(dyc, oracle.COL, oracle.SR, rht=True, sr_seed=7, rht_seed=11)),
+                      deq(oracle.quantize(xc, oracle.COL, oracle.RNE, rht=True, rht_seed=11))), M),
+    ]
+    n, flops, t0 = 0, 0.0, time.perf_counter()
     while True:
-        deq, gemm = oracle.dequant, oracle.gemm_f64
-        gemm(deq(oracle.quantize(xs, oracle.ROW)), deq(oracle.quantize(ws, oracle.TILE16)))
-        gemm(deq(oracle.quantize(dys, oracle.ROW, oracle.SR, sr_seed=7)), deq(oracle.quantize(wts, oracle.TILE16)))
-        gemm(deq(oracle.quantize(dyc, oracle.COL, oracle.SR, rht=True, sr_seed=7, rht_seed=11)),
-             deq(oracle.quantize(xc, oracle.COL, oracle.RNE, rht=True, rht_seed=11)))
+        for fn, klen in (blocks[n % 3:n % 3 + 1] if rotate else blocks):
+            fn()
+            flops += 2.0 * mb * nb * klen
         n += 1
         el = time.perf_counter() - t0
         if (reps is not None and n >= reps) or (reps is None and el >= budget_s):
             break
-    return {"value": round(n * flops_rep / el / 1e12, 6), "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
-            "sample": f"{n} x three output blocks (Fprop 64x128 K={K}, Dgrad 64x128 K={N}, Wgrad 128x64 K={M}) "
+    what = "one output block in turn of" if rotate else "three output blocks"
+    return {"value": round(flops / el / 1e12, 6), "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
+            "sample": f"{n} x {what} (Fprop 64x128 K={K}, Dgrad 64x128 K={N}, Wgrad 128x64 K={M}) "
                       f"with their operand rows quantized by the oracle; single-threaded C; {el:.1f} s",
-            "flops_per_rep": flops_rep, "seconds": round(el, 3)}
+            "flops_per_rep": round(flops / n), "seconds": round(el, 3)}
 
 
 def run_reference(args):
@@ -716,10 +722,11 @@ def run_reference(args):
         return
     import oracle
     oracle.build()
+    # a step is one of the three sampled GEMM blocks in turn, so K steps take ~0.15 K s
     for _ in range(args.warmup):
-        oracle_sample(reps=1)
+        oracle_sample(reps=1, rotate=True)
     t0 = time.perf_counter()
-    r = oracle_sample(reps=args.steps)
+    r = oracle_sample(reps=args.steps, rotate=True)
     el = time.perf_counter() - t0
     value = r["value"]
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
@@ -735,8 +742,10 @@ def run_reference(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=400,
+                    help="timed steps (the default, ~0.5 s of the headline step, lets the clock sampler "
+                         "take several readings under load)")
+    ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
