@@ -733,7 +733,7 @@ def run_reference(args):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(el / args.steps * 1e3, 2),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64 (oracle)",
             "data": "synthetic", "config": {"workload": WORKLOAD, "M": M, "K": K, "N": N,
-                                            "sample": "per step: one output block of each GEMM, full contraction"},
+                                            "sample": "per step: one output block of one GEMM (Fprop, Dgrad, Wgrad in turn), full contraction"},
             "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": 1, "kind": "oracle", "sample": r["sample"]},
             "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line))
