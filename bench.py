@@ -208,10 +208,14 @@ def run_sweep(args):
                                          transpose=(block == nv.TILE16))
                 ms = _timed(fn, max(3, args.steps), args.warmup)
                 gbs = R * C * bpe / (ms * 1e-3) / 1e9
+                # the one-read lower bound: the input read once plus the outputs (2D: W and W^T)
+                one = 2 + (bpe - 4)
                 print(json.dumps({"config": "quantizer_sweep", "mode": name, "R": R, "C": C, "elements": R * C,
                                   "log2_elements": p, "ms": round(ms, 4), "GB/s": round(gbs, 1),
                                   "hbm_frac": round(gbs / peaks["hbm_gbs"], 3), "peak_source": src,
-                                  "bytes_per_element": bpe, "inputs_exceed_l2": R * C * 2 > 129e6}))
+                                  "bytes_per_element": bpe, "inputs_exceed_l2": R * C * 2 > 129e6,
+                                  "one_read_bytes_per_element": one,
+                                  "one_read_frac": round(R * C * one / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 3)}))
             del x
             torch.cuda.empty_cache()
 
