@@ -212,6 +212,8 @@ NVFP4_API nvfp4_status nvfp4_gemm(const nvfp4_qtensor* A, const nvfp4_qtensor* B
  * bit for bit nvfp4_gemm (CTA-pair kernel, BF16) followed by nvfp4_sqrelu_backward, without
  * writing and re-reading dA.  H and D: BF16 [M, N], row pitches ldh, ldd >= N elements,
  * bases and pitches 16-byte aligned (else NVFP4_ERR_ALIGNMENT).  A, B as for nvfp4_gemm.
+ * Not on the page (its MLP activation is unspecified): a fusion of two steps of the MLP
+ * block built around the page's Dgrad GEMM [page ¶2, ¶3].
  */
 NVFP4_API nvfp4_status nvfp4_gemm_sqrelu_bwd(const nvfp4_qtensor* A, const nvfp4_qtensor* B, const void* H,
                                              int64_t ldh, void* D, int64_t ldd, uint32_t* dev_status,
@@ -241,7 +243,9 @@ NVFP4_API size_t nvfp4_sqrelu_maxima_bytes(void);
  * memory, 4-byte aligned; contents on entry ignored).  nvfp4_quantize_dual_sqrelu_premax
  * then needs no amax pass over H.  H: BF16 [M, N], pitch ldh >= N, base and pitch 16-byte
  * aligned; M % 16 == 0 and N % 16 == 0.  A, B as for nvfp4_gemm.  NVFP4_ERR_UNSUPPORTED on
- * a GPU with more than 152 multiprocessors (one partial per epilogue warp).
+ * a GPU with more than 152 multiprocessors (one partial per epilogue warp).  Not on the
+ * page: the tensor amax of the next quantization [page ¶2: the FP32 per-tensor scale]
+ * taken where the tensor is produced instead of in a pass of its own.
  */
 NVFP4_API nvfp4_status nvfp4_gemm_sqrelu_maxima(const nvfp4_qtensor* A, const nvfp4_qtensor* B, void* H,
                                                 int64_t ldh, uint64_t rht_seed, uint32_t* maxima,
