@@ -30,6 +30,7 @@ sys.path.insert(0, ROOT)
 M, K, N = 8192, 5120, 20480
 METRIC = "NVFP4 GEMM TFLOPS (Fprop/Dgrad/Wgrad at 8192x5120x20480); quantize GB/s"
 WORKLOAD = "ffn_up_8192x5120x20480"
+GEMM_KERNEL = "gemm_nvfp4_pair_kernel"
 FP4_PER_BF16 = 13.5 / 2.25          # nominal dense FP4 : BF16 tensor rate on GB300
 
 
@@ -84,53 +85,165 @@ def measured_peaks():
 
 
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons sampled every 100 ms during the timed region."""
+    """SM clock, power and clock-event (throttle) reasons of the GPU, read through NVML
+    (read-only queries) every ~2 ms by a background thread while armed, so even a 25 ms
+    timed region gets a dozen readings; falls back to ``nvidia-smi -lms 10`` when NVML
+    cannot be loaded.  ``summary()`` covers the samples taken since the last ``take()``."""
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    # NVML clock-event reason bits (nvml.h)
+    REASON_BITS = {"sw_power_cap": 0x4, "hw_slowdown": 0x8, "sw_thermal_slowdown": 0x20,
+                   "hw_thermal_slowdown": 0x40, "hw_power_brake_slowdown": 0x80}
 
-    def __init__(self, gpu_index: int):
-        self.gpu = gpu_index
-        self.proc = None
+    def __init__(self, cuda_index: int, interval_s: float = 0.002):
+        import threading
+        self.cuda_index = cuda_index
+        self.interval = interval_s
+        self.samples = []                  # (sm_mhz, power_w, reasons bitmask)
+        self.max_mhz = None
+        self.source = None
+        self._armed = threading.Event()
+        self._stop = threading.Event()
+        self._lock = threading.Lock()
+        self._thread = None
+        self._smi = None
+        self._nvml = self._open_nvml()
+
+    def _open_nvml(self):
+        import ctypes
+        try:
+            lib = ctypes.CDLL("libnvidia-ml.so.1")
+            if lib.nvmlInit_v2() != 0:
+                return None
+            h = ctypes.c_void_p()
+            ok = False
+            try:
+                import torch
+                u = str(torch.cuda.get_device_properties(self.cuda_index).uuid)
+                u = u if u.startswith("GPU-") else "GPU-" + u
+                ok = lib.nvmlDeviceGetHandleByUUID(u.encode(), ctypes.byref(h)) == 0
+            except Exception:
+                ok = False
+            if not ok and not os.environ.get("CUDA_VISIBLE_DEVICES"):
+                ok = lib.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(self.cuda_index), ctypes.byref(h)) == 0
+            if not ok:
+                return None
+            mx = ctypes.c_uint()
+            if lib.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx)) == 0:       # NVML_CLOCK_SM
+                self.max_mhz = float(mx.value)
+            self._reasons_fn = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+                getattr(lib, "nvmlDeviceGetCurrentClocksThrottleReasons")
+            self._h = h
+            self.source = "nvml"
+            return lib
+        except Exception:
+            return None
+
+    def _read_nvml(self):
+        import ctypes
+        c, p, r = ctypes.c_uint(), ctypes.c_uint(), ctypes.c_ulonglong()
+        lib = self._nvml
+        if lib.nvmlDeviceGetClockInfo(self._h, 1, ctypes.byref(c)) != 0:
+            return None
+        pw = p.value / 1000.0 if lib.nvmlDeviceGetPowerUsage(self._h, ctypes.byref(p)) == 0 else None
+        rs = r.value if self._reasons_fn(self._h, ctypes.byref(r)) == 0 else 0
+        return (float(c.value), pw, int(rs))
+
+    def _loop(self):
+        import time as _t
+        while not self._stop.is_set():
+            if not self._armed.wait(0.05):
+                continue
+            s = self._read_nvml()
+            if s is not None:
+                with self._lock:
+                    self.samples.append(s)
+            _t.sleep(self.interval)
 
     def __enter__(self):
-        try:
-            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
-                                          "--format=csv,noheader,nounits", "-lms", "100"],
-                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
-        except Exception:
-            self.proc = None
+        import threading
+        if self._nvml is not None:
+            self._thread = threading.Thread(target=self._loop, daemon=True)
+            self._thread.start()
         return self
 
     def __exit__(self, *a):
-        self.lines = []
-        if self.proc is not None:
-            self.proc.terminate()                 # no readings after the timed region (an idle GPU)
-            try:
-                out, _ = self.proc.communicate(timeout=5)
-            except Exception:
-                self.proc.kill()
-                out = ""
-            self.lines = [l for l in out.splitlines() if l.strip()]
+        self._stop.set()
+        self._armed.set()
+        if self._thread is not None:
+            self._thread.join(timeout=2)
+        if self._smi is not None:
+            self._smi_stop()
 
-    def summary(self):
-        sm, mx, reasons = [], None, set()
+    # -- timed regions ----------------------------------------------------------------
+    def arm(self):
+        if self._nvml is not None:
+            self._armed.set()
+        else:
+            self._smi_start()
+
+    def disarm(self):
+        if self._nvml is not None:
+            self._armed.clear()
+        else:
+            self._smi_stop()
+
+    def _smi_start(self):
+        try:
+            self._smi = subprocess.Popen(["nvidia-smi", f"--id={self.cuda_index}", f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "10"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.source = "nvidia-smi"
+        except Exception:
+            self._smi = None
+
+    def _smi_stop(self):
+        if self._smi is None:
+            return
+        self._smi.terminate()
+        try:
+            out, _ = self._smi.communicate(timeout=5)
+        except Exception:
+            self._smi.kill()
+            out = ""
+        self._smi = None
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for l in getattr(self, "lines", []):
+        for l in out.splitlines():
             f = [x.strip() for x in l.split(",")]
             if len(f) < 9:
                 continue
             try:
-                sm.append(float(f[1]))
-                mx = float(f[2])
+                sm, mx = float(f[1]), float(f[2])
             except ValueError:
                 continue
+            self.max_mhz = mx
+            bits = 0
             for n, v in zip(names, f[5:9]):
                 if v.lower() == "active":
-                    reasons.add(n)
-        if not sm:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
+                    bits |= self.REASON_BITS[n]
+            pw = None
+            try:
+                pw = float(f[3])
+            except ValueError:
+                pass
+            with self._lock:
+                self.samples.append((sm, pw, bits))
+
+    def take(self):
+        """Summary of the samples since the last take(), which it clears."""
+        with self._lock:
+            smp, self.samples = self.samples, []
+        if not smp:
+            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": ["unsampled"], "samples": 0,
+                    "source": self.source}
+        reasons = sorted({n for n, b in self.REASON_BITS.items() for _, _, r in smp if r & b})
+        pw = [p for _, p, _ in smp if p is not None]
+        return {"sm_mhz": statistics.median(s for s, _, _ in smp), "sm_min_mhz": min(s for s, _, _ in smp),
+                "sm_max_mhz": self.max_mhz, "reasons": reasons, "samples": len(smp),
+                "power_w_max": round(max(pw), 1) if pw else None, "source": self.source}
+
+    summary = take
 
 
 # --------------------------------------------------------------------------- our arm
@@ -163,29 +276,46 @@ def run_kernel_only(args):
         work()
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record()
-    for _ in range(args.steps):
-        work()
-    e1.record()
-    torch.cuda.synchronize()
+    with ClockSampler(0) as clk:
+        clk.arm()
+        e0.record()
+        for _ in range(args.steps):
+            work()
+        e1.record()
+        torch.cuda.synchronize()
+        clk.disarm()
+        clocks = clk.take()
     ms = e0.elapsed_time(e1) / args.steps
     print(json.dumps({"kernel": args.kernel, "value": round(per / (ms * 1e-3), 1), "unit": unit,
                       "ms_per_iter": round(ms, 4), "steps": args.steps, "device_status": nv.status_query(),
-                      "config": {"workload": WORKLOAD, "M": M, "K": K, "N": N}}))
+                      "clocks": clocks, "config": {"workload": WORKLOAD, "M": M, "K": K, "N": N}}))
+
+
+_CLK = None          # the ClockSampler of a --config run: armed inside every timed region
+
+
+def _clocks():
+    """Clock summary of the timed regions since the last JSON line (None without a sampler)."""
+    return _CLK.take() if _CLK is not None else None
 
 
 def _timed(fn, steps: int, warmup: int) -> float:
-    """ms per call of fn (CUDA events on the current stream, after warm-up)."""
+    """ms per call of fn (CUDA events on the current stream, after warm-up); the clock
+    sampler, when there is one, is armed for the timed region only."""
     import torch
     for _ in range(warmup):
         fn()
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if _CLK is not None:
+        _CLK.arm()
     e0.record()
     for _ in range(steps):
         fn()
     e1.record()
     torch.cuda.synchronize()
+    if _CLK is not None:
+        _CLK.disarm()
     return e0.elapsed_time(e1) / steps
 
 
@@ -215,7 +345,8 @@ def run_sweep(args):
                                   "hbm_frac": round(gbs / peaks["hbm_gbs"], 3), "peak_source": src,
                                   "bytes_per_element": bpe, "inputs_exceed_l2": R * C * 2 > 129e6,
                                   "one_read_bytes_per_element": one,
-                                  "one_read_frac": round(R * C * one / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 3)}))
+                                  "one_read_frac": round(R * C * one / (ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 3),
+                                  "clocks": _clocks()}))
             del x
             torch.cuda.empty_cache()
 
@@ -272,11 +403,15 @@ def run_mlp(args):
     torch.cuda.synchronize()
     evs = [[[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in names] for _ in range(args.steps)]
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if _CLK is not None:
+        _CLK.arm()
     e0.record(stream)
     for i in range(args.steps):
         step(args.warmup + i, evs[i])
     e1.record(stream)
     torch.cuda.synchronize()
+    if _CLK is not None:
+        _CLK.disarm()
     ms = e0.elapsed_time(e1) / args.steps
     flop = 2.0 * T * d * f
     per = {n: flop / (statistics.mean(evs[i][k][0].elapsed_time(evs[i][k][1]) for i in range(args.steps)) * 1e-3) / 1e12
@@ -284,7 +419,8 @@ def run_mlp(args):
     print(json.dumps({"config": "mlp_block_16384x5120x20480_sqrelu", "ms_per_step": round(ms, 4),
                       "tflops_step": round(6 * flop / (ms * 1e-3) / 1e12, 1),
                       "gemm_tflops": {k: round(v, 1) for k, v in per.items()},
-                      "launches_per_step": 2 * 2 + 2 * 3 + 2 * 2 + 6, "device_status": nv.status_query()}))
+                      "launches_per_step": 2 * 2 + 2 * 3 + 2 * 2 + 6, "clocks": _clocks(),
+                      "device_status": nv.status_query()}))
 
 
 def run_heavy(args):
@@ -314,6 +450,7 @@ def run_heavy(args):
         return X @ W.t(), dY @ W, dY.t() @ X
 
     t_g, t_f, t_b = (_timed(fn, args.steps, args.warmup) for fn in (gemms, full, bf16))
+    clk = _clocks()
     fp4, ref = full(), bf16()
     err = {n: round(((a.float() - b.float()).norm() / b.float().norm()).item(), 4)
            for n, a, b in zip(("fprop", "dgrad", "wgrad"), fp4, ref)}
@@ -331,7 +468,7 @@ def run_heavy(args):
                       "nvfp4_tflops_gemm": round(flop / (t_g * 1e-3) / 1e12, 1),
                       "bf16_tflops": round(flop / (t_b * 1e-3) / 1e12, 1),
                       "rel_error_vs_bf16": err, "wgrad_rne_rel_error_vs_bf16": wq,
-                      "device_status": nv.status_query()}))
+                      "clocks": clk, "device_status": nv.status_query()}))
 
 
 def run_yardstick(args):
@@ -387,6 +524,7 @@ def run_yardstick(args):
             out["notes"].append(f"fp8 {name}: {type(e).__name__}: {str(e)[:160]}")
         del a, b, qa, qb, d
         torch.cuda.empty_cache()
+    out["clocks"] = _clocks()
     out["device_status"] = nv.status_query()
     print(json.dumps(out))
 
@@ -435,6 +573,7 @@ def run_mx(args):
         gbs = dY.numel() * bpe / (t * 1e-3) / 1e9
         out["mx_quantize"][f"{mode}_{M}x{N}"] = {"ms": round(t, 4), "GB/s": round(gbs, 1),
                                                 "hbm_frac": round(gbs / peaks["hbm_gbs"], 3)}
+    out["clocks"] = _clocks()
     del X, W, dY
     torch.cuda.empty_cache()
     Mh, Kh, Nh = 16384, 4096, 14336
@@ -473,9 +612,15 @@ def run_ours(args):
     if args.kernel != "step":
         return run_kernel_only(args)
     if args.config != "ffn_up":
+        global _CLK
         torch.cuda.set_device(0)
-        return {"sweep": run_sweep, "mlp": run_mlp, "heavy": run_heavy, "yardstick": run_yardstick,
-                "mxfp4": run_mx}[args.config](args)
+        with ClockSampler(0) as clk:
+            _CLK = clk
+            try:
+                return {"sweep": run_sweep, "mlp": run_mlp, "heavy": run_heavy, "yardstick": run_yardstick,
+                        "mxfp4": run_mx}[args.config](args)
+            finally:
+                _CLK = None
 
     rank, world, local = env_rank()
     torch.cuda.set_device(local)
@@ -525,11 +670,14 @@ def run_ours(args):
         dist.barrier()
     torch.cuda.synchronize()
     with ClockSampler(local) as clk:
+        clk.arm()
         t0.record(stream)
         for i in range(args.steps):
             step(args.warmup + i, evs[i])
         t1.record(stream)
         torch.cuda.synchronize()
+        clk.disarm()
+        clocks = clk.take()
     if world > 1:
         dist.barrier()
     ms_total = max_over_ranks(t0.elapsed_time(t1), world, dev)
@@ -553,8 +701,16 @@ def run_ours(args):
     quant_gbs = {k: qbytes[k] / (per[k] * 1e-3) / 1e9 for k in qbytes}
     quant_ms = sum(per[k] for k in qbytes)
     peaks, peak_src = measured_peaks()
-    fp4_peak = peaks["bf16_tflops_sustained"] * FP4_PER_BF16
+    # The timed region is a short burst (tens of ms at the maximum SM clock), so the burst
+    # bf16 figure applies; FP4 dense peak = that x the nominal FP4 : BF16 rate ratio.
+    fp4_peak = peaks["bf16_tflops"] * FP4_PER_BF16
     achieved = 2.0 * M * N * K / (gemm_ms * 1e-3) / 1e12
+    # A second, hardware figure: ncu's sm__pipe_tensor_cycles_active counts 100 % at
+    # 16384 FP4 MACs (32768 flop) per SM per cycle, so at the sampled median SM clock the
+    # tensor pipes of all SMs top out at this rate.
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    pipe_mhz = clocks.get("sm_mhz") or peaks.get("sm_max_mhz", 2070.0)
+    pipe_ceiling = sms * 32768 * pipe_mhz * 1e6 / 1e12
 
     # End to end through the public API with host buffers: every step copies its inputs in
     # from pinned host memory, runs the layer and copies its results out.  Three streams and
@@ -654,8 +810,12 @@ def run_ours(args):
         "quantize_ms_per_step": round(quant_ms, 4),
         "roofline": {"bound": "tensor", "achieved": round(achieved, 1), "peak": round(fp4_peak, 1),
                      "unit": "TFLOP/s", "frac": round(achieved / fp4_peak, 4), "traffic": gemm_traffic_bytes(),
-                     "kernel": "gemm_nvfp4_pair_kernel",
-                     "peak_source": f"{peak_src} bf16 sustained x {FP4_PER_BF16:g} (nominal dense FP4:BF16)"},
+                     "kernel": GEMM_KERNEL,
+                     "peak_source": f"{peak_src} bf16 burst x {FP4_PER_BF16:g} (nominal dense FP4:BF16)",
+                     "tensor_pipe_ceiling": {"value": round(pipe_ceiling, 1), "unit": "TFLOP/s",
+                                             "frac": round(achieved / pipe_ceiling, 4),
+                                             "basis": f"{sms} SMs x 32768 FP4 flop/cycle (ncu tensor-pipe 100 %) "
+                                                      f"x {pipe_mhz:g} MHz (median sampled SM clock)"}},
         "quantize_roofline": {"bound": "hbm", "achieved": round(sum(qbytes.values()) / (quant_ms * 1e-3) / 1e9, 1),
                               "peak": peaks["hbm_gbs"], "unit": "GB/s",
                               "frac": round(sum(qbytes.values()) / (quant_ms * 1e-3) / 1e9 / peaks["hbm_gbs"], 4)},
@@ -663,7 +823,7 @@ def run_ours(args):
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
                 "overlap": "H2D copies, the layer step and D2H copies on three streams, two device input sets"},
         "gpu_launches": launches_per_step * args.steps,
-        "clocks": clk.summary(),
+        "clocks": clocks,
         "device_status": status,
         "cpu_baseline": cpu,
     }

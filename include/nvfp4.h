@@ -181,9 +181,11 @@ NVFP4_API nvfp4_status nvfp4_quantize_dual_sqrelu(const void* h, int32_t h_dtype
  *   loads the library until the process exits.  Calls needing more scratch than
  *   that are rejected with NVFP4_ERR_WORKSPACE (the amax grid is capped at 4096
  *   CTAs, so no tensor size needs more).
- *   Set-up: the first call on a device looks up the array's device address
- *   (cudaGetSymbolAddress) with that device current and caches it; make that
- *   first call before any stream capture.
+ *   Set-up: the first call in a CUDA context (normally a device's primary
+ *   context) looks up the array's device address there (cudaGetSymbolAddress)
+ *   and caches it under that context's id; make that first call before any
+ *   stream capture.  A context created later (after cudaDeviceReset, say) gets
+ *   its own lookup on its first call.
  *   Sharing: every call uses the same array; each amax CTA overwrites its own
  *   slot before the encode pass reads it, so nothing needs clearing between
  *   calls, but calls that overlap on the GPU (different streams, concurrently)
@@ -224,57 +226,67 @@ NVFP4_API nvfp4_status nvfp4_gemm_sqrelu_bwd(const nvfp4_qtensor* A, const nvfp4
  * tensor maxima the dual quantization of its output dH needs (max|dH| and max|RHT(dH)| along
  * rows with the RHT sign vector of rht_seed), as nvfp4_gemm_sqrelu_maxima does for relu(H)^2;
  * nvfp4_quantize_dual_premax then quantizes dH without an amax read.  dH is identical to
- * nvfp4_gemm_sqrelu_bwd's.  Additional rules: maxima non-NULL (nvfp4_sqrelu_maxima_bytes(),
- * 4-byte aligned), M % 16 == 0 and N % 16 == 0.
+ * nvfp4_gemm_sqrelu_bwd's.  Additional rules: maxima non-NULL, 4-byte aligned, maxima_bytes at
+ * least nvfp4_sqrelu_maxima_bytes(current device) (else NVFP4_ERR_WORKSPACE); M % 16 == 0 and
+ * N % 16 == 0.
  */
 NVFP4_API nvfp4_status nvfp4_gemm_sqrelu_bwd_maxima(const nvfp4_qtensor* A, const nvfp4_qtensor* B, const void* H,
                                                     int64_t ldh, void* D, int64_t ldd, uint64_t rht_seed,
-                                                    uint32_t* maxima, uint32_t* dev_status, void* stream);
+                                                    uint32_t* maxima, size_t maxima_bytes, uint32_t* dev_status,
+                                                    void* stream);
 
-/* Bytes of the partial-maxima buffer nvfp4_gemm_sqrelu_maxima writes (device memory). */
-NVFP4_API size_t nvfp4_sqrelu_maxima_bytes(void);
+/*
+ * Bytes of the partial-maxima buffer the *_maxima GEMMs write on CUDA device `device`: two
+ * halves (|x|, then |RHT(x)| / 4) of one uint32 partial per epilogue warp, four warps per CTA
+ * and at most one CTA per multiprocessor, so 2 * 4 * (multiprocessor count) * 4 bytes.  0 if the
+ * device cannot be queried.  A buffer of B bytes is read as two halves of B / 8 partials.
+ */
+NVFP4_API size_t nvfp4_sqrelu_maxima_bytes(int32_t device);
 
 /*
  * nvfp4_gemm_sqrelu_maxima -- the first GEMM of a squared-ReLU MLP with the next
  * quantization's tensor maxima in its epilogue: H = bf16(s_dec(A) s_dec(B) sum_k qA qB),
  * stored exactly as nvfp4_gemm (CTA-pair kernel, BF16) stores it, and, for A = relu(H)^2
  * as nvfp4_quantize_dual_sqrelu forms it, max|A| and max|RHT(A)| along rows (the RHT sign
- * vector of rht_seed) as partial maxima in `maxima` (nvfp4_sqrelu_maxima_bytes() of device
- * memory, 4-byte aligned; contents on entry ignored).  nvfp4_quantize_dual_sqrelu_premax
+ * vector of rht_seed) as partial maxima in `maxima` (maxima_bytes of device memory, at least
+ * nvfp4_sqrelu_maxima_bytes(current device), else NVFP4_ERR_WORKSPACE; 4-byte aligned;
+ * contents on entry ignored: the call writes every partial).  nvfp4_quantize_dual_sqrelu_premax
  * then needs no amax pass over H.  H: BF16 [M, N], pitch ldh >= N, base and pitch 16-byte
- * aligned; M % 16 == 0 and N % 16 == 0.  A, B as for nvfp4_gemm.  NVFP4_ERR_UNSUPPORTED on
- * a GPU with more than 152 multiprocessors (one partial per epilogue warp).  Not on the
- * page: the tensor amax of the next quantization [page ¶2: the FP32 per-tensor scale]
- * taken where the tensor is produced instead of in a pass of its own.
+ * aligned; M % 16 == 0 and N % 16 == 0.  A, B as for nvfp4_gemm.  Not on the page: the tensor
+ * amax of the next quantization [page ¶2: the FP32 per-tensor scale] taken where the tensor is
+ * produced instead of in a pass of its own.
  */
 NVFP4_API nvfp4_status nvfp4_gemm_sqrelu_maxima(const nvfp4_qtensor* A, const nvfp4_qtensor* B, void* H,
                                                 int64_t ldh, uint64_t rht_seed, uint32_t* maxima,
-                                                uint32_t* dev_status, void* stream);
+                                                size_t maxima_bytes, uint32_t* dev_status, void* stream);
 
 /*
  * nvfp4_quantize_dual_sqrelu_premax -- nvfp4_quantize_dual_sqrelu of H using the maxima that
  * nvfp4_gemm_sqrelu_maxima left for this same H (with rht_seed == params_col->rht_seed when
  * params_col->rht is set): only the two encode passes run, and the results are identical to
  * nvfp4_quantize_dual_sqrelu's.  BF16 H only (else NVFP4_ERR_UNSUPPORTED); no workspace;
- * other arguments as for nvfp4_quantize_dual_sqrelu.
+ * maxima_bytes is the size the GEMM was given (two halves of maxima_bytes / 8 partials;
+ * NVFP4_ERR_WORKSPACE if that is 0); other arguments as for nvfp4_quantize_dual_sqrelu.
  */
 NVFP4_API nvfp4_status nvfp4_quantize_dual_sqrelu_premax(const void* h, int32_t h_dtype, int64_t R, int64_t C,
                                                          int64_t ldh, const nvfp4_qparams* params_row,
                                                          const nvfp4_qtensor* out_row,
                                                          const nvfp4_qparams* params_col,
                                                          const nvfp4_qtensor* out_col, const uint32_t* maxima,
-                                                         uint32_t* dev_status, void* stream);
+                                                         size_t maxima_bytes, uint32_t* dev_status, void* stream);
 
 /*
  * nvfp4_quantize_dual_premax -- nvfp4_quantize_dual of x using the maxima that
  * nvfp4_gemm_sqrelu_bwd_maxima left for this same x (rht_seed == params_col->rht_seed when
  * params_col->rht is set): only the two encode passes run; results identical to
- * nvfp4_quantize_dual's.  BF16 x only (else NVFP4_ERR_UNSUPPORTED); no workspace.
+ * nvfp4_quantize_dual's.  BF16 x only (else NVFP4_ERR_UNSUPPORTED); no workspace; maxima_bytes
+ * as for nvfp4_quantize_dual_sqrelu_premax.
  */
 NVFP4_API nvfp4_status nvfp4_quantize_dual_premax(const void* x, int32_t x_dtype, int64_t R, int64_t C, int64_t ldx,
                                                   const nvfp4_qparams* params_row, const nvfp4_qtensor* out_row,
                                                   const nvfp4_qparams* params_col, const nvfp4_qtensor* out_col,
-                                                  const uint32_t* maxima, uint32_t* dev_status, void* stream);
+                                                  const uint32_t* maxima, size_t maxima_bytes, uint32_t* dev_status,
+                                                  void* stream);
 
 /*
  * MXFP4 -- the earlier 4-bit microscaling format the page compares NVFP4 with

@@ -92,11 +92,11 @@ def lib():
             "nvfp4_mx_quantize": (I32, [P, I32, I64, I64, I64, I32, QT, P]),
             "nvfp4_mx_gemm": (I32, [QT, QT, P, I32, I64, P, P]),
             "nvfp4_gemm_sqrelu_bwd": (I32, [QT, QT, P, I64, P, I64, P, P]),
-            "nvfp4_sqrelu_maxima_bytes": (SZ, []),
-            "nvfp4_gemm_sqrelu_maxima": (I32, [QT, QT, P, I64, U64, P, P, P]),
-            "nvfp4_quantize_dual_sqrelu_premax": (I32, [P, I32, I64, I64, I64, QP, QT, QP, QT, P, P, P]),
-            "nvfp4_gemm_sqrelu_bwd_maxima": (I32, [QT, QT, P, I64, P, I64, U64, P, P, P]),
-            "nvfp4_quantize_dual_premax": (I32, [P, I32, I64, I64, I64, QP, QT, QP, QT, P, P, P]),
+            "nvfp4_sqrelu_maxima_bytes": (SZ, [I32]),
+            "nvfp4_gemm_sqrelu_maxima": (I32, [QT, QT, P, I64, U64, P, SZ, P, P]),
+            "nvfp4_quantize_dual_sqrelu_premax": (I32, [P, I32, I64, I64, I64, QP, QT, QP, QT, P, SZ, P, P]),
+            "nvfp4_gemm_sqrelu_bwd_maxima": (I32, [QT, QT, P, I64, P, I64, U64, P, SZ, P, P]),
+            "nvfp4_quantize_dual_premax": (I32, [P, I32, I64, I64, I64, QP, QT, QP, QT, P, SZ, P, P]),
         }
         for name, (res, args) in sigs.items():
             fn = getattr(L, name)

@@ -173,7 +173,7 @@ def quantize_dual(x: torch.Tensor, row_round: int = L.RNE, col_round: int = L.RN
     if maxima is not None:
         fn = lib.nvfp4_quantize_dual_sqrelu_premax if pre == "sqrelu" else lib.nvfp4_quantize_dual_premax
         st = fn(_ptr(x), _DT[x.dtype], R, C, ld, ctypes.byref(pr), ctypes.byref(a), ctypes.byref(pc), ctypes.byref(b),
-                _ptr(maxima), dev_status(x.device).data_ptr(), _stream())
+                _ptr(maxima), maxima.numel() * maxima.element_size(), dev_status(x.device).data_ptr(), _stream())
         L.check(st, "nvfp4_quantize_dual_sqrelu_premax" if pre else "nvfp4_quantize_dual_premax")
         return qr, qc
     fn = lib.nvfp4_quantize_dual_sqrelu if pre == "sqrelu" else lib.nvfp4_quantize_dual
@@ -252,6 +252,14 @@ def mx_gemm(A: MXTensor, B: MXTensor, out: Optional[torch.Tensor] = None) -> tor
     return out
 
 
+def _maxima_buffer(device) -> torch.Tensor:
+    """A partial-maxima buffer for the *_maxima GEMMs on ``device`` (sized by its SM count)."""
+    nbytes = int(L.lib().nvfp4_sqrelu_maxima_bytes(torch.device(device).index))
+    if nbytes == 0:
+        raise NVFP4Error(L.ERR_CUDA, "cannot size the maxima buffer for this device")
+    return torch.empty(nbytes // 4, dtype=torch.int32, device=device)
+
+
 def gemm_sqrelu_maxima(A: QTensor, B: QTensor, rht_seed: int = 0, out: Optional[torch.Tensor] = None):
     """H = dequant(A) . dequant(B)^T in bf16 (as ``gemm`` stores it), plus the partial tensor
     maxima of relu(H)^2 that ``quantize_dual(H, ..., pre="sqrelu", maxima=m)`` needs, computed
@@ -261,10 +269,11 @@ def gemm_sqrelu_maxima(A: QTensor, B: QTensor, rht_seed: int = 0, out: Optional[
         out = torch.empty((M, N), dtype=torch.bfloat16, device=A.codes.device)
     _check_2d(out, "out")
     lib = L.lib()
-    m = torch.empty(int(lib.nvfp4_sqrelu_maxima_bytes()) // 4, dtype=torch.int32, device=out.device)
+    m = _maxima_buffer(out.device)
     a, b = A.c_struct(), B.c_struct()
     st = lib.nvfp4_gemm_sqrelu_maxima(ctypes.byref(a), ctypes.byref(b), _ptr(out), out.stride(0) if M > 1 else N,
-                                      rht_seed & (2**64 - 1), _ptr(m), dev_status(out.device).data_ptr(), _stream())
+                                      rht_seed & (2**64 - 1), _ptr(m), m.numel() * 4, dev_status(out.device).data_ptr(),
+                                      _stream())
     L.check(st, "nvfp4_gemm_sqrelu_maxima")
     return out, m
 
@@ -287,10 +296,10 @@ def gemm_sqrelu_backward(A: QTensor, B: QTensor, H: torch.Tensor, out: Optional[
     lib = L.lib()
     ldh, ldd = H.stride(0) if M > 1 else N, out.stride(0) if M > 1 else N
     if maxima:
-        m = torch.empty(int(lib.nvfp4_sqrelu_maxima_bytes()) // 4, dtype=torch.int32, device=out.device)
+        m = _maxima_buffer(out.device)
         st = lib.nvfp4_gemm_sqrelu_bwd_maxima(ctypes.byref(a), ctypes.byref(b), _ptr(H), ldh, _ptr(out), ldd,
-                                              rht_seed & (2**64 - 1), _ptr(m), dev_status(out.device).data_ptr(),
-                                              _stream())
+                                              rht_seed & (2**64 - 1), _ptr(m), m.numel() * 4,
+                                              dev_status(out.device).data_ptr(), _stream())
         L.check(st, "nvfp4_gemm_sqrelu_bwd_maxima")
         return out, m
     st = lib.nvfp4_gemm_sqrelu_bwd(ctypes.byref(a), ctypes.byref(b), _ptr(H), ldh, _ptr(out), ldd,

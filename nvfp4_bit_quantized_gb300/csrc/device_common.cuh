@@ -89,11 +89,15 @@ __device__ __forceinline__ uint32_t block_scale_code(float amax_b, float s_enc) 
     return e4m3_rn_sat(__fmul_rn(__fdiv_rn(amax_b, 6.0f), s_enc));
 }
 
-// RN(a / 6) for a block maximum a that is a bf16 value (8 significant bits):
-// q0 = RN(a * RN(1/6)) corrected once with the exact remainder a - 6 q0 (one fma).
-// Checked against the correctly rounded quotient for every positive finite bf16
-// value in exact rational arithmetic (no mismatch); three instructions instead of
-// the general division.
+// RN(a / 6) for a block maximum a that is a bf16 value (8 significant bits), by the
+// published correction step for division by a reciprocal (P. Markstein, "Computation
+// of elementary functions on the IBM RISC System/6000 processor", IBM J. Res. Dev. 34,
+// 1990; for a divisor known in advance, N. Brisebarre, J.-M. Muller, S. K. Raina,
+// IEEE Trans. Computers 53(8), 2004): q0 = RN(a * RN(1/6)), the exact remainder
+// r = a - 6 q0 from one fma, q = RN(q0 + r * RN(1/6)).  That the result is the
+// correctly rounded quotient on this input domain was checked for every positive
+// finite bf16 value in exact rational arithmetic (no mismatch); three instructions
+// instead of the general division.
 __device__ __forceinline__ float div6_bf16(float a) {
     const float inv6 = __uint_as_float(0x3E2AAAABu);        // RN(1/6)
     const float q0 = __fmul_rn(a, inv6);

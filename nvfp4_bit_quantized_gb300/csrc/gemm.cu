@@ -99,7 +99,8 @@ struct Params {
     int n_fastest;               // tile order: 1 = consecutive tiles walk N (A tile reused), 0 = walk M
     uint32_t* dev_status;
     uint64_t timeout_ns;
-    uint32_t* maxima;            // EPI_SQAMAX / EPI_DSQR_AMAX: 2 x kMaximaParts partial maxima (|X|, then |RHT(X)| / 4)
+    uint32_t* maxima;            // EPI_SQAMAX / EPI_DSQR_AMAX: 2 x maxima_parts partial maxima (|X|, then |RHT(X)| / 4)
+    int maxima_parts;            // partials per half of `maxima` (>= 4 x grid)
     uint64_t rht_seed;           // the RHT sign vector of the column quantization those maxima serve
 };
 
@@ -1122,12 +1123,12 @@ gemm_nvfp4_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_con
             const int gid = (int)blockIdx.x * 4 + q;
             if (lane == 0) {
                 p.maxima[gid] = mabs;
-                p.maxima[kMaximaParts + gid] = __float_as_uint(__fmul_rn(__uint_as_float(mrht), 0.25f)) & 0x7FFFFFFFu;
+                p.maxima[p.maxima_parts + gid] = __float_as_uint(__fmul_rn(__uint_as_float(mrht), 0.25f)) & 0x7FFFFFFFu;
             }
             if (blockIdx.x == 0)
-                for (int i = (int)gridDim.x * 4 + q * 32 + lane; i < kMaximaParts; i += 128) {
+                for (int i = (int)gridDim.x * 4 + q * 32 + lane; i < p.maxima_parts; i += 128) {
                     p.maxima[i] = 0u;
-                    p.maxima[kMaximaParts + i] = 0u;
+                    p.maxima[p.maxima_parts + i] = 0u;
                 }
         }
         if (h_pending)                                   // after an abort: let the H copies land first
@@ -1337,8 +1338,8 @@ nvfp4_status mx_gemm_impl(const nvfp4_qtensor* A, const nvfp4_qtensor* B, void* 
 // backward in its epilogue (CTA-pair kernel; bf16 H and D, 16-byte aligned bases and pitches).
 // With `maxima`, the epilogue also leaves dH's two tensor maxima for its dual quantization.
 nvfp4_status gemm_sqrelu_bwd_impl(const nvfp4_qtensor* A, const nvfp4_qtensor* B, const void* H, int64_t ldh,
-                                  void* D, int64_t ldd, uint64_t rht_seed, uint32_t* maxima, uint32_t* dev_status,
-                                  cudaStream_t stream) {
+                                  void* D, int64_t ldd, uint64_t rht_seed, uint32_t* maxima, size_t maxima_bytes,
+                                  uint32_t* dev_status, cudaStream_t stream) {
     using namespace gemm;
     if (!A || !B || !H || !D) return NVFP4_ERR_INVALID_ARG;
     if (!A->codes || !B->codes || !A->scales_mma || !B->scales_mma || !A->s_dec || !B->s_dec)
@@ -1358,7 +1359,8 @@ nvfp4_status gemm_sqrelu_bwd_impl(const nvfp4_qtensor* A, const nvfp4_qtensor* B
         return NVFP4_ERR_CUDA;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return NVFP4_ERR_CUDA;
-    if (maxima && 4 * sm_count(dev) > kMaximaParts) return NVFP4_ERR_UNSUPPORTED;
+    if (maxima && maxima_bytes < 2 * sizeof(uint32_t) * kMaximaWarpsPerCta * (size_t)sm_count(dev))
+        return NVFP4_ERR_WORKSPACE;                   // one partial per epilogue warp of every CTA
     Params p;
     std::memset(&p, 0, sizeof(p));
     p.sfa = A->scales_mma;
@@ -1379,6 +1381,7 @@ nvfp4_status gemm_sqrelu_bwd_impl(const nvfp4_qtensor* A, const nvfp4_qtensor* B
     p.dev_status = dev_status;
     p.timeout_ns = wait_timeout_ns();
     p.maxima = maxima;
+    p.maxima_parts = (int)std::min<size_t>(maxima_bytes / (2 * sizeof(uint32_t)), 1u << 30);
     p.rht_seed = rht_seed;
     const int pair_tiles = (int)((M + 255) / 256) * p.n_tiles;
     const cudaError_t e = maxima
@@ -1390,7 +1393,8 @@ nvfp4_status gemm_sqrelu_bwd_impl(const nvfp4_qtensor* A, const nvfp4_qtensor* B
 // H = s_dec(A) s_dec(B) A B^T in bf16, plus the partial maxima that quantizing A = relu(H)^2
 // in both orientations needs (CTA-pair kernel, EPI_SQAMAX).
 nvfp4_status gemm_sqrelu_maxima_impl(const nvfp4_qtensor* A, const nvfp4_qtensor* B, void* D, int64_t ldd,
-                                     uint64_t rht_seed, uint32_t* maxima, uint32_t* dev_status, cudaStream_t stream) {
+                                     uint64_t rht_seed, uint32_t* maxima, size_t maxima_bytes, uint32_t* dev_status,
+                                     cudaStream_t stream) {
     using namespace gemm;
     if (!A || !B || !D || !maxima) return NVFP4_ERR_INVALID_ARG;
     if (!A->codes || !B->codes || !A->scales_mma || !B->scales_mma || !A->s_dec || !B->s_dec)
@@ -1404,7 +1408,8 @@ nvfp4_status gemm_sqrelu_maxima_impl(const nvfp4_qtensor* A, const nvfp4_qtensor
         return NVFP4_ERR_ALIGNMENT;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return NVFP4_ERR_CUDA;
-    if (4 * sm_count(dev) > kMaximaParts) return NVFP4_ERR_UNSUPPORTED;   // one partial per epilogue warp
+    if (maxima_bytes < 2 * sizeof(uint32_t) * kMaximaWarpsPerCta * (size_t)sm_count(dev))
+        return NVFP4_ERR_WORKSPACE;                   // one partial per epilogue warp of every CTA
     CUtensorMap ta, tb, td;
     if (!make_codes_map(&ta, A->codes, M, K, BM) || !make_codes_map(&tb, B->codes, N, K, 128) ||
         !make_out_map(&td, D, M, N, ldd))
@@ -1429,6 +1434,7 @@ nvfp4_status gemm_sqrelu_maxima_impl(const nvfp4_qtensor* A, const nvfp4_qtensor
     p.dev_status = dev_status;
     p.timeout_ns = wait_timeout_ns();
     p.maxima = maxima;
+    p.maxima_parts = (int)std::min<size_t>(maxima_bytes / (2 * sizeof(uint32_t)), 1u << 30);
     p.rht_seed = rht_seed;
     const int pair_tiles = (int)((M + 255) / 256) * p.n_tiles;
     const cudaError_t e = launch_pair<false, EPI_SQAMAX>(ta, tb, td, td, p, pair_tiles, sm_count(dev), stream);
@@ -1437,26 +1443,31 @@ nvfp4_status gemm_sqrelu_maxima_impl(const nvfp4_qtensor* A, const nvfp4_qtensor
 
 }  // namespace nvfp4
 
-extern "C" size_t nvfp4_sqrelu_maxima_bytes(void) { return 2u * nvfp4::kMaximaParts * sizeof(uint32_t); }
+extern "C" size_t nvfp4_sqrelu_maxima_bytes(int32_t device) {
+    const int sms = nvfp4::sm_count(device);
+    return sms > 0 ? 2u * sizeof(uint32_t) * nvfp4::kMaximaWarpsPerCta * (size_t)sms : 0u;
+}
 
 extern "C" nvfp4_status nvfp4_gemm_sqrelu_maxima(const nvfp4_qtensor* A, const nvfp4_qtensor* B, void* H, int64_t ldh,
-                                                 uint64_t rht_seed, uint32_t* maxima, uint32_t* dev_status,
-                                                 void* stream) {
-    return nvfp4::gemm_sqrelu_maxima_impl(A, B, H, ldh, rht_seed, maxima, dev_status,
+                                                 uint64_t rht_seed, uint32_t* maxima, size_t maxima_bytes,
+                                                 uint32_t* dev_status, void* stream) {
+    return nvfp4::gemm_sqrelu_maxima_impl(A, B, H, ldh, rht_seed, maxima, maxima_bytes, dev_status,
                                           static_cast<cudaStream_t>(stream));
 }
 
 extern "C" nvfp4_status nvfp4_gemm_sqrelu_bwd(const nvfp4_qtensor* A, const nvfp4_qtensor* B, const void* H,
                                               int64_t ldh, void* D, int64_t ldd, uint32_t* dev_status,
                                               void* stream) {
-    return nvfp4::gemm_sqrelu_bwd_impl(A, B, H, ldh, D, ldd, 0, nullptr, dev_status, static_cast<cudaStream_t>(stream));
+    return nvfp4::gemm_sqrelu_bwd_impl(A, B, H, ldh, D, ldd, 0, nullptr, 0, dev_status,
+                                       static_cast<cudaStream_t>(stream));
 }
 
 extern "C" nvfp4_status nvfp4_gemm_sqrelu_bwd_maxima(const nvfp4_qtensor* A, const nvfp4_qtensor* B, const void* H,
                                                      int64_t ldh, void* D, int64_t ldd, uint64_t rht_seed,
-                                                     uint32_t* maxima, uint32_t* dev_status, void* stream) {
+                                                     uint32_t* maxima, size_t maxima_bytes, uint32_t* dev_status,
+                                                     void* stream) {
     if (!maxima) return NVFP4_ERR_INVALID_ARG;
-    return nvfp4::gemm_sqrelu_bwd_impl(A, B, H, ldh, D, ldd, rht_seed, maxima, dev_status,
+    return nvfp4::gemm_sqrelu_bwd_impl(A, B, H, ldh, D, ldd, rht_seed, maxima, maxima_bytes, dev_status,
                                        static_cast<cudaStream_t>(stream));
 }
 

@@ -19,8 +19,11 @@
 //                 covers 64 rows x 8*VEC columns; every load instruction reads
 //                 4 full 128-byte lines, every transposed store writes full
 //                 32-byte sectors (4 lanes x 8 bytes per output row).
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
+#include <algorithm>
 #include <cstdint>
 #include <cstdio>
 #include <mutex>
@@ -1242,9 +1245,12 @@ namespace nvfp4 {
 static nvfp4_status quantize_dual_premax_impl(const void* x, int32_t x_dtype, int64_t R, int64_t C, int64_t ldx,
                                               const nvfp4_qparams* p_row, const nvfp4_qtensor* out_row,
                                               const nvfp4_qparams* p_col, const nvfp4_qtensor* out_col,
-                                              const uint32_t* maxima, uint32_t* dev_status, cudaStream_t stream,
-                                              bool sqr) {
+                                              const uint32_t* maxima, size_t maxima_bytes, uint32_t* dev_status,
+                                              cudaStream_t stream, bool sqr) {
     if (!p_row || !p_col || !maxima) return NVFP4_ERR_INVALID_ARG;
+    // two halves of `parts` partial maxima each (what nvfp4_sqrelu_maxima_bytes sizes)
+    const size_t parts = maxima_bytes / (2 * sizeof(uint32_t));
+    if (parts == 0 || parts > (1u << 30)) return NVFP4_ERR_WORKSPACE;
     if (x_dtype != NVFP4_BF16) return NVFP4_ERR_UNSUPPORTED;
     if (p_row->block != NVFP4_BLOCK_1X16_ROW || p_col->block != NVFP4_BLOCK_1X16_COL) return NVFP4_ERR_INVALID_ARG;
     nvfp4_status st = check_quantize_args(x, x_dtype, R, C, ldx, p_row, out_row);
@@ -1256,10 +1262,10 @@ static nvfp4_status quantize_dual_premax_impl(const void* x, int32_t x_dtype, in
     if (cudaGetDevice(&dev) != cudaSuccess) return NVFP4_ERR_CUDA;
     const int sms = sm_count(dev);
     if (sms <= 0) return NVFP4_ERR_CUDA;
-    const uint32_t* part_col = p_col->rht ? maxima + kMaximaParts : maxima;
-    st = encode_pass(x, x_dtype, R, C, ldx, p_row, out_row, maxima, kMaximaParts, sms, dev_status, stream, sqr);
+    const uint32_t* part_col = p_col->rht ? maxima + parts : maxima;
+    st = encode_pass(x, x_dtype, R, C, ldx, p_row, out_row, maxima, (int)parts, sms, dev_status, stream, sqr);
     if (st != NVFP4_OK) return st;
-    return encode_pass(x, x_dtype, R, C, ldx, p_col, out_col, part_col, kMaximaParts, sms, dev_status, stream, sqr);
+    return encode_pass(x, x_dtype, R, C, ldx, p_col, out_col, part_col, (int)parts, sms, dev_status, stream, sqr);
 }
 }  // namespace nvfp4
 
@@ -1267,17 +1273,18 @@ extern "C" nvfp4_status nvfp4_quantize_dual_sqrelu_premax(const void* h, int32_t
                                                           int64_t ldh, const nvfp4_qparams* params_row,
                                                           const nvfp4_qtensor* out_row, const nvfp4_qparams* params_col,
                                                           const nvfp4_qtensor* out_col, const uint32_t* maxima,
-                                                          uint32_t* dev_status, void* stream) {
+                                                          size_t maxima_bytes, uint32_t* dev_status, void* stream) {
     return nvfp4::quantize_dual_premax_impl(h, h_dtype, R, C, ldh, params_row, out_row, params_col, out_col, maxima,
-                                            dev_status, static_cast<cudaStream_t>(stream), true);
+                                            maxima_bytes, dev_status, static_cast<cudaStream_t>(stream), true);
 }
 
 extern "C" nvfp4_status nvfp4_quantize_dual_premax(const void* x, int32_t x_dtype, int64_t R, int64_t C, int64_t ldx,
                                                    const nvfp4_qparams* params_row, const nvfp4_qtensor* out_row,
                                                    const nvfp4_qparams* params_col, const nvfp4_qtensor* out_col,
-                                                   const uint32_t* maxima, uint32_t* dev_status, void* stream) {
+                                                   const uint32_t* maxima, size_t maxima_bytes, uint32_t* dev_status,
+                                                   void* stream) {
     return nvfp4::quantize_dual_premax_impl(x, x_dtype, R, C, ldx, params_row, out_row, params_col, out_col, maxima,
-                                            dev_status, static_cast<cudaStream_t>(stream), false);
+                                            maxima_bytes, dev_status, static_cast<cudaStream_t>(stream), false);
 }
 
 extern "C" size_t nvfp4_quantize_dual_workspace_bytes(int64_t, int64_t) {
@@ -1311,19 +1318,55 @@ namespace {
 static __device__ __align__(256) uint32_t g_noalloc_partials[kMaxPartials];
 
 std::mutex g_noalloc_mutex;
-void* g_noalloc_addr[64] = {nullptr};
 
-// Device address of the scratch on `dev` (which must be the current device);
-// looked up on the first call for that device and cached.
-nvfp4_status noalloc_scratch(int dev, void** addr) {
-    if (dev < 0 || dev >= 64) return NVFP4_ERR_CUDA;
+// The scratch's address is a property of the CUDA context that loaded this library's module,
+// not of the device: after cudaDeviceReset (or a primary context that is released and created
+// again) the module is loaded anew and the array may move.  So the cache is keyed on the
+// context's process-unique id (cuCtxGetId), and a new context gets a fresh lookup.
+struct NoallocEntry { unsigned long long ctx_id; void* addr; };
+NoallocEntry g_noalloc_cache[16];
+int g_noalloc_used = 0, g_noalloc_next = 0;
+
+// Process-unique id of the calling thread's current context; 0 when there is none yet (or
+// the driver entry points are unavailable).
+unsigned long long current_ctx_id() {
+    static PFN_cuCtxGetCurrent_v4000 get_cur = nullptr;
+    static PFN_cuCtxGetId_v12000 get_id = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        cudaDriverEntryPointQueryResult q;
+        void* f = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 4000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_cur = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(f);
+        f = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &f, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(f);
+    });
+    CUcontext ctx = nullptr;
+    if (!get_cur || !get_id || get_cur(&ctx) != CUDA_SUCCESS || !ctx) return 0;
+    unsigned long long id = 0;
+    return get_id(ctx, &id) == CUDA_SUCCESS ? id : 0;
+}
+
+// Device address of the scratch in the current context, looked up once per context (the
+// lookup also creates the device's primary context if none is current yet) and cached.
+nvfp4_status noalloc_scratch(void** addr) {
     std::lock_guard<std::mutex> lk(g_noalloc_mutex);
-    if (!g_noalloc_addr[dev]) {
-        void* p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_noalloc_partials) != cudaSuccess || !p) return NVFP4_ERR_CUDA;
-        g_noalloc_addr[dev] = p;
+    unsigned long long id = current_ctx_id();
+    if (id != 0)
+        for (int i = 0; i < g_noalloc_used; ++i)
+            if (g_noalloc_cache[i].ctx_id == id) { *addr = g_noalloc_cache[i].addr; return NVFP4_OK; }
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_partials) != cudaSuccess || !p) return NVFP4_ERR_CUDA;
+    id = current_ctx_id();
+    if (id != 0) {                       // remember it (the oldest entry makes room)
+        g_noalloc_cache[g_noalloc_next] = NoallocEntry{id, p};
+        g_noalloc_next = (g_noalloc_next + 1) % 16;
+        g_noalloc_used = std::min(g_noalloc_used + 1, 16);
     }
-    *addr = g_noalloc_addr[dev];
+    *addr = p;
     return NVFP4_OK;
 }
 
@@ -1335,10 +1378,8 @@ extern "C" nvfp4_status nvfp4_quantize_noalloc(const void* x, int32_t x_dtype, i
                                                uint32_t* dev_status, void* stream) {
     if (!params) return NVFP4_ERR_INVALID_ARG;
     if (nvfp4_quantize_workspace_bytes(R, C, params) > sizeof(nvfp4::g_noalloc_partials)) return NVFP4_ERR_WORKSPACE;
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return NVFP4_ERR_CUDA;
     void* scratch = nullptr;
-    const nvfp4_status st = nvfp4::noalloc_scratch(dev, &scratch);
+    const nvfp4_status st = nvfp4::noalloc_scratch(&scratch);
     if (st != NVFP4_OK) return st;
     return nvfp4::quantize_impl(x, x_dtype, R, C, ldx, params, out, scratch, sizeof(nvfp4::g_noalloc_partials),
                                 dev_status, static_cast<cudaStream_t>(stream));

@@ -15,9 +15,10 @@
  *          +-1 sign vectors applied only to the Wgrad inputs; 2D (16x16) block
  *          scaling for weights so forward and backward see the same quantized
  *          weights; stochastic rounding on gradients only.
- *   ¶4  -- the three techniques are required together (skipping SR biases the
- *          gradients, skipping the RHT breaks Wgrad statistics, skipping 2D
- *          scaling breaks fwd/bwd consistency).
+ *   ¶4  -- the techniques only work as a set: each one the recipe drops costs
+ *          something specific (unbiased gradients without SR, sound weight-
+ *          gradient statistics without the RHT, matching forward and backward
+ *          weights without the 2D scales).
  * The page fixes no formulas.  Every step it leaves open is marked [reading]
  * below; each reading is the plainest one consistent with the page.
  *

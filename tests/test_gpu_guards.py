@@ -102,12 +102,12 @@ def test_gemms_stay_inside_their_buffers(nv, M, N, K):
             lib.nvfp4_gemm_force_path(0)
     H = _x(M, N, torch.bfloat16, 3)
     assert lib.nvfp4_gemm_sqrelu_bwd(ctypes.byref(a), ctypes.byref(b), H.data_ptr(), N, gb(M * N * 2), N, st, s) == 0
-    mbytes = int(lib.nvfp4_sqrelu_maxima_bytes())
+    mbytes = int(lib.nvfp4_sqrelu_maxima_bytes(torch.cuda.current_device()))
     if M % 16 == 0 and N % 16 == 0:
         assert lib.nvfp4_gemm_sqrelu_bwd_maxima(ctypes.byref(a), ctypes.byref(b), H.data_ptr(), N, gb(M * N * 2), N,
-                                                7, gb(mbytes), st, s) == 0
+                                                7, gb(mbytes), mbytes, st, s) == 0
         assert lib.nvfp4_gemm_sqrelu_maxima(ctypes.byref(a), ctypes.byref(b), gb(M * N * 2), N, 7, gb(mbytes),
-                                            st, s) == 0
+                                            mbytes, st, s) == 0
     ma = nv.mx_quantize(_x(M, K, torch.bfloat16, 4))
     mb = nv.mx_quantize(_x(N, K, torch.bfloat16, 5))
     mac, mbc = ma.c_struct(), mb.c_struct()

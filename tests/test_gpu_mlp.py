@@ -74,8 +74,35 @@ def test_sqrelu_matches_oracle(nv, oracle_mod):
     assert np.array_equal(host_input(dh.cpu()), oracle_mod.sqrelu_backward(hb, db))
 
 
-def test_mlp_block_small_full_oracle(nv, oracle_mod):
-    """256 tokens, 256 -> 1024 -> 256: every stage against the oracle."""
+def test_sqrelu_every_bf16_input_and_dense_backward(nv, oracle_mod):
+    """The forward over all 65536 bf16 inputs, and the backward over every bf16 h against
+    ~40 da values and every bf16 da against ~40 h values, equal the oracle (NaN results
+    compared as NaN, their payload being unspecified)."""
+    allb = torch.arange(65536, dtype=torch.int32).to(torch.int16).view(torch.bfloat16)
+    a = nv.sqrelu_forward(allb.cuda())
+    torch.cuda.synchronize()
+    assert np.array_equal(host_input(a.cpu()), oracle_mod.sqrelu_forward(host_input(allb)))
+    rng = np.random.default_rng(17)
+    part = np.concatenate([np.array([0x0000, 0x8000, 0x0001, 0x8001, 0x3F80, 0xBF80, 0x7F7F, 0xFF7F, 0x7F80,
+                                     0xFF80, 0x7FC0, 0x5F80], dtype=np.uint16),
+                           rng.integers(0, 65536, 28).astype(np.uint16)])
+    hb = np.concatenate([np.repeat(host_input(allb), part.size), np.tile(part, 65536)])
+    db = np.concatenate([np.tile(part, 65536), np.repeat(host_input(allb), part.size)])
+    to_t = lambda b: torch.from_numpy(b.view(np.int16)).view(torch.bfloat16).cuda()
+    dh = host_input(nv.sqrelu_backward(to_t(hb), to_t(db)).cpu())
+    ref = oracle_mod.sqrelu_backward(hb, db)
+    nan = lambda b: np.isnan(torch.from_numpy(b.view(np.int16)).view(torch.bfloat16).float().numpy())
+    assert np.array_equal(nan(dh), nan(ref))
+    assert np.array_equal(dh[~nan(ref)], ref[~nan(ref)])
+
+
+@pytest.mark.parametrize("fused", [False, True], ids=["unfused", "fused_as_benched"])
+def test_mlp_block_small_full_oracle(nv, oracle_mod, fused):
+    """256 tokens, 256 -> 1024 -> 256: every stage against the oracle.  ``fused`` runs the
+    step the way the MLP benchmark does (relu(H)^2 quantized from the maxima the fwd1
+    epilogue leaves; dH and its maxima from the dgrad2 epilogue): the quantizations of A and
+    dH that skip their amax pass must still equal the oracle's quantization of the same
+    tensors bit for bit, tensor scale included."""
     from nvfp4_bit_quantized_gb300 import inputs
     T, d, f = 256, 256, 1024
     X = inputs.normal((T, d), 1.0, 0, device="cuda")
@@ -83,7 +110,9 @@ def test_mlp_block_small_full_oracle(nv, oracle_mod):
     W2 = inputs.normal((d, f), 0.02, 2, device="cuda")
     dY = inputs.normal((T, d), 1e-3, 3, device="cuda")
     nv.reset_status()
-    o = mlp_step(nv, X, W1, W2, dY)
+    o = mlp_step(nv, X, W1, W2, dY, fused_dgrad=fused, fused_fwd=fused)
+    if fused:       # dA is never formed in the fused step; the plain GEMM gives the one dH must follow
+        o["dA"] = nv.gemm(o["dyq"], o["w2q"].transposed(), torch.bfloat16)
     assert nv.status_query() == 0
     om = oracle_mod
 
@@ -91,6 +120,7 @@ def test_mlp_block_small_full_oracle(nv, oracle_mod):
         r = om.quantize(x_bits, block, rnd, rht=rht, sr_seed=5, sr_offset=sr_offset, rht_seed=9)
         assert np.array_equal(q.codes.cpu().numpy(), r["codes"])
         assert np.array_equal(q.scales.cpu().numpy(), r["scales"])
+        assert np.float32(q.s_dec[0].item()) == np.float32(r["s_dec"])
         return r
 
     x, w1, w2, dy = host_input(X), host_input(W1), host_input(W2), host_input(dY)
@@ -187,6 +217,17 @@ def test_quantize_dual_sqrelu_equals_activation_then_quantize(nv, oracle_mod, rn
     assert np.array_equal(fr.scales.cpu().numpy(), r["scales"]) and np.array_equal(fc.scales.cpu().numpy(), c["scales"])
 
 
+def _same_as_oracle(om, fr, fc, x_bits, rnd, rht, sr_seed, sr_offset, rht_seed):
+    """The row and column operands quantized from epilogue maxima equal the oracle's
+    quantization of the tensor: codes, canonical scales and the tensor scale."""
+    r = om.quantize(x_bits, om.ROW, rnd, sr_seed=sr_seed, sr_offset=sr_offset)
+    c = om.quantize(x_bits, om.COL, rnd, rht=rht, sr_seed=sr_seed, sr_offset=sr_offset, rht_seed=rht_seed)
+    for q, ref in ((fr, r), (fc, c)):
+        assert np.array_equal(q.codes.cpu().numpy(), ref["codes"])
+        assert np.array_equal(q.scales.cpu().numpy(), ref["scales"])
+        assert np.float32(q.s_dec[0].item()) == np.float32(ref["s_dec"])
+
+
 @pytest.fixture
 def pair_path():
     from nvfp4_bit_quantized_gb300 import _lib as L
@@ -235,7 +276,7 @@ def test_gemm_sqrelu_backward_strided(nv, pair_path):
 @pytest.mark.parametrize("rnd,rht", [(0, True), (1, True), (0, False)])
 @pytest.mark.parametrize("M,N,K", [(256, 256, 256), (208, 336, 224), (512, 1024, 768), (16, 16, 32),
                                    (1040, 656, 544)])
-def test_gemm_sqrelu_maxima_then_quantize_equals_unfused(nv, pair_path, M, N, K, rnd, rht):
+def test_gemm_sqrelu_maxima_then_quantize_equals_unfused(nv, oracle_mod, pair_path, M, N, K, rnd, rht):
     """The first MLP GEMM with relu(H)^2's tensor maxima in its epilogue: H is bit for bit the
     CTA-pair GEMM's, and quantizing relu(H)^2 from those maxima (no amax read) gives the same
     codes, scales and tensor scales as the dual quantization with its own amax pass."""
@@ -255,11 +296,14 @@ def test_gemm_sqrelu_maxima_then_quantize_equals_unfused(nv, pair_path, M, N, K,
     for f, u in ((fr, ur), (fc, uc)):
         assert torch.equal(f.codes, u.codes) and torch.equal(f.scales, u.scales)
         assert torch.equal(f.scales_mma, u.scales_mma) and torch.equal(f.s_dec[:1], u.s_dec[:1])
+    # and against the oracle's quantization of relu(H)^2 itself
+    a = oracle_mod.sqrelu_forward(host_input(H.cpu()))
+    _same_as_oracle(oracle_mod, fr, fc, a, rnd, rht, sr_seed=3, sr_offset=2, rht_seed=7)
 
 
 @pytest.mark.parametrize("rht", [True, False])
 @pytest.mark.parametrize("M,N,K", [(256, 256, 256), (208, 336, 224), (512, 1024, 768), (16, 16, 32)])
-def test_gemm_sqrelu_backward_maxima_then_quantize_equals_unfused(nv, pair_path, M, N, K, rht):
+def test_gemm_sqrelu_backward_maxima_then_quantize_equals_unfused(nv, oracle_mod, pair_path, M, N, K, rht):
     """The fused Dgrad GEMM leaving dH's tensor maxima: dH is bit for bit the plain fused
     GEMM's, and the SR dual quantization of dH from those maxima (no amax read) equals the
     one with its own amax pass."""
@@ -280,3 +324,5 @@ def test_gemm_sqrelu_backward_maxima_then_quantize_equals_unfused(nv, pair_path,
     for f, u in ((fr, ur), (fc, uc)):
         assert torch.equal(f.codes, u.codes) and torch.equal(f.scales, u.scales)
         assert torch.equal(f.scales_mma, u.scales_mma) and torch.equal(f.s_dec[:1], u.s_dec[:1])
+    # and against the oracle's quantization of dH itself
+    _same_as_oracle(oracle_mod, fr, fc, host_input(dH.cpu()), nv.SR, rht, sr_seed=4, sr_offset=6, rht_seed=13)

@@ -178,25 +178,29 @@ def test_gemm_sqrelu_backward_rejects_bad_arguments(lib):
 
 def test_sqrelu_maxima_entries_reject_bad_arguments(lib):
     L = lib.lib()
-    assert L.nvfp4_sqrelu_maxima_bytes() == 2 * 608 * 4
+    # sized from the device's multiprocessor count: no device here, so 0 (never a fixed cap)
+    assert L.nvfp4_sqrelu_maxima_bytes(0) == 0 and L.nvfp4_sqrelu_maxima_bytes(-1) == 0
+    mb = 2 * 4 * 152 * 4
     A = lib.QTensorC(0x1000, None, 0x1000, 0x2000, None, None, 128, 256)
     B = lib.QTensorC(0x1000, None, 0x1000, 0x2000, None, None, 256, 256)
     f = L.nvfp4_gemm_sqrelu_maxima
-    assert f(ctypes.byref(A), ctypes.byref(B), 0x4000, 256, 0, None, None, None) == lib.ERR_INVALID_ARG   # no maxima
-    assert f(ctypes.byref(A), ctypes.byref(B), 0x4000, 256, 0, 0x8002, None, None) == lib.ERR_ALIGNMENT
+    assert f(ctypes.byref(A), ctypes.byref(B), 0x4000, 256, 0, None, mb, None, None) == lib.ERR_INVALID_ARG   # no maxima
+    assert f(ctypes.byref(A), ctypes.byref(B), 0x4000, 256, 0, 0x8002, mb, None, None) == lib.ERR_ALIGNMENT
     B.rows = 200                                                                                     # N % 16
-    assert f(ctypes.byref(A), ctypes.byref(B), 0x4000, 256, 0, 0x8000, None, None) == lib.ERR_SHAPE
+    assert f(ctypes.byref(A), ctypes.byref(B), 0x4000, 256, 0, 0x8000, mb, None, None) == lib.ERR_SHAPE
     pr, pc = _qp(lib, 0, 0, 0), _qp(lib, 1, 0, 1)
     sdec = 0x2000
     qr = lib.QTensorC(0x1000, 0x1000, None, sdec, None, None, 32, 64)
     qc = lib.QTensorC(0x1000, 0x1000, None, sdec, None, None, 64, 32)
     q = L.nvfp4_quantize_dual_sqrelu_premax
     assert q(0x1000, lib.F32, 32, 64, 64, ctypes.byref(pr), ctypes.byref(qr), ctypes.byref(pc), ctypes.byref(qc),
-             0x8000, None, None) == lib.ERR_UNSUPPORTED
+             0x8000, mb, None, None) == lib.ERR_UNSUPPORTED
     assert q(0x1000, lib.BF16, 32, 64, 64, ctypes.byref(pr), ctypes.byref(qr), ctypes.byref(pc), ctypes.byref(qc),
-             None, None, None) == lib.ERR_INVALID_ARG
+             None, mb, None, None) == lib.ERR_INVALID_ARG
     assert q(0x1000, lib.BF16, 32, 64, 64, ctypes.byref(pc), ctypes.byref(qr), ctypes.byref(pc), ctypes.byref(qc),
-             0x8000, None, None) == lib.ERR_INVALID_ARG                                             # row params
+             0x8000, mb, None, None) == lib.ERR_INVALID_ARG                                             # row params
+    assert q(0x1000, lib.BF16, 32, 64, 64, ctypes.byref(pr), ctypes.byref(qr), ctypes.byref(pc), ctypes.byref(qc),
+             0x8000, 4, None, None) == lib.ERR_WORKSPACE                                                # no partials
 
 
 def test_dh_maxima_entries_reject_bad_arguments(lib):
@@ -204,15 +208,16 @@ def test_dh_maxima_entries_reject_bad_arguments(lib):
     A = lib.QTensorC(0x1000, None, 0x1000, 0x2000, None, None, 128, 256)
     B = lib.QTensorC(0x1000, None, 0x1000, 0x2000, None, None, 256, 256)
     f = L.nvfp4_gemm_sqrelu_bwd_maxima
-    assert f(ctypes.byref(A), ctypes.byref(B), 0x8000, 256, 0x4000, 256, 0, None, None, None) == lib.ERR_INVALID_ARG
-    assert f(ctypes.byref(A), ctypes.byref(B), 0x8000, 256, 0x4000, 256, 0, 0x9002, None, None) == lib.ERR_ALIGNMENT
+    mb = 2 * 4 * 152 * 4
+    assert f(ctypes.byref(A), ctypes.byref(B), 0x8000, 256, 0x4000, 256, 0, None, mb, None, None) == lib.ERR_INVALID_ARG
+    assert f(ctypes.byref(A), ctypes.byref(B), 0x8000, 256, 0x4000, 256, 0, 0x9002, mb, None, None) == lib.ERR_ALIGNMENT
     B.rows = 200                                                                                     # N % 16
-    assert f(ctypes.byref(A), ctypes.byref(B), 0x8000, 256, 0x4000, 256, 0, 0x9000, None, None) == lib.ERR_SHAPE
+    assert f(ctypes.byref(A), ctypes.byref(B), 0x8000, 256, 0x4000, 256, 0, 0x9000, mb, None, None) == lib.ERR_SHAPE
     pr, pc = _qp(lib, 0, 1, 0), _qp(lib, 1, 1, 1)
     qr = lib.QTensorC(0x1000, 0x1000, None, 0x2000, None, None, 32, 64)
     qc = lib.QTensorC(0x1000, 0x1000, None, 0x2000, None, None, 64, 32)
     q = L.nvfp4_quantize_dual_premax
     assert q(0x1000, lib.F32, 32, 64, 64, ctypes.byref(pr), ctypes.byref(qr), ctypes.byref(pc), ctypes.byref(qc),
-             0x8000, None, None) == lib.ERR_UNSUPPORTED
+             0x8000, mb, None, None) == lib.ERR_UNSUPPORTED
     assert q(0x1000, lib.BF16, 32, 64, 64, ctypes.byref(pr), ctypes.byref(qr), ctypes.byref(pc), ctypes.byref(qc),
-             None, None, None) == lib.ERR_INVALID_ARG
+             None, mb, None, None) == lib.ERR_INVALID_ARG

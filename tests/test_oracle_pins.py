@@ -364,7 +364,7 @@ def test_brute_force_tile_encode(oracle_mod):
 
 @pytest.mark.parametrize("mode", ["row", "col", "col_rht", "tile"])
 def test_amax_element_is_at_scale_precision(oracle_mod, mode):
-    """[page ¶2] at least 6.25% of each block's values sit at near-FP8 precision: with
+    """[page ¶2] one value in sixteen per block (6.25 %) keeps roughly FP8 precision: with
     RNE, the block's largest element encodes to +-6 whenever the block scale is normal."""
     frac = FACTS["min_fraction_at_scale_precision"]["value"]
     assert frac == 1 / FACTS["block_elems"]["value"]
@@ -505,6 +505,86 @@ def test_bf16_rounding_helper_matches_torch(oracle_mod):
                         np.array([0.0, -0.0, 1.0, 3.0e38])]).astype(np.float32)
     ref = torch.from_numpy(x).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
     assert np.array_equal(oracle_mod._f32_to_bf16(x), ref)
+
+
+# ---------------------------------------------------------------- squared ReLU (MLP block) --
+# The reading (the page names no activation): relu(h) = h if h > 0 else +0 (so -0, negative
+# values and NaN give +0); a = relu(h)^2 and dh = da * (2 relu(h)) are each one fp32 operation
+# rounded to nearest, then rounded to nearest-even bf16.  The pins below take another route to
+# the same numbers: the product of two bf16 values has at most 16 significant bits and an
+# exponent far inside fp64's range, so it is exact in fp64; one conversion to fp32 (numpy's
+# IEEE cast, which overflows to inf and underflows gradually) is then the single fp32 rounding,
+# and torch's fp32 -> bf16 cast is the final rounding (not the oracle's bit arithmetic).
+
+ALL_BF16 = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+
+
+def _bf16_as_f64(bits: np.ndarray) -> np.ndarray:
+    return torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).to(torch.float64).numpy()
+
+
+def _f32_to_bf16_torch(x: np.ndarray) -> np.ndarray:
+    return torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32)).to(torch.bfloat16).view(
+        torch.int16).numpy().view(np.uint16)
+
+
+def _same_or_both_nan(got: np.ndarray, ref: np.ndarray) -> bool:
+    g, r = _bf16_as_f64(got), _bf16_as_f64(ref)
+    nan = np.isnan(r)
+    return bool(np.array_equal(np.isnan(g), nan) and np.array_equal(got[~nan], ref[~nan]))
+
+
+def test_sqrelu_forward_all_bf16_patterns(oracle_mod):
+    """a = relu(h)^2 for every one of the 65536 bf16 inputs (both zeros, subnormals, the
+    fp32 overflow of h^2 above ~1.8e19, inf, NaN): exact square -> one fp32 rounding -> bf16."""
+    h = _bf16_as_f64(ALL_BF16)
+    with np.errstate(over="ignore", invalid="ignore"):
+        pos = h > 0                                  # False for -0, negatives and NaN
+        sq = np.where(pos, h * h, 0.0)               # exact in fp64 (or inf for h = inf)
+        ref = _f32_to_bf16_torch(sq.astype(np.float32))
+        got = oracle_mod.sqrelu_forward(ALL_BF16)
+    assert _same_or_both_nan(got, ref)
+    # the reading's special cases, spelled out
+    assert got[0x0000] == 0 and got[0x8000] == 0                 # relu(+-0)^2 = +0
+    assert got[0x7FC0] == 0 and got[0xFFC0] == 0                 # NaN -> +0
+    assert got[0x3F80] == 0x3F80 and got[0xBF80] == 0            # 1 -> 1, -1 -> +0
+    assert got[0x4040] == 0x4110                                  # 3 -> 9
+    assert got[0x7F80] == 0x7F80 and got[0x5F80] == 0x7F80       # inf -> inf; 2^64 squared overflows fp32
+    assert got[0x0001] == 0                                       # smallest subnormal: 2^-266 underflows
+
+
+def _dense_pairs():
+    """Every bf16 h against special and random da values, and every bf16 da against
+    special and random h values."""
+    rng = np.random.default_rng(31)
+    special = np.array([0x0000, 0x8000, 0x0001, 0x8001, 0x007F, 0x0080, 0x3F80, 0xBF80, 0x4000, 0x3A83,
+                        0xBA83, 0x7F7F, 0xFF7F, 0x5F80, 0x5F7F, 0x1F80, 0x2000, 0x7F80, 0xFF80, 0x7FC0,
+                        0x0C00, 0x8C00, 0x3C00, 0x4300], dtype=np.uint16)
+    rand = rng.integers(0, 65536, 40).astype(np.uint16)
+    partners = np.concatenate([special, rand])
+    h = np.concatenate([np.repeat(ALL_BF16, partners.size), np.tile(partners, 65536)])
+    da = np.concatenate([np.tile(partners, 65536), np.repeat(ALL_BF16, partners.size)])
+    return h, da
+
+
+def test_sqrelu_backward_dense_sweep(oracle_mod):
+    """dh = da * 2 relu(h) over ~8.4 M (h, da) pairs: 2h exact then one fp32 rounding (inf
+    above the fp32 range), the exact product da * t then one fp32 rounding, then bf16."""
+    h_bits, da_bits = _dense_pairs()
+    h, da = _bf16_as_f64(h_bits), _bf16_as_f64(da_bits)
+    with np.errstate(over="ignore", invalid="ignore"):
+        t = np.where(h > 0, 2.0 * h, 0.0).astype(np.float32).astype(np.float64)
+        p = da * t                                   # exact for finite t; inf * 0 -> NaN
+        ref = _f32_to_bf16_torch(p.astype(np.float32))
+        got = oracle_mod.sqrelu_backward(h_bits, da_bits)
+    assert _same_or_both_nan(got, ref)
+    # spelled-out cases: the gradient through relu is 0 for h <= 0 and keeps da's sign
+    one, mone, three = 0x3F80, 0xBF80, 0x4040
+    assert oracle_mod.sqrelu_backward(np.array([three], np.uint16), np.array([one], np.uint16))[0] == 0x40C0  # 6
+    assert oracle_mod.sqrelu_backward(np.array([mone], np.uint16), np.array([one], np.uint16))[0] == 0x0000
+    assert oracle_mod.sqrelu_backward(np.array([mone], np.uint16), np.array([mone], np.uint16))[0] == 0x8000
+    with np.errstate(over="ignore"):
+        assert oracle_mod.sqrelu_backward(np.array([0x7F7F], np.uint16), np.array([one], np.uint16))[0] == 0x7F80
 
 
 # ---------------------------------------------------------------- MXFP4 (comparison format) --
