@@ -177,15 +177,25 @@ class ClockSampler:
             self._smi_stop()
 
     # -- timed regions ----------------------------------------------------------------
+    def _sample_now(self):
+        s = self._read_nvml()
+        if s is not None:
+            with self._lock:
+                self.samples.append(s)
+
     def arm(self):
+        """Start sampling (one reading right away, so even a short region has some)."""
         if self._nvml is not None:
+            self._sample_now()
             self._armed.set()
         else:
             self._smi_start()
 
     def disarm(self):
+        """Stop sampling (call right after the closing synchronize: one last reading under load)."""
         if self._nvml is not None:
             self._armed.clear()
+            self._sample_now()
         else:
             self._smi_stop()
 
@@ -432,12 +442,12 @@ def run_heavy(args):
     from nvfp4_bit_quantized_gb300 import inputs
     Mh, Kh, Nh = 16384, 4096, 14336
     X, W, dY = inputs.heavy_tailed_layer(Mh, Kh, Nh, seed=0, device="cuda")
-    wq = nv.quantize(W, nv.TILE16, nv.RNE, scales=False, transpose=True)
+    wq_op_w = nv.quantize(W, nv.TILE16, nv.RNE, scales=False, transpose=True)
     xq, xt = nv.quantize_dual(X, nv.RNE, nv.RNE, rht=True, rht_seed=11, scales=False)
     dyq, dyt = nv.quantize_dual(dY, nv.SR, nv.SR, rht=True, sr_seed=7, rht_seed=11, scales=False)
 
     def gemms():
-        return (nv.gemm(xq, wq, torch.bfloat16), nv.gemm(dyq, wq.transposed(), torch.bfloat16),
+        return (nv.gemm(xq, wq_op_w, torch.bfloat16), nv.gemm(dyq, wq_op_w.transposed(), torch.bfloat16),
                 nv.gemm(dyt, xt, torch.bfloat16))
 
     def full():
@@ -450,24 +460,36 @@ def run_heavy(args):
         return X @ W.t(), dY @ W, dY.t() @ X
 
     t_g, t_f, t_b = (_timed(fn, args.steps, args.warmup) for fn in (gemms, full, bf16))
-    clk = _clocks()
     fp4, ref = full(), bf16()
     err = {n: round(((a.float() - b.float()).norm() / b.float().norm()).item(), 4)
            for n, a, b in zip(("fprop", "dgrad", "wgrad"), fp4, ref)}
-    # the RHT's effect on the Wgrad product alone: both operands RNE, with and without the transform
-    wq = {}
-    for rht in (True, False):
-        gt = nv.quantize(dY, nv.COL, nv.RNE, rht=rht, rht_seed=11, scales=False)
-        at = nv.quantize(X, nv.COL, nv.RNE, rht=rht, rht_seed=11, scales=False)
-        d = nv.gemm(gt, at, torch.bfloat16).float()
-        wq["rht" if rht else "no_rht"] = round(((d - ref[2].float()).norm() / ref[2].float().norm()).item(), 4)
+    clk = _clocks()
+    # the RHT's effect on the Wgrad product alone, with and without the transform: both operands
+    # RNE, and the recipe's rounding (dY stochastic, X RNE); on this layer (outliers are whole
+    # channels, which the transform along tokens cannot spread) and on the same layer with its
+    # outliers along the tokens instead (the Wgrad contraction axis)
+    def wgrad_rht_effect(Xw, dYw, refw):
+        out = {}
+        for name, rnd in (("rne", nv.RNE), ("recipe_sr_dy", nv.SR)):
+            out[name] = {}
+            for rht in (True, False):
+                gt = nv.quantize(dYw, nv.COL, rnd, rht=rht, sr_seed=7, rht_seed=11, scales=False)
+                at = nv.quantize(Xw, nv.COL, nv.RNE, rht=rht, rht_seed=11, scales=False)
+                d = nv.gemm(gt, at, torch.bfloat16).float()
+                out[name]["rht" if rht else "no_rht"] = round(((d - refw.float()).norm() / refw.float().norm()).item(), 4)
+        return out
+    wq = {"channel_outliers": wgrad_rht_effect(X, dY, ref[2])}
+    del fp4, ref, X, dY, wq_op_w
+    torch.cuda.empty_cache()
+    Xt, _, dYt = inputs.heavy_tailed_token_outliers(Mh, Kh, Nh, seed=0, device="cuda")
+    wq["token_outliers"] = wgrad_rht_effect(Xt, dYt, dYt.t() @ Xt)
     flop = 3 * 2.0 * Mh * Kh * Nh
     print(json.dumps({"config": "heavy_tailed_16384x4096x14336", "nvfp4_gemm_ms": round(t_g, 4),
                       "nvfp4_step_ms": round(t_f, 4), "bf16_cublas_ms": round(t_b, 4),
                       "speedup_gemm_only": round(t_b / t_g, 2), "speedup_with_quantization": round(t_b / t_f, 2),
                       "nvfp4_tflops_gemm": round(flop / (t_g * 1e-3) / 1e12, 1),
                       "bf16_tflops": round(flop / (t_b * 1e-3) / 1e12, 1),
-                      "rel_error_vs_bf16": err, "wgrad_rne_rel_error_vs_bf16": wq,
+                      "rel_error_vs_bf16": err, "wgrad_rht_effect_rel_error_vs_bf16": wq,
                       "clocks": clk, "device_status": nv.status_query()}))
 
 
@@ -781,7 +803,7 @@ def run_ours(args):
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
-        cpu = oracle_sample(budget_s=args.cpu_seconds)
+        cpu = cpu_baseline(args.cpu_seconds)
 
     if world > 1:
         dist.destroy_process_group()
@@ -832,7 +854,7 @@ def run_ours(args):
 
 # --------------------------------------------------------------------------- oracle (CPU) arm
 
-def oracle_sample(budget_s: float = 15.0, reps: int | None = None, rotate: bool = False):
+def oracle_sample(budget_s: float = 15.0, reps: int | None = None, rotate: bool = False, threads: int = 1):
     """Times the CPU oracle on a bounded sample of the step: one output block of
     each GEMM with the full contraction length of the workload, the oracle
     quantizing the operand rows that block needs:
@@ -840,7 +862,9 @@ def oracle_sample(budget_s: float = 15.0, reps: int | None = None, rotate: bool 
       Dgrad  64x128 block of dX, N = 20480  (dY rows 1x16 SR, W^T rows 16x16)
       Wgrad 128x64  block of dW, M = 8192   (dY^T, X^T columns with the RHT; SR / RNE)
     With ``rotate`` a rep is one of the three blocks in turn (a third of the work).
-    value = sampled GEMM flops / oracle time (single-threaded C)."""
+    ``threads`` > 1 splits each quantization's rows and each GEMM block's rows among
+    that many threads (the oracle's threaded entry points; identical results).
+    value = sampled GEMM flops / oracle time."""
     import numpy as np
     import oracle
     import torch
@@ -856,13 +880,14 @@ def oracle_sample(budget_s: float = 15.0, reps: int | None = None, rotate: bool 
     wts = bits(inputs.normal((nb, N), 0.02, 3))          # W^T rows (= W columns)
     dyc = bits(inputs.normal((M, nb), 1e-3, 4))          # dY columns
     xc = bits(inputs.normal((M, mb), 1.0, 5))            # X columns
-    deq, gemm = oracle.dequant, oracle.gemm_f64
+    deq, th = oracle.dequant, threads
+    q = lambda *a, **k: oracle.quantize(*a, threads=th, **k)
+    gemm = lambda a, b: oracle.gemm_f64(a, b, threads=th)
     blocks = [
-        (lambda: gemm(deq(oracle.quantize(xs, oracle.ROW)), deq(oracle.quantize(ws, oracle.TILE16))), K),
-        (lambda: gemm(deq(oracle.quantize(dys, oracle.ROW, oracle.SR, sr_seed=7)),
-                      deq(oracle.quantize(wts, oracle.TILE16))), N),
-        (lambda: gemm(deq(oracle.quantize(dyc, oracle.COL, oracle.SR, rht=True, sr_seed=7, rht_seed=11)),
-                      deq(oracle.quantize(xc, oracle.COL, oracle.RNE, rht=True, rht_seed=11))), M),
+        (lambda: gemm(deq(q(xs, oracle.ROW)), deq(q(ws, oracle.TILE16))), K),
+        (lambda: gemm(deq(q(dys, oracle.ROW, oracle.SR, sr_seed=7)), deq(q(wts, oracle.TILE16))), N),
+        (lambda: gemm(deq(q(dyc, oracle.COL, oracle.SR, rht=True, sr_seed=7, rht_seed=11)),
+                      deq(q(xc, oracle.COL, oracle.RNE, rht=True, rht_seed=11))), M),
     ]
     n, flops, t0 = 0, 0.0, time.perf_counter()
     while True:
@@ -874,10 +899,57 @@ def oracle_sample(budget_s: float = 15.0, reps: int | None = None, rotate: bool 
         if (reps is not None and n >= reps) or (reps is None and el >= budget_s):
             break
     what = "one output block in turn of" if rotate else "three output blocks"
-    return {"value": round(flops / el / 1e12, 6), "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
+    how = "single-threaded C" if threads <= 1 else f"C on {threads} threads"
+    return {"value": round(flops / el / 1e12, 6), "unit": "TFLOP/s", "cores": max(1, threads), "kind": "oracle",
             "sample": f"{n} x {what} (Fprop 64x128 K={K}, Dgrad 64x128 K={N}, Wgrad 128x64 K={M}) "
-                      f"with their operand rows quantized by the oracle; single-threaded C; {el:.1f} s",
+                      f"with their operand rows quantized by the oracle; {how}; {el:.1f} s",
             "flops_per_rep": round(flops / n), "seconds": round(el, 3)}
+
+
+# Algorithmic bytes per element of one quantization with bf16 input, as the GPU sweep counts them:
+# the input read twice (tensor amax, then encode), codes 0.5 B, scales 1/16 B (16x16: 1/256 B).
+ORACLE_QUANT_MODES = [("row_rne", dict(block=0), 4.5625), ("row_sr", dict(block=0, round_mode=1, sr_seed=1), 4.5625),
+                      ("tile16_rne", dict(block=2), 2 + 2 + 0.5 + 1 / 256),
+                      ("col_rht_sr", dict(block=1, round_mode=1, rht=True, sr_seed=1, rht_seed=2), 4.5625)]
+
+
+def oracle_quantize_rates(rows: int, cols: int, threads: int) -> dict:
+    """GB/s (algorithmic bytes, as the GPU's) of the oracle quantizing a bf16 [rows, cols]
+    tensor shaped like dY (N(0, 1e-3)) in the four modes, on ``threads`` threads."""
+    import numpy as np
+    import oracle
+    import torch
+    from nvfp4_bit_quantized_gb300 import inputs
+    x = inputs.normal((rows, cols), 1e-3, 6).contiguous().view(torch.int16).numpy().view(np.uint16)
+    out = {}
+    for name, kw, bpe in ORACLE_QUANT_MODES:
+        t0 = time.perf_counter()
+        oracle.quantize(x, threads=threads, **kw)
+        el = time.perf_counter() - t0
+        out[name] = round(x.size * bpe / el / 1e9, 3)
+    return out
+
+
+def cpu_baseline(budget_s: float) -> dict:
+    """The oracle on this host's cores (sched_getaffinity count) and on one core: sampled GEMM
+    blocks (TFLOP/s; ``value``) and the four quantizer modes (GB/s; full dY size on all cores,
+    a 1/cores slice of its columns on one core)."""
+    import oracle
+    oracle.build()
+    cores = oracle.host_cores()
+    t0 = time.perf_counter()
+    g_all = oracle_sample(budget_s=budget_s / 4, threads=cores)
+    g_one = oracle_sample(budget_s=budget_s / 4, threads=1)
+    q_all = oracle_quantize_rates(M, N, cores)
+    q_one = oracle_quantize_rates(M, max(16, (N // cores) // 16 * 16), 1)
+    return {"value": g_all["value"], "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+            "sample": g_all["sample"],
+            "one_core": {"value": g_one["value"], "unit": "TFLOP/s", "sample": g_one["sample"]},
+            "quantize_gbs": {"all_cores": q_all, "one_core": q_one,
+                             "tensor_all_cores": f"bf16 [{M}, {N}] (dY-shaped, N(0, 1e-3))",
+                             "tensor_one_core": f"bf16 [{M}, {max(16, (N // cores) // 16 * 16)}]",
+                             "bytes_per_element": {n: round(b, 4) for n, _, b in ORACLE_QUANT_MODES}},
+            "seconds": round(time.perf_counter() - t0, 1)}
 
 
 def run_reference(args):
@@ -886,11 +958,12 @@ def run_reference(args):
         return
     import oracle
     oracle.build()
-    # a step is one of the three sampled GEMM blocks in turn, so K steps take ~0.15 K s
+    cores = oracle.host_cores()
+    # a step is one of the three sampled GEMM blocks in turn, on all of this host's cores
     for _ in range(args.warmup):
-        oracle_sample(reps=1, rotate=True)
+        oracle_sample(reps=1, rotate=True, threads=cores)
     t0 = time.perf_counter()
-    r = oracle_sample(reps=args.steps, rotate=True)
+    r = oracle_sample(reps=args.steps, rotate=True, threads=cores)
     el = time.perf_counter() - t0
     value = r["value"]
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
@@ -898,7 +971,7 @@ def run_reference(args):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64 (oracle)",
             "data": "synthetic", "config": {"workload": WORKLOAD, "M": M, "K": K, "N": N,
                                             "sample": "per step: one output block of one GEMM (Fprop, Dgrad, Wgrad in turn), full contraction"},
-            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": 1, "kind": "oracle", "sample": r["sample"]},
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle", "sample": r["sample"]},
             "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line))
 

@@ -55,6 +55,18 @@ def outlier_columns(x: torch.Tensor, frac: float, factor: float, seed: int) -> t
     return x
 
 
+def outlier_rows(x: torch.Tensor, frac: float, factor: float, seed: int) -> torch.Tensor:
+    """Scale round(frac * R) seeded rows of ``x`` by ``factor`` (in place; returns x)."""
+    R = x.shape[0]
+    n = int(round(frac * R))
+    if n == 0:
+        return x
+    g = _gen(seed, "cpu")
+    rows = torch.randperm(R, generator=g)[:n].to(x.device)
+    x[rows] = (x[rows].float() * factor).to(x.dtype)
+    return x
+
+
 # ---- the workloads ---------------------------------------------------------------
 
 def linear_layer(M: int, K: int, N: int, seed: int = 0, dtype=torch.bfloat16, device="cpu"):
@@ -75,6 +87,19 @@ def heavy_tailed_layer(M: int, K: int, N: int, seed: int = 0, device="cpu"):
     outlier_columns(X, 0.01, 50.0, seed + 100)
     W = normal((N, K), 0.02, seed + 1, torch.bfloat16, device)
     dY = student_t((M, N), 4, seed + 2, scale=1e-3, device=device)
+    return X, W, dY
+
+
+def heavy_tailed_token_outliers(M: int, K: int, N: int, seed: int = 0, device="cpu"):
+    """The heavy-tailed layer with its outliers along the tokens (the Wgrad contraction axis)
+    instead of the channels: X Student-t(3) and dY Student-t(4) x 1e-3 with the same seeded
+    1% of tokens (rows of both) x50, W ~ N(0,0.02); all bf16.  An outlier token dominates
+    every 16-token block of the column (Wgrad) quantization it falls in."""
+    X = student_t((M, K), 3, seed, device=device)
+    W = normal((N, K), 0.02, seed + 1, torch.bfloat16, device)
+    dY = student_t((M, N), 4, seed + 2, scale=1e-3, device=device)
+    outlier_rows(X, 0.01, 50.0, seed + 200)
+    outlier_rows(dY, 0.01, 50.0, seed + 200)
     return X, W, dY
 
 

@@ -3,8 +3,9 @@
 Only ``tests/``, ``__graft_entry__.smoke()`` and the ``cpu_baseline`` / reference
 legs of ``bench.py`` may import this package.  The CUDA path shares nothing with
 it.  The arithmetic lives in ``nvfp4_oracle.c`` (plain C, single-threaded,
-``-ffp-contract=off``); this module only compiles it with gcc and marshals numpy
-arrays through ctypes.  Each C function cites the passage of the news page
+``-ffp-contract=off``; ``threads=`` runs the same per-row steps on several threads,
+only to time the oracle on all host cores); this module only compiles it with gcc
+and marshals numpy arrays through ctypes.  Each C function cites the passage of the news page
 "NVIDIA NVFP4 paper: 4-bit pretrain hits FP8 parity (12B, 10T tokens)" it
 follows, and marks every reading the page leaves open.
 """
@@ -28,7 +29,7 @@ RNE, SR = 0, 1
 ROW, COL, TILE16 = 0, 1, 2
 ERR_NONFINITE = 7
 
-_CFLAGS = ["-O2", "-std=c11", "-fPIC", "-shared", "-ffp-contract=off", "-fno-fast-math",
+_CFLAGS = ["-O2", "-std=c11", "-fPIC", "-shared", "-pthread", "-ffp-contract=off", "-fno-fast-math",
            "-Wall", "-Wno-unused-function"]
 
 
@@ -67,6 +68,10 @@ def _load():
         "orc_dequant": (None, [P, P, c.c_float, c.c_int64, c.c_int64, c.c_int, c.c_int64,
                                c.c_int64, P]),
         "orc_gemm_f64": (None, [P, P, c.c_int64, c.c_int64, c.c_int64, P]),
+        "orc_quantize_mt": (c.c_int, [P, c.c_int, c.c_int64, c.c_int64, c.c_int64, c.c_int, c.c_int,
+                                      c.c_int, c.c_uint64, c.c_uint32, c.c_uint64, P, P, P, P,
+                                      c.c_int64, c.c_int64, c.c_int]),
+        "orc_gemm_f64_mt": (None, [P, P, c.c_int64, c.c_int64, c.c_int64, P, c.c_int]),
         "orc_e4m3_encode_array": (None, [P, c.c_int64, P]),
         "orc_e2m1_encode_rne_array": (None, [P, c.c_int64, P]),
         "orc_e2m1_encode_sr_array": (None, [P, P, c.c_int64, P]),
@@ -160,13 +165,14 @@ def rht16(v, sign_mask: int) -> np.ndarray:
 
 def quantize(x: np.ndarray, block: int, round_mode: int = RNE, rht: bool = False,
              sr_seed: int = 0, sr_offset: int = 0, rht_seed: int = 0,
-             row_begin: int = 0, row_end: int = -1, ldx: int | None = None) -> dict:
+             row_begin: int = 0, row_end: int = -1, ldx: int | None = None, threads: int = 1) -> dict:
     """Quantize ``x`` ([R, C] float32, or uint16 holding bf16 bits).
 
     Returns dict(codes, scales, s_dec, amax, rows, cols).  For ``block == COL``
     the operand is x^T: codes [C, R/2], scales [C, R/16].  For ``TILE16`` the
     scales are the [R/16, C/16] tile grid.  Rows outside [row_begin, row_end)
-    of the operand are left zero.
+    of the operand are left zero.  ``threads`` > 1 splits the same per-row work among
+    that many threads (identical results; for timing on all host cores).
     """
     if x.dtype == np.float32:
         dtype = F32
@@ -185,9 +191,9 @@ def quantize(x: np.ndarray, block: int, round_mode: int = RNE, rht: bool = False
         scales = np.zeros((rows, cols // 16), dtype=np.uint8)
     s_dec = np.zeros(1, dtype=np.float32)
     amax = np.zeros(1, dtype=np.float32)
-    st = _load().orc_quantize(_ptr(x), dtype, R, C, ld, block, round_mode, int(bool(rht)),
-                              sr_seed, sr_offset, rht_seed, _ptr(codes), _ptr(scales),
-                              _ptr(s_dec), _ptr(amax), row_begin, row_end)
+    args = (_ptr(x), dtype, R, C, ld, block, round_mode, int(bool(rht)), sr_seed, sr_offset, rht_seed,
+            _ptr(codes), _ptr(scales), _ptr(s_dec), _ptr(amax), row_begin, row_end)
+    st = _load().orc_quantize(*args) if threads <= 1 else _load().orc_quantize_mt(*args, int(threads))
     if st == ERR_NONFINITE:
         raise FloatingPointError("non-finite tensor amax")
     if st != 0:
@@ -207,16 +213,27 @@ def dequant(q: dict, row_begin: int = 0, row_end: int | None = None) -> np.ndarr
     return out
 
 
-def gemm_f64(A: np.ndarray, B: np.ndarray) -> np.ndarray:
-    """C = A . B^T in fp64 (plain dot products)."""
+def gemm_f64(A: np.ndarray, B: np.ndarray, threads: int = 1) -> np.ndarray:
+    """C = A . B^T in fp64 (plain dot products); ``threads`` > 1 splits C's rows."""
     A = np.ascontiguousarray(A, dtype=np.float64)
     B = np.ascontiguousarray(B, dtype=np.float64)
     M, K = A.shape
     N, K2 = B.shape
     assert K == K2
     C = np.empty((M, N), dtype=np.float64)
-    _load().orc_gemm_f64(_ptr(A), _ptr(B), M, N, K, _ptr(C))
+    if threads <= 1:
+        _load().orc_gemm_f64(_ptr(A), _ptr(B), M, N, K, _ptr(C))
+    else:
+        _load().orc_gemm_f64_mt(_ptr(A), _ptr(B), M, N, K, _ptr(C), int(threads))
     return C
+
+
+def host_cores() -> int:
+    """Cores this process may run on (sched_getaffinity), for the threaded timings."""
+    try:
+        return len(os.sched_getaffinity(0))
+    except (AttributeError, OSError):
+        return os.cpu_count() or 1
 
 
 # --- squared ReLU of the dense MLP block (plain numpy float32) -------------------------

@@ -1,6 +1,7 @@
 /*
- * nvfp4_oracle.c -- plain, slow, single-threaded CPU oracle for NVFP4 quantization
- * and the block-scaled GEMM.
+ * nvfp4_oracle.c -- plain, slow CPU oracle for NVFP4 quantization and the
+ * block-scaled GEMM (single-threaded; orc_quantize_mt / orc_gemm_f64_mt split the
+ * same per-row work among threads only to time it on all host cores).
  *
  * TEST INFRASTRUCTURE ONLY.  Only tests/, __graft_entry__.smoke() and the
  * cpu_baseline / reference legs of bench.py may load this library.  The CUDA
@@ -36,6 +37,7 @@
  */
 #include <float.h>
 #include <math.h>
+#include <pthread.h>
 #include <stdint.h>
 #include <stdlib.h>
 #include <string.h>
@@ -329,6 +331,115 @@ static float block_multiplier(uint8_t sb_code, float s_enc) {
 }
 
 /*
+ * The steps of one quantization over a range of the operand's rows.  orc_quantize runs
+ * each step over all rows in turn; orc_quantize_mt runs the same steps with the rows split
+ * among threads.  Every element's arithmetic is the same either way, and the tensor amax is
+ * a maximum of non-negative values, which does not depend on the order it is taken in.
+ */
+typedef struct {
+    const void* x;
+    int dtype;
+    int64_t ldx, rows, cols;
+    int block, round_mode, rht;
+    uint64_t sr_seed;
+    uint32_t sr_offset, sign_mask;
+    uint8_t* codes;
+    uint8_t* scales;
+    float* T;                              /* the operand in fp32, [rows, cols] */
+    float s_enc;
+} QuantJob;
+
+/* Step 1 for rows [r0, r1): T in fp32, with the RHT for the Wgrad operands. */
+static void q_build_rows(QuantJob* q, int64_t r0, int64_t r1) {
+    for (int64_t i = r0; i < r1; ++i)
+        for (int64_t j = 0; j < q->cols; ++j)
+            q->T[i * q->cols + j] = (q->block == ORC_BLOCK_1X16_COL) ? load_elem(q->x, q->dtype, q->ldx, j, i)
+                                                                   : load_elem(q->x, q->dtype, q->ldx, i, j);
+    if (q->rht)
+        for (int64_t i = r0; i < r1; ++i)
+            for (int64_t j = 0; j < q->cols; j += 16)
+                orc_rht16(&q->T[i * q->cols + j], q->sign_mask, &q->T[i * q->cols + j]);
+}
+
+/* Step 2 over rows [r0, r1): the largest |T| and whether every value is finite. */
+static void q_amax_rows(const QuantJob* q, int64_t r0, int64_t r1, float* amax, int* finite) {
+    float m = 0.0f;
+    int fin = 1;
+    for (int64_t i = r0 * q->cols; i < r1 * q->cols; ++i) {
+        float a = fabsf(q->T[i]);
+        if (!isfinite(a)) fin = 0;
+        else if (a > m) m = a;
+    }
+    *amax = m;
+    *finite = fin;
+}
+
+/* Steps 4-5 for rows [r0, r1) (multiples of the block height): block scales, element
+   codes, nibble packing. */
+static void q_encode_rows(QuantJob* q, int64_t r0, int64_t r1) {
+    const int64_t cols = q->cols;
+    const float s_enc = q->s_enc;
+    uint32_t stream = (q->block == ORC_BLOCK_1X16_COL) ? 1u : 0u;
+    int bh = (q->block == ORC_BLOCK_16X16) ? 16 : 1;   /* block height in rows */
+    for (int64_t i0 = r0; i0 < r1; i0 += bh) {
+        for (int64_t j0 = 0; j0 < cols; j0 += 16) {
+            float amax_b = 0.0f;
+            for (int di = 0; di < bh; ++di)
+                for (int dj = 0; dj < 16; ++dj) {
+                    float a = fabsf(q->T[(i0 + di) * cols + j0 + dj]);
+                    if (a > amax_b) amax_b = a;
+                }
+            uint8_t sb = block_scale_code(amax_b, s_enc);
+            float e_b = block_multiplier(sb, s_enc);
+            if (q->block == ORC_BLOCK_16X16) q->scales[(i0 / 16) * (cols / 16) + j0 / 16] = sb;
+            else q->scales[i0 * (cols / 16) + j0 / 16] = sb;
+            for (int di = 0; di < bh; ++di)
+                for (int dj = 0; dj < 16; ++dj) {
+                    int64_t i = i0 + di, j = j0 + dj;
+                    float y = q->T[i * cols + j] * e_b;
+                    int code;
+                    if (q->round_mode == ORC_ROUND_SR)
+                        code = orc_e2m1_encode_sr(y, orc_sr_bits(q->sr_seed, stream, q->sr_offset,
+                                                                 (uint64_t)(i * cols + j)));
+                    else
+                        code = orc_e2m1_encode_rne(y);
+                    uint8_t* byte = &q->codes[i * (cols / 2) + j / 2];
+                    if ((j & 1) == 0) *byte = (uint8_t)((*byte & 0xF0) | code);
+                    else *byte = (uint8_t)((*byte & 0x0F) | (code << 4));
+                }
+        }
+    }
+}
+
+/* Argument checks and the job shared by both entry points; 0 or an ORC_ERR_* code. */
+static int q_setup(QuantJob* q, const void* x, int dtype, int64_t R, int64_t C, int64_t ldx, int block,
+                   int round_mode, int rht, uint64_t sr_seed, uint32_t sr_offset, uint64_t rht_seed,
+                   uint8_t* codes, uint8_t* scales, int64_t* row_begin, int64_t* row_end) {
+    if (R < 0 || C < 0 || ldx < C) return ORC_ERR_ARG;
+    if (rht && block != ORC_BLOCK_1X16_COL) return ORC_ERR_ARG;
+    q->rows = (block == ORC_BLOCK_1X16_COL) ? C : R;
+    q->cols = (block == ORC_BLOCK_1X16_COL) ? R : C;
+    if (q->cols % 16 != 0) return ORC_ERR_ARG;
+    if (block == ORC_BLOCK_16X16 && q->rows % 16 != 0) return ORC_ERR_ARG;
+    if (*row_end < 0 || *row_end > q->rows) *row_end = q->rows;
+    if (*row_begin < 0) *row_begin = 0;
+    if (block == ORC_BLOCK_16X16 && (*row_begin % 16 != 0 || *row_end % 16 != 0)) return ORC_ERR_ARG;
+    q->x = x; q->dtype = dtype; q->ldx = ldx; q->block = block; q->round_mode = round_mode; q->rht = rht;
+    q->sr_seed = sr_seed; q->sr_offset = sr_offset; q->sign_mask = rht ? orc_rht_sign_mask(rht_seed) : 0u;
+    q->codes = codes; q->scales = scales; q->s_enc = 1.0f;
+    q->T = (float*)malloc(sizeof(float) * (size_t)(q->rows * q->cols > 0 ? q->rows * q->cols : 1));
+    return q->T ? ORC_OK : ORC_ERR_ARG;
+}
+
+/* Step 3: the tensor scale from amax_t; writes s_dec and amax_t. */
+static void q_tensor_scale(QuantJob* q, float amax_t, float* s_dec_out, float* amax_out) {
+    if (amax_out) *amax_out = amax_t;
+    q->s_enc = tensor_s_enc(amax_t);
+    float s_dec = 1.0f / q->s_enc;
+    if (s_dec_out) *s_dec_out = s_dec;
+}
+
+/*
  * orc_quantize: quantize x [R, C] (row pitch ldx elements) to NVFP4.
  *
  * The quantized operand T has logical shape [rows, cols] with blocks along cols:
@@ -348,77 +459,95 @@ int orc_quantize(const void* x, int dtype, int64_t R, int64_t C, int64_t ldx,
                  uint64_t sr_seed, uint32_t sr_offset, uint64_t rht_seed,
                  uint8_t* codes, uint8_t* scales, float* s_dec_out, float* amax_out,
                  int64_t row_begin, int64_t row_end) {
-    if (R < 0 || C < 0 || ldx < C) return ORC_ERR_ARG;
-    if (rht && block != ORC_BLOCK_1X16_COL) return ORC_ERR_ARG;
-    int64_t rows = (block == ORC_BLOCK_1X16_COL) ? C : R;
-    int64_t cols = (block == ORC_BLOCK_1X16_COL) ? R : C;
-    if (cols % 16 != 0) return ORC_ERR_ARG;
-    if (block == ORC_BLOCK_16X16 && rows % 16 != 0) return ORC_ERR_ARG;
-    if (row_end < 0 || row_end > rows) row_end = rows;
-    if (row_begin < 0) row_begin = 0;
-    if (block == ORC_BLOCK_16X16 && (row_begin % 16 != 0 || row_end % 16 != 0)) return ORC_ERR_ARG;
-
+    QuantJob q;
+    int st = q_setup(&q, x, dtype, R, C, ldx, block, round_mode, rht, sr_seed, sr_offset, rht_seed, codes, scales,
+                     &row_begin, &row_end);
+    if (st != ORC_OK) return st;
     /* Step 1: T in fp32 (with the RHT for the Wgrad operands). */
-    float* T = (float*)malloc(sizeof(float) * (size_t)(rows * cols > 0 ? rows * cols : 1));
-    if (!T) return ORC_ERR_ARG;
-    for (int64_t i = 0; i < rows; ++i)
-        for (int64_t j = 0; j < cols; ++j)
-            T[i * cols + j] = (block == ORC_BLOCK_1X16_COL) ? load_elem(x, dtype, ldx, j, i)
-                                                          : load_elem(x, dtype, ldx, i, j);
-    if (rht) {
-        uint32_t mask = orc_rht_sign_mask(rht_seed);
-        for (int64_t i = 0; i < rows; ++i)
-            for (int64_t j = 0; j < cols; j += 16) orc_rht16(&T[i * cols + j], mask, &T[i * cols + j]);
-    }
-
+    q_build_rows(&q, 0, q.rows);
     /* Step 2: tensor amax over T, exactly as it will be quantized. */
+    float amax_t;
+    int finite;
+    q_amax_rows(&q, 0, q.rows, &amax_t, &finite);
+    if (!finite) { free(q.T); return ORC_ERR_NONFINITE; }
+    /* Step 3: tensor scale. */
+    q_tensor_scale(&q, amax_t, s_dec_out, amax_out);
+    /* Steps 4-5: block scales, element codes, nibble packing. */
+    q_encode_rows(&q, row_begin, row_end);
+    free(q.T);
+    return ORC_OK;
+}
+
+/* ------------------------------------------------------------------------- */
+/* The same quantization and the fp64 GEMM with their rows split among threads */
+/* (POSIX threads), for timing the oracle on all of a machine's cores.  Results */
+/* equal the single-threaded functions' bit for bit.                           */
+/* ------------------------------------------------------------------------- */
+typedef struct {
+    QuantJob* q;
+    int phase;                             /* 0: build, 1: amax, 2: encode */
+    int64_t r0, r1;
+    float amax;
+    int finite;
+} QuantPart;
+
+static void* q_worker(void* arg) {
+    QuantPart* w = (QuantPart*)arg;
+    if (w->phase == 0) q_build_rows(w->q, w->r0, w->r1);
+    else if (w->phase == 1) q_amax_rows(w->q, w->r0, w->r1, &w->amax, &w->finite);
+    else q_encode_rows(w->q, w->r0, w->r1);
+    return NULL;
+}
+
+/* Runs `phase` over rows [r0, r1) in nthreads pieces (multiples of `align` rows). */
+static int q_run_phase(QuantJob* q, QuantPart* parts, int nthreads, int phase, int64_t r0, int64_t r1,
+                       int64_t align) {
+    int64_t n = r1 - r0;
+    int64_t per = ((n + nthreads - 1) / nthreads + align - 1) / align * align;
+    pthread_t tid[256];
+    int started = 0;
+    for (int t = 0; t < nthreads; ++t) {
+        parts[t].q = q;
+        parts[t].phase = phase;
+        parts[t].r0 = r0 + t * per < r1 ? r0 + t * per : r1;
+        parts[t].r1 = r0 + (t + 1) * per < r1 ? r0 + (t + 1) * per : r1;
+        parts[t].amax = 0.0f;
+        parts[t].finite = 1;
+    }
+    for (int t = 1; t < nthreads; ++t) {
+        if (pthread_create(&tid[t], NULL, q_worker, &parts[t]) != 0) break;
+        started = t;
+    }
+    for (int t = started + 1; t < nthreads; ++t) q_worker(&parts[t]);   /* threads that did not start */
+    q_worker(&parts[0]);
+    for (int t = 1; t <= started; ++t) pthread_join(tid[t], NULL);
+    return ORC_OK;
+}
+
+int orc_quantize_mt(const void* x, int dtype, int64_t R, int64_t C, int64_t ldx,
+                    int block, int round_mode, int rht,
+                    uint64_t sr_seed, uint32_t sr_offset, uint64_t rht_seed,
+                    uint8_t* codes, uint8_t* scales, float* s_dec_out, float* amax_out,
+                    int64_t row_begin, int64_t row_end, int nthreads) {
+    if (nthreads < 1) nthreads = 1;
+    if (nthreads > 256) nthreads = 256;
+    QuantJob q;
+    int st = q_setup(&q, x, dtype, R, C, ldx, block, round_mode, rht, sr_seed, sr_offset, rht_seed, codes, scales,
+                     &row_begin, &row_end);
+    if (st != ORC_OK) return st;
+    QuantPart parts[256];
+    q_run_phase(&q, parts, nthreads, 0, 0, q.rows, 1);
+    q_run_phase(&q, parts, nthreads, 1, 0, q.rows, 1);
     float amax_t = 0.0f;
     int finite = 1;
-    for (int64_t i = 0; i < rows * cols; ++i) {
-        float a = fabsf(T[i]);
-        if (!isfinite(a)) finite = 0;
-        else if (a > amax_t) amax_t = a;
+    for (int t = 0; t < nthreads; ++t) {
+        if (!parts[t].finite) finite = 0;
+        if (parts[t].amax > amax_t) amax_t = parts[t].amax;
     }
-    if (!finite) { free(T); return ORC_ERR_NONFINITE; }
-    if (amax_out) *amax_out = amax_t;
-
-    /* Step 3: tensor scale. */
-    float s_enc = tensor_s_enc(amax_t);
-    float s_dec = 1.0f / s_enc;
-    if (s_dec_out) *s_dec_out = s_dec;
-
-    /* Steps 4-5: block scales, element codes, nibble packing. */
-    uint32_t stream = (block == ORC_BLOCK_1X16_COL) ? 1u : 0u;
-    int bh = (block == ORC_BLOCK_16X16) ? 16 : 1;       /* block height in rows */
-    for (int64_t i0 = row_begin; i0 < row_end; i0 += bh) {
-        for (int64_t j0 = 0; j0 < cols; j0 += 16) {
-            float amax_b = 0.0f;
-            for (int di = 0; di < bh; ++di)
-                for (int dj = 0; dj < 16; ++dj) {
-                    float a = fabsf(T[(i0 + di) * cols + j0 + dj]);
-                    if (a > amax_b) amax_b = a;
-                }
-            uint8_t sb = block_scale_code(amax_b, s_enc);
-            float e_b = block_multiplier(sb, s_enc);
-            if (block == ORC_BLOCK_16X16) scales[(i0 / 16) * (cols / 16) + j0 / 16] = sb;
-            else scales[i0 * (cols / 16) + j0 / 16] = sb;
-            for (int di = 0; di < bh; ++di)
-                for (int dj = 0; dj < 16; ++dj) {
-                    int64_t i = i0 + di, j = j0 + dj;
-                    float y = T[i * cols + j] * e_b;
-                    int code;
-                    if (round_mode == ORC_ROUND_SR)
-                        code = orc_e2m1_encode_sr(y, orc_sr_bits(sr_seed, stream, sr_offset,
-                                                                 (uint64_t)(i * cols + j)));
-                    else
-                        code = orc_e2m1_encode_rne(y);
-                    uint8_t* byte = &codes[i * (cols / 2) + j / 2];
-                    if ((j & 1) == 0) *byte = (uint8_t)((*byte & 0xF0) | code);
-                    else *byte = (uint8_t)((*byte & 0x0F) | (code << 4));
-                }
-        }
-    }
-    free(T);
+    if (!finite) { free(q.T); return ORC_ERR_NONFINITE; }
+    q_tensor_scale(&q, amax_t, s_dec_out, amax_out);
+    q_run_phase(&q, parts, nthreads, 2, row_begin, row_end, block == ORC_BLOCK_16X16 ? 16 : 1);
+    free(q.T);
     return ORC_OK;
 }
 
@@ -441,13 +570,47 @@ void orc_dequant(const uint8_t* codes, const uint8_t* scales, float s_dec,
 }
 
 /* O8. C[M, N] = A[M, K] . B[N, K]^T in fp64, plain dot products in k order. */
-void orc_gemm_f64(const double* A, const double* B, int64_t M, int64_t N, int64_t K, double* C) {
-    for (int64_t m = 0; m < M; ++m)
+static void gemm_rows(const double* A, const double* B, int64_t m0, int64_t m1, int64_t N, int64_t K, double* C) {
+    for (int64_t m = m0; m < m1; ++m)
         for (int64_t n = 0; n < N; ++n) {
             double s = 0.0;
             for (int64_t k = 0; k < K; ++k) s += A[m * K + k] * B[n * K + k];
             C[m * N + n] = s;
         }
+}
+
+void orc_gemm_f64(const double* A, const double* B, int64_t M, int64_t N, int64_t K, double* C) {
+    gemm_rows(A, B, 0, M, N, K, C);
+}
+
+typedef struct { const double* A; const double* B; int64_t m0, m1, N, K; double* C; } GemmPart;
+
+static void* gemm_worker(void* arg) {
+    GemmPart* g = (GemmPart*)arg;
+    gemm_rows(g->A, g->B, g->m0, g->m1, g->N, g->K, g->C);
+    return NULL;
+}
+
+/* orc_gemm_f64 with the rows of C split among nthreads threads (same dot products). */
+void orc_gemm_f64_mt(const double* A, const double* B, int64_t M, int64_t N, int64_t K, double* C, int nthreads) {
+    if (nthreads < 1) nthreads = 1;
+    if (nthreads > 256) nthreads = 256;
+    GemmPart parts[256];
+    pthread_t tid[256];
+    int64_t per = (M + nthreads - 1) / nthreads;
+    int started = 0;
+    for (int t = 0; t < nthreads; ++t) {
+        int64_t a = t * per < M ? t * per : M, b = (t + 1) * per < M ? (t + 1) * per : M;
+        GemmPart g = {A, B, a, b, N, K, C};
+        parts[t] = g;
+    }
+    for (int t = 1; t < nthreads; ++t) {
+        if (pthread_create(&tid[t], NULL, gemm_worker, &parts[t]) != 0) break;
+        started = t;
+    }
+    for (int t = started + 1; t < nthreads; ++t) gemm_worker(&parts[t]);
+    gemm_worker(&parts[0]);
+    for (int t = 1; t <= started; ++t) pthread_join(tid[t], NULL);
 }
 
 /* ------------------------------------------------------------------------- */

@@ -111,8 +111,14 @@ def test_mlp_block_small_full_oracle(nv, oracle_mod, fused):
     dY = inputs.normal((T, d), 1e-3, 3, device="cuda")
     nv.reset_status()
     o = mlp_step(nv, X, W1, W2, dY, fused_dgrad=fused, fused_fwd=fused)
-    if fused:       # dA is never formed in the fused step; the plain GEMM gives the one dH must follow
-        o["dA"] = nv.gemm(o["dyq"], o["w2q"].transposed(), torch.bfloat16)
+    if fused:       # dA is never formed in the fused step; the plain GEMM on the same (CTA-pair)
+        # kernel gives the one dH must follow bit for bit
+        from nvfp4_bit_quantized_gb300 import _lib as L
+        L.lib().nvfp4_gemm_force_path(2)
+        try:
+            o["dA"] = nv.gemm(o["dyq"], o["w2q"].transposed(), torch.bfloat16)
+        finally:
+            L.lib().nvfp4_gemm_force_path(0)
     assert nv.status_query() == 0
     om = oracle_mod
 

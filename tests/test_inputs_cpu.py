@@ -48,3 +48,16 @@ def test_heavy_tailed_layer_structure():
     assert kurt > 6                                            # a normal's kurtosis is 3
     g = dY.float().flatten().double()
     assert abs(g.std().item() / 1e-3 - math.sqrt(2)) < 0.2     # t(4) has variance 4 / (4 - 2) = 2
+
+
+def test_token_outlier_layer_structure():
+    """Outliers along the tokens: the same 1% of rows of X and dY are x50, no channel is."""
+    X, W, dY = inputs.heavy_tailed_token_outliers(2048, 512, 384, seed=0)
+    assert X.shape == (2048, 512) and W.shape == (384, 512) and dY.shape == (2048, 384)
+    rx = X.float().abs().median(dim=1).values
+    rg = dY.float().abs().median(dim=1).values
+    bx = set((rx > 10 * rx.median()).nonzero().flatten().tolist())
+    bg = set((rg > 10 * rg.median()).nonzero().flatten().tolist())
+    assert len(bx) == round(0.01 * 2048) and bx == bg              # 20 tokens, the same in X and dY
+    cx = X.float().abs().median(dim=0).values
+    assert (cx > 10 * cx.median()).sum() == 0                      # no outlier channels
