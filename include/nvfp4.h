@@ -237,8 +237,8 @@ NVFP4_API nvfp4_status nvfp4_gemm_sqrelu_bwd_maxima(const nvfp4_qtensor* A, cons
 
 /*
  * Bytes of the partial-maxima buffer the *_maxima GEMMs write on CUDA device `device`: two
- * halves (|x|, then |RHT(x)| / 4) of one uint32 partial per epilogue warp, four warps per CTA
- * and at most one CTA per multiprocessor, so 2 * 4 * (multiprocessor count) * 4 bytes.  0 if the
+ * halves (|x|, then |RHT(x)| / 4) of one uint32 partial per epilogue warp, eight warps per CTA
+ * and at most one CTA per multiprocessor, so 2 * 8 * (multiprocessor count) * 4 bytes.  0 if the
  * device cannot be queried.  A buffer of B bytes is read as two halves of B / 8 partials.
  */
 NVFP4_API size_t nvfp4_sqrelu_maxima_bytes(int32_t device);

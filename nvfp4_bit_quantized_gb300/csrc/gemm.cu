@@ -565,28 +565,34 @@ gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
 // receives its own 128 rows of the accumulator.  Per CTA and stage the ring
 // holds A 16 KB + B 16 KB + scales 6 KB = 38 KB, five stages deep.
 //
+// Sixteen warps in four warpgroups; registers move from the first two warpgroups to the
+// epilogue's (setmaxnreg: 96 each for warpgroups 0-1, 160 each for 2-3):
 //   warp 0      TMA producer of the codes tiles (two tensor copies per K tile);
-//   warp 10     producer of the scale tiles (three 2 KB bulk copies per K tile).
+//   warp 2      producer of the scale tiles (three 2 KB bulk copies per K tile).
 //               Issuing a TMA copy occupies the issuing thread for about 100
 //               cycles, so with one thread issuing all five the codes tiles of a
 //               freed stage started late;
 //   warp 1      (leader) one lane issues the MMAs and commits them to both CTAs;
-//   warps 6-9   scale warps: shared memory -> registers -> TMEM (tcgen05.st), then
+//   warps 4-7   scale warps: shared memory -> registers -> TMEM (tcgen05.st), then
 //               tell the leader that this CTA's scales and codes tiles are ready;
-//   warps 2-5   epilogue: tcgen05.ld of the 32-lane quarter, x alpha (packed
-//               multiplies), bf16, 128-byte swizzled 32 x 64 boxes, TMA stores.
-//               Each warp has two box slots (32 KB in all): it converts two boxes
-//               while the rest of the accumulator is loaded, hands the accumulator
-//               back, and only then issues the stores and converts the last two.
+//   warps 8-15  epilogue, two warps per 32-lane TMEM quarter, each owning 128 of the
+//               256 accumulator columns: two tcgen05.ld of 64 columns, one wait, and
+//               the accumulator is handed back -- the MMAs of the next tile start
+//               while the warps convert (x alpha with packed multiplies, bf16) their
+//               two 32 x 64 boxes through one 128-byte swizzled 4 KB slot each and
+//               TMA-store them.
 // Cross-CTA signals: the leader's MMA commits are multicast to both CTAs'
 // barriers; the follower's scale and epilogue warps arrive remotely on the
 // leader's sf_ready / acc_empty barriers.
 // ============================================================================
-constexpr int P_THREADS = 352;                                         // 11 warps
+constexpr int P_THREADS = 512;                                         // 16 warps (4 warpgroups)
+constexpr int P_EPI_WARP0 = 8;                                         // epilogue warps 8-15
+constexpr int P_REGS_LOW = 96, P_REGS_HIGH = 160;                      // setmaxnreg split (of 128 each at launch)
+static_assert(2 * 128 * P_REGS_LOW + 2 * 128 * P_REGS_HIGH <= P_THREADS * 128, "register split within the launch's registers");
 constexpr int P_B_BYTES = 128 * BKB;                                   // half of N per CTA
 constexpr int P_STAGE_BYTES = A_BYTES + P_B_BYTES + SFA_BYTES + SFB_BYTES;   // 38 KB
 constexpr int P_STAGES = 5;
-constexpr int P_STAGING_BYTES = 4 * 2 * BOX_BYTES;                     // two boxes per epilogue warp
+constexpr int P_STAGING_BYTES = 8 * BOX_BYTES;                         // one box slot per epilogue warp
 constexpr int P_RING_BYTES = P_STAGES * P_STAGE_BYTES;
 constexpr int P_SMEM_BYTES = P_RING_BYTES + P_STAGING_BYTES + BAR_BYTES + 1024;   // + base alignment
 static_assert(P_STAGE_BYTES % 1024 == 0, "pair stages must stay 1024-byte aligned");
@@ -692,47 +698,6 @@ __device__ __forceinline__ void box_to_smem_dsqr(const uint32_t (&v)[64], uint8_
     }
 }
 
-// 64 accumulator columns -> x alpha -> 32 packed bf16 words (the same rounding as box_to_smem),
-// and those words into a box: word 4c + i of row `lane` in 16-byte chunk c (swizzled).
-__device__ __forceinline__ void pack_bf16_64(const uint32_t (&v)[64], uint32_t (&pk)[32], float alpha) {
-    const float2 al = make_float2(alpha, alpha);
-#pragma unroll
-    for (int i = 0; i < 32; ++i) {
-        const __nv_bfloat162 h = __float22bfloat162_rn(
-            __fmul2_rn(make_float2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1])), al));
-        pk[i] = *reinterpret_cast<const uint32_t*>(&h);
-    }
-}
-__device__ __forceinline__ void packed_to_box(const uint32_t (&pk)[32], uint8_t* box, int lane) {
-    uint8_t* row = box + lane * 128;
-#pragma unroll
-    for (int c = 0; c < 8; ++c)
-        *reinterpret_cast<uint4*>(row + ((c ^ (lane & 7)) << 4)) =
-            make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
-}
-
-// The squared-ReLU backward of box_to_smem_dsqr from dA already packed to bf16 (pack_bf16_64):
-// the H box in the slot is replaced by dH, with the same arithmetic.
-__device__ __forceinline__ void packed_dsqr_to_box(const uint32_t (&pk)[32], uint8_t* box, int lane) {
-    uint8_t* row = box + lane * 128;
-#pragma unroll
-    for (int c = 0; c < 8; ++c) {
-        uint4* slot = reinterpret_cast<uint4*>(row + ((c ^ (lane & 7)) << 4));
-        const uint4 hq = *slot;
-        const uint32_t hw[4] = {hq.x, hq.y, hq.z, hq.w};
-        uint32_t w[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const uint32_t da = pk[4 * c + i];
-            const float hl = bf16_lo(hw[i]), hh = bf16_hi(hw[i]);
-            const float2 t = make_float2(hl > 0.0f ? __fmul_rn(2.0f, hl) : 0.0f, hh > 0.0f ? __fmul_rn(2.0f, hh) : 0.0f);
-            const __nv_bfloat162 dh = __float22bfloat162_rn(__fmul2_rn(make_float2(bf16_lo(da), bf16_hi(da)), t));
-            w[i] = *reinterpret_cast<const uint32_t*>(&dh);
-        }
-        *slot = make_uint4(w[0], w[1], w[2], w[3]);
-    }
-}
-
 template <int EPI>
 __device__ __forceinline__ void box_out(const uint32_t (&v)[64], uint8_t* box, int lane, float alpha) {
     if constexpr (EPI == EPI_DSQR || EPI == EPI_DSQR_AMAX) box_to_smem_dsqr(v, box, lane, alpha);
@@ -801,8 +766,8 @@ gemm_nvfp4_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_con
     uint64_t* acc_full = sf_ready + STAGES;              // accumulator complete (leader's commit)
     uint64_t* acc_empty = acc_full + 1;                  // leader: 8 epilogue warps drained
     uint64_t* drain = acc_empty + 1;
-    uint64_t* h_full = drain + 1;                        // DSQR: per epilogue warp, its H boxes landed
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(h_full + 4);
+    uint64_t* h_full = drain + 1;                        // DSQR: per epilogue warp, its H box landed
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(h_full + 8);
     volatile uint32_t* abort_flag = tmem_slot + 1;
     // identical in both CTAs (same kernel, same dynamic smem base), so layout_ok is uniform
     const bool layout_ok = (reinterpret_cast<uintptr_t>(tmem_slot + 2) - reinterpret_cast<uintptr_t>(smem_raw)) <=
@@ -822,9 +787,9 @@ gemm_nvfp4_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_con
             mbar_init(&sf_ready[s], 8);
         }
         mbar_init(acc_full, 1);
-        mbar_init(acc_empty, 8);
+        mbar_init(acc_empty, 16);
         mbar_init(drain, 1);
-        for (int q = 0; q < 4; ++q) mbar_init(&h_full[q], 1);
+        for (int e = 0; e < 8; ++e) mbar_init(&h_full[e], 1);
         *abort_flag = 0u;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
@@ -842,10 +807,14 @@ gemm_nvfp4_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_con
     const int cluster = blockIdx.x >> 1, nclusters = gridDim.x >> 1;
     const uint32_t sf_ready_leader = map_to_rank(smem_addr(&sf_ready[0]), 0);
     const uint32_t acc_empty_leader = map_to_rank(smem_addr(acc_empty), 0);
-
-    if (warp == 0 || warp == 10) {
+    // Registers move from the producer / MMA / scale warpgroups (0-1) to the epilogue's (2-3):
+    // each warpgroup enters one branch whose first instruction is its setmaxnreg, so the
+    // compiler allocates every role's code within its share.
+    if (warp < P_EPI_WARP0) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" :: "n"(P_REGS_LOW));
+    if (warp == 0 || warp == 2) {
         // ------------------------------------------------ producers (each CTA, its own halves):
-        // warp 0 the codes tiles, warp 10 the scale tiles, both over the same ring
+        // warp 0 the codes tiles, warp 2 the scale tiles, both over the same ring
         if (lane == 0) {
             const bool codes = warp == 0;
             uint64_t* landed = codes ? full : sf_loaded;
@@ -933,8 +902,8 @@ gemm_nvfp4_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_con
                 mbar_wait_bounded(drain, 0u, p.timeout_ns, nullptr, p.dev_status);
             }
         }
-    } else if (warp >= 6) {
-        // ------------------------------------------------ scale warps 6-9 (each CTA, its own TMEM)
+    } else if (warp >= 4 && warp < P_EPI_WARP0) {
+        // ------------------------------------------------ scale warps 4-7 (each CTA, its own TMEM)
         const int q = warp & 3;
         const uint32_t tq = tmem + ((uint32_t)(q * 32) << 16);
         uint32_t stage = 0, phase = 0;
@@ -1011,128 +980,107 @@ gemm_nvfp4_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_con
                 if (++stage == STAGES) { stage = 0; phase ^= 1u; }
             }
         }
+    }
     } else {
-        // ------------------------------------------------ epilogue (warps 2-5, each CTA, its 128 rows)
-        const int q = warp & 3;
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" :: "n"(P_REGS_HIGH));
+        // ------------------------------------------------ epilogue (warps 8-15, each CTA, its 128 rows)
+        const int e = warp - P_EPI_WARP0;                // 0-7
+        const int q = warp & 3;                          // TMEM lane quarter (warp % 4)
+        const int h = e >> 2;                            // accumulator columns [128 h, 128 h + 128)
         const float alpha = MX ? 1.0f : __fmul_rn(*p.sdec_a, *p.sdec_b);   // MXFP4 has no tensor scale
-        const uint32_t tmem_row = tmem + ((uint32_t)(q * 32) << 16);
-        uint8_t* stg = staging + q * (2 * BOX_BYTES);
+        const uint32_t tmem_row = tmem + ((uint32_t)(q * 32) << 16) + ACC_COL + 128u * h;
+        uint8_t* slot = staging + e * BOX_BYTES;
         const uint64_t stream_pol = l2_evict_first_policy();
         uint32_t acc_phase = 0, h_phase = 0;
-        bool h_pending = false;                          // DSQR: H boxes in flight into the slots
+        bool h_pending = false;                          // DSQR: an H box in flight into the slot
         uint32_t mabs = 0u, mrht = 0u;                   // AMAX: running maxima (float bits)
         const uint32_t sign_mask = AMAX ? rht_sign_mask(p.rht_seed) : 0u;
         bool ok = true;
         for (int tile = cluster; tile < tiles && ok; tile += nclusters) {
             int mp, nt;
             tile_coords(p, tile, m_pairs, mp, nt);
-            const int m0 = mp * 256 + (int)rank * 128 + q * 32, n0 = nt * BN;
-            // DSQR: H boxes b0, b0+1 of this warp's 32 rows into the two slots (boxes past M or N
-            // read the fill value; their results are never stored), and the wait for them
-            auto load_h2 = [&](int b0) {
+            const int m0 = mp * 256 + (int)rank * 128 + q * 32, nb = nt * BN + 128 * h;
+            // DSQR: the H box of output box b (columns nb + 64 b) into the slot, and the wait for it
+            // (boxes past M or N read the fill value; their results are never stored)
+            auto load_h = [&](int b) {
                 if (lane == 0) {
-                    mbar_arrive_expect_tx(&h_full[q], 2 * BOX_BYTES);
-                    for (int b = 0; b < 2; ++b)
-                        tma_load_2d_hint(smem_addr(stg + b * BOX_BYTES), &tmH, n0 + (b0 + b) * BOX_COLS, m0,
-                                         smem_addr(&h_full[q]), stream_pol);
+                    mbar_arrive_expect_tx(&h_full[e], BOX_BYTES);
+                    tma_load_2d_hint(smem_addr(slot), &tmH, nb + b * BOX_COLS, m0, smem_addr(&h_full[e]), stream_pol);
                 }
                 h_pending = true;
             };
-            auto wait_h2 = [&]() -> bool {
-                if (!mbar_wait_bounded(&h_full[q], h_phase, p.timeout_ns, abort_flag, p.dev_status)) return false;
+            auto wait_h = [&]() -> bool {
+                if (!mbar_wait_bounded(&h_full[e], h_phase, p.timeout_ns, abort_flag, p.dev_status)) return false;
                 h_phase ^= 1u;
                 h_pending = false;
                 return true;
             };
-            if (lane == 0) bulk_wait_read0();            // the previous tile's stores have left the slots
-            __syncwarp();
-            if constexpr (DSQR) load_h2(0);
-            if (!mbar_wait_bounded(acc_full, acc_phase, p.timeout_ns, abort_flag, p.dev_status)) break;
-            tc_fence_after();
-            auto store2 = [&](int b0) {                  // TMA-store boxes b0, b0+1 from the two slots
-                fence_proxy_async_smem();
+            // box b from the slot: TMA store (clipped at M and N), then its maxima
+            auto store_box = [&](int b) {
+                fence_proxy_async_smem();                // generic-proxy writes -> visible to TMA
                 __syncwarp();
-                if (lane == 0 && m0 < p.M) {
-                    for (int b = 0; b < 2; ++b)
-                        if (n0 + (b0 + b) * BOX_COLS < p.N)
-                            tma_store_2d_hint(&tmD, smem_addr(stg + b * BOX_BYTES), n0 + (b0 + b) * BOX_COLS, m0,
-                                              stream_pol);
+                if (lane == 0) {
+                    if (m0 < p.M && nb + b * BOX_COLS < p.N)
+                        tma_store_2d_hint(&tmD, smem_addr(slot), nb + b * BOX_COLS, m0, stream_pol);
                     bulk_commit();
                 }
+                if constexpr (AMAX) box_maxima<SQR_MAX>(slot, lane, m0, p.M, nb + b * BOX_COLS, p.N, sign_mask, mabs, mrht);
             };
-            uint32_t va[64], vb[64];
-            tmem_ld_64cols(tmem_row + ACC_COL, va);
-            tmem_ld_64cols(tmem_row + ACC_COL + 64, vb);
-            tmem_ld_wait();
-            reg_fence64(va);
-            reg_fence64(vb);
+            auto slot_free = [&]() {                     // the last store has read the slot (and every lane is done with it)
+                __syncwarp();
+                if (lane == 0) bulk_wait_read0();
+                __syncwarp();
+            };
+            slot_free();
             if constexpr (DSQR) {
-                if (!wait_h2()) { ok = false; break; }
+                if (lane == 0) fence_proxy_async_smem();
+                load_h(0);
             }
-            box_out<EPI>(va, stg, lane, alpha);
-            tmem_ld_64cols(tmem_row + ACC_COL + 128, va);
-            box_out<EPI>(vb, stg + BOX_BYTES, lane, alpha);
+            if (!mbar_wait_bounded(acc_full, acc_phase, p.timeout_ns, abort_flag, p.dev_status)) break;
+            tc_fence_after();
+            uint32_t va[64], vb[64];
+            tmem_ld_64cols(tmem_row, va);
+            tmem_ld_64cols(tmem_row + 64, vb);
             tmem_ld_wait();
             reg_fence64(va);
-            tmem_ld_64cols(tmem_row + ACC_COL + 192, vb);
-            tmem_ld_wait();
             reg_fence64(vb);
-            // AMAX: the last two boxes as packed bf16 (half the registers), so the maxima of the
-            // first two fit beside them
-            uint32_t pa[32], pb[32];
-            if constexpr (AMAX) {
-                pack_bf16_64(va, pa, alpha);
-                pack_bf16_64(vb, pb, alpha);
-            }
-            // the whole accumulator is in registers or shared memory: hand it back
+            // this warp's 128 columns are in registers: hand its share of the accumulator back
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive_cluster(acc_empty_leader);
-            store2(0);
-            if constexpr (AMAX) {                        // read alongside the stores: both only read the slots
-                box_maxima<SQR_MAX>(stg, lane, m0, p.M, n0, p.N, sign_mask, mabs, mrht);
-                box_maxima<SQR_MAX>(stg + BOX_BYTES, lane, m0, p.M, n0 + BOX_COLS, p.N, sign_mask, mabs, mrht);
-            }
-            if (lane == 0) bulk_wait_read0();
-            __syncwarp();
             if constexpr (DSQR) {
-                load_h2(2);
-                if (!wait_h2()) { ok = false; break; }
+                if (!wait_h()) { ok = false; break; }
             }
-            if constexpr (EPI == EPI_SQAMAX) {
-                packed_to_box(pa, stg, lane);
-                packed_to_box(pb, stg + BOX_BYTES, lane);
-            } else if constexpr (EPI == EPI_DSQR_AMAX) {
-                packed_dsqr_to_box(pa, stg, lane);
-                packed_dsqr_to_box(pb, stg + BOX_BYTES, lane);
-            } else {
-                box_out<EPI>(va, stg, lane, alpha);
-                box_out<EPI>(vb, stg + BOX_BYTES, lane, alpha);
+            box_out<EPI>(va, slot, lane, alpha);
+            store_box(0);
+            slot_free();
+            if constexpr (DSQR) {
+                if (lane == 0) fence_proxy_async_smem();
+                load_h(1);
+                if (!wait_h()) { ok = false; break; }
             }
-            store2(2);
-            if constexpr (AMAX) {
-                box_maxima<SQR_MAX>(stg, lane, m0, p.M, n0 + 2 * BOX_COLS, p.N, sign_mask, mabs, mrht);
-                box_maxima<SQR_MAX>(stg + BOX_BYTES, lane, m0, p.M, n0 + 3 * BOX_COLS, p.N, sign_mask, mabs, mrht);
-            }
+            box_out<EPI>(vb, slot, lane, alpha);
+            store_box(1);
             acc_phase ^= 1u;
         }
         if constexpr (AMAX) {
             // this warp's partials; the first CTA zeroes the slots no CTA of this grid owns
             mabs = __reduce_max_sync(0xFFFFFFFFu, mabs);
             mrht = __reduce_max_sync(0xFFFFFFFFu, mrht);
-            const int gid = (int)blockIdx.x * 4 + q;
+            const int gid = (int)blockIdx.x * kMaximaWarpsPerCta + e;
             if (lane == 0) {
                 p.maxima[gid] = mabs;
                 p.maxima[p.maxima_parts + gid] = __float_as_uint(__fmul_rn(__uint_as_float(mrht), 0.25f)) & 0x7FFFFFFFu;
             }
             if (blockIdx.x == 0)
-                for (int i = (int)gridDim.x * 4 + q * 32 + lane; i < p.maxima_parts; i += 128) {
+                for (int i = (int)gridDim.x * kMaximaWarpsPerCta + e * 32 + lane; i < p.maxima_parts;
+                     i += kMaximaWarpsPerCta * 32) {
                     p.maxima[i] = 0u;
                     p.maxima[p.maxima_parts + i] = 0u;
                 }
         }
-        if (h_pending)                                   // after an abort: let the H copies land first
-            mbar_wait_bounded(&h_full[q], h_phase, p.timeout_ns, nullptr, p.dev_status);
+        if (h_pending)                                   // after an abort: let the H copy land first
+            mbar_wait_bounded(&h_full[e], h_phase, p.timeout_ns, nullptr, p.dev_status);
         if (lane == 0) bulk_wait0();
         __syncwarp();
     }
@@ -1211,6 +1159,16 @@ cudaError_t launch_pair(const CUtensorMap& ta, const CUtensorMap& tb, const CUte
         attr_err = cudaFuncSetAttribute(gemm_nvfp4_pair_kernel<MX, EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                         P_SMEM_BYTES);
         if (attr_err != cudaSuccess) return;
+        // The kernel moves registers between warpgroups with setmaxnreg; the epilogue's
+        // increase only completes if the launch holds at least the split's total, so a build
+        // that allocated fewer registers per thread is never launched.
+        cudaFuncAttributes fa;
+        attr_err = cudaFuncGetAttributes(&fa, gemm_nvfp4_pair_kernel<MX, EPI>);
+        if (attr_err != cudaSuccess) return;
+        if (fa.numRegs * P_THREADS < 2 * 128 * P_REGS_LOW + 2 * 128 * P_REGS_HIGH) {
+            attr_err = cudaErrorInvalidConfiguration;
+            return;
+        }
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(2 * (sms / 2), 1, 1);
         cfg.blockDim = dim3(P_THREADS, 1, 1);

@@ -10,9 +10,9 @@
 namespace nvfp4 {
 
 // Partial maxima a producing GEMM epilogue leaves for the quantizer (nvfp4_gemm_sqrelu_maxima):
-// one per epilogue warp (four per CTA, at most one CTA per SM), for |A| then for |RHT(A)| / 4.
+// one per epilogue warp (eight per CTA, at most one CTA per SM), for |A| then for |RHT(A)| / 4.
 // A buffer of B bytes holds two halves of B / 8 partials each.
-constexpr int kMaximaWarpsPerCta = 4;
+constexpr int kMaximaWarpsPerCta = 8;
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
