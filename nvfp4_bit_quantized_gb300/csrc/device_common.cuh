@@ -85,27 +85,31 @@ __device__ __forceinline__ float e4m3_to_f32(uint32_t code) {
     return __half2float(__ushort_as_half((unsigned short)(h2 & 0xFFFFu)));
 }
 
-__device__ __forceinline__ uint32_t block_scale_code(float amax_b, float s_enc) {
-    return e4m3_rn_sat(__fmul_rn(__fdiv_rn(amax_b, 6.0f), s_enc));
-}
-
-// RN(a / 6) for a block maximum a that is a bf16 value (8 significant bits), by the
-// published correction step for division by a reciprocal (P. Markstein, "Computation
-// of elementary functions on the IBM RISC System/6000 processor", IBM J. Res. Dev. 34,
-// 1990; for a divisor known in advance, N. Brisebarre, J.-M. Muller, S. K. Raina,
-// IEEE Trans. Computers 53(8), 2004): q0 = RN(a * RN(1/6)), the exact remainder
-// r = a - 6 q0 from one fma, q = RN(q0 + r * RN(1/6)).  That the result is the
-// correctly rounded quotient on this input domain was checked for every positive
-// finite bf16 value in exact rational arithmetic (no mismatch); three instructions
-// instead of the general division.
-__device__ __forceinline__ float div6_bf16(float a) {
+// RN(a / 6) by the published correction step for division by a reciprocal
+// (P. Markstein, "Computation of elementary functions on the IBM RISC System/6000
+// processor", IBM J. Res. Dev. 34, 1990; for a divisor known in advance, N. Brisebarre,
+// J.-M. Muller, S. K. Raina, IEEE Trans. Computers 53(8), 2004): q0 = RN(a * RN(1/6)),
+// the exact remainder r = a - 6 q0 from one fma, q = RN(q0 + r * RN(1/6)).  Three
+// instructions instead of the general division.  The result is the correctly rounded
+// quotient for every positive finite bf16 value and for every fp32 a >= 6 * 2^-126
+// (a normal quotient); below that the quotient is subnormal and the step can miss by
+// one unit, so div6_rn falls back to the IEEE division there.  Both claims are checked
+// in exact arithmetic on the host, over every bf16 value and every fp32 significand.
+__device__ __forceinline__ float div6_correction(float a) {
     const float inv6 = __uint_as_float(0x3E2AAAABu);        // RN(1/6)
     const float q0 = __fmul_rn(a, inv6);
     const float r = __fmaf_rn(-q0, 6.0f, a);
     return __fmaf_rn(r, inv6, q0);
 }
+__device__ __forceinline__ float div6_rn(float a) {
+    return a >= 0x1.8p-124f ? div6_correction(a) : __fdiv_rn(a, 6.0f);   // 0x1.8p-124 = 6 * 2^-126
+}
+
+__device__ __forceinline__ uint32_t block_scale_code(float amax_b, float s_enc) {
+    return e4m3_rn_sat(__fmul_rn(div6_rn(amax_b), s_enc));
+}
 __device__ __forceinline__ uint32_t block_scale_code_bf16(float amax_b, float s_enc) {
-    return e4m3_rn_sat(__fmul_rn(div6_bf16(amax_b), s_enc));
+    return e4m3_rn_sat(__fmul_rn(div6_correction(amax_b), s_enc));
 }
 
 __device__ __forceinline__ float block_multiplier(uint32_t sb_code, float s_enc) {

@@ -26,6 +26,7 @@
 #include <algorithm>
 #include <cstdint>
 #include <cstdio>
+#include <map>
 #include <mutex>
 #include <set>
 #include <utility>
@@ -581,6 +582,35 @@ template <> struct Block16<float> {               // 64 bytes
     }
 };
 
+// One 1x16 row block of bf16 x (elements col .. col + 15 of row r, as eight packed
+// words): the block scale, the sixteen codes and their stores.
+template <bool SR>
+__device__ __forceinline__ void encode_row_block_bf16(const uint32_t (&w)[8], int64_t r, int64_t col, int64_t C,
+                                                      float s_enc, const float* eb_table, const PhiloxKey& key,
+                                                      uint32_t sr_offset, const QOut& out, int64_t nkb) {
+    const uint32_t m = max_abs_bf16x2(max_abs_bf16x2(max_abs_bf16x2(w[0], w[1]), max_abs_bf16x2(w[2], w[3])),
+                                      max_abs_bf16x2(max_abs_bf16x2(w[4], w[5]), max_abs_bf16x2(w[6], w[7])));
+    const uint32_t sb = block_scale_code_bf16(__uint_as_float(bf16x2_abs_max_bits(m)), s_enc);
+    const float2 eb = make_float2(eb_table[sb], eb_table[sb]);
+    float y[16];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        const float2 v = __fmul2_rn(make_float2(bf16_lo(w[j]), bf16_hi(w[j])), eb);
+        y[2 * j] = v.x;
+        y[2 * j + 1] = v.y;
+    }
+    uint2 codes;
+    if constexpr (SR) {
+        const Philox4 p = sr_philox(key, 0u, sr_offset, (uint64_t)(r * C + col) >> 4);   // C % 16 == 0
+        codes = e2m1x16_sr(y, p.w);
+    } else {
+        codes = e2m1x16_rn(y);
+    }
+    *reinterpret_cast<uint2*>(out.codes + r * (C / 2) + col / 2) = codes;
+    if (out.scales) out.scales[r * (C / 16) + col / 16] = (uint8_t)sb;
+    if (out.scales_mma) out.scales_mma[mma_sf_offset(r, col / 16, nkb)] = (uint8_t)sb;
+}
+
 template <typename T, bool SR, bool SQR = false>
 __global__ void __launch_bounds__(kThreads) encode_row_kernel(const T* __restrict__ x, int64_t R, int64_t C,
                                                               int64_t ldx, const uint32_t* __restrict__ partials,
@@ -609,20 +639,17 @@ __global__ void __launch_bounds__(kThreads) encode_row_kernel(const T* __restric
         return ok;
     };
     auto encode = [&](uint32_t (&raw)[B::WORDS], int64_t r, int64_t bk) {
-        if constexpr (SQR && sizeof(T) == 2) {
+        if constexpr (sizeof(T) == 2) {
+            if constexpr (SQR) {
 #pragma unroll
-            for (int i = 0; i < B::WORDS; ++i) raw[i] = sqrelu_bf16x2(raw[i]);
+                for (int i = 0; i < B::WORDS; ++i) raw[i] = sqrelu_bf16x2(raw[i]);
+            }
+            encode_row_block_bf16<SR>(raw, r, bk * 16, C, sc.s_enc, g_eb_table, key, sr_offset, out, nkb);
+            return;
         }
         float f[16];
         B::unpack(raw, f);
-        uint32_t sb;
-        if constexpr (sizeof(T) == 2) {
-            const uint32_t m = max_abs_bf16x2(max_abs_bf16x2(max_abs_bf16x2(raw[0], raw[1]), max_abs_bf16x2(raw[2], raw[3])),
-                                              max_abs_bf16x2(max_abs_bf16x2(raw[4], raw[5]), max_abs_bf16x2(raw[6], raw[7])));
-            sb = block_scale_code_bf16(__uint_as_float(bf16x2_abs_max_bits(m)), sc.s_enc);
-        } else {
-            sb = block_scale_code(abs_max16(f), sc.s_enc);
-        }
+        const uint32_t sb = block_scale_code(abs_max16(f), sc.s_enc);
         const float2 eb = make_float2(g_eb_table[sb], g_eb_table[sb]);
         float y[16];
 #pragma unroll
@@ -779,6 +806,68 @@ __global__ void __launch_bounds__(kPatchThreads, kPatchCtasPerSm) encode_col_ker
             if (out.scales) out.scales[c * (R / 16) + s] = (uint8_t)sb;
             if (out.scales_mma) out.scales_mma[mma_sf_offset(c, s, nkb)] = (uint8_t)sb;
         }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Pass 2 of a dual quantization of bf16 x (the row operand, and the column operand
+// with the RHT along rows) in one read of x.  Each patch, once in shared memory, is
+// encoded as the column operand exactly as encode_col_kernel does, then as the row
+// operand: lanes 2j and 2j + 1 hold the two 8-column halves of the same 16-column
+// blocks of 16 rows, so lane 2j + h takes rows 8h .. 8h + 7 of those blocks and reads
+// both halves back from the pair's slots.  Per element the arithmetic is that of the
+// two single-operand kernels.
+// ---------------------------------------------------------------------------
+template <bool SR, bool SQR>
+__global__ void __launch_bounds__(kPatchThreads, kPatchCtasPerSm) encode_dual_kernel(
+    const uint16_t* __restrict__ x, int64_t R, int64_t C, int64_t ldx, const uint32_t* __restrict__ part_row,
+    const uint32_t* __restrict__ part_col, int nparts, QOut out_row, QOut out_col, uint64_t seed_row,
+    uint64_t seed_col, uint32_t off_row, uint32_t off_col, uint64_t rht_seed, uint32_t* dev_status) {
+    __shared__ float eb_row[128];
+    const uint32_t sign_mask = rht_sign_mask(rht_seed);
+    const Scales s_row = tensor_scales(part_row, nparts, out_row.s_dec, dev_status, eb_row);
+    const Scales s_col = tensor_scales(part_col, nparts, out_col.s_dec, dev_status);
+    const PhiloxKey key_row = philox_key(seed_row), key_col = philox_key(seed_col);
+    const int64_t tiles_c = (C + 63) / 64;
+    const int64_t tiles = ((R + 63) / 64) * tiles_c;
+    const int64_t nkb_col = (R + 255) / 256, nkb_row = (C + 255) / 256;
+    const int lane = threadIdx.x & 31, half = lane & 1;
+    const int warp = threadIdx.x >> 5;
+    const int64_t warp0 = (int64_t)blockIdx.x * (kPatchThreads / 32) + warp;
+    const int64_t nwarps = (int64_t)gridDim.x * (kPatchThreads / 32);
+    const bool fold = __fmul_rn(g_eb_table[126], 0.25f) >= FLT_MIN;
+    // this lane pair's two 16-byte chunks of a row, slot 0
+    const uint32_t pair_base = smem_addr(patch_smem) + (uint32_t)(warp * 2 * kPatchSlotBytes + (lane & ~1) * 16);
+    PatchPipe<uint16_t> pp(x, ldx, R, C, warp0, nwarps, tiles, tiles_c, patch_smem);
+    while (pp.next()) {
+        __syncwarp();                                // the partner lane's copy has landed too
+        if (pp.ok) {
+            {
+                uint4 v[16];
+                pp.read(v);
+#pragma unroll
+                for (int i = 0; i < 16; ++i) v[i] = pre16<uint16_t, SQR>(v[i]);
+                encode_col_patch_bf16<SR, true>(v, pp.r0, pp.c0, R, sign_mask, fold, g_eb_table, s_col.s_enc, key_col,
+                                                off_col, out_col, nkb_col);
+            }
+            const int64_t col = pp.c0 & ~(int64_t)15;
+            const uint32_t base = pair_base + pp.rslot * kPatchSlotBytes + (uint32_t)(half * 8 * 512);
+#pragma unroll 2
+            for (int i = 0; i < 8; ++i) {
+                uint32_t w[8];
+                asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%8];\n\t"
+                             "ld.shared.v4.u32 {%4, %5, %6, %7}, [%8+16];"
+                             : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3]), "=r"(w[4]), "=r"(w[5]), "=r"(w[6]), "=r"(w[7])
+                             : "r"(base + i * 512) : "memory");
+                if constexpr (SQR) {
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) w[k] = sqrelu_bf16x2(w[k]);
+                }
+                encode_row_block_bf16<SR>(w, pp.r0 + half * 8 + i, col, C, s_row.s_enc, eb_row, key_row, off_row,
+                                          out_row, nkb_row);
+            }
+        }
+        __syncwarp();                                // done with the partner's slot before it is refilled
     }
 }
 
@@ -1016,10 +1105,37 @@ nvfp4_status check_quantize_args(const void* x, int32_t x_dtype, int64_t R, int6
     return NVFP4_OK;
 }
 
-int amax_grid(int sms, int64_t R, int64_t C, bool is16) {
-    const int64_t chunks = (R == 0 || C == 0) ? 0 : R * (C / (is16 ? 8 : 4));
-    const int g = (int)std::min<int64_t>((int64_t)sms * 8, std::max<int64_t>(1, (chunks + kThreads * 4 - 1) / (kThreads * 4)));
-    return std::min(g, kMaxPartials);
+// CTAs of one kernel resident on an SM at once (registers and shared memory),
+// looked up once per kernel and device.
+template <typename K>
+int resident_per_sm(K* kern, int threads, size_t smem) {
+    static std::mutex mu;
+    static std::map<std::pair<int, const void*>, int> cache;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 1;
+    std::lock_guard<std::mutex> lk(mu);
+    const auto key = std::make_pair(dev, reinterpret_cast<const void*>(kern));
+    const auto it = cache.find(key);
+    if (it != cache.end()) return it->second;
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, threads, smem) != cudaSuccess) {
+        (void)cudaGetLastError();
+        n = 1;
+    }
+    n = std::max(n, 1);
+    cache[key] = n;
+    return n;
+}
+
+// Launch a grid-stride kernel of kThreads threads with one wave of resident CTAs
+// (the SM count times the kernel's occupancy), or fewer when the work is smaller;
+// *grid = the CTAs launched.
+template <typename K, typename... Args>
+cudaError_t launch_resident(K* kern, int64_t work_ctas, int sms, int* grid, cudaStream_t stream, Args... args) {
+    const int64_t wave = (int64_t)sms * resident_per_sm(kern, kThreads, 0);
+    *grid = (int)std::max<int64_t>(1, std::min<int64_t>(std::min<int64_t>(wave, work_ctas), kMaxPartials));
+    kern<<<*grid, kThreads, 0, stream>>>(args...);
+    return cudaGetLastError();
 }
 
 // Grid of the patch kernels: one CTA (eight warps) per SM at most, one warp per
@@ -1066,18 +1182,16 @@ cudaError_t amax_pass(const void* x, bool is16, int64_t R, int64_t C, int64_t ld
         return is16 ? launch_patch(amax_rht_kernel<uint16_t>, *g1, stream, (const uint16_t*)x, R, C, ldx, rht_seed, partials)
                     : launch_patch(amax_rht_kernel<float>, *g1, stream, (const float*)x, R, C, ldx, rht_seed, partials);
     }
-    *g1 = amax_grid(sms, R, C, is16);
+    const int64_t work = (chunks + kThreads * 4 - 1) / (kThreads * 4);
     const uint16_t* xb = (const uint16_t*)x;
     if (ldx == C) {
-        if (is16 && sqr) amax_flat_kernel<uint16_t, true><<<*g1, kThreads, 0, stream>>>(xb, chunks, partials);
-        else if (is16) amax_flat_kernel<uint16_t><<<*g1, kThreads, 0, stream>>>(xb, chunks, partials);
-        else amax_flat_kernel<float><<<*g1, kThreads, 0, stream>>>((const float*)x, chunks, partials);
-    } else {
-        if (is16 && sqr) amax_kernel<uint16_t, true><<<*g1, kThreads, 0, stream>>>(xb, R, C, ldx, partials);
-        else if (is16) amax_kernel<uint16_t><<<*g1, kThreads, 0, stream>>>(xb, R, C, ldx, partials);
-        else amax_kernel<float><<<*g1, kThreads, 0, stream>>>((const float*)x, R, C, ldx, partials);
+        if (is16 && sqr) return launch_resident(amax_flat_kernel<uint16_t, true>, work, sms, g1, stream, xb, chunks, partials);
+        if (is16) return launch_resident(amax_flat_kernel<uint16_t>, work, sms, g1, stream, xb, chunks, partials);
+        return launch_resident(amax_flat_kernel<float>, work, sms, g1, stream, (const float*)x, chunks, partials);
     }
-    return cudaGetLastError();
+    if (is16 && sqr) return launch_resident(amax_kernel<uint16_t, true>, work, sms, g1, stream, xb, R, C, ldx, partials);
+    if (is16) return launch_resident(amax_kernel<uint16_t>, work, sms, g1, stream, xb, R, C, ldx, partials);
+    return launch_resident(amax_kernel<float>, work, sms, g1, stream, (const float*)x, R, C, ldx, partials);
 }
 
 // The kernels' view of an output, with the padding of its tensor-core scale layout
@@ -1113,7 +1227,8 @@ nvfp4_status encode_pass(const void* x, int32_t x_dtype, int64_t R, int64_t C, i
 
     const bool sr = p->round == NVFP4_ROUND_SR;
     const int64_t row_warps = empty ? 0 : R * ((C / 16 + 31) / 32);
-    const int g_row = (int)std::max<int64_t>(1, std::min<int64_t>((int64_t)sms * 8, (row_warps + 7) / 8));
+    const int64_t row_ctas = (row_warps + 7) / 8;
+    int g_row = 0;
     const int g_patch = patch_grid(sms, R, C, is16);
     // 32-byte loads when every 16-element block starts on a 32-byte boundary
     const int v8 = ((reinterpret_cast<uintptr_t>(x) & 31u) == 0 && ((size_t)ldx * esz) % 32 == 0) ? 1 : 0;
@@ -1124,9 +1239,8 @@ nvfp4_status encode_pass(const void* x, int32_t x_dtype, int64_t R, int64_t C, i
     do {                                                                                                   \
         const T* xt = (const T*)x;                                                                         \
         if (p->block == NVFP4_BLOCK_1X16_ROW) {                                                            \
-            if (sr) encode_row_kernel<T, true><<<g_row, kThreads, 0, stream>>>(xt, R, C, ldx, partials, g1, q, ss, so, v8, dev_status); \
-            else encode_row_kernel<T, false><<<g_row, kThreads, 0, stream>>>(xt, R, C, ldx, partials, g1, q, ss, so, v8, dev_status); \
-            e = cudaGetLastError();                                                                        \
+            if (sr) e = launch_resident(encode_row_kernel<T, true>, row_ctas, sms, &g_row, stream, xt, R, C, ldx, partials, g1, q, ss, so, v8, dev_status); \
+            else e = launch_resident(encode_row_kernel<T, false>, row_ctas, sms, &g_row, stream, xt, R, C, ldx, partials, g1, q, ss, so, v8, dev_status); \
         } else if (p->block == NVFP4_BLOCK_1X16_COL) {                                                     \
             if (sr && p->rht) e = launch_patch(encode_col_kernel<T, true, true>, g_patch, stream, xt, R, C, ldx, partials, g1, q, ss, so, rs, dev_status); \
             else if (sr) e = launch_patch(encode_col_kernel<T, true, false>, g_patch, stream, xt, R, C, ldx, partials, g1, q, ss, so, rs, dev_status); \
@@ -1141,9 +1255,8 @@ nvfp4_status encode_pass(const void* x, int32_t x_dtype, int64_t R, int64_t C, i
         // bf16 with the squared-ReLU load transform (row and column operands only)
         const uint16_t* xt = (const uint16_t*)x;
         if (p->block == NVFP4_BLOCK_1X16_ROW) {
-            if (sr) encode_row_kernel<uint16_t, true, true><<<g_row, kThreads, 0, stream>>>(xt, R, C, ldx, partials, g1, q, ss, so, v8, dev_status);
-            else encode_row_kernel<uint16_t, false, true><<<g_row, kThreads, 0, stream>>>(xt, R, C, ldx, partials, g1, q, ss, so, v8, dev_status);
-            e = cudaGetLastError();
+            if (sr) e = launch_resident(encode_row_kernel<uint16_t, true, true>, row_ctas, sms, &g_row, stream, xt, R, C, ldx, partials, g1, q, ss, so, v8, dev_status);
+            else e = launch_resident(encode_row_kernel<uint16_t, false, true>, row_ctas, sms, &g_row, stream, xt, R, C, ldx, partials, g1, q, ss, so, v8, dev_status);
         } else if (p->block == NVFP4_BLOCK_1X16_COL) {
             if (sr && p->rht) e = launch_patch(encode_col_kernel<uint16_t, true, true, true>, g_patch, stream, xt, R, C, ldx, partials, g1, q, ss, so, rs, dev_status);
             else if (sr) e = launch_patch(encode_col_kernel<uint16_t, true, false, true>, g_patch, stream, xt, R, C, ldx, partials, g1, q, ss, so, rs, dev_status);
@@ -1182,6 +1295,34 @@ nvfp4_status quantize_impl(const void* x, int32_t x_dtype, int64_t R, int64_t C,
     return encode_pass(x, x_dtype, R, C, ldx, p, out, partials, g1, sms, dev_status, stream);
 }
 
+// Whether a dual quantization takes the fused encode (one read of x for both operands):
+// bf16 x, a non-empty tensor, the RHT column operand and one rounding mode for both.
+bool dual_fused(int32_t x_dtype, int64_t R, int64_t C, const nvfp4_qparams* p_row, const nvfp4_qparams* p_col) {
+    return x_dtype == NVFP4_BF16 && R > 0 && C > 0 && p_col->rht && p_row->round == p_col->round;
+}
+
+// Pass 2 of a dual quantization that dual_fused accepts: one encode_dual_kernel launch.
+nvfp4_status encode_dual_pass(const void* x, int64_t R, int64_t C, int64_t ldx, const nvfp4_qparams* p_row,
+                              const nvfp4_qtensor* out_row, const nvfp4_qparams* p_col, const nvfp4_qtensor* out_col,
+                              const uint32_t* part_row, const uint32_t* part_col, int g1, int sms,
+                              uint32_t* dev_status, cudaStream_t stream, bool sqr) {
+    QOut qr, qc;
+    nvfp4_status st = prepare_output(p_row, out_row, R, C, &qr, stream);
+    if (st != NVFP4_OK) return st;
+    st = prepare_output(p_col, out_col, R, C, &qc, stream);
+    if (st != NVFP4_OK) return st;
+    const int g = patch_grid(sms, R, C, true);
+    const uint16_t* xb = static_cast<const uint16_t*>(x);
+    auto launch = [&](auto* kern) {
+        return launch_patch(kern, g, stream, xb, R, C, ldx, part_row, part_col, g1, qr, qc, p_row->sr_seed,
+                            p_col->sr_seed, p_row->sr_offset, p_col->sr_offset, p_col->rht_seed, dev_status);
+    };
+    const bool sr = p_row->round == NVFP4_ROUND_SR;
+    const cudaError_t e = sr ? (sqr ? launch(encode_dual_kernel<true, true>) : launch(encode_dual_kernel<true, false>))
+                             : (sqr ? launch(encode_dual_kernel<false, true>) : launch(encode_dual_kernel<false, false>));
+    return e == cudaSuccess ? NVFP4_OK : NVFP4_ERR_CUDA;
+}
+
 nvfp4_status quantize_dual_impl(const void* x, int32_t x_dtype, int64_t R, int64_t C, int64_t ldx,
                                 const nvfp4_qparams* p_row, const nvfp4_qtensor* out_row,
                                 const nvfp4_qparams* p_col, const nvfp4_qtensor* out_col, void* ws,
@@ -1215,6 +1356,9 @@ nvfp4_status quantize_dual_impl(const void* x, int32_t x_dtype, int64_t R, int64
         if (amax_pass(x, is16, R, C, ldx, false, 0, part_plain, sms, &g1, stream, sqr) != cudaSuccess) return NVFP4_ERR_CUDA;
         part_col = part_plain;
     }
+    if (dual_fused(x_dtype, R, C, p_row, p_col))
+        return encode_dual_pass(x, R, C, ldx, p_row, out_row, p_col, out_col, part_plain, part_col, g1, sms, dev_status,
+                                stream, sqr);
     st = encode_pass(x, x_dtype, R, C, ldx, p_row, out_row, part_plain, g1, sms, dev_status, stream, sqr);
     if (st != NVFP4_OK) return st;
     return encode_pass(x, x_dtype, R, C, ldx, p_col, out_col, part_col, g1, sms, dev_status, stream, sqr);
@@ -1263,6 +1407,9 @@ static nvfp4_status quantize_dual_premax_impl(const void* x, int32_t x_dtype, in
     const int sms = sm_count(dev);
     if (sms <= 0) return NVFP4_ERR_CUDA;
     const uint32_t* part_col = p_col->rht ? maxima + parts : maxima;
+    if (dual_fused(x_dtype, R, C, p_row, p_col))
+        return encode_dual_pass(x, R, C, ldx, p_row, out_row, p_col, out_col, maxima, part_col, (int)parts, sms,
+                                dev_status, stream, sqr);
     st = encode_pass(x, x_dtype, R, C, ldx, p_row, out_row, maxima, (int)parts, sms, dev_status, stream, sqr);
     if (st != NVFP4_OK) return st;
     return encode_pass(x, x_dtype, R, C, ldx, p_col, out_col, part_col, (int)parts, sms, dev_status, stream, sqr);

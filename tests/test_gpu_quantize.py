@@ -162,9 +162,10 @@ def test_dual_quantization_matches_two_single_calls(nv, oracle_mod, dtype, shape
     assert np.array_equal(qr.codes.cpu().numpy(), r["codes"]) and np.array_equal(qc.codes.cpu().numpy(), c["codes"])
 
 
-@pytest.mark.parametrize("rnd_row,rnd_col", [(1, 0), (0, 1)])
+@pytest.mark.parametrize("rnd_row,rnd_col", [(1, 0), (0, 1), (1, 1), (0, 0)])
 def test_dual_quantization_mixed_rounding_and_seeds(nv, oracle_mod, rnd_row, rnd_col):
-    """Row and column operands with different rounding modes, SR seeds and offsets."""
+    """Row and column operands with different SR seeds and offsets, with different rounding
+    modes (two encode kernels) and with one mode for both (the fused encode)."""
     x = _input((192, 320), torch.bfloat16, seed=77).cuda()
     qr, qc = nv.quantize_dual(x, rnd_row, rnd_col, rht=True, sr_seed=11, sr_offset=5, rht_seed=6,
                               col_sr_seed=23, col_sr_offset=9)
