@@ -582,12 +582,28 @@ template <> struct Block16<float> {               // 64 bytes
     }
 };
 
-// One 1x16 row block of bf16 x (elements col .. col + 15 of row r, as eight packed
-// words): the block scale, the sixteen codes and their stores.
+// Where one row block's results go: its 8 code bytes, its scale in the canonical and in
+// the tensor-core layout (either may be null), and its Philox group (element index / 16).
+struct RowDst {
+    uint8_t* codes;
+    uint8_t* scale;
+    uint8_t* scale_mma;
+    uint64_t group;
+};
+__device__ __forceinline__ RowDst row_dst(const QOut& out, int64_t r, int64_t col, int64_t C, int64_t nkb) {
+    RowDst d;
+    d.codes = out.codes + r * (C / 2) + col / 2;
+    d.scale = out.scales ? out.scales + r * (C / 16) + col / 16 : nullptr;
+    d.scale_mma = out.scales_mma ? out.scales_mma + mma_sf_offset(r, col / 16, nkb) : nullptr;
+    d.group = (uint64_t)(r * C + col) >> 4;                  // C % 16 == 0
+    return d;
+}
+
+// One 1x16 row block of bf16 x (as eight packed words): the block scale, the sixteen
+// codes and their stores.
 template <bool SR>
-__device__ __forceinline__ void encode_row_block_bf16(const uint32_t (&w)[8], int64_t r, int64_t col, int64_t C,
-                                                      float s_enc, const float* eb_table, const PhiloxKey& key,
-                                                      uint32_t sr_offset, const QOut& out, int64_t nkb) {
+__device__ __forceinline__ void encode_row_block_bf16(const uint32_t (&w)[8], const RowDst& d, float s_enc,
+                                                      const float* eb_table, const PhiloxKey& key, uint32_t sr_offset) {
     const uint32_t m = max_abs_bf16x2(max_abs_bf16x2(max_abs_bf16x2(w[0], w[1]), max_abs_bf16x2(w[2], w[3])),
                                       max_abs_bf16x2(max_abs_bf16x2(w[4], w[5]), max_abs_bf16x2(w[6], w[7])));
     const uint32_t sb = block_scale_code_bf16(__uint_as_float(bf16x2_abs_max_bits(m)), s_enc);
@@ -601,14 +617,14 @@ __device__ __forceinline__ void encode_row_block_bf16(const uint32_t (&w)[8], in
     }
     uint2 codes;
     if constexpr (SR) {
-        const Philox4 p = sr_philox(key, 0u, sr_offset, (uint64_t)(r * C + col) >> 4);   // C % 16 == 0
+        const Philox4 p = sr_philox(key, 0u, sr_offset, d.group);
         codes = e2m1x16_sr(y, p.w);
     } else {
         codes = e2m1x16_rn(y);
     }
-    *reinterpret_cast<uint2*>(out.codes + r * (C / 2) + col / 2) = codes;
-    if (out.scales) out.scales[r * (C / 16) + col / 16] = (uint8_t)sb;
-    if (out.scales_mma) out.scales_mma[mma_sf_offset(r, col / 16, nkb)] = (uint8_t)sb;
+    *reinterpret_cast<uint2*>(d.codes) = codes;
+    if (d.scale) *d.scale = (uint8_t)sb;
+    if (d.scale_mma) *d.scale_mma = (uint8_t)sb;
 }
 
 template <typename T, bool SR, bool SQR = false>
@@ -644,7 +660,7 @@ __global__ void __launch_bounds__(kThreads) encode_row_kernel(const T* __restric
 #pragma unroll
                 for (int i = 0; i < B::WORDS; ++i) raw[i] = sqrelu_bf16x2(raw[i]);
             }
-            encode_row_block_bf16<SR>(raw, r, bk * 16, C, sc.s_enc, g_eb_table, key, sr_offset, out, nkb);
+            encode_row_block_bf16<SR>(raw, row_dst(out, r, bk * 16, C, nkb), sc.s_enc, g_eb_table, key, sr_offset);
             return;
         }
         float f[16];
@@ -692,8 +708,16 @@ __device__ __forceinline__ void encode_col_patch_bf16(const uint4 (&v)[16], int6
     const float quarter = RHT ? 0.25f : 1.0f;
     float2 t[4][16];
     unpack_patch_bf16<false>(v, sign_mask, t);
+    // Operand rows c0 + j (j < 8): codes R/2 bytes apart, canonical scales R/16 apart,
+    // Philox groups R/16 apart (R % 16 == 0, r0 % 16 == 0), tensor-core scales 16 bytes
+    // apart (c0 % 8 == 0 keeps c0 + j inside one group of 32 operand rows).
+    const int64_t hr = R / 2, sr = R / 16;
+    uint8_t* cdst = out.codes + c0 * hr + r0 / 2;
+    uint8_t* sdst = out.scales ? out.scales + c0 * sr + r0 / 16 : nullptr;
+    uint8_t* mdst = out.scales_mma ? out.scales_mma + mma_sf_offset(c0, r0 / 16, nkb) : nullptr;
+    uint64_t grp = (uint64_t)(c0 * sr + r0 / 16);
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {                    // columns c0 + 2k, c0 + 2k + 1
+    for (int k = 0; k < 4; ++k) {                    // operand rows c0 + 2k, c0 + 2k + 1
         if constexpr (RHT) hadamard16_x2(t[k]);
         float m0, m1;
         col_pair_abs_max(t[k], m0, m1);
@@ -710,29 +734,30 @@ __device__ __forceinline__ void encode_col_patch_bf16(const uint4 (&v)[16], int6
             y0[i] = u.x;
             y1[i] = u.y;
         }
-        const int64_t c = c0 + 2 * k;                // operand rows c, c + 1
         uint2 codes0, codes1;
         if constexpr (SR) {
-            const Philox4 p0 = sr_philox(key, 1u, sr_offset, (uint64_t)(c * R + r0) >> 4);   // r0 % 16 == 0
-            const Philox4 p1 = sr_philox(key, 1u, sr_offset, (uint64_t)((c + 1) * R + r0) >> 4);
+            const Philox4 p0 = sr_philox(key, 1u, sr_offset, grp);
+            const Philox4 p1 = sr_philox(key, 1u, sr_offset, grp + (uint64_t)sr);
             codes0 = e2m1x16_sr(y0, p0.w);
             codes1 = e2m1x16_sr(y1, p1.w);
         } else {
             codes0 = e2m1x16_rn(y0);
             codes1 = e2m1x16_rn(y1);
         }
-        *reinterpret_cast<uint2*>(out.codes + c * (R / 2) + r0 / 2) = codes0;
-        *reinterpret_cast<uint2*>(out.codes + (c + 1) * (R / 2) + r0 / 2) = codes1;
-        const int64_t s = r0 / 16;
-        if (out.scales) {
-            out.scales[c * (R / 16) + s] = (uint8_t)sb0;
-            out.scales[(c + 1) * (R / 16) + s] = (uint8_t)sb1;
+        *reinterpret_cast<uint2*>(cdst) = codes0;
+        *reinterpret_cast<uint2*>(cdst + hr) = codes1;
+        if (sdst) {
+            sdst[0] = (uint8_t)sb0;
+            sdst[sr] = (uint8_t)sb1;
+            sdst += 2 * sr;
         }
-        if (out.scales_mma) {                        // rows c, c + 1 (c even): 16 bytes apart
-            uint8_t* d = out.scales_mma + mma_sf_offset(c, s, nkb);
-            d[0] = (uint8_t)sb0;
-            d[16] = (uint8_t)sb1;
+        if (mdst) {
+            mdst[0] = (uint8_t)sb0;
+            mdst[16] = (uint8_t)sb1;
+            mdst += 32;
         }
+        cdst += 2 * hr;
+        grp += 2 * (uint64_t)sr;
     }
 }
 
@@ -850,7 +875,9 @@ __global__ void __launch_bounds__(kPatchThreads, kPatchCtasPerSm) encode_dual_ke
                 encode_col_patch_bf16<SR, true>(v, pp.r0, pp.c0, R, sign_mask, fold, g_eb_table, s_col.s_enc, key_col,
                                                 off_col, out_col, nkb_col);
             }
-            const int64_t col = pp.c0 & ~(int64_t)15;
+            // rows r0 + 8h + i: the tensor-core scale offset steps by 16 per row (no carry out
+            // of the row's low five bits, as r0 % 16 == 0 and 8h + i < 16)
+            RowDst d = row_dst(out_row, pp.r0 + half * 8, pp.c0 & ~(int64_t)15, C, nkb_row);
             const uint32_t base = pair_base + pp.rslot * kPatchSlotBytes + (uint32_t)(half * 8 * 512);
 #pragma unroll 2
             for (int i = 0; i < 8; ++i) {
@@ -863,8 +890,11 @@ __global__ void __launch_bounds__(kPatchThreads, kPatchCtasPerSm) encode_dual_ke
 #pragma unroll
                     for (int k = 0; k < 8; ++k) w[k] = sqrelu_bf16x2(w[k]);
                 }
-                encode_row_block_bf16<SR>(w, pp.r0 + half * 8 + i, col, C, s_row.s_enc, eb_row, key_row, off_row,
-                                          out_row, nkb_row);
+                encode_row_block_bf16<SR>(w, d, s_row.s_enc, eb_row, key_row, off_row);
+                d.codes += C / 2;
+                if (d.scale) d.scale += C / 16;
+                if (d.scale_mma) d.scale_mma += 16;
+                d.group += (uint64_t)(C / 16);
             }
         }
         __syncwarp();                                // done with the partner's slot before it is refilled
