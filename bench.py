@@ -329,9 +329,38 @@ def _timed(fn, steps: int, warmup: int) -> float:
     return e0.elapsed_time(e1) / steps
 
 
+def _graph_timed(fn, reps: int, warmup: int) -> float:
+    """ms per call of fn with the host out of the loop: reps calls captured once into a CUDA
+    graph, the graph replayed twice and timed with CUDA events (the clock sampler armed for the
+    replays).  Small tensors would otherwise measure the Python and launch overhead per call."""
+    import torch
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for _ in range(reps):
+            fn()
+    g.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if _CLK is not None:
+        _CLK.arm()
+    e0.record()
+    g.replay()
+    g.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    if _CLK is not None:
+        _CLK.disarm()
+    del g
+    return e0.elapsed_time(e1) / (2 * reps)
+
+
 def run_sweep(args):
     """Quantizer bandwidth sweep: bf16 [R, C], R*C ~ 2^p, C in {5120, 20480}, 0.1% outlier
-    columns x100; four modes.  One JSON line per case (GB/s of algorithmic bytes)."""
+    columns x100; four modes.  One JSON line per case (GB/s of algorithmic bytes, timed by CUDA
+    graph replay; the plain per-call loop, host overhead included, beside it)."""
     import torch
     import nvfp4_bit_quantized_gb300 as nv
     from nvfp4_bit_quantized_gb300 import inputs
@@ -346,12 +375,14 @@ def run_sweep(args):
             for name, block, rnd, rht, bpe in modes:
                 fn = lambda: nv.quantize(x, block, rnd, rht=rht, sr_seed=1, rht_seed=2, scales=False,
                                          transpose=(block == nv.TILE16))
-                ms = _timed(fn, max(3, args.steps), args.warmup)
+                ms_host = _timed(fn, max(3, args.steps), args.warmup)
+                ms = _graph_timed(fn, max(3, args.steps), args.warmup)
                 gbs = R * C * bpe / (ms * 1e-3) / 1e9
                 # the one-read lower bound: the input read once plus the outputs (2D: W and W^T)
                 one = 2 + (bpe - 4)
                 print(json.dumps({"config": "quantizer_sweep", "mode": name, "R": R, "C": C, "elements": R * C,
-                                  "log2_elements": p, "ms": round(ms, 4), "GB/s": round(gbs, 1),
+                                  "log2_elements": p, "ms": round(ms, 4), "timing": "cuda graph replay",
+                                  "ms_host_loop": round(ms_host, 4), "GB/s": round(gbs, 1),
                                   "hbm_frac": round(gbs / peaks["hbm_gbs"], 3), "peak_source": src,
                                   "bytes_per_element": bpe, "inputs_exceed_l2": R * C * 2 > 129e6,
                                   "one_read_bytes_per_element": one,

@@ -143,8 +143,10 @@ NVFP4_API size_t nvfp4_quantize_dual_workspace_bytes(int64_t R, int64_t C);
  * nvfp4_quantize_dual -- both quantizations a tensor needs in training, from
  * one amax read: the 1X16_ROW operand (params_row, out_row: [R, C]) and the
  * 1X16_COL operand (params_col, out_col: [C, R], with or without the RHT).  With
- * the RHT the single amax pass computes |x| and |RHT(x)| maxima together;
- * results are identical to two nvfp4_quantize calls with the same parameters.
+ * the RHT the single amax pass computes |x| and |RHT(x)| maxima together, and for
+ * BF16 x with one rounding mode for both operands a single encode pass writes both
+ * (x is read twice in all); results are identical to two nvfp4_quantize calls with
+ * the same parameters.
  * Used for X (Fprop operand + the Wgrad operand saved for the backward pass) and
  * for dY (Dgrad + Wgrad operands).  Same argument rules as nvfp4_quantize.
  */
