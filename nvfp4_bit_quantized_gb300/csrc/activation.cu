@@ -20,6 +20,8 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 }
 
 __global__ void sqrelu_fwd_kernel(const uint4* __restrict__ h, uint4* __restrict__ a, int64_t n8) {
+    pdl_launch_dependents();
+    pdl_wait();
     for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n8; i += (int64_t)gridDim.x * blockDim.x) {
         const uint4 v = ld_stream(h + i);
         const uint32_t w[4] = {v.x, v.y, v.z, v.w};
@@ -36,6 +38,8 @@ __global__ void sqrelu_fwd_kernel(const uint4* __restrict__ h, uint4* __restrict
 
 __global__ void sqrelu_bwd_kernel(const uint4* __restrict__ h, const uint4* __restrict__ da, uint4* __restrict__ dh,
                                   int64_t n8) {
+    pdl_launch_dependents();
+    pdl_wait();
     for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n8; i += (int64_t)gridDim.x * blockDim.x) {
         const uint4 hv = ld_stream(h + i), gv = ld_stream(da + i);
         const uint32_t hw[4] = {hv.x, hv.y, hv.z, hv.w}, gw[4] = {gv.x, gv.y, gv.z, gv.w};
@@ -67,9 +71,10 @@ extern "C" nvfp4_status nvfp4_sqrelu_forward(const void* h, void* a, int64_t n, 
     if (n == 0) return NVFP4_OK;
     if (!h || !a) return NVFP4_ERR_INVALID_ARG;
     if (!aligned16(h) || !aligned16(a)) return NVFP4_ERR_ALIGNMENT;
-    sqrelu_fwd_kernel<<<grid_for(n / 8), 256, 0, static_cast<cudaStream_t>(stream)>>>(
-        static_cast<const uint4*>(h), static_cast<uint4*>(a), n / 8);
-    return cudaGetLastError() == cudaSuccess ? NVFP4_OK : NVFP4_ERR_CUDA;
+    const cudaError_t e = launch_pdl(sqrelu_fwd_kernel, dim3(grid_for(n / 8)), dim3(256), 0,
+                                     static_cast<cudaStream_t>(stream), static_cast<const uint4*>(h),
+                                     static_cast<uint4*>(a), n / 8);
+    return e == cudaSuccess ? NVFP4_OK : NVFP4_ERR_CUDA;
 }
 
 extern "C" nvfp4_status nvfp4_sqrelu_backward(const void* h, const void* da, void* dh, int64_t n, void* stream) {
@@ -77,7 +82,8 @@ extern "C" nvfp4_status nvfp4_sqrelu_backward(const void* h, const void* da, voi
     if (n == 0) return NVFP4_OK;
     if (!h || !da || !dh) return NVFP4_ERR_INVALID_ARG;
     if (!aligned16(h) || !aligned16(da) || !aligned16(dh)) return NVFP4_ERR_ALIGNMENT;
-    sqrelu_bwd_kernel<<<grid_for(n / 8), 256, 0, static_cast<cudaStream_t>(stream)>>>(
-        static_cast<const uint4*>(h), static_cast<const uint4*>(da), static_cast<uint4*>(dh), n / 8);
-    return cudaGetLastError() == cudaSuccess ? NVFP4_OK : NVFP4_ERR_CUDA;
+    const cudaError_t e = launch_pdl(sqrelu_bwd_kernel, dim3(grid_for(n / 8)), dim3(256), 0,
+                                     static_cast<cudaStream_t>(stream), static_cast<const uint4*>(h),
+                                     static_cast<const uint4*>(da), static_cast<uint4*>(dh), n / 8);
+    return e == cudaSuccess ? NVFP4_OK : NVFP4_ERR_CUDA;
 }

@@ -28,6 +28,11 @@ __device__ __forceinline__ void set_status(uint32_t* dev_status, uint32_t code) 
 // ----------------------------------------------------------------------------
 // bf16 / fp32 element access.  A 16-byte chunk holds 8 bf16 or 4 fp32 values.
 // ----------------------------------------------------------------------------
+// Programmatic dependent launch (see launch_pdl): the successor kernel may launch now, and
+// this kernel waits until its predecessor has completed and its writes are visible.
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 

@@ -335,6 +335,8 @@ template <bool STAGED>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
 gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                   const __grid_constant__ CUtensorMap tmD, const Params p) {
+    pdl_launch_dependents();
+    pdl_wait();
     using C = Cfg<STAGED>;
     constexpr int STAGES = C::STAGES;
     extern __shared__ uint8_t smem_raw[];
@@ -756,6 +758,8 @@ gemm_nvfp4_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_con
     constexpr bool DSQR = EPI == EPI_DSQR || EPI == EPI_DSQR_AMAX;   // output dH from dA and H
     constexpr bool AMAX = EPI == EPI_SQAMAX || EPI == EPI_DSQR_AMAX; // leave the output's tensor maxima
     constexpr bool SQR_MAX = EPI == EPI_SQAMAX;                      // ... of relu(output)^2
+    // the next kernel may launch now; this one touches global memory only after pdl_wait below
+    pdl_launch_dependents();
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* staging = smem + P_RING_BYTES;
@@ -776,6 +780,7 @@ gemm_nvfp4_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_con
     const uint32_t rank = cluster_rank();
     const bool leader = rank == 0;
     if (!layout_ok) {
+        pdl_wait();
         if (threadIdx.x == 0) set_status(p.dev_status, NVFP4_ERR_UNSUPPORTED);
         return;
     }
@@ -801,6 +806,8 @@ gemm_nvfp4_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_con
     tc_fence_before();
     cluster_sync();                                      // barriers initialised in both CTAs
     tc_fence_after();
+    // the prologue (barriers, TMEM) overlapped the previous kernel's tail; its results are needed now
+    pdl_wait();
     const uint32_t tmem = *tmem_slot;
     const int m_pairs = (p.M + 255) / 256;
     const int tiles = m_pairs * p.n_tiles;
@@ -1145,8 +1152,8 @@ cudaError_t launch(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorM
                                         Cfg<STAGED>::SMEM_BYTES);
     });
     if (attr_err != cudaSuccess) return attr_err;
-    gemm_nvfp4_kernel<STAGED><<<grid, NUM_THREADS, Cfg<STAGED>::SMEM_BYTES, stream>>>(ta, tb, td, p);
-    return cudaGetLastError();
+    return launch_pdl(gemm_nvfp4_kernel<STAGED>, dim3(grid), dim3(NUM_THREADS), Cfg<STAGED>::SMEM_BYTES, stream, ta, tb,
+                      td, p);
 }
 
 template <bool MX, int EPI = EPI_PLAIN>
@@ -1180,8 +1187,8 @@ cudaError_t launch_pair(const CUtensorMap& ta, const CUtensorMap& tb, const CUte
     });
     if (attr_err != cudaSuccess) return attr_err;
     const int clusters = std::max(1, std::min(pair_tiles, max_clusters));
-    gemm_nvfp4_pair_kernel<MX, EPI><<<2 * clusters, P_THREADS, P_SMEM_BYTES, stream>>>(ta, tb, td, th, p);
-    return cudaGetLastError();
+    return launch_pdl(gemm_nvfp4_pair_kernel<MX, EPI>, dim3(2 * clusters), dim3(P_THREADS), P_SMEM_BYTES, stream, ta, tb,
+                      td, th, p);
 }
 
 int g_force_path = 0;      // 0: automatic, 1: single-CTA kernel, 2: CTA-pair kernel (tests)

@@ -16,6 +16,28 @@ constexpr int kMaximaWarpsPerCta = 8;
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// Launches a library kernel with programmatic stream serialization: it may be scheduled while
+// the previous kernel in the stream drains, overlapping its launch and prologue with that
+// kernel's tail.  Every kernel of the library lets its successor launch at once
+// (griddepcontrol.launch_dependents) and waits for its predecessor to complete, with its
+// writes visible (griddepcontrol.wait), before it reads or writes global memory; after a
+// kernel launched without the attribute the wait returns at once.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                              Args... args) {
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
+}
+
 // Multiprocessor count of `dev`, cached (152 on GB300).
 int sm_count(int dev);
 

@@ -95,6 +95,8 @@ template <typename T>
 __global__ void __launch_bounds__(kRowThreads)
 mx_row_kernel(const T* __restrict__ x, int64_t ldx, int R, int C, int64_t nkt, uint8_t* __restrict__ codes,
               uint8_t* __restrict__ scales, uint8_t* __restrict__ scales_mma) {
+    pdl_launch_dependents();
+    pdl_wait();
     const int nb = C >> 5;
     const int64_t total = (int64_t)R * nb;
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
@@ -115,6 +117,8 @@ template <typename T>
 __global__ void __launch_bounds__(kColCols)
 mx_col_kernel(const T* __restrict__ x, int64_t ldx, int R, int C, int64_t nkt, uint8_t* __restrict__ codes_t,
               uint8_t* __restrict__ scales, uint8_t* __restrict__ scales_mma) {
+    pdl_launch_dependents();
+    pdl_wait();
     __shared__ __align__(16) T tile[kColRows][kColCols];
     constexpr int kChunk = 16 / sizeof(T);                     // elements per 16-byte load
     constexpr int kChunksPerRow = kColCols / kChunk;
@@ -198,27 +202,31 @@ extern "C" nvfp4_status nvfp4_mx_quantize(const void* x, int32_t x_dtype, int64_
     if (out->scales_mma && (rows % 128 != 0 || cols % 256 != 0))
         if (cudaMemsetAsync(out->scales_mma, 0, nvfp4_mx_scales_mma_bytes(rows, cols), stream) != cudaSuccess)
             return NVFP4_ERR_CUDA;
+    cudaError_t e = cudaSuccess;
     if (!col) {
         const int64_t work = R * (C / 32);
         if (x_dtype == NVFP4_BF16) {
             auto k = mx::mx_row_kernel<uint16_t>;
-            k<<<mx::grid_for(k, mx::kRowThreads, work, dev), mx::kRowThreads, 0, stream>>>(
-                static_cast<const uint16_t*>(x), ldx, (int)R, (int)C, nkt, out->codes, out->scales, out->scales_mma);
+            e = launch_pdl(k, dim3(mx::grid_for(k, mx::kRowThreads, work, dev)), dim3(mx::kRowThreads), 0, stream,
+                           static_cast<const uint16_t*>(x), ldx, (int)R, (int)C, nkt, out->codes, out->scales,
+                           out->scales_mma);
         } else {
             auto k = mx::mx_row_kernel<float>;
-            k<<<mx::grid_for(k, mx::kRowThreads, work, dev), mx::kRowThreads, 0, stream>>>(
-                static_cast<const float*>(x), ldx, (int)R, (int)C, nkt, out->codes, out->scales, out->scales_mma);
+            e = launch_pdl(k, dim3(mx::grid_for(k, mx::kRowThreads, work, dev)), dim3(mx::kRowThreads), 0, stream,
+                           static_cast<const float*>(x), ldx, (int)R, (int)C, nkt, out->codes, out->scales,
+                           out->scales_mma);
         }
     } else {
         // x walks the column tiles (neighbouring CTAs read neighbouring pieces of the same rows)
         const int64_t row_tiles = (R + mx::kColRows - 1) / mx::kColRows;
         const dim3 grid((unsigned)((C + mx::kColCols - 1) / mx::kColCols), (unsigned)row_tiles);
         if (x_dtype == NVFP4_BF16)
-            mx::mx_col_kernel<uint16_t><<<grid, mx::kColCols, 0, stream>>>(
-                static_cast<const uint16_t*>(x), ldx, (int)R, (int)C, nkt, out->codes, out->scales, out->scales_mma);
+            e = launch_pdl(mx::mx_col_kernel<uint16_t>, grid, dim3(mx::kColCols), 0, stream,
+                           static_cast<const uint16_t*>(x), ldx, (int)R, (int)C, nkt, out->codes, out->scales,
+                           out->scales_mma);
         else
-            mx::mx_col_kernel<float><<<grid, mx::kColCols, 0, stream>>>(
-                static_cast<const float*>(x), ldx, (int)R, (int)C, nkt, out->codes, out->scales, out->scales_mma);
+            e = launch_pdl(mx::mx_col_kernel<float>, grid, dim3(mx::kColCols), 0, stream, static_cast<const float*>(x),
+                           ldx, (int)R, (int)C, nkt, out->codes, out->scales, out->scales_mma);
     }
-    return cudaGetLastError() == cudaSuccess ? NVFP4_OK : NVFP4_ERR_CUDA;
+    return e == cudaSuccess ? NVFP4_OK : NVFP4_ERR_CUDA;
 }

@@ -100,6 +100,8 @@ __device__ __forceinline__ void block_max_store(uint32_t m, uint32_t* partials) 
 template <typename T, bool SQR = false>
 __global__ void __launch_bounds__(kThreads) amax_kernel(const T* __restrict__ x, int64_t R, int64_t C,
                                                         int64_t ldx, uint32_t* __restrict__ partials) {
+    pdl_launch_dependents();
+    pdl_wait();
     constexpr int VEC = Vec<T>::N;
     const int lane = threadIdx.x & 31;
     const int64_t cpr = C / VEC;
@@ -139,6 +141,8 @@ __global__ void __launch_bounds__(kThreads) amax_kernel(const T* __restrict__ x,
 template <typename T, bool SQR = false>
 __global__ void __launch_bounds__(kThreads) amax_flat_kernel(const T* __restrict__ x, int64_t nchunks,
                                                              uint32_t* __restrict__ partials) {
+    pdl_launch_dependents();
+    pdl_wait();
     constexpr int VEC = Vec<T>::N;
     constexpr int U = 8;
     const int64_t stride = (int64_t)gridDim.x * kThreads;
@@ -355,6 +359,8 @@ template <typename T>
 __global__ void __launch_bounds__(kPatchThreads, kPatchCtasPerSm) amax_rht_kernel(const T* __restrict__ x, int64_t R, int64_t C,
                                                             int64_t ldx, uint64_t rht_seed,
                                                             uint32_t* __restrict__ partials) {
+    pdl_launch_dependents();
+    pdl_wait();
     constexpr int VEC = Vec<T>::N;
     const int64_t tiles_c = (C + 8 * VEC - 1) / (8 * VEC);
     const int64_t tiles = ((R + 63) / 64) * tiles_c;
@@ -415,6 +421,8 @@ __global__ void __launch_bounds__(kPatchThreads, kPatchCtasPerSm) amax_dual_kern
                                                              int64_t ldx, uint64_t rht_seed,
                                                              uint32_t* __restrict__ partials_plain,
                                                              uint32_t* __restrict__ partials_rht) {
+    pdl_launch_dependents();
+    pdl_wait();
     constexpr int VEC = Vec<T>::N;
     const int64_t tiles_c = (C + 8 * VEC - 1) / (8 * VEC);
     const int64_t tiles = ((R + 63) / 64) * tiles_c;
@@ -632,6 +640,8 @@ __global__ void __launch_bounds__(kThreads) encode_row_kernel(const T* __restric
                                                               int64_t ldx, const uint32_t* __restrict__ partials,
                                                               int nparts, QOut out, uint64_t sr_seed,
                                                               uint32_t sr_offset, int v8, uint32_t* dev_status) {
+    pdl_launch_dependents();
+    pdl_wait();
     using B = Block16<T>;
     const Scales sc = tensor_scales(partials, nparts, out.s_dec, dev_status);
     const PhiloxKey key = philox_key(sr_seed);
@@ -770,6 +780,8 @@ __global__ void __launch_bounds__(kPatchThreads, kPatchCtasPerSm) encode_col_ker
                                                               int nparts, QOut out, uint64_t sr_seed,
                                                               uint32_t sr_offset, uint64_t rht_seed,
                                                               uint32_t* dev_status) {
+    pdl_launch_dependents();
+    pdl_wait();
     constexpr int VEC = Vec<T>::N;
     const uint32_t sign_mask = RHT ? rht_sign_mask(rht_seed) : 0u;
     const Scales sc = tensor_scales(partials, nparts, out.s_dec, dev_status);
@@ -848,6 +860,8 @@ __global__ void __launch_bounds__(kPatchThreads, kPatchCtasPerSm) encode_dual_ke
     const uint16_t* __restrict__ x, int64_t R, int64_t C, int64_t ldx, const uint32_t* __restrict__ part_row,
     const uint32_t* __restrict__ part_col, int nparts, QOut out_row, QOut out_col, uint64_t seed_row,
     uint64_t seed_col, uint32_t off_row, uint32_t off_col, uint64_t rht_seed, uint32_t* dev_status) {
+    pdl_launch_dependents();
+    pdl_wait();
     __shared__ float eb_row[128];
     const uint32_t sign_mask = rht_sign_mask(rht_seed);
     const Scales s_row = tensor_scales(part_row, nparts, out_row.s_dec, dev_status, eb_row);
@@ -909,6 +923,8 @@ __global__ void __launch_bounds__(kPatchThreads, kPatchCtasPerSm) encode_2d_kern
                                                              int64_t ldx, const uint32_t* __restrict__ partials,
                                                              int nparts, QOut out, uint64_t sr_seed,
                                                              uint32_t sr_offset, uint32_t* dev_status) {
+    pdl_launch_dependents();
+    pdl_wait();
     constexpr int VEC = Vec<T>::N;
     constexpr int LPT = 16 / VEC;                    // lanes per 16-column tile
     const Scales sc = tensor_scales(partials, nparts, out.s_dec, dev_status);
@@ -1164,8 +1180,7 @@ template <typename K, typename... Args>
 cudaError_t launch_resident(K* kern, int64_t work_ctas, int sms, int* grid, cudaStream_t stream, Args... args) {
     const int64_t wave = (int64_t)sms * resident_per_sm(kern, kThreads, 0);
     *grid = (int)std::max<int64_t>(1, std::min<int64_t>(std::min<int64_t>(wave, work_ctas), kMaxPartials));
-    kern<<<*grid, kThreads, 0, stream>>>(args...);
-    return cudaGetLastError();
+    return launch_pdl(kern, dim3(*grid), dim3(kThreads), 0, stream, args...);
 }
 
 // Grid of the patch kernels: one CTA (eight warps) per SM at most, one warp per
@@ -1199,8 +1214,7 @@ template <typename K, typename... Args>
 cudaError_t launch_patch(K* kern, int grid, cudaStream_t stream, Args... args) {
     const cudaError_t e = allow_patch_smem(kern);
     if (e != cudaSuccess) return e;
-    kern<<<grid, kPatchThreads, kPatchSmemBytes, stream>>>(args...);
-    return cudaGetLastError();
+    return launch_pdl(kern, dim3(grid), dim3(kPatchThreads), kPatchSmemBytes, stream, args...);
 }
 
 // Pass 1 for one quantization: per-CTA partial maxima of |x| or |RHT(x)|; *g1 = their count.
