@@ -273,7 +273,7 @@ def run_kernel_only(args):
         wq = nv.quantize(W, nv.TILE16, nv.RNE, scales=False, transpose=False)
         del dY
         out = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
-        work = lambda: nv.gemm(xq, wq, out=out)
+        work = lambda: nv.gemm(xq, wq, out=out, split_tail=True)
         unit, per = "TFLOP/s", 2.0 * M * N * K / 1e12
     else:
         def work():
@@ -422,7 +422,7 @@ def run_mlp(args):
             elif maxima:
                 out = nv.gemm_sqrelu_maxima(a, b, rht_seed=9)
             else:
-                out = nv.gemm(a, b, torch.bfloat16)
+                out = nv.gemm(a, b, torch.bfloat16, split_tail=True)
             if ev is not None:
                 ev[k][1].record(stream)
             return out
@@ -484,14 +484,17 @@ def run_heavy(args):
     dyq, dyt = nv.quantize_dual(dY, nv.SR, nv.SR, rht=True, sr_seed=7, rht_seed=11, scales=False)
 
     def gemms():
-        return (nv.gemm(xq, wq_op_w, torch.bfloat16), nv.gemm(dyq, wq_op_w.transposed(), torch.bfloat16),
-                nv.gemm(dyt, xt, torch.bfloat16))
+        return (nv.gemm(xq, wq_op_w, torch.bfloat16, split_tail=True),
+                nv.gemm(dyq, wq_op_w.transposed(), torch.bfloat16, split_tail=True),
+                nv.gemm(dyt, xt, torch.bfloat16, split_tail=True))
 
     def full():
         w = nv.quantize(W, nv.TILE16, nv.RNE, scales=False, transpose=True)
         a, at = nv.quantize_dual(X, nv.RNE, nv.RNE, rht=True, rht_seed=11, scales=False)
         g, gt = nv.quantize_dual(dY, nv.SR, nv.SR, rht=True, sr_seed=7, rht_seed=11, scales=False)
-        return nv.gemm(a, w, torch.bfloat16), nv.gemm(g, w.transposed(), torch.bfloat16), nv.gemm(gt, at, torch.bfloat16)
+        return (nv.gemm(a, w, torch.bfloat16, split_tail=True),
+                nv.gemm(g, w.transposed(), torch.bfloat16, split_tail=True),
+                nv.gemm(gt, at, torch.bfloat16, split_tail=True))
 
     def bf16():
         return X @ W.t(), dY @ W, dY.t() @ X
@@ -550,7 +553,7 @@ def run_yardstick(args):
         qa = nv.quantize(a, nv.ROW, nv.RNE, scales=False)
         qb = nv.quantize(b, nv.ROW, nv.RNE, scales=False)
         d = torch.empty((m, n), dtype=torch.bfloat16, device="cuda")
-        t = _timed(lambda: nv.gemm(qa, qb, out=d), args.steps, args.warmup)
+        t = _timed(lambda: nv.gemm(qa, qb, out=d, split_tail=True), args.steps, args.warmup)
         out["ours_tflops"][name] = round(flop / (t * 1e-3) / 1e12, 1)
         try:
             if fp4 is None:
@@ -704,14 +707,14 @@ def run_ours(args):
         mark(1)
         xq, xt = nv.quantize_dual(X, nv.RNE, nv.RNE, rht=True, rht_seed=11, scales=False)
         mark(2)
-        Y = nv.gemm(xq, wq, torch.bfloat16)
+        Y = nv.gemm(xq, wq, torch.bfloat16, split_tail=True)
         mark(3)
         dyq, dyt = nv.quantize_dual(dY, nv.SR, nv.SR, rht=True, sr_seed=7, sr_offset=sr_offset, rht_seed=11,
                                     scales=False)
         mark(4)
-        dX = nv.gemm(dyq, wq.transposed(), torch.bfloat16)
+        dX = nv.gemm(dyq, wq.transposed(), torch.bfloat16, split_tail=True)
         mark(5)
-        dW = nv.gemm(dyt, xt, torch.bfloat16)
+        dW = nv.gemm(dyt, xt, torch.bfloat16, split_tail=True)
         mark(6)
         return Y, dX, dW
 
@@ -819,11 +822,11 @@ def run_ours(args):
             Yd, dXd, dWd = outs[i % 2]
             wq = nv.quantize(ws, nv.TILE16, nv.RNE, scales=False, transpose=True)
             xq, xt = nv.quantize_dual(xs, nv.RNE, nv.RNE, rht=True, rht_seed=11, scales=False)
-            nv.gemm(xq, wq, out=Yd)
+            nv.gemm(xq, wq, out=Yd, split_tail=True)
             dyq, dyt = nv.quantize_dual(ys, nv.SR, nv.SR, rht=True, sr_seed=7, sr_offset=first + i,
                                         rht_seed=11, scales=False)
-            nv.gemm(dyq, wq.transposed(), out=dXd)
-            nv.gemm(dyt, xt, out=dWd)
+            nv.gemm(dyq, wq.transposed(), out=dXd, split_tail=True)
+            nv.gemm(dyt, xt, out=dWd, split_tail=True)
             fin = torch.cuda.Event()
             fin.record(stream)
             done[i % 2] = fin

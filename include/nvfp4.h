@@ -210,6 +210,33 @@ NVFP4_API nvfp4_status nvfp4_gemm(const nvfp4_qtensor* A, const nvfp4_qtensor* B
                         int64_t ldd, uint32_t* dev_status, void* stream);
 
 /*
+ * Bytes of the workspace nvfp4_gemm_ws uses on CUDA device `device` (partial sums for one
+ * 256 x 256 fp32 tile per pair of multiprocessors, and a few counters); 0 if the device cannot
+ * be queried.
+ */
+NVFP4_API size_t nvfp4_gemm_workspace_bytes(int32_t device);
+
+/*
+ * nvfp4_gemm_ws -- nvfp4_gemm that may balance the last, partial wave of output tiles over all
+ * multiprocessors: when the tiles do not divide evenly among the SM pairs, the tiles of the
+ * last wave are cut in two along K, computed by different SM pairs, whose fp32 partial sums
+ * meet in `workspace` (an order-free sum of two; whichever half finishes second stores the
+ * tile, and no SM waits for another).  NVFP4 operands, BF16 output through the CTA-pair
+ * kernel; otherwise the call is nvfp4_gemm.  Results are deterministic; the split tiles' sums
+ * are grouped differently from nvfp4_gemm's (a different fp32 rounding, well inside the GEMM's
+ * error bound), the other tiles are identical to nvfp4_gemm's.  Same arguments as nvfp4_gemm,
+ * plus: workspace -- device memory of at least nvfp4_gemm_workspace_bytes(current device)
+ * bytes (else NVFP4_ERR_WORKSPACE), 16-byte aligned, zero-filled before its first use; every
+ * call leaves it as the next call needs it, unless the call reports an error on dev_status, after
+ * which it must be zero-filled again.  Calls that may run concurrently (other streams) need
+ * workspaces of their own.  workspace NULL: exactly nvfp4_gemm.  Not on the page: a scheduling
+ * choice for the page's three GEMMs [page ¶2, ¶3].
+ */
+NVFP4_API nvfp4_status nvfp4_gemm_ws(const nvfp4_qtensor* A, const nvfp4_qtensor* B, void* D, int32_t d_dtype,
+                                     int64_t ldd, void* workspace, size_t workspace_bytes, uint32_t* dev_status,
+                                     void* stream);
+
+/*
  * nvfp4_gemm_sqrelu_bwd -- the Dgrad GEMM of a squared-ReLU MLP with the activation's
  * backward in its epilogue: with dA = bf16(s_dec(A) s_dec(B) sum_k qA qB) (what nvfp4_gemm
  * stores in BF16), D[m, n] = bf16(dA[m, n] * (H[m, n] > 0 ? 2 H[m, n] : +0)) in fp32 --

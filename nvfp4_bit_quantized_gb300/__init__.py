@@ -14,10 +14,12 @@ from __future__ import annotations
 
 from .api import (QTensor, quantize, quantize_dual, gemm, linear_fprop, linear_dgrad, linear_wgrad, quantize_weight,
                   status_query, dev_status, reset_status, scales_mma_bytes, NVFP4Error, sqrelu_forward,
-                  sqrelu_backward, gemm_sqrelu_backward, gemm_sqrelu_maxima, MXTensor, mx_quantize, mx_gemm, mx_scales_mma_bytes)
+                  sqrelu_backward, gemm_sqrelu_backward, gemm_sqrelu_maxima, MXTensor, mx_quantize, mx_gemm, mx_scales_mma_bytes,
+                  reset_gemm_workspaces)
 from ._lib import F32, BF16, RNE, SR, ROW, COL, TILE16, EXPORTS, LIB_PATH
 
 __all__ = ["QTensor", "quantize", "quantize_dual", "gemm", "linear_fprop", "linear_dgrad", "linear_wgrad", "quantize_weight",
            "status_query", "dev_status", "reset_status", "scales_mma_bytes", "NVFP4Error", "sqrelu_forward",
            "sqrelu_backward", "gemm_sqrelu_backward", "gemm_sqrelu_maxima", "MXTensor", "mx_quantize", "mx_gemm", "mx_scales_mma_bytes",
+           "reset_gemm_workspaces",
            "F32", "BF16", "RNE", "SR", "ROW", "COL", "TILE16", "EXPORTS", "LIB_PATH"]

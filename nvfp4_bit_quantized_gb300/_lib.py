@@ -17,7 +17,7 @@ ROW, COL, TILE16 = 0, 1, 2
 EXPORTS = [
     "nvfp4_scales_mma_bytes", "nvfp4_quantize_workspace_bytes", "nvfp4_quantize", "nvfp4_quantize_noalloc",
     "nvfp4_quantize_dual_workspace_bytes", "nvfp4_quantize_dual", "nvfp4_quantize_dual_sqrelu",
-    "nvfp4_gemm",
+    "nvfp4_gemm", "nvfp4_gemm_workspace_bytes", "nvfp4_gemm_ws",
     "nvfp4_linear_workspace_bytes", "nvfp4_linear_fprop", "nvfp4_linear_dgrad", "nvfp4_linear_wgrad",
     "nvfp4_status_query", "nvfp4_status_string", "nvfp4_set_wait_timeout_ns", "nvfp4_debug_e4m3",
     "nvfp4_debug_e2m1", "nvfp4_debug_philox", "nvfp4_selftest_wait_timeout", "nvfp4_gemm_force_path",
@@ -73,6 +73,8 @@ def lib():
             "nvfp4_quantize_dual": (I32, [P, I32, I64, I64, I64, QP, QT, QP, QT, P, SZ, P, P]),
             "nvfp4_quantize_dual_sqrelu": (I32, [P, I32, I64, I64, I64, QP, QT, QP, QT, P, SZ, P, P]),
             "nvfp4_gemm": (I32, [QT, QT, P, I32, I64, P, P]),
+            "nvfp4_gemm_workspace_bytes": (SZ, [I32]),
+            "nvfp4_gemm_ws": (I32, [QT, QT, P, I32, I64, P, SZ, P, P]),
             "nvfp4_linear_workspace_bytes": (SZ, [I64, I64, I64]),
             "nvfp4_linear_fprop": (I32, [P, I32, I64, I64, I64, QT, P, I32, I64, P, SZ, P, P]),
             "nvfp4_linear_dgrad": (I32, [P, I32, I64, I64, I64, QT, U64, U32, P, I32, I64, P, SZ, P, P]),

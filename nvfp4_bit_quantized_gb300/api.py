@@ -188,13 +188,47 @@ def quantize_weight(W: torch.Tensor) -> QTensor:
     return quantize(W, L.TILE16, L.RNE, transpose=True)
 
 
-def gemm(A: QTensor, B: QTensor, out_dtype=torch.bfloat16, out: Optional[torch.Tensor] = None) -> torch.Tensor:
-    """D[M, N] = dequant(A) . dequant(B)^T on the tcgen05 block-scaled FP4 tensor cores."""
+_gemm_ws = {}
+
+
+def _gemm_workspace(device) -> torch.Tensor:
+    """The split-tail workspace of ``gemm(..., split_tail=True)`` for this device and stream:
+    zero-filled once; every call leaves it zeroed (after a device error, call
+    ``reset_gemm_workspaces``)."""
+    dev = torch.device(device)
+    key = (dev.index, _stream())
+    t = _gemm_ws.get(key)
+    if t is None:
+        nbytes = int(L.lib().nvfp4_gemm_workspace_bytes(dev.index))
+        if nbytes == 0:
+            raise NVFP4Error(L.ERR_CUDA, "cannot size the GEMM workspace for this device")
+        t = torch.zeros(nbytes, dtype=torch.uint8, device=dev)
+        _gemm_ws[key] = t
+    return t
+
+
+def reset_gemm_workspaces() -> None:
+    """Zero-fill every cached split-tail workspace (needed after a GEMM reported a device error)."""
+    for t in _gemm_ws.values():
+        t.zero_()
+
+
+def gemm(A: QTensor, B: QTensor, out_dtype=torch.bfloat16, out: Optional[torch.Tensor] = None,
+         split_tail: bool = False) -> torch.Tensor:
+    """D[M, N] = dequant(A) . dequant(B)^T on the tcgen05 block-scaled FP4 tensor cores.
+    With ``split_tail`` (nvfp4_gemm_ws), the tiles of the last partial wave are cut in two along
+    K over more SM pairs (deterministic; those tiles' fp32 sums are grouped differently)."""
     M, N = A.rows, B.rows
     if out is None:
         out = torch.empty((M, N), dtype=out_dtype, device=A.codes.device)
     _check_2d(out, "out")
     a, b = A.c_struct(), B.c_struct()
+    if split_tail:
+        ws = _gemm_workspace(out.device)
+        st = L.lib().nvfp4_gemm_ws(ctypes.byref(a), ctypes.byref(b), _ptr(out), _DT[out.dtype], out.stride(0),
+                                   _ptr(ws), ws.numel(), dev_status(out.device).data_ptr(), _stream())
+        L.check(st, "nvfp4_gemm_ws")
+        return out
     st = L.lib().nvfp4_gemm(ctypes.byref(a), ctypes.byref(b), _ptr(out), _DT[out.dtype], out.stride(0),
                             dev_status(out.device).data_ptr(), _stream())
     L.check(st, "nvfp4_gemm")

@@ -102,6 +102,12 @@ struct Params {
     uint32_t* maxima;            // EPI_SQAMAX / EPI_DSQR_AMAX: 2 x maxima_parts partial maxima (|X|, then |RHT(X)| / 4)
     int maxima_parts;            // partials per half of `maxima` (>= 4 x grid)
     uint64_t rht_seed;           // the RHT sign vector of the column quantization those maxima serve
+    // Split tail (pair kernel, EPI_PLAIN, with a caller workspace): the r tiles of the last,
+    // partial wave are cut into `split` parts along K, one part per cluster, so the last wave
+    // takes 1 / split of a tile's time.  split = 1: every tile is computed whole.
+    int split;
+    float* split_ws;             // per tail tile, CTA and epilogue warp: 32 x 128 fp32 sums (left at 0)
+    uint32_t* split_cnt;         // per tail tile, CTA and epilogue warp: halves arrived (left at 0)
 };
 
 // Epilogue variants of the CTA-pair kernel.
@@ -119,6 +125,35 @@ constexpr int EPI_PLAIN = 0, EPI_DSQR = 1, EPI_SQAMAX = 2, EPI_DSQR_AMAX = 3;
 __device__ __forceinline__ void tile_coords(const Params& p, int tile, int m_count, int& m, int& n) {
     if (p.n_fastest) { n = tile % p.n_tiles; m = tile / p.n_tiles; }
     else { m = tile % m_count; n = tile / m_count; }
+}
+
+// Work item i of cluster c (of P) in the pair kernel: the whole tiles c, c + P, ... of the full
+// waves, then at most one item of the last, partial wave -- the whole tile (split = 1) or, with
+// split = S, part c % S of tail tile c / S: K tiles [part nkt / S, (part + 1) nkt / S).  The host
+// keeps S <= nkt and (tail tiles) x S <= P.  False when cluster c has no item i.
+struct PairItem {
+    int tile, kb, ke;
+    int part;                    // -1: a whole tile
+};
+__device__ __forceinline__ bool pair_item(const Params& p, int tiles, int c, int P, int i, PairItem& it) {
+    const int waves = tiles / P;
+    if (i < waves) {
+        it.tile = c + i * P; it.kb = 0; it.ke = p.nkt; it.part = -1;
+        return true;
+    }
+    if (i > waves) return false;
+    const int r = tiles - waves * P;
+    if (p.split <= 1) {
+        if (c >= r) return false;
+        it.tile = waves * P + c; it.kb = 0; it.ke = p.nkt; it.part = -1;
+        return true;
+    }
+    if (c >= r * p.split) return false;
+    it.part = c % p.split;
+    it.tile = waves * P + c / p.split;
+    it.kb = it.part * p.nkt / p.split;
+    it.ke = (it.part + 1) * p.nkt / p.split;
+    return true;
 }
 
 // ---- PTX wrappers ---------------------------------------------------------------
@@ -738,6 +773,46 @@ __device__ __forceinline__ void box_maxima(const uint8_t* box, int lane, int m0,
     }
 }
 
+// One half of a split tail tile (see pair_item; the host splits in two, so two parts meet).
+// The warp adds its 32 x 128 fp32 partial sums (va: columns 0-63, vb: 64-127 of its slice) into
+// the tile's sum buffer in the workspace with vector reductions -- laid out as 32 groups of four
+// columns x 32 lanes x 16 bytes, so each is one 512-byte run -- and counts itself in on the
+// tile's counter.  The half that arrives second (returns true) loads the finished sums into
+// va / vb for the normal epilogue and leaves buffer and counter at zero for the next call; the
+// first returns false and stores nothing.  0 + a + b == 0 + b + a in fp32, so the result does not
+// depend on which half finishes first, and no half waits for the other.  (The reductions flush
+// subnormal values; the accumulator of E2M1 x E4M3 products is a multiple of 2^-20, never
+// subnormal.)
+__device__ __forceinline__ bool split_partial(const Params& p, int tail_tile, uint32_t rank, int e, int lane,
+                                              uint32_t (&va)[64], uint32_t (&vb)[64]) {
+    float4* buf = reinterpret_cast<float4*>(p.split_ws + (((size_t)tail_tile * 2 + rank) * 8 + e) * (32 * 128));
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+        const uint32_t* v = j < 16 ? &va[4 * j] : &vb[4 * (j - 16)];
+        asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};"
+                     :: "l"(buf + j * 32 + lane), "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]) : "memory");
+    }
+    __threadfence();
+    __syncwarp();
+    uint32_t* cnt = p.split_cnt + ((size_t)tail_tile * 2 + rank) * 8 + e;
+    uint32_t before = 0;
+    if (lane == 0) before = atomicAdd(cnt, 1u);
+    before = __shfl_sync(0xFFFFFFFFu, before, 0);
+    if (before == 0) return false;
+    __threadfence();
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+        const float4 x = __ldcg(buf + j * 32 + lane);
+        uint32_t* v = j < 16 ? &va[4 * j] : &vb[4 * (j - 16)];
+        v[0] = __float_as_uint(x.x); v[1] = __float_as_uint(x.y);
+        v[2] = __float_as_uint(x.z); v[3] = __float_as_uint(x.w);
+    }
+#pragma unroll
+    for (int j = 0; j < 32; ++j) __stcg(buf + j * 32 + lane, make_float4(0.0f, 0.0f, 0.0f, 0.0f));
+    if (lane == 0) *cnt = 0u;
+    return true;
+}
+
 __device__ __forceinline__ void tmem_ld_64cols(uint32_t taddr, uint32_t (&v)[64]) {
     tmem_ld_32cols_nowait(taddr, *reinterpret_cast<uint32_t (*)[32]>(&v[0]));
     tmem_ld_32cols_nowait(taddr + 32, *reinterpret_cast<uint32_t (*)[32]>(&v[32]));
@@ -748,8 +823,9 @@ __device__ __forceinline__ void reg_fence64(uint32_t (&v)[64]) {
 }
 
 // MX: MXFP4 operands.  EPI: the epilogue variant (EPI_DSQR reads H through tmH: bf16, same
-// shape and box as D).
-template <bool MX, int EPI>
+// shape and box as D).  SPLIT: the tail tiles are cut in two along K (p.split == 2; NVFP4 with
+// EPI_PLAIN only) -- a separate instantiation, so kernels that never split carry none of it.
+template <bool MX, int EPI, bool SPLIT = false>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(P_THREADS, 1)
 gemm_nvfp4_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                        const __grid_constant__ CUtensorMap tmD, const __grid_constant__ CUtensorMap tmH,
@@ -828,9 +904,10 @@ gemm_nvfp4_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_con
             uint32_t stage = 0, phase = 0;
             uint32_t issued_mask = 0, issued_phase = 0;
             bool ok = true;
-            for (int tile = cluster; tile < tiles && ok; tile += nclusters) {
+            PairItem it;
+            for (int item = 0; ok && pair_item(p, tiles, cluster, nclusters, item, it); ++item) {
                 int mp, nt;
-                tile_coords(p, tile, m_pairs, mp, nt);
+                tile_coords(p, it.tile, m_pairs, mp, nt);
                 const int mrow = mp * 256 + (int)rank * 128;      // this CTA's A rows
                 const int nrow = nt * BN + (int)rank * 128;       // this CTA's B rows
                 const bool second_sfb = (nt * BN + 128) < p.N;
@@ -839,7 +916,7 @@ gemm_nvfp4_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_con
                 const bool has_sfa = mrow < p.M;
                 constexpr uint32_t SFT = PairSf<MX>::TILE;
                 const uint32_t sf_bytes = (has_sfa ? SFT : 0) + (second_sfb ? 2 * SFT : SFT);
-                for (int kt = 0; kt < p.nkt; ++kt) {
+                for (int kt = it.kb; kt < it.ke; ++kt) {
                     if (!mbar_wait_bounded(&empty[stage], phase ^ 1u, p.timeout_ns, abort_flag, p.dev_status)) {
                         ok = false;
                         break;
@@ -877,13 +954,14 @@ gemm_nvfp4_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_con
         if (lane == 0 && leader) {
             uint32_t stage = 0, phase = 0, acc_phase = 0;
             bool ok = true, issued = false;
-            for (int tile = cluster; tile < tiles && ok; tile += nclusters) {
+            PairItem it;
+            for (int item = 0; ok && pair_item(p, tiles, cluster, nclusters, item, it); ++item) {
                 if (!mbar_wait_bounded(acc_empty, acc_phase ^ 1u, p.timeout_ns, abort_flag, p.dev_status)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
-                for (int kt = 0; kt < p.nkt; ++kt) {
+                for (int kt = it.kb; kt < it.ke; ++kt) {
                     if (!mbar_wait_bounded(&sf_ready[stage], phase, p.timeout_ns, abort_flag, p.dev_status)) {
                         ok = false;
                         break;
@@ -895,7 +973,7 @@ gemm_nvfp4_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_con
 #pragma unroll
                     for (int j = 0; j < 4; ++j)
                         tc_mma_pair<MX>(tmem + ACC_COL, da + 2 * j, db + 2 * j, tsf + 4 * j, tsf + 16 + 8 * j,
-                                        (kt | j) != 0 ? 1u : 0u);
+                                        (kt != it.kb || j != 0) ? 1u : 0u);
                     issued = true;
                     tc_commit_pair(smem_addr(&empty[stage]));
                     if (++stage == STAGES) { stage = 0; phase ^= 1u; }
@@ -915,8 +993,9 @@ gemm_nvfp4_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_con
         const uint32_t tq = tmem + ((uint32_t)(q * 32) << 16);
         uint32_t stage = 0, phase = 0;
         bool ok = true;
-        for (int tile = cluster; tile < tiles && ok; tile += nclusters) {
-            for (int kt = 0; kt < p.nkt; ++kt) {
+        PairItem it;
+        for (int item = 0; ok && pair_item(p, tiles, cluster, nclusters, item, it); ++item) {
+            for (int kt = it.kb; kt < it.ke; ++kt) {
                 if (!mbar_wait_bounded(&sf_loaded[stage], phase, p.timeout_ns, abort_flag, p.dev_status)) {
                     ok = false;
                     break;
@@ -1003,9 +1082,10 @@ gemm_nvfp4_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_con
         uint32_t mabs = 0u, mrht = 0u;                   // AMAX: running maxima (float bits)
         const uint32_t sign_mask = AMAX ? rht_sign_mask(p.rht_seed) : 0u;
         bool ok = true;
-        for (int tile = cluster; tile < tiles && ok; tile += nclusters) {
+        PairItem it;
+        for (int item = 0; ok && pair_item(p, tiles, cluster, nclusters, item, it); ++item) {
             int mp, nt;
-            tile_coords(p, tile, m_pairs, mp, nt);
+            tile_coords(p, it.tile, m_pairs, mp, nt);
             const int m0 = mp * 256 + (int)rank * 128 + q * 32, nb = nt * BN + 128 * h;
             // DSQR: the H box of output box b (columns nb + 64 b) into the slot, and the wait for it
             // (boxes past M or N read the fill value; their results are never stored)
@@ -1055,6 +1135,11 @@ gemm_nvfp4_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_con
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive_cluster(acc_empty_leader);
+            acc_phase ^= 1u;
+            if constexpr (SPLIT) {
+                if (it.part >= 0 && !split_partial(p, it.tile - tiles / nclusters * nclusters, rank, e, lane, va, vb))
+                    continue;
+            }
             if constexpr (DSQR) {
                 if (!wait_h()) { ok = false; break; }
             }
@@ -1068,7 +1153,6 @@ gemm_nvfp4_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_con
             }
             box_out<EPI>(vb, slot, lane, alpha);
             store_box(1);
-            acc_phase ^= 1u;
         }
         if constexpr (AMAX) {
             // this warp's partials; the first CTA zeroes the slots no CTA of this grid owns
@@ -1156,21 +1240,29 @@ cudaError_t launch(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorM
                       td, p);
 }
 
-template <bool MX, int EPI = EPI_PLAIN>
-cudaError_t launch_pair(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& td, const CUtensorMap& th,
-                        const Params& p, int pair_tiles, int sms, cudaStream_t stream) {
+// Split-tail workspace: a sum buffer per tail tile (at most one per cluster; each CTA's 128 x 256
+// fp32), then the arrival counters (per tail tile, CTA and epilogue warp); both start at zero
+// and every call leaves them at zero.
+constexpr int kSplitMaxWaves = 16;       // split the tail only below this many full waves
+inline size_t split_partials_bytes(int sms) { return (size_t)(sms / 2) * 2 * 128 * 256 * sizeof(float); }
+inline size_t split_ws_bytes(int sms) { return split_partials_bytes(sms) + (size_t)(sms / 2) * 2 * 8 * sizeof(uint32_t); }
+
+// One-time set-up of a pair-kernel instantiation: its shared memory, the register check and
+// the clusters that fit at once.
+template <bool MX, int EPI, bool SPLIT>
+cudaError_t pair_setup(int sms, int* max_clusters) {
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
-    static int max_clusters = 0;
+    static int clusters = 0;
     std::call_once(once, [sms] {
-        attr_err = cudaFuncSetAttribute(gemm_nvfp4_pair_kernel<MX, EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        P_SMEM_BYTES);
+        attr_err = cudaFuncSetAttribute(gemm_nvfp4_pair_kernel<MX, EPI, SPLIT>,
+                                        cudaFuncAttributeMaxDynamicSharedMemorySize, P_SMEM_BYTES);
         if (attr_err != cudaSuccess) return;
         // The kernel moves registers between warpgroups with setmaxnreg; the epilogue's
         // increase only completes if the launch holds at least the split's total, so a build
         // that allocated fewer registers per thread is never launched.
         cudaFuncAttributes fa;
-        attr_err = cudaFuncGetAttributes(&fa, gemm_nvfp4_pair_kernel<MX, EPI>);
+        attr_err = cudaFuncGetAttributes(&fa, gemm_nvfp4_pair_kernel<MX, EPI, SPLIT>);
         if (attr_err != cudaSuccess) return;
         if (fa.numRegs * P_THREADS < 2 * 128 * P_REGS_LOW + 2 * 128 * P_REGS_HIGH) {
             attr_err = cudaErrorInvalidConfiguration;
@@ -1181,14 +1273,46 @@ cudaError_t launch_pair(const CUtensorMap& ta, const CUtensorMap& tb, const CUte
         cfg.blockDim = dim3(P_THREADS, 1, 1);
         cfg.dynamicSmemBytes = P_SMEM_BYTES;
         int n = 0;
-        if (cudaOccupancyMaxActiveClusters(&n, gemm_nvfp4_pair_kernel<MX, EPI>, &cfg) != cudaSuccess || n <= 0)
+        if (cudaOccupancyMaxActiveClusters(&n, gemm_nvfp4_pair_kernel<MX, EPI, SPLIT>, &cfg) != cudaSuccess || n <= 0)
             n = sms / 2;
-        max_clusters = n;
+        clusters = n;
     });
-    if (attr_err != cudaSuccess) return attr_err;
+    *max_clusters = clusters;
+    return attr_err;
+}
+
+template <bool MX, int EPI = EPI_PLAIN>
+cudaError_t launch_pair(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& td, const CUtensorMap& th,
+                        Params p, int pair_tiles, int sms, cudaStream_t stream, void* split_ws = nullptr) {
+    int max_clusters = 0;
+    const cudaError_t err = pair_setup<MX, EPI, false>(sms, &max_clusters);
+    if (err != cudaSuccess) return err;
     const int clusters = std::max(1, std::min(pair_tiles, max_clusters));
-    return launch_pdl(gemm_nvfp4_pair_kernel<MX, EPI>, dim3(2 * clusters), dim3(P_THREADS), P_SMEM_BYTES, stream, ta, tb,
-                      td, th, p);
+    // Split tail: cut the last partial wave's r tiles in two along K so that it takes half a
+    // tile's time, when there are clusters for both halves (2 r <= clusters), K spans two K
+    // tiles, and the waves are few enough for half a tile to outweigh the split kernel's longer
+    // epilogue (measured: worth it at 9 waves, not at 22).  Two halves meet by order-free fp32
+    // reductions (deterministic); more parts would need an order-fixed sum the reductions
+    // cannot give.  NVFP4 only (MXFP4's power-of-two scales reach the subnormal range the
+    // reductions flush).
+    p.split = 1;
+    const int r = pair_tiles % clusters;
+    if constexpr (EPI == EPI_PLAIN && !MX) {
+        if (split_ws && r != 0 && 2 * r <= clusters && p.nkt >= 2 && pair_tiles / clusters < kSplitMaxWaves) {
+            int split_clusters = 0;
+            const cudaError_t e2 = pair_setup<MX, EPI, true>(sms, &split_clusters);
+            if (e2 != cudaSuccess) return e2;
+            if (split_clusters == max_clusters) {
+                p.split = 2;
+                p.split_ws = static_cast<float*>(split_ws);
+                p.split_cnt = reinterpret_cast<uint32_t*>(static_cast<uint8_t*>(split_ws) + split_partials_bytes(sms));
+                return launch_pdl(gemm_nvfp4_pair_kernel<MX, EPI, true>, dim3(2 * clusters), dim3(P_THREADS),
+                                  P_SMEM_BYTES, stream, ta, tb, td, th, p);
+            }
+        }
+    }
+    return launch_pdl(gemm_nvfp4_pair_kernel<MX, EPI, false>, dim3(2 * clusters), dim3(P_THREADS), P_SMEM_BYTES,
+                      stream, ta, tb, td, th, p);
 }
 
 int g_force_path = 0;      // 0: automatic, 1: single-CTA kernel, 2: CTA-pair kernel (tests)
@@ -1196,7 +1320,7 @@ int g_force_path = 0;      // 0: automatic, 1: single-CTA kernel, 2: CTA-pair ke
 }  // namespace gemm
 
 nvfp4_status gemm_impl(const nvfp4_qtensor* A, const nvfp4_qtensor* B, void* D, int32_t d_dtype, int64_t ldd,
-                       uint32_t* dev_status, cudaStream_t stream) {
+                       uint32_t* dev_status, cudaStream_t stream, void* ws, size_t ws_bytes) {
     using namespace gemm;
     if (!A || !B || !D) return NVFP4_ERR_INVALID_ARG;
     if (d_dtype != NVFP4_F32 && d_dtype != NVFP4_BF16) return NVFP4_ERR_INVALID_ARG;
@@ -1216,6 +1340,7 @@ nvfp4_status gemm_impl(const nvfp4_qtensor* A, const nvfp4_qtensor* B, void* D, 
 
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return NVFP4_ERR_CUDA;
+    if (ws && (ws_bytes < split_ws_bytes(sm_count(dev)) || !aligned16(ws))) return NVFP4_ERR_WORKSPACE;
     Params p;
     p.sfa = A->scales_mma;
     p.sfb = B->scales_mma;
@@ -1249,7 +1374,7 @@ nvfp4_status gemm_impl(const nvfp4_qtensor* A, const nvfp4_qtensor* B, void* D, 
     if (pair) {
         CUtensorMap tb2;      // B boxes of 128 rows (each CTA loads its half of the N tile)
         if (!make_codes_map(&tb2, B->codes, N, K, 128)) return NVFP4_ERR_CUDA;
-        e = launch_pair<false>(ta, tb2, td, td, p, pair_tiles, sm_count(dev), stream);
+        e = launch_pair<false>(ta, tb2, td, td, p, pair_tiles, sm_count(dev), stream, ws);
     } else {
         e = staged ? launch<true>(ta, tb, td, p, grid, stream) : launch<false>(ta, tb, td, p, grid, stream);
     }
@@ -1447,5 +1572,17 @@ extern "C" void nvfp4_gemm_force_path(int32_t path) { nvfp4::gemm::g_force_path 
 
 extern "C" nvfp4_status nvfp4_gemm(const nvfp4_qtensor* A, const nvfp4_qtensor* B, void* D, int32_t d_dtype,
                                    int64_t ldd, uint32_t* dev_status, void* stream) {
-    return nvfp4::gemm_impl(A, B, D, d_dtype, ldd, dev_status, static_cast<cudaStream_t>(stream));
+    return nvfp4::gemm_impl(A, B, D, d_dtype, ldd, dev_status, static_cast<cudaStream_t>(stream), nullptr, 0);
+}
+
+extern "C" size_t nvfp4_gemm_workspace_bytes(int32_t device) {
+    const int sms = nvfp4::sm_count(device);
+    return sms > 0 ? nvfp4::gemm::split_ws_bytes(sms) : 0u;
+}
+
+extern "C" nvfp4_status nvfp4_gemm_ws(const nvfp4_qtensor* A, const nvfp4_qtensor* B, void* D, int32_t d_dtype,
+                                      int64_t ldd, void* workspace, size_t workspace_bytes, uint32_t* dev_status,
+                                      void* stream) {
+    return nvfp4::gemm_impl(A, B, D, d_dtype, ldd, dev_status, static_cast<cudaStream_t>(stream), workspace,
+                            workspace_bytes);
 }

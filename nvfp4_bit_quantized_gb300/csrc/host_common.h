@@ -48,7 +48,8 @@ nvfp4_status quantize_impl(const void* x, int32_t x_dtype, int64_t R, int64_t C,
                            const nvfp4_qparams* p, const nvfp4_qtensor* out, void* ws, size_t ws_bytes,
                            uint32_t* dev_status, cudaStream_t stream);
 
+// ws: optional split-tail workspace (nvfp4_gemm_ws), NULL for tile-by-tile work.
 nvfp4_status gemm_impl(const nvfp4_qtensor* A, const nvfp4_qtensor* B, void* D, int32_t d_dtype, int64_t ldd,
-                       uint32_t* dev_status, cudaStream_t stream);
+                       uint32_t* dev_status, cudaStream_t stream, void* ws = nullptr, size_t ws_bytes = 0);
 
 }  // namespace nvfp4

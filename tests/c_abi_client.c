@@ -19,6 +19,7 @@ int main(void) {
     CHECK(nvfp4_scales_mma_bytes(128, 256) == 2048);
     CHECK(nvfp4_mx_scales_mma_bytes(128, 256) == 1024);
     CHECK(nvfp4_sqrelu_maxima_bytes(-1) == 0);      /* sized per device: no such device */
+    CHECK(nvfp4_gemm_workspace_bytes(-1) == 0);
 
     nvfp4_qparams p;
     memset(&p, 0, sizeof p);
@@ -47,6 +48,7 @@ int main(void) {
     a.rows = 128; a.cols = 256;
     b.rows = 256; b.cols = 128;                      /* K mismatch */
     CHECK(nvfp4_gemm(&a, &b, (void*)0x4000, NVFP4_BF16, 256, NULL, NULL) == NVFP4_ERR_SHAPE);
+    CHECK(nvfp4_gemm_ws(&a, &b, (void*)0x4000, NVFP4_BF16, 256, NULL, 0, NULL, NULL) == NVFP4_ERR_SHAPE);
     CHECK(nvfp4_mx_gemm(&a, &b, (void*)0x4000, NVFP4_F32, 256, NULL, NULL) == NVFP4_ERR_UNSUPPORTED);
     printf("%s %d\n", fails ? "failed" : "ok", fails);
     return fails != 0;

@@ -136,3 +136,72 @@ def test_operands_read_identically_by_cublaslt(nv):
     ref = lib.float() * (qa.s_dec[0] * qb.s_dec[0]).float()
     rel = ((ours - ref).norm() / ref.norm()).item()
     assert rel < 4e-3, rel
+
+
+# ---- split tail (nvfp4_gemm_ws): the last partial wave's tiles cut along K over all SM pairs
+
+def _pair_plan(M, N, K):
+    """Tiles, tail tiles and parts of the split-tail schedule (one SM pair per cluster)."""
+    clusters = torch.cuda.get_device_properties(0).multi_processor_count // 2
+    tiles = ((M + 255) // 256) * ((N + 255) // 256)
+    clusters = min(clusters, tiles)
+    r = tiles % clusters
+    nkt = (K + 255) // 256
+    split = r != 0 and 2 * r <= clusters and nkt >= 2 and tiles // clusters < 16
+    return tiles, r, (2 if split else 1)
+
+
+@pytest.mark.parametrize("M,N,K", [(2048, 2560, 1024), (8192, 1280, 512), (2000, 2600, 544)])
+def test_split_tail_gemm_matches_oracle_and_tile_by_tile(nv, oracle_mod, M, N, K):
+    """With a workspace the tail tiles are summed from two K halves: the result stays
+    within the GEMM bound of the fp64 oracle, differs from the tile-by-tile kernel only in
+    those tiles (a different fp32 grouping), and is deterministic."""
+    tiles, r, parts = _pair_plan(M, N, K)
+    assert parts >= 2, "shape chosen to split its tail"
+    qa, qb = _operands(nv, M, N, K, seed=M + 3 * N + K)
+    nv.reset_status()
+    d_split = nv.gemm(qa, qb, torch.bfloat16, split_tail=True)
+    d_again = nv.gemm(qa, qb, torch.bfloat16, split_tail=True)
+    d_whole = nv.gemm(qa, qb, torch.bfloat16)
+    torch.cuda.synchronize()
+    assert nv.status_query() == 0
+    assert torch.equal(d_split, d_again)
+    ref = bf16_round(oracle_mod.gemm_f64(oracle_mod.dequant(qtensor_to_oracle(qa, 0)),
+                                         oracle_mod.dequant(qtensor_to_oracle(qb, 0)),
+                                         threads=oracle_mod.host_cores()))
+    assert rel_fro(d_split.float().cpu().numpy(), ref) <= TOL
+    differ = (d_split != d_whole).sum().item()
+    assert differ <= (r / tiles) * M * N, (differ, r, tiles)
+    assert rel_fro(d_split.float().cpu().numpy(), d_whole.float().cpu().numpy()) <= 1e-3
+
+
+def test_split_tail_workspace_left_ready_and_in_bounds(nv):
+    """Calls of different shapes share one workspace (each leaves its counters at zero), and
+    nothing is written past the declared workspace size."""
+    from nvfp4_bit_quantized_gb300 import _lib as L
+    nbytes = int(L.lib().nvfp4_gemm_workspace_bytes(0))
+    assert nbytes > 0
+    ws = torch.zeros(nbytes + 4096, dtype=torch.uint8, device="cuda")
+    ws[nbytes:] = 0xA5
+    import ctypes
+    from nvfp4_bit_quantized_gb300.api import dev_status, _ptr, _stream
+
+    def run(qa, qb, M, N):
+        out = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+        a, b = qa.c_struct(), qb.c_struct()
+        st = L.lib().nvfp4_gemm_ws(ctypes.byref(a), ctypes.byref(b), _ptr(out), L.BF16, N, _ptr(ws), nbytes,
+                                   dev_status(out.device).data_ptr(), _stream())
+        assert st == 0
+        return out
+    first = _operands(nv, 2048, 2560, 1024, seed=41)
+    second = _operands(nv, 8192, 1280, 512, seed=42)
+    nv.reset_status()
+    o1 = run(*first, 2048, 2560)
+    run(*second, 8192, 1280)
+    o3 = run(*first, 2048, 2560)
+    torch.cuda.synchronize()
+    assert nv.status_query() == 0
+    assert torch.equal(o1, o3)
+    assert torch.all(ws[nbytes:] == 0xA5)
+    # sum buffers and arrival counters are back at zero, ready for the next call
+    assert torch.count_nonzero(ws[:nbytes]).item() == 0

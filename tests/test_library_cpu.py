@@ -176,6 +176,21 @@ def test_gemm_sqrelu_backward_rejects_bad_arguments(lib):
     assert f(ctypes.byref(A), ctypes.byref(B), 0x8000, 256, 0x4000, 256, None, None) == lib.ERR_INVALID_ARG
 
 
+def test_gemm_ws_rejects_bad_arguments_before_touching_the_device(lib):
+    """nvfp4_gemm_ws: the shape and pointer checks of nvfp4_gemm come first (no device
+    here); the workspace is sized per device, so without one the size is 0."""
+    L = lib.lib()
+    assert L.nvfp4_gemm_workspace_bytes(0) == 0 and L.nvfp4_gemm_workspace_bytes(-1) == 0
+    A = lib.QTensorC(0x1000, None, 0x1000, 0x2000, None, None, 128, 256)
+    B = lib.QTensorC(0x1000, None, 0x1000, 0x2000, None, None, 256, 128)     # K mismatch
+    g = L.nvfp4_gemm_ws
+    assert g(ctypes.byref(A), ctypes.byref(B), 0x4000, lib.BF16, 256, 0x8000, 1 << 20, None, None) == lib.ERR_SHAPE
+    B.cols = 256
+    assert g(ctypes.byref(A), ctypes.byref(B), None, lib.BF16, 256, 0x8000, 1 << 20, None, None) == lib.ERR_INVALID_ARG
+    A.codes = 0x1004
+    assert g(ctypes.byref(A), ctypes.byref(B), 0x4000, lib.BF16, 256, None, 0, None, None) == lib.ERR_ALIGNMENT
+
+
 def test_sqrelu_maxima_entries_reject_bad_arguments(lib):
     L = lib.lib()
     # sized from the device's multiprocessor count: no device here, so 0 (never a fixed cap)
