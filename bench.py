@@ -536,14 +536,16 @@ def run_heavy(args):
 def run_yardstick(args):
     """Library yardsticks at the three GEMM shapes of the bench workload (context, not the
     target): the same NVFP4 operands through torch._scaled_mm's block-scaled FP4 path
-    (cuBLASLt) where this torch offers it -- also a cross-check of the result -- and an FP8
-    (e4m3, per-tensor scale) GEMM through torch._scaled_mm, against this library's GEMM."""
+    (cuBLASLt) where this torch offers it -- also a cross-check of the result -- and FP8 (e4m3)
+    GEMMs through torch._scaled_mm, with a per-tensor scale and block-scaled (MXFP8: one UE8M0
+    scale per 32 elements along K), against this library's GEMM."""
     import torch
     import nvfp4_bit_quantized_gb300 as nv
     from nvfp4_bit_quantized_gb300 import inputs
     shapes = {"fprop": (M, K, N), "dgrad": (M, N, K), "wgrad": (N, M, K)}     # (rows of A, K, rows of B)
     out = {"config": "gemm_yardsticks", "shapes_MKN": {}, "ours_tflops": {}, "cublaslt_nvfp4_tflops": {},
-           "cublaslt_fp8_tflops": {}, "nvfp4_vs_cublaslt_rel_diff": {}, "notes": []}
+           "cublaslt_fp8_tflops": {}, "cublaslt_mxfp8_tflops": {}, "mxfp8_vs_fp8_rel_diff": {},
+           "nvfp4_vs_cublaslt_rel_diff": {}, "notes": []}
     fp4 = getattr(torch, "float4_e2m1fn_x2", None)
     for name, (m, k, n) in shapes.items():
         out["shapes_MKN"][name] = [m, k, n]
@@ -573,18 +575,39 @@ def run_yardstick(args):
         except Exception as e:                                    # not offered by this torch / cuBLASLt
             out["cublaslt_nvfp4_tflops"][name] = None
             out["notes"].append(f"nvfp4 {name}: {type(e).__name__}: {str(e)[:160]}")
+        a8 = a.to(torch.float8_e4m3fn)
+        b8 = b.to(torch.float8_e4m3fn).t()
+        r8 = None
         try:
-            a8 = a.to(torch.float8_e4m3fn)
-            b8 = b.to(torch.float8_e4m3fn).t()
             one = torch.ones((), dtype=torch.float32, device="cuda")
             fn = lambda: torch._scaled_mm(a8, b8, one, one, out_dtype=torch.bfloat16)
-            fn()
+            r8 = fn()
             t = _timed(fn, args.steps, args.warmup)
             out["cublaslt_fp8_tflops"][name] = round(flop / (t * 1e-3) / 1e12, 1)
         except Exception as e:
             out["cublaslt_fp8_tflops"][name] = None
             out["notes"].append(f"fp8 {name}: {type(e).__name__}: {str(e)[:160]}")
-        del a, b, qa, qb, d
+        try:
+            # block-scaled FP8 (MXFP8): the same e4m3 codes with every block scale 2^0 (UE8M0 code
+            # 127), so the result must equal the per-tensor one; the scale layout is cuBLASLt's
+            # 128 x 4 tiling, whose content is uniform here
+            e8m0 = getattr(torch, "float8_e8m0fnu", None)
+            if e8m0 is None:
+                raise RuntimeError("torch has no float8_e8m0fnu")
+            kb = ((k // 32) + 3) // 4 * 4
+            sa8 = torch.full((((m + 127) // 128) * 128 * kb,), 127, dtype=torch.uint8, device="cuda").view(e8m0)
+            sb8 = torch.full((((n + 127) // 128) * 128 * kb,), 127, dtype=torch.uint8, device="cuda").view(e8m0)
+            fn = lambda: torch._scaled_mm(a8, b8, sa8, sb8, out_dtype=torch.bfloat16)
+            rm = fn()
+            torch.cuda.synchronize()
+            if r8 is not None:
+                out["mxfp8_vs_fp8_rel_diff"][name] = round(((rm.float() - r8.float()).norm() / r8.float().norm()).item(), 6)
+            t = _timed(fn, args.steps, args.warmup)
+            out["cublaslt_mxfp8_tflops"][name] = round(flop / (t * 1e-3) / 1e12, 1)
+        except Exception as e:
+            out["cublaslt_mxfp8_tflops"][name] = None
+            out["notes"].append(f"mxfp8 {name}: {type(e).__name__}: {str(e)[:160]}")
+        del a, b, qa, qb, d, a8, b8
         torch.cuda.empty_cache()
     out["clocks"] = _clocks()
     out["device_status"] = nv.status_query()
