@@ -190,6 +190,12 @@ __device__ __forceinline__ void tma_load_2d_hint(uint32_t dst, const CUtensorMap
         " [%0], [%1, {%2, %3}], [%4], %5;"
         :: "r"(dst), "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y), "r"(bar), "l"(pol) : "memory");
 }
+// 1-D bulk copy multicast to the CTAs of `mask` (same shared-memory offset and barrier offset in each).
+__device__ __forceinline__ void bulk_load_mc(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar, uint16_t mask) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster"
+                 " [%0], [%1], %2, [%3], %4;"
+                 :: "r"(dst), "l"(src), "r"(bytes), "r"(bar), "h"(mask) : "memory");
+}
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void bulk_wait_read0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
 __device__ __forceinline__ void bulk_wait0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
@@ -605,10 +611,13 @@ gemm_nvfp4_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
 // Sixteen warps in four warpgroups; registers move from the first two warpgroups to the
 // epilogue's (setmaxnreg: 96 each for warpgroups 0-1, 160 each for 2-3):
 //   warp 0      TMA producer of the codes tiles (two tensor copies per K tile);
-//   warp 2      producer of the scale tiles (three 2 KB bulk copies per K tile).
+//   warp 2      producer of the scale tiles: its A rows' 2 KB, and one of the B tile's two
+//               2 KB blocks multicast to both CTAs (each CTA needs all of B's scales; the
+//               pair releases every stage at once, so the copies need no extra wait).
 //               Issuing a TMA copy occupies the issuing thread for about 100
-//               cycles, so with one thread issuing all five the codes tiles of a
-//               freed stage started late;
+//               cycles, so with one thread issuing every copy the codes tiles of a
+//               freed stage started late; each copy per K tile costs the kernel
+//               2-3 % of its time, so the B scale blocks are split between the CTAs;
 //   warp 1      (leader) one lane issues the MMAs and commits them to both CTAs;
 //   warps 4-7   scale warps: shared memory -> registers -> TMEM (tcgen05.st), then
 //               tell the leader that this CTA's scales and codes tiles are ready;
@@ -933,10 +942,11 @@ gemm_nvfp4_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_con
                         mbar_arrive_expect_tx(&sf_loaded[stage], sf_bytes);
                         if (has_sfa)
                             bulk_load(smem_addr(sSFA), p.sfa + ((size_t)(mrow / 128) * p.nkt + kt) * SFT, SFT, bar);
-                        bulk_load(smem_addr(sSFB), p.sfb + ((size_t)(2 * nt) * p.nkt + kt) * SFT, SFT, bar);
-                        if (second_sfb)
-                            bulk_load(smem_addr(sSFB + SFT), p.sfb + ((size_t)(2 * nt + 1) * p.nkt + kt) * SFT,
-                                      SFT, bar);
+                        // both CTAs need all of the tile's B scales: CTA r loads 128-row block r
+                        // (when it exists) into both; the pair releases every stage at once
+                        if (rank == 0 || second_sfb)
+                            bulk_load_mc(smem_addr(sSFB + rank * SFT), p.sfb + ((size_t)(2 * nt + rank) * p.nkt + kt) * SFT,
+                                         SFT, bar, (uint16_t)0x3);
                     }
                     issued_mask |= 1u << stage;
                     issued_phase = (issued_phase & ~(1u << stage)) | (phase << stage);
@@ -947,6 +957,12 @@ gemm_nvfp4_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_con
                 for (int s = 0; s < STAGES; ++s)
                     if (issued_mask & (1u << s))
                         mbar_wait_bounded(&landed[s], (issued_phase >> s) & 1u, p.timeout_ns, nullptr, p.dev_status);
+                // a multicast scale copy lands in the other CTA too, whose barrier this thread
+                // cannot wait on: give it a fixed 50 us, far above a copy's latency
+                if (!codes) {
+                    const uint64_t t0 = global_ns();
+                    while (global_ns() - t0 < 50000ull) {}
+                }
             }
         }
     } else if (warp == 1) {
