@@ -205,3 +205,32 @@ def test_split_tail_workspace_left_ready_and_in_bounds(nv):
     assert torch.all(ws[nbytes:] == 0xA5)
     # sum buffers and arrival counters are back at zero, ready for the next call
     assert torch.count_nonzero(ws[:nbytes]).item() == 0
+
+
+def test_split_tail_gemms_on_two_streams_use_their_own_workspaces(nv):
+    """Split-tail GEMMs queued on two side streams at once (no synchronisation between them) give
+    the same bits as the same calls made one after another on one stream: each stream gets its own
+    workspace, so their tail tiles' partial sums and counters never meet."""
+    M, N, K = 2048, 2560, 1024
+    assert _pair_plan(M, N, K)[2] == 2, "shape chosen to split its tail"
+    qa, qb = _operands(nv, M, N, K, seed=91)
+    qc, qd = _operands(nv, M, N, K, seed=92)
+    nv.reset_status()
+    ref1 = nv.gemm(qa, qb, torch.bfloat16, split_tail=True)
+    ref2 = nv.gemm(qc, qd, torch.bfloat16, split_tail=True)
+    torch.cuda.synchronize()
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+    s1.wait_stream(torch.cuda.current_stream())
+    s2.wait_stream(torch.cuda.current_stream())
+    outs1, outs2 = [], []
+    for _ in range(4):
+        with torch.cuda.stream(s1):
+            outs1.append(nv.gemm(qa, qb, torch.bfloat16, split_tail=True))
+        with torch.cuda.stream(s2):
+            outs2.append(nv.gemm(qc, qd, torch.bfloat16, split_tail=True))
+    torch.cuda.synchronize()
+    assert nv.status_query() == 0
+    for d in outs1:
+        assert torch.equal(d, ref1)
+    for d in outs2:
+        assert torch.equal(d, ref2)
