@@ -210,19 +210,30 @@ constexpr int kPatchSlotBytes = 16 * 32 * 16;
 constexpr int kPatchThreads = 128;                                          // 4 warps per CTA
 constexpr int kPatchCtasPerSm = 3;                                          // by registers (~140 / thread) and shared memory
 constexpr int kPatchSmemBytes = (kPatchThreads / 32) * 2 * kPatchSlotBytes;   // 64 KB per CTA
+// The maxima passes do little arithmetic per byte: two copies in flight per warp (three slots,
+// 96 KB per CTA, two CTAs per SM) keep more bytes on the way than the encoders' one.
+constexpr int kAmaxAhead = 2;
+constexpr int kAmaxCtasPerSm = 2;
+constexpr int kAmaxSmemBytes = (kPatchThreads / 32) * (kAmaxAhead + 1) * kPatchSlotBytes;
 constexpr int kBandGroup = 8;                                               // bands per tile group (power of 2)
 
-template <typename T>
+template <typename T, int AHEAD = 1>
 struct PatchPipe {
     static constexpr int VEC = Vec<T>::N;
+    static constexpr int SLOTS = AHEAD + 1;         // the current patch + AHEAD copies in flight
     const T* x;
-    int64_t ldx, R, C, tiles, nwarps, tile;
+    int64_t ldx, R, C, tiles, nwarps;
+    int64_t tile;                    // tile index of the current patch
+    int64_t itile;                   // tile index of the next copy to issue
     Walk2D w;
     int rg, cc;
-    uint32_t sbase;                 // shared address of this lane's slot 0, row 0
-    uint32_t slot = 0, rslot = 0;
-    int64_t r0 = 0, c0 = 0, nr0 = 0, nc0 = 0;   // current patch / the one in flight
-    bool ok = false, nok = false;
+    uint32_t sbase;                  // shared address of this lane's slot 0, row 0
+    uint32_t islot = 0, rslot = 0;   // slot of the next copy / of the current patch
+    int64_t r0 = 0, c0 = 0;          // current patch
+    bool ok = false;
+    int64_t qr[AHEAD], qc[AHEAD];    // copies in flight, oldest first
+    bool qok[AHEAD];
+    uint32_t qslot[AHEAD];
 
     // Tile order: groups of kBandGroup 64-row bands, column-major inside a group, so
     // neighbouring warps (the warps of a CTA and of the next CTA) take vertically adjacent
@@ -233,44 +244,60 @@ struct PatchPipe {
                                          int64_t nwarps_, int64_t /*tiles*/, int64_t tiles_c, uint8_t* smem)
         : x(x_), ldx(ldx_), R(R_), C(C_),
           tiles((((R_ + 63) / 64 + kBandGroup - 1) / kBandGroup) * kBandGroup * tiles_c), nwarps(nwarps_),
-          tile(warp0), w(warp0, nwarps_, kBandGroup * (tiles_c > 0 ? tiles_c : 1)) {
+          tile(warp0), itile(warp0), w(warp0, nwarps_, kBandGroup * (tiles_c > 0 ? tiles_c : 1)) {
         const int lane = threadIdx.x & 31;
         rg = lane >> 3;
         cc = lane & 7;
-        sbase = smem_addr(smem) + (uint32_t)((threadIdx.x >> 5) * 2 * kPatchSlotBytes + lane * 16);
-        if (tile < tiles) issue(0);
-        else commit();
+        sbase = smem_addr(smem) + (uint32_t)((threadIdx.x >> 5) * SLOTS * kPatchSlotBytes + lane * 16);
+#pragma unroll
+        for (int k = 0; k < AHEAD; ++k) issue_next(k);
     }
     __device__ __forceinline__ static void commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-    // copies the patch at the walker's position into slot s (one commit group)
-    __device__ __forceinline__ void issue(uint32_t s) {
-        nr0 = (w.row * kBandGroup + (w.col & (kBandGroup - 1))) * 64 + rg * 16;
-        nc0 = (w.col / kBandGroup) * (8 * VEC) + cc * VEC;
-        nok = nr0 < R && nc0 < C;
-        if (nok) {
-            const char* src = reinterpret_cast<const char*>(x + nr0 * ldx + nc0);
-            const int64_t pitch = ldx * (int64_t)sizeof(T);
+    // copies the patch at the walker's position (tile itile) into the next slot as queue entry k
+    // (one commit group, empty past the last tile), then steps the walker
+    __device__ __forceinline__ void issue_next(int k) {
+        qslot[k] = islot;
+        qok[k] = false;
+        qr[k] = 0;
+        qc[k] = 0;
+        if (itile < tiles) {
+            const int64_t nr = (w.row * kBandGroup + (w.col & (kBandGroup - 1))) * 64 + rg * 16;
+            const int64_t nc = (w.col / kBandGroup) * (8 * VEC) + cc * VEC;
+            qr[k] = nr;
+            qc[k] = nc;
+            qok[k] = nr < R && nc < C;
+            if (qok[k]) {
+                const char* src = reinterpret_cast<const char*>(x + nr * ldx + nc);
+                const int64_t pitch = ldx * (int64_t)sizeof(T);
 #pragma unroll
-            for (int i = 0; i < 16; ++i)
-                asm volatile("cp.async.cg.shared.global [%0], [%1], 16;"
-                             :: "r"(sbase + s * kPatchSlotBytes + i * 512), "l"(src + i * pitch) : "memory");
+                for (int i = 0; i < 16; ++i)
+                    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;"
+                                 :: "r"(sbase + islot * kPatchSlotBytes + i * 512), "l"(src + i * pitch) : "memory");
+            }
         }
         commit();
+        w.advance();
+        itile += nwarps;
+        islot = islot + 1 == SLOTS ? 0u : islot + 1;
     }
-    // Makes the next patch of this warp current (r0, c0, ok) and starts the copy of the
-    // one after it; false when the warp has no patch left.
+    // Makes the next patch of this warp current (r0, c0, ok) and starts the copy AHEAD patches
+    // after it; false when the warp has no patch left.
     __device__ __forceinline__ bool next() {
         if (tile >= tiles) return false;
-        r0 = nr0;
-        c0 = nc0;
-        ok = nok;
-        rslot = slot;
-        slot ^= 1u;
-        w.advance();
-        if (tile + nwarps < tiles) issue(slot);
-        else commit();
+        r0 = qr[0];
+        c0 = qc[0];
+        ok = qok[0];
+        rslot = qslot[0];
+#pragma unroll
+        for (int k = 0; k + 1 < AHEAD; ++k) {
+            qr[k] = qr[k + 1];
+            qc[k] = qc[k + 1];
+            qok[k] = qok[k + 1];
+            qslot[k] = qslot[k + 1];
+        }
+        issue_next(AHEAD - 1);
         tile += nwarps;
-        asm volatile("cp.async.wait_group 1;" ::: "memory");     // the current patch has landed
+        asm volatile("cp.async.wait_group %0;" :: "n"(AHEAD) : "memory");   // the current patch has landed
         return true;
     }
     __device__ __forceinline__ uint4 read_row(int i) const {
@@ -356,7 +383,7 @@ __device__ __forceinline__ void col_pair_abs_max(const float2 (&t)[16], float& m
 
 // amax of RHT(x) along rows: the Wgrad operands' tensor amax after the transform.
 template <typename T>
-__global__ void __launch_bounds__(kPatchThreads, kPatchCtasPerSm) amax_rht_kernel(const T* __restrict__ x, int64_t R, int64_t C,
+__global__ void __launch_bounds__(kPatchThreads, kAmaxCtasPerSm) amax_rht_kernel(const T* __restrict__ x, int64_t R, int64_t C,
                                                             int64_t ldx, uint64_t rht_seed,
                                                             uint32_t* __restrict__ partials) {
     pdl_launch_dependents();
@@ -369,7 +396,7 @@ __global__ void __launch_bounds__(kPatchThreads, kPatchCtasPerSm) amax_rht_kerne
     const uint32_t sign_mask = rht_sign_mask(rht_seed);
     if constexpr (sizeof(T) == 2) {
         float m = 0.0f;
-        PatchPipe<T> pp(x, ldx, R, C, warp0, nwarps, tiles, tiles_c, patch_smem);
+        PatchPipe<T, kAmaxAhead> pp(x, ldx, R, C, warp0, nwarps, tiles, tiles_c, patch_smem);
         while (pp.next()) {
             if (!pp.ok) continue;
             const int64_t r0 = pp.r0, c0 = pp.c0;
@@ -392,7 +419,7 @@ __global__ void __launch_bounds__(kPatchThreads, kPatchCtasPerSm) amax_rht_kerne
     }
     float m = 0.0f;
     bool bad = false;                                // NaN: fmaxf would drop it
-    PatchPipe<T> pp(x, ldx, R, C, warp0, nwarps, tiles, tiles_c, patch_smem);
+    PatchPipe<T, kAmaxAhead> pp(x, ldx, R, C, warp0, nwarps, tiles, tiles_c, patch_smem);
     while (pp.next()) {
         if (!pp.ok) continue;
         const int64_t r0 = pp.r0, c0 = pp.c0;
@@ -417,7 +444,7 @@ __global__ void __launch_bounds__(kPatchThreads, kPatchCtasPerSm) amax_rht_kerne
 // Both tensor amaxes of a dual quantization in one read: |x| (row operand) and
 // |RHT(x)| along rows (column operand).
 template <typename T, bool SQR = false>
-__global__ void __launch_bounds__(kPatchThreads, kPatchCtasPerSm) amax_dual_kernel(const T* __restrict__ x, int64_t R, int64_t C,
+__global__ void __launch_bounds__(kPatchThreads, kAmaxCtasPerSm) amax_dual_kernel(const T* __restrict__ x, int64_t R, int64_t C,
                                                              int64_t ldx, uint64_t rht_seed,
                                                              uint32_t* __restrict__ partials_plain,
                                                              uint32_t* __restrict__ partials_rht) {
@@ -433,7 +460,7 @@ __global__ void __launch_bounds__(kPatchThreads, kPatchCtasPerSm) amax_dual_kern
     bool bad = false;
     if constexpr (sizeof(T) == 2) {
         uint32_t mpk = 0u;                           // packed bf16 |x| maxima
-        PatchPipe<T> pp(x, ldx, R, C, warp0, nwarps, tiles, tiles_c, patch_smem);
+        PatchPipe<T, kAmaxAhead> pp(x, ldx, R, C, warp0, nwarps, tiles, tiles_c, patch_smem);
         while (pp.next()) {
             if (!pp.ok) continue;
             const int64_t r0 = pp.r0, c0 = pp.c0;
@@ -456,7 +483,7 @@ __global__ void __launch_bounds__(kPatchThreads, kPatchCtasPerSm) amax_dual_kern
         mp = __uint_as_float(bf16x2_abs_max_bits(mpk));
         mr = __uint_as_float(__float_as_uint(__fmul_rn(fabsf(mr), 0.25f)) & 0x7FFFFFFFu);
     } else {
-    PatchPipe<T> pp(x, ldx, R, C, warp0, nwarps, tiles, tiles_c, patch_smem);
+    PatchPipe<T, kAmaxAhead> pp(x, ldx, R, C, warp0, nwarps, tiles, tiles_c, patch_smem);
     while (pp.next()) {
         if (!pp.ok) continue;
         const int64_t r0 = pp.r0, c0 = pp.c0;
@@ -1185,10 +1212,10 @@ cudaError_t launch_resident(K* kern, int64_t work_ctas, int sms, int* grid, cuda
 
 // Grid of the patch kernels: one CTA (eight warps) per SM at most, one warp per
 // 64 x (8 * 16 B) tile at least.
-int patch_grid(int sms, int64_t R, int64_t C, bool is16) {
+int patch_grid(int sms, int64_t R, int64_t C, bool is16, int ctas_per_sm = kPatchCtasPerSm) {
     const int vec = is16 ? 8 : 4;
     const int64_t tiles = (R == 0 || C == 0) ? 0 : ((R + 63) / 64) * ((C + 8 * vec - 1) / (8 * vec));
-    const int64_t g = std::max<int64_t>(1, std::min<int64_t>((int64_t)sms * kPatchCtasPerSm,
+    const int64_t g = std::max<int64_t>(1, std::min<int64_t>((int64_t)sms * ctas_per_sm,
                                                              (tiles + kPatchThreads / 32 - 1) / (kPatchThreads / 32)));
     return (int)std::min<int64_t>(g, kMaxPartials);
 }
@@ -1196,7 +1223,7 @@ int patch_grid(int sms, int64_t R, int64_t C, bool is16) {
 // The patch kernels' dynamic shared memory (the cp.async double buffer), allowed once
 // per kernel and device.
 template <typename K>
-cudaError_t allow_patch_smem(K* kern) {
+cudaError_t allow_patch_smem(K* kern, int bytes = kPatchSmemBytes) {
     static std::mutex mu;
     static std::set<std::pair<int, const void*>> done;
     int dev = 0;
@@ -1205,7 +1232,7 @@ cudaError_t allow_patch_smem(K* kern) {
     std::lock_guard<std::mutex> lk(mu);
     const auto key = std::make_pair(dev, reinterpret_cast<const void*>(kern));
     if (done.count(key)) return cudaSuccess;
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kPatchSmemBytes);
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
     if (e == cudaSuccess) done.insert(key);
     return e;
 }
@@ -1216,15 +1243,22 @@ cudaError_t launch_patch(K* kern, int grid, cudaStream_t stream, Args... args) {
     if (e != cudaSuccess) return e;
     return launch_pdl(kern, dim3(grid), dim3(kPatchThreads), kPatchSmemBytes, stream, args...);
 }
+// The maxima passes: kAmaxAhead copies in flight per warp (more shared memory, fewer CTAs).
+template <typename K, typename... Args>
+cudaError_t launch_patch_amax(K* kern, int grid, cudaStream_t stream, Args... args) {
+    const cudaError_t e = allow_patch_smem(kern, kAmaxSmemBytes);
+    if (e != cudaSuccess) return e;
+    return launch_pdl(kern, dim3(grid), dim3(kPatchThreads), kAmaxSmemBytes, stream, args...);
+}
 
 // Pass 1 for one quantization: per-CTA partial maxima of |x| or |RHT(x)|; *g1 = their count.
 cudaError_t amax_pass(const void* x, bool is16, int64_t R, int64_t C, int64_t ldx, bool rht, uint64_t rht_seed,
                       uint32_t* partials, int sms, int* g1, cudaStream_t stream, bool sqr = false) {
     const int64_t chunks = (R == 0 || C == 0) ? 0 : R * (C / (is16 ? 8 : 4));
     if (rht) {
-        *g1 = patch_grid(sms, R, C, is16);
-        return is16 ? launch_patch(amax_rht_kernel<uint16_t>, *g1, stream, (const uint16_t*)x, R, C, ldx, rht_seed, partials)
-                    : launch_patch(amax_rht_kernel<float>, *g1, stream, (const float*)x, R, C, ldx, rht_seed, partials);
+        *g1 = patch_grid(sms, R, C, is16, kAmaxCtasPerSm);
+        return is16 ? launch_patch_amax(amax_rht_kernel<uint16_t>, *g1, stream, (const uint16_t*)x, R, C, ldx, rht_seed, partials)
+                    : launch_patch_amax(amax_rht_kernel<float>, *g1, stream, (const float*)x, R, C, ldx, rht_seed, partials);
     }
     const int64_t work = (chunks + kThreads * 4 - 1) / (kThreads * 4);
     const uint16_t* xb = (const uint16_t*)x;
@@ -1389,11 +1423,11 @@ nvfp4_status quantize_dual_impl(const void* x, int32_t x_dtype, int64_t R, int64
     int g1 = 0;
     if (p_col->rht) {
         // one read of x for both tensor amaxes
-        g1 = patch_grid(sms, R, C, is16);
+        g1 = patch_grid(sms, R, C, is16, kAmaxCtasPerSm);
         const cudaError_t e = !is16
-            ? launch_patch(amax_dual_kernel<float>, g1, stream, (const float*)x, R, C, ldx, p_col->rht_seed, part_plain, part_col)
-            : sqr ? launch_patch(amax_dual_kernel<uint16_t, true>, g1, stream, (const uint16_t*)x, R, C, ldx, p_col->rht_seed, part_plain, part_col)
-                  : launch_patch(amax_dual_kernel<uint16_t>, g1, stream, (const uint16_t*)x, R, C, ldx, p_col->rht_seed, part_plain, part_col);
+            ? launch_patch_amax(amax_dual_kernel<float>, g1, stream, (const float*)x, R, C, ldx, p_col->rht_seed, part_plain, part_col)
+            : sqr ? launch_patch_amax(amax_dual_kernel<uint16_t, true>, g1, stream, (const uint16_t*)x, R, C, ldx, p_col->rht_seed, part_plain, part_col)
+                  : launch_patch_amax(amax_dual_kernel<uint16_t>, g1, stream, (const uint16_t*)x, R, C, ldx, p_col->rht_seed, part_plain, part_col);
         if (e != cudaSuccess) return NVFP4_ERR_CUDA;
     } else {
         // without the RHT both operands share the plain amax
