@@ -210,8 +210,9 @@ constexpr int kPatchSlotBytes = 16 * 32 * 16;
 constexpr int kPatchThreads = 128;                                          // 4 warps per CTA
 constexpr int kPatchCtasPerSm = 3;                                          // by registers (~140 / thread) and shared memory
 constexpr int kPatchSmemBytes = (kPatchThreads / 32) * 2 * kPatchSlotBytes;   // 64 KB per CTA
-// The maxima passes do little arithmetic per byte: two copies in flight per warp (three slots,
-// 96 KB per CTA, two CTAs per SM) keep more bytes on the way than the encoders' one.
+// The maxima passes and the 16x16 encoder do little arithmetic per byte: two copies in flight per
+// warp (three slots, 96 KB per CTA, two CTAs per SM) keep more bytes on the way than the row /
+// column encoders' one (those are bound by their arithmetic and want the third CTA's warps).
 constexpr int kAmaxAhead = 2;
 constexpr int kAmaxCtasPerSm = 2;
 constexpr int kAmaxSmemBytes = (kPatchThreads / 32) * (kAmaxAhead + 1) * kPatchSlotBytes;
@@ -946,7 +947,7 @@ __global__ void __launch_bounds__(kPatchThreads, kPatchCtasPerSm) encode_dual_ke
 // Pass 2, 16x16 tiles (weights): writes W and W^T codes from one tile scale.
 // ---------------------------------------------------------------------------
 template <typename T, bool SR>
-__global__ void __launch_bounds__(kPatchThreads, kPatchCtasPerSm) encode_2d_kernel(const T* __restrict__ x, int64_t R, int64_t C,
+__global__ void __launch_bounds__(kPatchThreads, kAmaxCtasPerSm) encode_2d_kernel(const T* __restrict__ x, int64_t R, int64_t C,
                                                              int64_t ldx, const uint32_t* __restrict__ partials,
                                                              int nparts, QOut out, uint64_t sr_seed,
                                                              uint32_t sr_offset, uint32_t* dev_status) {
@@ -962,7 +963,7 @@ __global__ void __launch_bounds__(kPatchThreads, kPatchCtasPerSm) encode_2d_kern
     const int64_t nkb = (C + 255) / 256, nkb_t = (R + 255) / 256;
     const int64_t warp0 = (int64_t)blockIdx.x * (kPatchThreads / 32) + (threadIdx.x >> 5);
     const int64_t nwarps = (int64_t)gridDim.x * (kPatchThreads / 32);
-    PatchPipe<T> pp(x, ldx, R, C, warp0, nwarps, tiles, tiles_c, patch_smem);
+    PatchPipe<T, kAmaxAhead> pp(x, ldx, R, C, warp0, nwarps, tiles, tiles_c, patch_smem);
     if constexpr (sizeof(T) == 2) {
         // bf16: tile maxima on the packed words, then row by row from shared memory; the
         // W^T codes come from two 8 x 8 nibble transposes of the 16 row words.
@@ -1243,7 +1244,8 @@ cudaError_t launch_patch(K* kern, int grid, cudaStream_t stream, Args... args) {
     if (e != cudaSuccess) return e;
     return launch_pdl(kern, dim3(grid), dim3(kPatchThreads), kPatchSmemBytes, stream, args...);
 }
-// The maxima passes: kAmaxAhead copies in flight per warp (more shared memory, fewer CTAs).
+// The maxima passes and the 16x16 encoder: kAmaxAhead copies in flight per warp (more shared
+// memory, fewer CTAs).
 template <typename K, typename... Args>
 cudaError_t launch_patch_amax(K* kern, int grid, cudaStream_t stream, Args... args) {
     const cudaError_t e = allow_patch_smem(kern, kAmaxSmemBytes);
@@ -1308,6 +1310,7 @@ nvfp4_status encode_pass(const void* x, int32_t x_dtype, int64_t R, int64_t C, i
     const int64_t row_ctas = (row_warps + 7) / 8;
     int g_row = 0;
     const int g_patch = patch_grid(sms, R, C, is16);
+    const int g_deep = patch_grid(sms, R, C, is16, kAmaxCtasPerSm);
     // 32-byte loads when every 16-element block starts on a 32-byte boundary
     const int v8 = ((reinterpret_cast<uintptr_t>(x) & 31u) == 0 && ((size_t)ldx * esz) % 32 == 0) ? 1 : 0;
     const uint64_t ss = p->sr_seed;
@@ -1325,8 +1328,8 @@ nvfp4_status encode_pass(const void* x, int32_t x_dtype, int64_t R, int64_t C, i
             else if (p->rht) e = launch_patch(encode_col_kernel<T, false, true>, g_patch, stream, xt, R, C, ldx, partials, g1, q, ss, so, rs, dev_status); \
             else e = launch_patch(encode_col_kernel<T, false, false>, g_patch, stream, xt, R, C, ldx, partials, g1, q, ss, so, rs, dev_status); \
         } else {                                                                                           \
-            if (sr) e = launch_patch(encode_2d_kernel<T, true>, g_patch, stream, xt, R, C, ldx, partials, g1, q, ss, so, dev_status); \
-            else e = launch_patch(encode_2d_kernel<T, false>, g_patch, stream, xt, R, C, ldx, partials, g1, q, ss, so, dev_status); \
+            if (sr) e = launch_patch_amax(encode_2d_kernel<T, true>, g_deep, stream, xt, R, C, ldx, partials, g1, q, ss, so, dev_status); \
+            else e = launch_patch_amax(encode_2d_kernel<T, false>, g_deep, stream, xt, R, C, ldx, partials, g1, q, ss, so, dev_status); \
         }                                                                                                  \
     } while (0)
     if (is16 && sqr) {
