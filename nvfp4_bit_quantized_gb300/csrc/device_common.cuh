@@ -241,10 +241,11 @@ __device__ __forceinline__ void hadamard16_x2(float2 (&t)[16]) {
 // ----------------------------------------------------------------------------
 struct Philox4 { uint32_t w[4]; };
 
-// The ten round keys, computed once per thread (the key is a launch parameter).
+// The ten round keys.  The quantizers get them as a kernel parameter, computed on the host, so
+// each round's xor reads its key straight from the parameter bank.
 struct PhiloxKey { uint32_t k0[10], k1[10]; };
 
-__device__ __forceinline__ PhiloxKey philox_key(uint64_t seed) {
+__host__ __device__ __forceinline__ PhiloxKey philox_key(uint64_t seed) {
     PhiloxKey k;
     uint32_t a = (uint32_t)seed, b = (uint32_t)(seed >> 32);
 #pragma unroll

@@ -666,13 +666,13 @@ __device__ __forceinline__ void encode_row_block_bf16(const uint32_t (&w)[8], co
 template <typename T, bool SR, bool SQR = false>
 __global__ void __launch_bounds__(kThreads) encode_row_kernel(const T* __restrict__ x, int64_t R, int64_t C,
                                                               int64_t ldx, const uint32_t* __restrict__ partials,
-                                                              int nparts, QOut out, uint64_t sr_seed,
+                                                              int nparts, QOut out, const PhiloxKey sr_key,
                                                               uint32_t sr_offset, int v8, uint32_t* dev_status) {
     pdl_launch_dependents();
     pdl_wait();
     using B = Block16<T>;
     const Scales sc = tensor_scales(partials, nparts, out.s_dec, dev_status);
-    const PhiloxKey key = philox_key(sr_seed);
+    const PhiloxKey& key = sr_key;
     const int lane = threadIdx.x & 31;
     const int64_t bpr = C / 16;                      // blocks per row
     const int64_t spr = (bpr + 31) / 32;             // warp segments per row
@@ -805,7 +805,7 @@ __device__ __forceinline__ void encode_col_patch_bf16(const uint4 (&v)[16], int6
 template <typename T, bool SR, bool RHT, bool SQR = false>
 __global__ void __launch_bounds__(kPatchThreads, kPatchCtasPerSm) encode_col_kernel(const T* __restrict__ x, int64_t R, int64_t C,
                                                               int64_t ldx, const uint32_t* __restrict__ partials,
-                                                              int nparts, QOut out, uint64_t sr_seed,
+                                                              int nparts, QOut out, const PhiloxKey sr_key,
                                                               uint32_t sr_offset, uint64_t rht_seed,
                                                               uint32_t* dev_status) {
     pdl_launch_dependents();
@@ -813,7 +813,7 @@ __global__ void __launch_bounds__(kPatchThreads, kPatchCtasPerSm) encode_col_ker
     constexpr int VEC = Vec<T>::N;
     const uint32_t sign_mask = RHT ? rht_sign_mask(rht_seed) : 0u;
     const Scales sc = tensor_scales(partials, nparts, out.s_dec, dev_status);
-    const PhiloxKey key = philox_key(sr_seed);
+    const PhiloxKey& key = sr_key;
     const int64_t tiles_c = (C + 8 * VEC - 1) / (8 * VEC);
     const int64_t tiles = ((R + 63) / 64) * tiles_c;
     const int64_t nkb = (R + 255) / 256;             // operand cols = R
@@ -886,15 +886,14 @@ __global__ void __launch_bounds__(kPatchThreads, kPatchCtasPerSm) encode_col_ker
 template <bool SR, bool SQR>
 __global__ void __launch_bounds__(kPatchThreads, kPatchCtasPerSm) encode_dual_kernel(
     const uint16_t* __restrict__ x, int64_t R, int64_t C, int64_t ldx, const uint32_t* __restrict__ part_row,
-    const uint32_t* __restrict__ part_col, int nparts, QOut out_row, QOut out_col, uint64_t seed_row,
-    uint64_t seed_col, uint32_t off_row, uint32_t off_col, uint64_t rht_seed, uint32_t* dev_status) {
+    const uint32_t* __restrict__ part_col, int nparts, QOut out_row, QOut out_col, const PhiloxKey key_row,
+    const PhiloxKey key_col, uint32_t off_row, uint32_t off_col, uint64_t rht_seed, uint32_t* dev_status) {
     pdl_launch_dependents();
     pdl_wait();
     __shared__ float eb_row[128];
     const uint32_t sign_mask = rht_sign_mask(rht_seed);
     const Scales s_row = tensor_scales(part_row, nparts, out_row.s_dec, dev_status, eb_row);
     const Scales s_col = tensor_scales(part_col, nparts, out_col.s_dec, dev_status);
-    const PhiloxKey key_row = philox_key(seed_row), key_col = philox_key(seed_col);
     const int64_t tiles_c = (C + 63) / 64;
     const int64_t tiles = ((R + 63) / 64) * tiles_c;
     const int64_t nkb_col = (R + 255) / 256, nkb_row = (C + 255) / 256;
@@ -949,14 +948,14 @@ __global__ void __launch_bounds__(kPatchThreads, kPatchCtasPerSm) encode_dual_ke
 template <typename T, bool SR>
 __global__ void __launch_bounds__(kPatchThreads, kAmaxCtasPerSm) encode_2d_kernel(const T* __restrict__ x, int64_t R, int64_t C,
                                                              int64_t ldx, const uint32_t* __restrict__ partials,
-                                                             int nparts, QOut out, uint64_t sr_seed,
+                                                             int nparts, QOut out, const PhiloxKey sr_key,
                                                              uint32_t sr_offset, uint32_t* dev_status) {
     pdl_launch_dependents();
     pdl_wait();
     constexpr int VEC = Vec<T>::N;
     constexpr int LPT = 16 / VEC;                    // lanes per 16-column tile
     const Scales sc = tensor_scales(partials, nparts, out.s_dec, dev_status);
-    const PhiloxKey key = philox_key(sr_seed);
+    const PhiloxKey& key = sr_key;
     const int lane = threadIdx.x & 31, cc = lane & 7;
     const int64_t tiles_c = (C + 8 * VEC - 1) / (8 * VEC);
     const int64_t tiles = ((R + 63) / 64) * tiles_c;
@@ -1313,7 +1312,7 @@ nvfp4_status encode_pass(const void* x, int32_t x_dtype, int64_t R, int64_t C, i
     const int g_deep = patch_grid(sms, R, C, is16, kAmaxCtasPerSm);
     // 32-byte loads when every 16-element block starts on a 32-byte boundary
     const int v8 = ((reinterpret_cast<uintptr_t>(x) & 31u) == 0 && ((size_t)ldx * esz) % 32 == 0) ? 1 : 0;
-    const uint64_t ss = p->sr_seed;
+    const PhiloxKey ss = philox_key(p->sr_seed);
     const uint32_t so = p->sr_offset;
     cudaError_t e = cudaSuccess;
 #define NVFP4_LAUNCH_T(T)                                                                                  \
@@ -1395,8 +1394,8 @@ nvfp4_status encode_dual_pass(const void* x, int64_t R, int64_t C, int64_t ldx, 
     const int g = patch_grid(sms, R, C, true);
     const uint16_t* xb = static_cast<const uint16_t*>(x);
     auto launch = [&](auto* kern) {
-        return launch_patch(kern, g, stream, xb, R, C, ldx, part_row, part_col, g1, qr, qc, p_row->sr_seed,
-                            p_col->sr_seed, p_row->sr_offset, p_col->sr_offset, p_col->rht_seed, dev_status);
+        return launch_patch(kern, g, stream, xb, R, C, ldx, part_row, part_col, g1, qr, qc, philox_key(p_row->sr_seed),
+                            philox_key(p_col->sr_seed), p_row->sr_offset, p_col->sr_offset, p_col->rht_seed, dev_status);
     };
     const bool sr = p_row->round == NVFP4_ROUND_SR;
     const cudaError_t e = sr ? (sqr ? launch(encode_dual_kernel<true, true>) : launch(encode_dual_kernel<true, false>))
